@@ -1,0 +1,395 @@
+// Stage 4: one attention over the selected compressed entries plus the sliding
+// window of raw tokens, under a single softmax ("DeepSeek-V4 本地部署，SGLang 把活
+// 做絕了", sec. "Kernel 層一堆狠活": SWA and the extra C4/C128 attention in one
+// call; heads padded for the tensor-core tile as in "SGLang 如何为 DeepSeek V4
+// 打造「Day-0」推理加速", sec. "3.2 高 TP 下的 FlashMLA 头填充").
+//
+//   l_j = scale * q_h . K_j,  o_h = sum_j softmax(l)_j V_j,  K = V = the bf16 latent row
+//
+// GB300 mapping.  One CTA = one 64-key tile range (a "split") x one half of the
+// 512 V columns.  Heads are the MMA M dimension, padded to 128 (TMEM lane h =
+// head h = thread h).  Per key tile:
+//   gather 64 rows (cp.async 16 B, paged addressing) into a 128-byte-swizzled
+//   K-major tile; S = Q K^T with tcgen05.mma (M=128, N=64, K=512) into TMEM;
+//   each thread reads its head's 64 logits (tcgen05.ld), updates its running
+//   max/sum (online softmax; the running max only moves when a tile raises it
+//   by more than 2^8, then O is rescaled in TMEM); P (bf16) goes to shared memory;
+//   O += P V with tcgen05.mma (M=128, N=256, K=64) where the same K tile is read
+//   as an MN-major B operand.
+// S uses TMEM columns [256, 320), the O half [0, 256).  Splits are merged by a
+// log-sum-exp kernel (or written directly when a request has one split).
+#include "common.cuh"
+#include "internal.h"
+
+namespace csa {
+
+constexpr int AT_T = 128;
+constexpr int AT_M = 128;
+constexpr int AT_KT = 64;
+constexpr int AT_DH = 256;
+constexpr uint32_t SM_Q = 0;                       // 8 slabs x 128 rows x 128 B
+constexpr uint32_t SM_K = 131072;                  // 8 slabs x 64 rows x 128 B
+constexpr uint32_t SM_P = 196608;                  // 128 rows x 128 B
+constexpr uint32_t SM_BAR = 212992;                // 2 mbarriers
+constexpr uint32_t SM_TMEM = SM_BAR + 16;
+constexpr uint32_t SM_KPTR = SM_BAR + 64;          // 64 row pointers
+constexpr uint32_t SM_KOK = SM_KPTR + 64 * 8;      // 64-bit valid mask
+constexpr uint32_t AT_SMEM = SM_KOK + 64 + 1024;   // + alignment slack
+constexpr uint32_t Q_SLAB = AT_M * 128;
+constexpr uint32_t K_SLAB = AT_KT * 128;
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
+constexpr float RESCALE_THRESHOLD = 8.0f;          // log2 units
+
+struct AttnArgs {
+    const uint16_t* q;
+    int H;
+    float sl2;                 // scale * log2(e)
+    DPaged kc, kr;
+    const int32_t* sel;
+    int64_t sel_stride;
+    int n_sel;
+    const int64_t* n_tokens;
+    int ratio;
+    int64_t N;
+    int swa;
+    int tps, S;
+    float* part_o;             // [B][S][H][512]
+    float* part_ml;            // [B][S][H][2]  (max in log2 units, sum)
+    uint16_t* out;
+    float* lse;
+    int32_t* status;
+};
+
+__device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk) {  // byte offset inside a 128-B-row slab
+    return row * 128u + ((chunk ^ (row & 7u)) << 4);
+}
+
+__global__ void __launch_bounds__(AT_T, 1) attn_kernel(AttnArgs a) {
+    extern __shared__ uint8_t at_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(at_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(sm);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int half = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
+    const uint32_t bar_s = sbase + SM_BAR, bar_o = sbase + SM_BAR + 8;
+    const uint8_t** kptr = reinterpret_cast<const uint8_t**>(sm + SM_KPTR);
+    uint64_t* kok = reinterpret_cast<uint64_t*>(sm + SM_KOK);
+
+    const int64_t N = a.n_tokens ? a.n_tokens[b] : a.N;
+    const int64_t W = N < a.swa ? N : a.swa;
+    const int64_t n_c = a.sel ? a.n_sel : (a.n_tokens ? N / a.ratio : a.n_sel);
+    const int64_t n_keys = n_c + W;
+    const int64_t T = (n_keys + AT_KT - 1) / AT_KT;
+    const int64_t t0 = (int64_t)split * a.tps;
+    const int64_t t1 = t0 + a.tps < T ? t0 + a.tps : T;
+    const int H = a.H;
+    const int h = tid;  // head row owned by this thread
+
+    float m_run = -INFINITY, l_run = 0.f;
+    if (t0 < t1) {
+        if (warp == 0) {
+            tmem_alloc(sbase + SM_TMEM, 512);
+            tmem_relinquish();
+        }
+        if (tid == 0) {
+            mbar_init(bar_s, 1);
+            mbar_init(bar_o, 1);
+            fence_mbar_init();
+        }
+        // Q -> swizzled K-major tile (rows >= H are zero)
+        const uint16_t* qb = a.q + (int64_t)b * H * D;
+        for (int c = tid; c < AT_M * 64; c += AT_T) {
+            const uint32_t row = c >> 6, ch = c & 63;
+            const uint32_t dst = sbase + SM_Q + (ch >> 3) * Q_SLAB + swz(row, ch & 7);
+            if ((int)row < H)
+                cp_async16(dst, qb + row * D + ch * 8);
+            else
+                st_shared_zero16(dst);
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + SM_TMEM);
+        const uint32_t t_o = tmem;            // O half: columns [0, 256)
+        const uint32_t t_s = tmem + AT_DH;    // S: columns [256, 320)
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        bool ok = true;
+
+        int it = 0;
+        for (int64_t tile = t0; tile < t1; ++tile, ++it) {
+            // ---- key rows of this tile
+            if (tid < AT_KT) {
+                const int64_t j = tile * AT_KT + tid;
+                const uint8_t* p = nullptr;
+                if (j < n_c) {
+                    const int64_t g = a.sel ? (int64_t)__ldg(a.sel + (int64_t)b * a.sel_stride + j) : j;
+                    if (g >= 0) p = row_addr(a.kc, b, g, ROW_BYTES, a.status);
+                } else if (j < n_keys) {
+                    p = row_addr(a.kr, b, N - W + (j - n_c), ROW_BYTES, a.status);
+                }
+                kptr[tid] = p;
+                const unsigned m = __ballot_sync(0xffffffffu, p != nullptr);
+                if (lane == 0) reinterpret_cast<uint32_t*>(kok)[warp] = m;
+            }
+            // the previous tile's P.V must be done before K/V and P are overwritten
+            if (it > 0 && !mbar_wait(bar_o, (uint32_t)((it - 1) & 1))) ok = false;
+            __syncthreads();
+            for (int c = tid; c < AT_KT * 64; c += AT_T) {
+                const uint32_t row = c >> 6, ch = c & 63;
+                const uint32_t dst = sbase + SM_K + (ch >> 3) * K_SLAB + swz(row, ch & 7);
+                const uint8_t* src = kptr[row];
+                if (src)
+                    cp_async16(dst, src + ch * 16);
+                else
+                    st_shared_zero16(dst);
+            }
+            cp_async_commit();
+            cp_async_wait_all();
+            fence_proxy_async_smem();
+            __syncthreads();
+            // ---- S = Q K^T  (M=128, N=64, K=512: 8 slabs x 4 steps of 16)
+            if (tid == 0) {
+                tc_fence_after();
+                constexpr uint32_t id_s = idesc_bf16_f32(AT_M, AT_KT, false);
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = sdesc_sw128(sbase + SM_Q + s * Q_SLAB + kk * 32, 16, 1024);
+                        const uint64_t bd = sdesc_sw128(sbase + SM_K + s * K_SLAB + kk * 32, 16, 1024);
+                        tc_mma_f16(t_s, ad, bd, id_s, (s | kk) ? 1u : 0u);
+                    }
+                tc_commit(bar_s);
+            }
+            if (!mbar_wait(bar_s, (uint32_t)(it & 1))) ok = false;
+            tc_fence_after();
+            // ---- online softmax for row h
+            uint32_t sr[2][32];
+            tc_ld32(t_s + lane_off, sr[0]);
+            tc_ld32(t_s + lane_off + 32, sr[1]);
+            tc_wait_ld();
+            const uint64_t valid = *kok;
+            float x[64];
+            float mt = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                const bool v = (valid >> j) & 1ull;
+                x[j] = v ? __uint_as_float(sr[j >> 5][j & 31]) * a.sl2 : -INFINITY;
+                mt = fmaxf(mt, x[j]);
+            }
+            float alpha = 1.f;
+            if (mt > -INFINITY) {
+                if (m_run == -INFINITY) {
+                    m_run = mt;
+                } else if (mt > m_run + RESCALE_THRESHOLD) {
+                    alpha = exp2f(m_run - mt);
+                    m_run = mt;
+                }
+            }
+            // rescale O (columns of this CTA's half) when the running max moved
+            const bool need = it > 0 && alpha != 1.f;
+            if (__any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+                for (int c = 0; c < AT_DH; c += 32) {
+                    uint32_t o[32];
+                    tc_ld32(t_o + lane_off + c, o);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tc_st32(t_o + lane_off + c, o);
+                }
+                tc_wait_st();
+            }
+            float lsum = 0.f;
+            uint32_t pk[32];
+#pragma unroll
+            for (int j = 0; j < 64; j += 2) {
+                const float p0 = m_run == -INFINITY ? 0.f : exp2f(x[j] - m_run);
+                const float p1 = m_run == -INFINITY ? 0.f : exp2f(x[j + 1] - m_run);
+                const uint32_t w = pack_bf16x2(p0, p1);
+                pk[j >> 1] = w;
+                lsum += bf16lo(w) + bf16hi(w);
+            }
+            l_run = l_run * alpha + lsum;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                st_shared_v4(sbase + SM_P + swz((uint32_t)h, (uint32_t)c),
+                             make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            // ---- O += P V  (M=128, N=256, K=64: 4 steps of 16 keys); V read MN-major from the K tile
+            if (tid == 0) {
+                tc_fence_after();
+                constexpr uint32_t id_o = idesc_bf16_f32(AT_M, AT_DH, true);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t ad = sdesc_sw128(sbase + SM_P + kk * 32, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(sbase + SM_K + (uint32_t)(half * 4) * K_SLAB + kk * 16 * 128,
+                                                    K_SLAB, 1024);
+                    tc_mma_f16(t_o, ad, bd, id_o, (it > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc_commit(bar_o);
+            }
+        }
+        if (!mbar_wait(bar_o, (uint32_t)((it - 1) & 1))) ok = false;
+        tc_fence_after();
+        if (!ok && tid == 0) raise_status(a.status, CSA_ERR_TIMEOUT);
+        // ---- epilogue: this thread's O row (256 columns of its half)
+        const bool direct = a.S == 1;
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        for (int c = 0; c < AT_DH; c += 32) {
+            uint32_t o[32];
+            tc_ld32(t_o + lane_off + c, o);
+            tc_wait_ld();
+            if (h < H) {
+                const int col = half * AT_DH + c;
+                if (direct) {
+                    uint16_t* dst = a.out + ((int64_t)b * H + h) * D + col;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        uint4 v;
+                        v.x = pack_bf16x2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
+                        v.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+                        v.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+                        v.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
+                        *reinterpret_cast<uint4*>(dst + e) = v;
+                    }
+                } else {
+                    float* dst = a.part_o + (((int64_t)b * a.S + split) * H + h) * D + col;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4*>(dst + e) =
+                            make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]), __uint_as_float(o[e + 2]),
+                                        __uint_as_float(o[e + 3]));
+                }
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) tmem_dealloc(tmem, 512);
+    }
+    if (h < H && half == 0) {
+        if (a.S == 1) {
+            if (a.lse) a.lse[(int64_t)b * H + h] = l_run > 0.f ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
+        } else {
+            float* ml = a.part_ml + (((int64_t)b * a.S + split) * H + h) * 2;
+            ml[0] = m_run;
+            ml[1] = l_run;
+        }
+    }
+}
+
+// Log-sum-exp merge of the splits: one CTA per (head, request), 4 columns per thread.
+__global__ void __launch_bounds__(128) attn_merge_kernel(AttnArgs a) {
+    const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+    const int H = a.H, S = a.S;
+    const float* ml = a.part_ml + ((int64_t)b * S * H) * 2;
+    float M = -INFINITY;
+    for (int s = 0; s < S; ++s) {
+        const float l = ml[((int64_t)s * H + h) * 2 + 1];
+        if (l > 0.f) M = fmaxf(M, ml[((int64_t)s * H + h) * 2]);
+    }
+    float L = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < S; ++s) {
+        const float m = ml[((int64_t)s * H + h) * 2], l = ml[((int64_t)s * H + h) * 2 + 1];
+        if (!(l > 0.f)) continue;
+        const float w = exp2f(m - M);
+        L = fmaf(w, l, L);
+        const float4 v = *reinterpret_cast<const float4*>(a.part_o + (((int64_t)b * S + s) * H + h) * D + tid * 4);
+        o.x = fmaf(w, v.x, o.x);
+        o.y = fmaf(w, v.y, o.y);
+        o.z = fmaf(w, v.z, o.z);
+        o.w = fmaf(w, v.w, o.w);
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    uint2 r;
+    r.x = pack_bf16x2(o.x * inv, o.y * inv);
+    r.y = pack_bf16x2(o.z * inv, o.w * inv);
+    *reinterpret_cast<uint2*>(a.out + ((int64_t)b * H + h) * D + tid * 4) = r;
+    if (tid == 0 && a.lse) a.lse[(int64_t)b * H + h] = L > 0.f ? (M + log2f(L)) * LN2 : -INFINITY;
+}
+
+// Split heuristic (device independent so workspace sizes are stable): about one
+// wave of 2*B*S CTAs on 152 SMs, at most one split per key tile.
+static void plan_splits(int B, int64_t max_keys, int* tps, int* S) {
+    const int64_t T = (max_keys + AT_KT - 1) / AT_KT;
+    int64_t s = 76 / (B > 0 ? B : 1);
+    if (s < 1) s = 1;
+    if (s > T) s = T;
+    if (s < 1) s = 1;
+    int64_t t = (T + s - 1) / s;
+    if (t < 1) t = 1;
+    s = (T + t - 1) / t;
+    if (s < 1) s = 1;
+    *tps = (int)t;
+    *S = (int)s;
+}
+
+size_t attn_workspace_bytes(int B, int H, int64_t max_keys) {
+    int tps, S;
+    plan_splits(B, max_keys, &tps, &S);
+    if (S == 1) return 0;
+    const size_t po = (size_t)B * S * H * D * sizeof(float);
+    const size_t pm = (size_t)B * S * H * 2 * sizeof(float);
+    return ((po + 255) & ~size_t(255)) + pm;
+}
+
+static DPaged to_dev(const HPaged& h) {
+    DPaged d;
+    d.base = static_cast<const uint8_t*>(h.base);
+    d.pt = h.pt;
+    d.pt_stride = h.pt_stride;
+    d.page_stride = h.page_stride;
+    d.n_pages = h.n_pages;
+    d.rpp = h.rpp;
+    return d;
+}
+
+cudaError_t launch_attn(const AttnLaunch& h, cudaStream_t s, bool pdl) {
+    AttnArgs a;
+    a.q = static_cast<const uint16_t*>(h.q);
+    a.H = h.H;
+    a.sl2 = h.scale * LOG2E;
+    a.kc = to_dev(h.kv_c);
+    a.kr = to_dev(h.kv_raw);
+    a.sel = h.sel;
+    a.sel_stride = h.sel_stride;
+    a.n_sel = h.n_sel;
+    a.n_tokens = h.n_tokens;
+    a.ratio = h.ratio;
+    a.N = h.N;
+    a.swa = h.swa;
+    plan_splits(h.B, h.max_keys, &a.tps, &a.S);
+    const size_t po = (size_t)h.B * a.S * h.H * D * sizeof(float);
+    a.part_o = static_cast<float*>(h.ws);
+    a.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(h.ws) + ((po + 255) & ~size_t(255)));
+    a.out = static_cast<uint16_t*>(h.out);
+    a.lse = h.lse;
+    a.status = h.status;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)AT_SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.gridDim = dim3(2, (unsigned)a.S, (unsigned)h.B);
+    cfg.blockDim = dim3(AT_T, 1, 1);
+    cfg.dynamicSmemBytes = AT_SMEM;
+    cfg.stream = s;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, attn_kernel, a);
+    if (e != cudaSuccess || a.S == 1) return e;
+    cfg.gridDim = dim3((unsigned)h.H, (unsigned)h.B, 1);
+    cfg.blockDim = dim3(128, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&cfg, attn_merge_kernel, a);
+}
+
+}  // namespace csa

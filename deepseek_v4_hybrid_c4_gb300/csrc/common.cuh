@@ -1,0 +1,63 @@
+// Device-side helpers shared by the libcsa kernels: paged-row addressing, the
+// sticky status word, the order-preserving score key, bf16 packing.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cstdint>
+
+#include "csa.h"
+#include "ptx.cuh"
+
+namespace csa {
+
+constexpr int D = 512;        // latent dim (K = V row), bf16 -> 1024 B per row
+constexpr int DI = 128;       // index-key dim
+constexpr int ROW_BYTES = D * 2;
+
+// A paged row buffer as the kernels see it (see csa_paged in csa.h).  For a
+// batch, request b uses page_table + b * pt_stride.
+struct DPaged {
+    const uint8_t* base;
+    const int32_t* pt;   // nullptr -> contiguous (physical page = logical page)
+    int64_t pt_stride;   // int32 entries between requests' page tables
+    int64_t page_stride; // bytes
+    int64_t n_pages;
+    int32_t rpp;         // rows per page
+};
+
+// Record an error code in the sticky device status word (bit code-1).
+CSA_DEV void raise_status(int32_t* status, int code) {
+    if (status) atomicOr(status, 1 << (code - 1));
+}
+
+// Address of logical row r of request b, or nullptr (and CSA_ERR_DEVICE_BOUNDS) when
+// its page id falls outside the pool.
+CSA_DEV const uint8_t* row_addr(const DPaged& p, int b, int64_t r, int row_bytes, int32_t* status) {
+    const int64_t lp = r / p.rpp;
+    const int64_t slot = r - lp * p.rpp;
+    int64_t pp = lp;
+    if (p.pt) pp = __ldg(p.pt + (int64_t)b * p.pt_stride + lp);
+    if (pp < 0 || pp >= p.n_pages) {
+        raise_status(status, CSA_ERR_DEVICE_BOUNDS);
+        return nullptr;
+    }
+    return p.base + pp * p.page_stride + slot * (int64_t)row_bytes;
+}
+
+// Order-preserving 32-bit image of an fp32 score: larger score <-> larger key,
+// -0 and +0 map to the same key.
+CSA_DEV uint32_t score_key(float s) {
+    uint32_t u = __float_as_uint(s);
+    if (u == 0x80000000u) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+CSA_DEV float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+CSA_DEV float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+CSA_DEV uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+}  // namespace csa

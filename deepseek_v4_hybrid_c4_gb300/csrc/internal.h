@@ -1,0 +1,104 @@
+// Host-side launchers shared between the libcsa translation units.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "csa.h"
+
+namespace csa {
+
+constexpr int kLatentRowBytes = 1024;  // one bf16 latent row (512 dims)
+constexpr int kHistBins = 2048;        // first top-k digit: key >> 21
+
+struct HPaged {            // host copy of a paged buffer description (see csa_paged)
+    const void* base;
+    const int32_t* pt;     // device page table(s) or nullptr
+    int64_t pt_stride;     // entries between requests' tables
+    int64_t page_stride;   // bytes
+    int64_t n_pages;
+    int32_t rpp;
+};
+
+// Stage 1.  Single mode (n_tokens == nullptr): groups [first, first + count) of one
+// sequence.  Batched mode: request b = blockIdx.y compresses [n_done[b], n_tokens[b]/ratio).
+// hist_zero (nullable): [B][kHistBins] counters cleared by block (0, b) for stage 2.
+struct CompressLaunch {
+    HPaged raw, out;
+    const float* w_gate;
+    const float* b_pos;
+    int ratio;
+    int B;
+    const int64_t* n_tokens;
+    const int64_t* n_done;
+    int64_t first, count;
+    uint32_t* hist_zero;
+    int32_t* status;
+};
+cudaError_t launch_compress(const CompressLaunch& a, cudaStream_t s, bool pdl);
+
+// Stage 2.  Single mode (n_tokens == nullptr): one sequence of G candidates.
+// Batched: request b has n_tokens[b] / ratio candidates; scores at b * score_stride.
+struct ScoreLaunch {
+    const void* q_idx;     // bf16 [B, Hi, 128]
+    const float* w_h;      // fp32 [B, Hi]
+    int Hi;
+    HPaged kidx;
+    bool fp8;
+    float* scores;
+    int64_t score_stride;
+    int B;
+    const int64_t* n_tokens;
+    int ratio;
+    int64_t G;             // single mode
+    int64_t max_G;         // host bound (grid sizing)
+    uint32_t* hist;        // fused first-digit histogram [B][kHistBins] (zeroed beforehand) or nullptr
+    int32_t* status;
+};
+cudaError_t launch_score(const ScoreLaunch& a, cudaStream_t s, bool pdl);
+
+// Stage 3.  Request b's scores: single: [0, G); offsets mode: [offsets[b], offsets[b+1]);
+// decode mode: b * score_stride + [0, n_tokens[b] / ratio).  hist (nullable): the
+// first digit's histogram from stage 2.
+struct TopkLaunch {
+    const float* scores;
+    int B;
+    int64_t G;                 // single mode
+    const int64_t* offsets;    // offsets mode
+    const int64_t* n_tokens;   // decode mode
+    int ratio;
+    int64_t score_stride;
+    int k;
+    int32_t* idx_out;          // [B, k]
+    uint32_t* keys_out;        // [B, k] or nullptr
+    const uint32_t* hist;
+    int32_t* status;
+};
+cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t s, bool pdl);
+
+// Stage 4 (+ log-sum-exp merge).  Per request b: keys = sel rows of kv_c (n_sel of
+// them, -1 = padding; sel == nullptr: rows 0..n_c-1 with n_c = n_tokens/ratio in
+// decode mode or n_sel in single mode) followed by the last min(swa, N) raw rows.
+struct AttnLaunch {
+    const void* q;             // bf16 [B, H, 512]
+    int H;
+    float scale;
+    HPaged kv_c, kv_raw;
+    const int32_t* sel;        // [B, sel_stride] or nullptr (dense)
+    int64_t sel_stride;
+    int n_sel;                 // sparse: selection length; dense single: number of rows
+    int B;
+    const int64_t* n_tokens;   // decode mode (device) or nullptr
+    int ratio;
+    int64_t N;                 // single mode: raw tokens
+    int64_t max_keys;          // host bound on keys per request
+    int swa;
+    void* out;                 // bf16 [B, H, 512]
+    float* lse;                // [B, H] or nullptr
+    void* ws;
+    size_t ws_bytes;
+    int32_t* status;
+};
+size_t attn_workspace_bytes(int B, int H, int64_t max_keys);
+cudaError_t launch_attn(const AttnLaunch& a, cudaStream_t s, bool pdl);
+
+}  // namespace csa

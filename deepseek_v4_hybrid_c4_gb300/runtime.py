@@ -1,0 +1,111 @@
+"""Device-resident decode batch: holds the pools, page tables, per-request
+queries and the workspace on the GPU and fills one csa_decode_params.
+
+PyTorch is used here only to own device memory; every stage runs in libcsa.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (CSA_BF16, CSA_FP8_E4M3, csa_decode, csa_decode_params, csa_decode_timed,
+               csa_decode_workspace_size)
+
+
+def _dev(x, dtype, device):
+    t = x if isinstance(x, torch.Tensor) else torch.as_tensor(x)
+    return t.to(device=device, dtype=dtype).contiguous()
+
+
+def _bits(x, dev):
+    """Move bf16/fp8 data (typed tensor or numpy bit patterns) to the device without conversion."""
+    if isinstance(x, torch.Tensor):
+        t = x
+        if t.dtype == torch.bfloat16:
+            t = t.view(torch.int16)
+        elif t.dtype == torch.float8_e4m3fn:
+            t = t.view(torch.uint8)
+        return t.to(dev).contiguous()
+    import numpy as np
+    a = np.ascontiguousarray(x)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(a).to(dev)
+
+
+class DecodeBatch:
+    """One fused decode step over B requests.
+
+    Pools (bf16 / fp8 data given as raw bit patterns or typed tensors):
+      raw_pool   [n_pages * rows_per_page, 512] bf16      raw latent KV, 64-token pages
+      c_pool     [n_pages * c_rpp, 512] bf16              compressed entries (shadow pages unless
+                                                          c_page_table is given)
+      kidx_pool  [n_pages * c_rpp, 128] bf16 / fp8        index keys (C4 only)
+    page_table [B, P] int32, n_tokens / n_groups_done [B] int64, q [B, H, 512] bf16,
+    q_idx [B, Hi, 128] bf16, w_h [B, Hi] fp32, w_gate [512] fp32, b_pos [ratio] fp32.
+    """
+
+    def __init__(self, *, ratio, H, Hi, k, swa, scale, kdtype, rows_per_page, raw_pool, c_pool, kidx_pool,
+                 page_table, n_tokens, n_groups_done, q, q_idx, w_h, w_gate, b_pos, n_pages, max_tokens=None,
+                 c_page_table=None, c_rows_per_page=0, c_n_pages=0, device="cuda"):
+        dev = torch.device(device)
+        i32, i64, f32 = torch.int32, torch.int64, torch.float32
+        self.ratio, self.H, self.Hi, self.k, self.swa = ratio, H, Hi, k, swa
+        self.raw_pool = _bits(raw_pool, dev)
+        self.c_pool = _bits(c_pool, dev)
+        self.kidx_pool = None if kidx_pool is None else _bits(kidx_pool, dev)
+        self.page_table = _dev(page_table, i32, dev)
+        self.c_page_table = None if c_page_table is None else _dev(c_page_table, i32, dev)
+        self.n_tokens = _dev(n_tokens, i64, dev)
+        self.n_groups_done = _dev(n_groups_done, i64, dev)
+        self.q = _bits(q, dev)
+        self.B = int(self.n_tokens.shape[0])
+        self.q_idx = _bits(q_idx, dev) if Hi else torch.zeros(8, dtype=torch.int16, device=dev)
+        self.w_h = _dev(w_h, f32, dev) if Hi else torch.zeros(4, dtype=f32, device=dev)
+        self.w_gate = _dev(w_gate, f32, dev)
+        self.b_pos = _dev(b_pos, f32, dev)
+        self.out = torch.zeros((self.B, H, 512), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.zeros((self.B, H), dtype=f32, device=dev)
+        self.sel = torch.zeros((self.B, max(k, 1)), dtype=i32, device=dev) if ratio == 4 else None
+        if max_tokens is None:
+            max_tokens = int(torch.as_tensor(n_tokens).max())
+        c_rpp = c_rows_per_page if c_page_table is not None else rows_per_page // ratio
+        p = csa_decode_params()
+        p.B, p.ratio, p.H, p.Hi, p.k, p.swa = self.B, ratio, H, Hi, k, swa
+        p.scale = float(scale)
+        p.k_dtype = CSA_BF16 if kdtype == "bf16" else CSA_FP8_E4M3
+        p.max_tokens = int(max_tokens)
+        p.n_tokens = self.n_tokens.data_ptr()
+        p.n_groups_done = self.n_groups_done.data_ptr()
+        p.kv_raw = self.raw_pool.data_ptr()
+        p.raw_rows_per_page = rows_per_page
+        p.raw_page_stride = rows_per_page * 1024
+        p.kv_c = self.c_pool.data_ptr()
+        p.c_page_stride = c_rpp * 1024
+        if self.kidx_pool is not None:
+            p.k_idx = self.kidx_pool.data_ptr()
+            p.kidx_page_stride = c_rpp * (256 if kdtype == "bf16" else 128)
+        p.n_pages = int(n_pages)
+        p.page_table = self.page_table.data_ptr()
+        p.page_table_stride = int(self.page_table.shape[1])
+        if self.c_page_table is not None:
+            p.c_page_table = self.c_page_table.data_ptr()
+            p.c_page_table_stride = int(self.c_page_table.shape[1])
+            p.c_rows_per_page = c_rows_per_page
+            p.c_n_pages = int(c_n_pages)
+        p.w_gate = self.w_gate.data_ptr()
+        p.b_pos = self.b_pos.data_ptr()
+        p.q = self.q.data_ptr()
+        p.q_idx = self.q_idx.data_ptr()
+        p.w_h = self.w_h.data_ptr()
+        p.out = self.out.data_ptr()
+        p.lse = self.lse.data_ptr()
+        p.sel = self.sel.data_ptr() if self.sel is not None else None
+        self.params = p
+        self.ws_bytes = csa_decode_workspace_size(p)  # 0 also when the parameters are rejected: run() reports why
+        self.ws = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
+
+    def run(self, stream=None, events=None) -> None:
+        if events is None:
+            csa_decode(self.params, self.ws, self.ws_bytes, stream)
+        else:
+            csa_decode_timed(self.params, self.ws, self.ws_bytes, stream, events)

@@ -1,0 +1,219 @@
+/*
+ * libcsa: the decode step of a C4 hybrid-sparse-attention layer on GB300 (sm_103a).
+ *
+ * The operation (web pages, cited by title and section):
+ *   [V4-deploy] "DeepSeek-V4 本地部署，SGLang 把活做絕了", sec. "V4 到底改了啥":
+ *       every layer attends a sliding window of the last 128 raw tokens (SWA) plus
+ *       either C4 (4:1 compression of the KV, top-512 sparse selection) or C128
+ *       (128:1 compression, attended densely).
+ *     sec. "Kernel 層一堆狠活": SWA and the extra (C4/C128) attention in ONE call;
+ *       Flash Compressor (load -> score -> softmax -> weighted sum -> store in one
+ *       on-chip pass); Lightning TopK (top-512 of 256K candidates at 1M context by
+ *       a cluster-of-8 radix select instead of a global sort).
+ *   [Day-0] "SGLang 如何为 DeepSeek V4 打造「Day-0」推理加速",
+ *     sec. "创新 2：Flash Compressor + Lightning TopK": per-CTA 10-bit histograms,
+ *       reduced inside the cluster to a threshold, then a local scatter of the
+ *       entries above it; warp-local softmax for C4, one CTA per group for C128.
+ *     sec. "创新 1：ShadowRadix": one virtual token-slot space projected onto the
+ *       physical pools ("shadow" pages) -- adopted here as the paging convention.
+ *   The pages print no formulas; the problem statement fixes them:
+ *     gate      s_i = kv_i . w_gate + b_pos[i]               (i = position in the group)
+ *     score[g]  = sum_h w_h * ReLU(q_idx[h] . k_idx[g])       (fp32, fixed order below)
+ *     top-k     by descending score, ties to the lower index.
+ *
+ * Shapes fixed in this version: latent D = 512 (K = V = the latent row, bf16),
+ * index dim 128, ratio in {4, 128}, k <= 2048, swa <= 128, query heads
+ * 1 <= H <= 128 (padded to the 128-row tensor-core tile inside), index heads
+ * 1 <= Hi <= 16.
+ *
+ * Conventions for every entry point
+ *  - Pointers are DEVICE pointers unless stated otherwise; the caller owns all
+ *    memory (inputs, outputs, workspace).  libcsa never allocates, frees or
+ *    synchronises on these calls: work is enqueued on `stream` and the call
+ *    returns.  The stream is a cudaStream_t passed as void* (0 = legacy default).
+ *  - Argument/shape errors return synchronously, before anything is enqueued.
+ *    A failed launch returns CSA_ERR_CUDA.  Errors a kernel detects (a page id
+ *    outside the pool, a bounded wait that ran out) are OR-ed into a sticky
+ *    per-device status word read with csa_read_device_status(); kernels never
+ *    trap or assert.
+ *  - Alignment: every bf16/fp8 row buffer and query pointer must be 16-byte
+ *    aligned, fp32/int32 arrays 4-byte aligned; page strides are multiples of 16.
+ */
+#ifndef CSA_H_
+#define CSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    CSA_OK = 0,
+    CSA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer */
+    CSA_ERR_UNSUPPORTED = 2,   /* outside the fixed limits above */
+    CSA_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+    CSA_ERR_TIMEOUT = 4,       /* device status: a bounded wait ran out */
+    CSA_ERR_DEVICE_BOUNDS = 5, /* device status: a page id / index outside its pool (access skipped) */
+    CSA_ERR_WORKSPACE = 6      /* workspace missing or smaller than the *_workspace_size query */
+} csa_status;
+
+typedef enum { CSA_BF16 = 0, CSA_FP8_E4M3 = 1, CSA_FP32 = 2 } csa_dtype;
+
+/*
+ * A paged row buffer (the ShadowRadix "physical pool" view).
+ * Logical row r lives in logical page p = r / rows_per_page, slot s = r % rows_per_page;
+ * its bytes start at base + P * page_stride_bytes + s * row_bytes, where
+ * P = page_table[p] (device int32) or P = p when page_table is NULL (contiguous).
+ * row_bytes is fixed by the tensor (1024 for a bf16 latent row, 256 for a bf16
+ * index key, 128 for an fp8 index key).  n_pages bounds P (device-checked).
+ */
+typedef struct {
+    void* base;
+    const int32_t* page_table; /* device, or NULL */
+    int32_t rows_per_page;     /* >= 1 */
+    int64_t page_stride_bytes; /* >= rows_per_page * row_bytes, multiple of 16 */
+    int64_t n_pages;           /* physical pages in the pool */
+} csa_paged;
+
+/*
+ * Stage 1, standalone (prefill): softmax-gated ratio:1 compression
+ * ([V4-deploy] "Kernel 層一堆狠活", Flash Compressor; [Day-0] "创新 2").
+ * For each group j in [first_group, first_group + n_groups): tokens
+ * ratio*j .. ratio*j+ratio-1 of kv_raw (bf16 [n_tokens, 512]),
+ *   s_i = kv_i . w_gate + b_pos[i], a = softmax(s), c_j = sum_i a_i kv_i,
+ * fp32 arithmetic, written as bf16 (RN) to row j of kv_c_out.
+ * w_gate: fp32 [512]; b_pos: fp32 [ratio].  ratio 4: one warp per group;
+ * ratio 128: one CTA per group.  Requires (first_group + n_groups) * ratio <= n_tokens.
+ */
+csa_status csa_compress(csa_paged kv_raw, int64_t n_tokens, int32_t ratio, const float* w_gate,
+                        const float* b_pos, int64_t first_group, int64_t n_groups, csa_paged kv_c_out,
+                        void* stream);
+
+/*
+ * Stage 2: index score of every candidate ([V4-deploy] "Kernel 層一堆狠活", indexer).
+ * q_idx bf16 [Hi, 128] (contiguous), w_h fp32 [Hi], k_idx rows ([G, 128], bf16 or
+ * fp8-e4m3 per k_dtype; paged tables need rows_per_page % 16 == 0), scores fp32 [G].
+ * Bit-exact fixed order:
+ *   P[t] = q[8t]*k[8t], then P[t] = fma(q[8t+i], k[8t+i], P[t]) for i = 1..7  (t = 0..15)
+ *   S1[t] = P[t] + P[t+8]; S2[t] = S1[t] + S1[t+4]; S3[t] = S2[t] + S2[t+2]; dot = S3[0] + S3[1]
+ *   acc = 0; acc = fma(w_h, dot > 0 ? dot : +0, acc) for h = 0..Hi-1
+ */
+csa_status csa_index_score(const void* q_idx, const float* w_h, int32_t Hi, csa_paged k_idx, csa_dtype k_dtype,
+                           int64_t G, float* scores, void* stream);
+
+/*
+ * Stage 3: top-k ([Day-0] "创新 2", Lightning TopK: cluster-of-8 radix select,
+ * histograms reduced through distributed shared memory).
+ * scores fp32 [G] -> idx_out int32 [k]: the indices of the min(k, G) largest
+ * scores ordered by (score desc, index asc), then -1 padding.  Scores compare
+ * through the order-preserving key (-0 == +0; key = bits ^ (sign ? ~0 : 1<<31)).
+ * keys_out (nullable) uint32 [k] receives those keys (0 for padding).
+ * One cluster per request; no workspace.  G <= 2^31 - 1.
+ */
+csa_status csa_topk(const float* scores, int64_t G, int32_t k, int32_t* idx_out, uint32_t* keys_out, void* stream);
+
+/*
+ * Batched stage 3 over a ragged batch: request b owns scores[offsets[b] .. offsets[b+1])
+ * (offsets: device int64 [B+1]), writes idx_out[b*k .. b*k+k) (indices local to
+ * the request).  max_G: host-side bound on every request's length.
+ */
+csa_status csa_topk_batched(const float* scores, const int64_t* offsets, int32_t B, int64_t max_G, int32_t k,
+                            int32_t* idx_out, uint32_t* keys_out, void* stream);
+
+/*
+ * Stage 4: one attention over the selected compressed entries plus the last
+ * W = min(swa, n_tokens) raw tokens under a single softmax ([V4-deploy]
+ * "Kernel 層一堆狠活": FlashMLA's one call for SWA + extra attention).
+ * q bf16 [H, 512]; kv_c: compressed pool (bf16 rows); sel int32 [n_sel] row ids
+ * into kv_c (entries < 0 are padding and ignored), or NULL for all rows
+ * 0..n_sel-1 (dense C128); kv_raw: raw pool (bf16 rows, n_tokens of them).
+ * For head h: l_j = scale * q_h . K_j, o_h = softmax(l) . V (K = V = the row);
+ * out bf16 [H, 512]; lse fp32 [H] (natural log, nullable).
+ * tcgen05 tensor cores (M = 128 padded heads, 64-key tiles), keys split across
+ * CTAs and merged by log-sum-exp.  Workspace: csa_sparse_attn_workspace_size().
+ */
+csa_status csa_sparse_attn(const void* q, int32_t H, float scale, csa_paged kv_c, const int32_t* sel, int32_t n_sel,
+                           csa_paged kv_raw, int64_t n_tokens, int32_t swa, void* out, float* lse, void* workspace,
+                           size_t ws_bytes, void* stream);
+size_t csa_sparse_attn_workspace_size(int32_t H, int32_t n_sel, int32_t swa);
+
+/*
+ * The fused decode step over a ragged batch of B requests ([V4-deploy] "V4 到底改了啥",
+ * "Kernel 層一堆狠活"; [Day-0] "创新 2").  Per request b, with N = n_tokens[b],
+ * G = N / ratio, done = n_groups_done[b]:
+ *   1. compress groups [done, G) of the raw KV into the compressed pool (stage 1);
+ *   2. ratio 4:   score all G candidates (stage 2), select the top k (stage 3),
+ *                 attend the selection + SWA (stage 4);
+ *      ratio 128: attend all G compressed entries + SWA (stage 4, dense).
+ * Paging: one page table per request (row b of page_table, page_table_stride
+ * int32 entries apart) maps logical page p (raw tokens p*rpp .. p*rpp+rpp-1,
+ * rpp = raw_rows_per_page) to a physical page id.  With c_page_table == NULL the
+ * compressed pool and the index-key pool are SHADOW pools: they use the same
+ * physical page id and hold rpp / ratio rows per page (needs rpp % ratio == 0).
+ * Otherwise c_page_table (row b, c_page_table_stride apart) pages them with
+ * c_rows_per_page rows per page.
+ * Per-request lengths live in device memory (so the call can be captured in a
+ * CUDA graph once and replayed); max_tokens is a host-side bound used to size grids.
+ */
+typedef struct {
+    int32_t B, ratio, H, Hi, k, swa;
+    float scale;
+    csa_dtype k_dtype;           /* index-key storage: CSA_BF16 or CSA_FP8_E4M3 */
+    int64_t max_tokens;          /* >= every n_tokens[b] */
+    const int64_t* n_tokens;     /* device [B], multiples of ratio, >= ratio */
+    const int64_t* n_groups_done;/* device [B], 0 <= done <= G */
+    /* pools shared by the batch */
+    void* kv_raw;                /* bf16 rows of 1024 B */
+    int32_t raw_rows_per_page;
+    int64_t raw_page_stride;     /* bytes */
+    void* kv_c;                  /* compressed pool, bf16 rows of 1024 B (written for pending groups) */
+    int64_t c_page_stride;       /* bytes */
+    const void* k_idx;           /* index keys (ratio 4), rows of 256 B (bf16) or 128 B (fp8) */
+    int64_t kidx_page_stride;    /* bytes */
+    int64_t n_pages;             /* physical pages in every pool (bounds check) */
+    const int32_t* page_table;   /* device [B, page_table_stride] */
+    int64_t page_table_stride;
+    const int32_t* c_page_table; /* device [B, c_page_table_stride] or NULL (shadow paging) */
+    int64_t c_page_table_stride;
+    int32_t c_rows_per_page;     /* used when c_page_table != NULL */
+    int64_t c_n_pages;           /* used when c_page_table != NULL */
+    /* layer weights */
+    const float* w_gate;         /* fp32 [512] */
+    const float* b_pos;          /* fp32 [ratio] */
+    /* per-request queries */
+    const void* q;               /* bf16 [B, H, 512] */
+    const void* q_idx;           /* bf16 [B, Hi, 128] (ratio 4) */
+    const float* w_h;            /* fp32 [B, Hi] (ratio 4) */
+    /* outputs */
+    void* out;                   /* bf16 [B, H, 512] */
+    float* lse;                  /* fp32 [B, H], nullable */
+    int32_t* sel;                /* int32 [B, k], nullable (ratio 4): the selected candidates */
+} csa_decode_params;
+
+csa_status csa_decode(const csa_decode_params* p, void* workspace, size_t ws_bytes, void* stream);
+size_t csa_decode_workspace_size(const csa_decode_params* p);
+
+/*
+ * csa_decode with stage timing: stage_events (host array of 5 cudaEvent_t, created
+ * by the caller with timing enabled) are recorded on `stream` before stage 1 and
+ * after stages 1 (compress), 2 (score), 3 (top-k) and 4 (attention + merge).  For
+ * ratio 128 the score and top-k events are recorded back to back.  NULL = csa_decode.
+ */
+csa_status csa_decode_timed(const csa_decode_params* p, void* workspace, size_t ws_bytes, void* stream,
+                            void* const* stage_events);
+
+/* Read and clear the calling device's sticky status word (synchronises `stream`).
+ * *out receives a bit set: bit (code-1) for each csa_status code raised on the device. */
+csa_status csa_read_device_status(void* stream, int32_t* out);
+
+const char* csa_status_string(csa_status s);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int32_t csa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CSA_H_ */

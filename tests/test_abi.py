@@ -1,0 +1,69 @@
+"""The C ABI: the shared library loads and exports every entry point declared in include/csa.h
+(no compute: this runs without a GPU)."""
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "csa.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(csa_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def libpath():
+    from deepseek_v4_hybrid_c4_gb300 import build
+    return build.build()
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ["csa_compress", "csa_index_score", "csa_topk", "csa_sparse_attn", "csa_decode"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(libpath):
+    out = subprocess.run(["nm", "-D", "--defined-only", libpath], capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (csa_\w+)", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+
+
+def test_library_loads_and_answers_host_queries(libpath):
+    import ctypes
+    import deepseek_v4_hybrid_c4_gb300 as csa
+    L = csa.lib()
+    assert csa.csa_version() >= 100
+    assert csa.status_string(csa.CSA_ERR_WORKSPACE) == "workspace missing or too small"
+    for n in declared_functions():
+        assert hasattr(L, n)
+    # argument validation is synchronous and touches no device memory
+    assert L.csa_topk(None, 10, 4, None, None, None) == csa.CSA_ERR_INVALID_ARG
+    assert L.csa_topk(None, 10, 0, None, None, None) == csa.CSA_ERR_UNSUPPORTED
+    p = csa.csa_decode_params()
+    assert L.csa_decode(ctypes.byref(p), None, 0, None) == csa.CSA_ERR_UNSUPPORTED
+    assert csa.csa_decode_workspace_size(p) == 0
+
+
+def test_binding_has_the_c_names():
+    import deepseek_v4_hybrid_c4_gb300 as csa
+    for n in declared_functions():
+        if n not in ("csa_status_string",):
+            assert callable(getattr(csa, n)), n
+
+
+def test_product_path_does_not_reach_the_oracle():
+    """The package never imports the oracle or the generators."""
+    pkg = os.path.join(ROOT, "deepseek_v4_hybrid_c4_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+(oracle|synth)\b", src, re.M), f
+                assert "liboracle" not in src and "orc_" not in src, f
