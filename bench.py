@@ -1,0 +1,335 @@
+"""Benchmark of the C4 sparse-attention decode step (libcsa on GB300).
+
+One step = the fused decode of one C4 layer at 1M context, bs = 1 (N = 1,048,576 raw
+tokens -> 262,144 candidates -> top-512, plus SWA 128; 128 query heads, 8 index heads,
+64-token pages under a random page-table permutation; one pending group compressed).
+Prints one JSON line.  Inputs are synthetic (seeded generators) and resident in HBM
+before timing; L2 (129 MB) is flushed with a 256 MiB write before every timed step.
+The step is captured once in a CUDA graph and replayed; a second, eager pass records
+CUDA events between the stages for the per-stage breakdown and the roofline of the
+dominant kernel.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+--impl reference times the CPU oracle (the only reference this method has: the pages
+ship no code) on the same workload.
+Multi-GPU: one process per GPU (torchrun); requests are independent, so ranks run
+replicas with no collective on the data path ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "C4 sparse-attn decode µs/layer-step @1M ctx bs=1; HBM GB/s as % of GB300 peak"
+WORKLOAD = "c4-decode-1M-bs1-paged (N=1048576, G=262144, k=512, SWA=128, H=128, Hi=8, 64-token pages)"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def algorithmic_bytes(case):
+    """Bytes the step must move through HBM (scores stay in L2 and are not counted)."""
+    r = case.requests[0]
+    G = r.n_tokens // case.ratio
+    kidx = G * 128 * (2 if case.kdtype == "bf16" else 1)
+    pages = (r.n_tokens + case.rows_per_page - 1) // case.rows_per_page * 4  # page table (int32)
+    gather = case.k * 1024 + min(case.swa, r.n_tokens) * 1024
+    q = case.H * 512 * 2 + case.Hi * 128 * 2 + case.Hi * 4
+    out = case.H * 512 * 2 + case.H * 4
+    comp = (G - r.n_groups_done) * (case.ratio * 1024 + 1024)
+    return dict(total=kidx + pages + gather + q + out + comp, score_kernel=kidx)
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    def __init__(self, out_csv):
+        self.out_csv = out_csv
+        self.proc = None
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.f = open(self.out_csv, "w")
+            dev = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0]
+            sel = [f"--id={dev}"] if dev.isdigit() else []
+            self.proc = subprocess.Popen(["nvidia-smi"] + sel + [f"--query-gpu={q}", "--format=csv,noheader",
+                                                                 "-lms", "100"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.2)
+            self.proc.terminate()
+            self.proc.wait()
+            self.f.close()
+
+    def summary(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = [l.strip().split(",") for l in open(self.out_csv) if l.strip()]
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1].split()[0]))
+                mx = float(r[2].split()[0])
+                for n, v in zip(names, r[5:9]):
+                    if "Active" in v and "Not" not in v:
+                        reasons.add(n)
+            except Exception:
+                continue
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def oracle_step_times(case, n_min, budget_s):
+    """The oracle's decode step (single-threaded, as it stands), repeated."""
+    import oracle
+    oracle.build()
+    r = case.requests[0]
+    times = []
+    t_end = time.perf_counter() + budget_s
+    while len(times) < n_min or (time.perf_counter() < t_end and len(times) < 50):
+        t0 = time.perf_counter()
+        oracle.decode_request(r, ratio=case.ratio, w_gate=case.w_gate, b_pos=case.b_pos, k=case.k, swa=case.swa,
+                              scale=case.scale, kdtype=case.kdtype)
+        times.append(time.perf_counter() - t0)
+    return times
+
+
+def run_reference(args, rank):
+    """--impl reference: the CPU oracle on the host cores, rank 0 only."""
+    if rank != 0:
+        return
+    import synth
+    case = synth.config(2)
+    times = oracle_step_times(case, args.warmup + args.steps, 0.0)[args.warmup:]
+    us = statistics.mean(times) * 1e6
+    line = {"impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": "µs/layer-step",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (fp32 index score)",
+            "data": "synthetic (seeded Philox4x32-10 generators)",
+            "config": {"workload": WORKLOAD, "l2": "n/a (CPU)"},
+            "cpu_baseline": {"value": round(us, 1), "unit": "µs/layer-step", "cores": 1, "kind": "oracle",
+                             "sample": f"{args.steps} full decode steps of the 1M workload after {args.warmup} "
+                                       f"untimed; host nproc={os.cpu_count()}"},
+            "e2e": {"value": round(us, 1), "unit": "µs/layer-step", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def _score_source_sha():
+    p = os.path.join(ROOT, "deepseek_v4_hybrid_c4_gb300", "csrc", "score.cu")
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+def _attn_splits(case):
+    keys = case.k + case.swa
+    T = (keys + 63) // 64
+    s = max(1, min(T, 76 // max(1, case.B)))
+    t = (T + s - 1) // s
+    return (T + t - 1) // t
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    if args.impl == "reference":
+        return run_reference(args, rank)
+
+    import torch
+    import synth
+    import __graft_entry__
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    __graft_entry__.build()
+    import deepseek_v4_hybrid_c4_gb300 as csa
+
+    case = synth.config(2)
+    batch = __graft_entry__.case_to_batch(case, f"cuda:{local}")
+    stream = torch.cuda.Stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if not dist:
+            return x
+        t = torch.tensor([x], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            batch.run(stream)
+    barrier()
+    assert csa.csa_read_device_status(stream) == 0
+
+    # ---- the step as one CUDA graph
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        batch.run(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            flush.zero_()
+            graph.replay()
+    barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clk_path = os.path.join(ROOT, "gpurun_out", "bench_clocks.csv") if os.path.isdir(
+        os.path.join(ROOT, "gpurun_out")) else "/tmp/bench_clocks.csv"
+    clocks = ClockSampler(clk_path)
+    barrier()
+    with clocks:
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                flush.zero_()
+                ev[i][0].record(stream)
+                graph.replay()
+                ev[i][1].record(stream)
+        barrier()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = max_over_ranks(statistics.mean(step_ms))
+    assert csa.csa_read_device_status(stream) == 0
+
+    # ---- eager pass with events between the stages (breakdown + dominant-kernel roofline)
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    for row in sev:  # libcsa re-records these inside the step; torch only needs to know they exist
+        for e in row:
+            e.record(stream)
+    barrier()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush.zero_()
+            batch.run(stream, sev[i])
+    barrier()
+    stage_ms = [[sev[i][j].elapsed_time(sev[i][j + 1]) for i in range(args.steps)] for j in range(4)]
+    eager_ms = statistics.mean(sev[i][0].elapsed_time(sev[i][4]) for i in range(args.steps))
+
+    # ---- end to end through host buffers: the new token's state goes up, the output comes back
+    hq = batch.q.cpu().pin_memory()
+    hqi = batch.q_idx.cpu().pin_memory()
+    hwh = batch.w_h.cpu().pin_memory()
+    hout = torch.empty(batch.out.shape, dtype=batch.out.dtype).pin_memory()
+    hlse = torch.empty(batch.lse.shape, dtype=batch.lse.dtype).pin_memory()
+    r0 = case.requests[0]
+    G = r0.n_tokens // case.ratio
+    t0 = r0.n_groups_done * case.ratio
+    row0 = int(r0.pages[t0 // case.rows_per_page]) * case.rows_per_page + t0 % case.rows_per_page
+    n_new = (G - r0.n_groups_done) * case.ratio  # the completed group's raw tokens (inside one page)
+    hraw = batch.raw_pool[row0: row0 + n_new].cpu().pin_memory()
+    c_rpp = case.c_rows_per_page()
+    krow = int(r0.pages[(G - 1) // c_rpp]) * c_rpp + (G - 1) % c_rpp
+    hkidx = batch.kidx_pool[krow: krow + 1].cpu().pin_memory()
+    h2d = (hq.numel() * 2 + hqi.numel() * 2 + hwh.numel() * 4 + hraw.numel() * 2 +
+           hkidx.numel() * hkidx.element_size())
+    d2h = hout.numel() * 2 + hlse.numel() * 4
+    e2e_ms = []
+    barrier()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            batch.q.copy_(hq, non_blocking=True)
+            batch.q_idx.copy_(hqi, non_blocking=True)
+            batch.w_h.copy_(hwh, non_blocking=True)
+            batch.raw_pool[row0: row0 + n_new].copy_(hraw, non_blocking=True)
+            batch.kidx_pool[krow: krow + 1].copy_(hkidx, non_blocking=True)
+            graph.replay()
+            hout.copy_(batch.out, non_blocking=True)
+            hlse.copy_(batch.lse, non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            e2e_ms.append(e0.elapsed_time(e1))
+    barrier()
+    e2e = max_over_ranks(statistics.mean(e2e_ms))
+
+    if rank != 0:
+        dist.destroy_process_group()
+        return
+    peak, peak_kind = peaks()
+    ab = algorithmic_bytes(case)
+    score_ms = statistics.mean(stage_ms[1])
+    achieved = ab["score_kernel"] / (score_ms * 1e-3) / 1e9
+    step_gbs = ab["total"] / (ms * 1e-3) / 1e9
+    traffic = None
+    tp = os.path.join(ROOT, "profiles", "score_kernel_traffic.json")
+    if os.path.exists(tp):
+        try:
+            d = json.load(open(tp))
+            if d.get("kernel_source_sha") == _score_source_sha():
+                traffic = d.get("traffic_bytes_per_launch")
+        except Exception:
+            traffic = None
+    line = {
+        "metric": METRIC, "value": round(ms * 1e3 / world, 3), "unit": "µs/layer-step", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (fp32 accumulate; fp32 fixed-order index score)",
+        "data": "synthetic (seeded Philox4x32-10 generators; shapes of the 1M-context workload)",
+        "config": {"workload": WORKLOAD, "l2": "flushed (256 MiB write) before every timed step",
+                   "launch": "one CUDA graph per step",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "stages_us_eager": {n: round(statistics.mean(v) * 1e3, 3) for n, v in
+                            zip(["compress", "score", "topk", "attn"], stage_ms)},
+        "eager_step_us": round(eager_ms * 1e3, 3),
+        "step_roofline": {"bound": "hbm", "algorithmic_bytes": ab["total"], "achieved": round(step_gbs, 1),
+                          "peak": peak, "unit": "GB/s", "frac": round(step_gbs / peak, 4),
+                          "peak_source": f"{peak_kind} (copy)"},
+        "roofline": {"kernel": "score_kernel (stage 2, index score)", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "algorithmic_bytes_per_launch": ab["score_kernel"],
+                     "peak_source": f"{peak_kind} (burst copy)"},
+        "e2e": {"value": round(e2e * 1e3 / world, 3), "unit": "µs/layer-step", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": args.steps * (4 + (1 if _attn_splits(case) > 1 else 0)),
+        "clocks": clocks.summary(),
+    }
+    if not args.no_cpu_baseline:
+        times = oracle_step_times(case, 3, 15.0)
+        line["cpu_baseline"] = {"value": round(statistics.median(times) * 1e6, 1), "unit": "µs/layer-step",
+                                "cores": 1, "kind": "oracle",
+                                "sample": f"{len(times)} full decode steps of the same 1M workload (median); "
+                                          f"host nproc={os.cpu_count()}"}
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
