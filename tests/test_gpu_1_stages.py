@@ -261,11 +261,11 @@ def test_attn_single_key_returns_its_row(csa):
 def test_attn_rescale_path_increasing_logits(csa):
     """Logits that rise by ~10 (log2 units) per 64-key tile: with 8192 keys each CTA owns several tiles,
     so the running max moves past the threshold inside a CTA and O is rescaled in TMEM.  Head 0's query
-    is scaled up so the key rows stay O(1)."""
+    is scaled up so the key rows (and the outputs) stay well inside O(1)."""
     H, G = 64, 8192
     q = synth.normal_bf16((H, 512), 8, 1)
     qf = bf16_bits_to_f64(q)
-    qf[0] *= 16.0
+    qf[0] *= 256.0
     q[0] = np.asarray(np.asarray(qf[0], np.float32).view(np.uint32) >> 16, np.uint16)
     qf = bf16_bits_to_f64(q)
     cpool = synth.normal_bf16((G, 512), 8, 2)
@@ -281,7 +281,7 @@ def test_attn_rescale_path_increasing_logits(csa):
     sel = np.arange(G, dtype=np.int32)
     out, lse = _attn_gpu(csa, cpool, raw, q, sel, 128, scale)
     _, f64, rlse = oracle.sparse_attn(q, scale, cpool, sel, raw, 128)
-    assert np.abs(bf16_bits_to_f64(cpool)).max() < 16
+    assert np.abs(bf16_bits_to_f64(cpool)).max() < 1
     assert_close(bf16_bits_to_f64(out), f64, "attention with rising maxima")
     assert np.abs(lse - rlse).max() <= 1e-3 * max(1.0, np.abs(rlse).max())
 
