@@ -361,7 +361,7 @@ csa_status csa_decode_timed(const csa_decode_params* p, void* workspace, size_t 
         l.max_G = max_G;
         l.hist = hist;
         l.status = st;
-        e = launch_score(l, s, false);
+        e = launch_score(l, s, ev == nullptr);
         if (e != cudaSuccess) return CSA_ERR_CUDA;
         mark(2);
         // 3. top-k per request
@@ -379,7 +379,7 @@ csa_status csa_decode_timed(const csa_decode_params* p, void* workspace, size_t 
         t.keys_out = nullptr;
         t.hist = hist;
         t.status = st;
-        e = launch_topk(t, s, false);
+        e = launch_topk(t, s, ev == nullptr);
         if (e != cudaSuccess) return CSA_ERR_CUDA;
         mark(3);
         sel = sel_out;
@@ -409,7 +409,7 @@ csa_status csa_decode_timed(const csa_decode_params* p, void* workspace, size_t 
     a.ws = ws + L.attn;
     a.ws_bytes = L.total - L.attn;
     a.status = st;
-    e = launch_attn(a, s, false);
+    e = launch_attn(a, s, ev == nullptr);
     mark(4);
     return from_cuda(e);
 }

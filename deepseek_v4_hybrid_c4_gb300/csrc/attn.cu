@@ -86,6 +86,10 @@ __global__ void __launch_bounds__(AT_T, 1) attn_kernel(AttnArgs a) {
     const int h = tid;  // head row owned by this thread
 
     float m_run = -INFINITY, l_run = 0.f;
+    if (t0 >= t1) {
+        pdl_wait();
+        pdl_launch_dependents();
+    }
     if (t0 < t1) {
         if (warp == 0) {
             tmem_alloc(sbase + SM_TMEM, 512);
@@ -106,6 +110,10 @@ __global__ void __launch_bounds__(AT_T, 1) attn_kernel(AttnArgs a) {
             else
                 st_shared_zero16(dst);
         }
+        // everything above touches only inputs of the step; the selection and the freshly
+        // compressed rows come from the preceding kernels
+        pdl_wait();
+        pdl_launch_dependents();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
@@ -282,26 +290,48 @@ __global__ void __launch_bounds__(AT_T, 1) attn_kernel(AttnArgs a) {
 
 // Log-sum-exp merge of the splits: one CTA per (head, request), 4 columns per thread.
 __global__ void __launch_bounds__(128) attn_merge_kernel(AttnArgs a) {
+    pdl_wait();
     const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
     const int H = a.H, S = a.S;
     const float* ml = a.part_ml + ((int64_t)b * S * H) * 2;
+    const float* po = a.part_o + ((int64_t)b * S * H + h) * D + tid * 4;
     float M = -INFINITY;
     for (int s = 0; s < S; ++s) {
-        const float l = ml[((int64_t)s * H + h) * 2 + 1];
-        if (l > 0.f) M = fmaxf(M, ml[((int64_t)s * H + h) * 2]);
+        const float2 v = *reinterpret_cast<const float2*>(ml + ((int64_t)s * H + h) * 2);
+        if (v.y > 0.f) M = fmaxf(M, v.x);
     }
     float L = 0.f;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < S; ++s) {
-        const float m = ml[((int64_t)s * H + h) * 2], l = ml[((int64_t)s * H + h) * 2 + 1];
-        if (!(l > 0.f)) continue;
-        const float w = exp2f(m - M);
-        L = fmaf(w, l, L);
-        const float4 v = *reinterpret_cast<const float4*>(a.part_o + (((int64_t)b * S + s) * H + h) * D + tid * 4);
-        o.x = fmaf(w, v.x, o.x);
-        o.y = fmaf(w, v.y, o.y);
-        o.z = fmaf(w, v.z, o.z);
-        o.w = fmaf(w, v.w, o.w);
+    int s = 0;
+    for (; s + 4 <= S; s += 4) {  // four splits' loads in flight at once
+        float2 v[4];
+        float4 x[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            v[u] = *reinterpret_cast<const float2*>(ml + ((int64_t)(s + u) * H + h) * 2);
+            x[u] = *reinterpret_cast<const float4*>(po + (int64_t)(s + u) * H * D);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (!(v[u].y > 0.f)) continue;
+            const float w = exp2f(v[u].x - M);
+            L = fmaf(w, v[u].y, L);
+            o.x = fmaf(w, x[u].x, o.x);
+            o.y = fmaf(w, x[u].y, o.y);
+            o.z = fmaf(w, x[u].z, o.z);
+            o.w = fmaf(w, x[u].w, o.w);
+        }
+    }
+    for (; s < S; ++s) {
+        const float2 v = *reinterpret_cast<const float2*>(ml + ((int64_t)s * H + h) * 2);
+        if (!(v.y > 0.f)) continue;
+        const float4 x = *reinterpret_cast<const float4*>(po + (int64_t)s * H * D);
+        const float w = exp2f(v.x - M);
+        L = fmaf(w, v.y, L);
+        o.x = fmaf(w, x.x, o.x);
+        o.y = fmaf(w, x.y, o.y);
+        o.z = fmaf(w, x.z, o.z);
+        o.w = fmaf(w, x.w, o.w);
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     uint2 r;

@@ -87,6 +87,7 @@ __device__ __forceinline__ void store_row16(const DPaged& out, int b, int64_t g,
 
 // C4: one warp per group of 4 tokens; gate dots reduced with warp shuffles.
 __global__ void __launch_bounds__(256) compress_r4_kernel(CompressArgs a) {
+    pdl_launch_dependents();  // the score kernel reads none of this kernel's outputs until its epilogue
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.y;
     zero_hist(a, b);
@@ -142,6 +143,7 @@ constexpr int R128_WARPS = 8;
 __global__ void __launch_bounds__(256) compress_r128_kernel(CompressArgs a) {
     __shared__ float sm_m[R128_WARPS], sm_l[R128_WARPS];
     __shared__ __align__(16) float sm_acc[R128_WARPS][D];
+    pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.y;
     zero_hist(a, b);

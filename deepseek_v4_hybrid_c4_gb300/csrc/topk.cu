@@ -147,6 +147,8 @@ __global__ void __launch_bounds__(TK_T, 1) topk_kernel(TopkArgs a) {
     extern __shared__ __align__(16) uint8_t tk_raw[];
     TkSmem& sm = *reinterpret_cast<TkSmem*>(tk_raw);
     const int tid = threadIdx.x;
+    pdl_wait();               // scores (and the fused histogram) come from the preceding kernel
+    pdl_launch_dependents();
     const uint32_t rank = cluster_ctarank();
     const int b = blockIdx.x / TK_CL;
 
