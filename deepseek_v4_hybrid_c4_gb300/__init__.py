@@ -65,6 +65,7 @@ def lib() -> ctypes.CDLL:
         L.csa_sparse_attn_workspace_size.restype = sz
         L.csa_decode.argtypes = [ctypes.POINTER(csa_decode_params), vp, sz, vp]
         L.csa_decode_timed.argtypes = [ctypes.POINTER(csa_decode_params), vp, sz, vp, ctypes.POINTER(vp)]
+        L.csa_decode_noalloc.argtypes = [ctypes.POINTER(csa_decode_params), vp]
         L.csa_decode_workspace_size.argtypes = [ctypes.POINTER(csa_decode_params)]
         L.csa_decode_workspace_size.restype = sz
         L.csa_read_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
@@ -72,7 +73,7 @@ def lib() -> ctypes.CDLL:
         L.csa_status_string.restype = ctypes.c_char_p
         L.csa_version.restype = i32
         for name in ("csa_compress", "csa_index_score", "csa_topk", "csa_topk_batched", "csa_sparse_attn",
-                     "csa_decode", "csa_decode_timed", "csa_read_device_status"):
+                     "csa_decode", "csa_decode_timed", "csa_decode_noalloc", "csa_read_device_status"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -167,6 +168,11 @@ def csa_decode_timed(p: csa_decode_params, workspace, ws_bytes: int, stream=None
         arr = (ctypes.c_void_p * 5)(*[e.cuda_event for e in events])
     _check(lib().csa_decode_timed(ctypes.byref(p), _ptr(workspace), ws_bytes, _stream(stream), arr),
            "csa_decode_timed")
+
+
+def csa_decode_noalloc(p: csa_decode_params, stream=None) -> None:
+    """csa_decode with the library's own fixed 16 MiB scratch (for callers that cannot allocate)."""
+    _check(lib().csa_decode_noalloc(ctypes.byref(p), _stream(stream)), "csa_decode_noalloc")
 
 
 def csa_read_device_status(stream=None) -> int:

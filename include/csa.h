@@ -204,6 +204,22 @@ size_t csa_decode_workspace_size(const csa_decode_params* p);
 csa_status csa_decode_timed(const csa_decode_params* p, void* workspace, size_t ws_bytes, void* stream,
                             void* const* stage_events);
 
+/*
+ * csa_decode without a workspace argument, for callers that cannot allocate device
+ * memory: code that runs inside an allocator or memory-pool callback, a host that
+ * only hands the library its input and output buffers, or a runtime that forbids
+ * cudaMalloc once it has started.  (The pages have no counterpart: this is a
+ * packaging of csa_decode, not part of the method.)
+ * The scratch comes from a fixed 16 MiB array in libcsa's own device memory, which
+ * every GPU that loads the library holds until the process exits; a call whose
+ * csa_decode_workspace_size() exceeds 16 MiB returns CSA_ERR_WORKSPACE and enqueues
+ * nothing.  Nothing is allocated and no scratch contents need to start at zero.
+ * The first call on a device looks up the array's device address (with that device
+ * current); make that first call before any stream capture.  Every call shares the
+ * one array, so calls that overlap on the GPU (other streams, other threads) race.
+ */
+csa_status csa_decode_noalloc(const csa_decode_params* p, void* stream);
+
 /* Read and clear the calling device's sticky status word (synchronises `stream`).
  * *out receives a bit set: bit (code-1) for each csa_status code raised on the device. */
 csa_status csa_read_device_status(void* stream, int32_t* out);
