@@ -21,7 +21,7 @@
 // distinct banks.  A consumer warp takes two units (32 rows) at a time.
 // Persistent grid, two CTAs per SM.
 //
-// Optional fused epilogue: a per-warp histogram of the top 11 bits of each score's
+// Optional fused epilogue: a per-warp (16-bit) histogram of the top 11 bits of each score's
 // order-preserving key (the first digit of the top-k radix select), flushed per
 // request into a global [B][2048] histogram.
 #include <cuda.h>
@@ -38,7 +38,7 @@ constexpr int SC_CONSUMERS = 4;              // consumer warps; each takes 32 ro
 constexpr int SC_THREADS = (SC_CONSUMERS + 1) * 32;
 constexpr int SC_UNIT = 16;                  // rows per unit (one TMA box height)
 constexpr int SC_SUPER = 32;                 // rows per consumer-warp step
-constexpr int SC_STAGES = 12;                // units in flight per CTA
+constexpr int SC_STAGES = 18;                // units in flight per CTA
 constexpr int SC_STAGE_BYTES = SC_UNIT * 256;  // bf16 unit (fp8 uses half)
 
 struct ScoreArgs {
@@ -84,7 +84,13 @@ struct StepCursor {
 };
 
 __device__ __forceinline__ uint64_t pk2(float lo, float hi) {
-    return ((uint64_t)__float_as_uint(hi) << 32) | (uint64_t)__float_as_uint(lo);
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+// Two {q_h[8a+i], q_h[8a+64+i]} pairs (heads h, h+1) straight into 64-bit registers.
+__device__ __forceinline__ void ld_qpairs(uint32_t addr, uint64_t& p0, uint64_t& p1) {
+    asm volatile("ld.shared.v2.u64 {%0, %1}, [%2];" : "=l"(p0), "=l"(p1) : "r"(addr));
 }
 __device__ __forceinline__ float lo2(uint64_t v) { return __uint_as_float((uint32_t)v); }
 __device__ __forceinline__ float hi2(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
@@ -157,7 +163,7 @@ __global__ void __launch_bounds__(SC_THREADS, 2) score_kernel(const __grid_const
     uint64_t* full = reinterpret_cast<uint64_t*>(ws_all + SC_CONSUMERS * 16);
     uint64_t* empty = full + SC_STAGES;
     int* meta = reinterpret_cast<int*>(empty + SC_STAGES);                     // page valid flag per stage
-    uint32_t* hist_all = reinterpret_cast<uint32_t*>(meta + SC_STAGES + 4);     // [warp][kHistBins]
+    uint16_t* hist_all = reinterpret_cast<uint16_t*>(meta + SC_STAGES + 4);     // [warp][kHistBins], 16-bit
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_launch_dependents();  // the top-k kernel may be scheduled now; it waits for this grid to finish
@@ -173,51 +179,67 @@ __global__ void __launch_bounds__(SC_THREADS, 2) score_kernel(const __grid_const
     __syncthreads();
 
     if (warp == SC_CONSUMERS) {
-        // ---------------- producer: one lane issues the TMA copies, two units per step
-        if (lane == 0) {
+        // ---------------- producer warp: the 32 lanes look up the pages of 32 upcoming units
+        // at once (independent loads), then lane 0 issues their TMA copies in order.
+        if (lane == 0)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kmap)) : "memory");
-            StepCursor cur;
-            int64_t u = 0;  // units issued by this CTA
-            for (int64_t i = 0;; ++i) {
-                const int64_t w = blockIdx.x + i * gridDim.x;
-                if (!cur.seek(a, w)) break;
-                const int64_t g0 = (w - cur.base) * SC_SUPER;
-                bool stop = false;
-                for (int h = 0; h < 2; ++h, ++u) {
+        StepCursor cur;  // each lane walks the same step sequence (monotone seeks)
+        bool stop = false;
+        for (int64_t r = 0; !stop; ++r) {
+            // unit r*32 + lane of this CTA = half (lane & 1) of this CTA's step r*16 + lane/2
+            const int64_t i = r * 16 + (lane >> 1);
+            const int64_t w = blockIdx.x + i * gridDim.x;
+            int kind = 0;      // 0: past the end, 1: copy, 2: nothing to copy (beyond G / bad page)
+            int slot = 0, page = 0;
+            if (cur.seek(a, w)) {
+                const int64_t gr = (w - cur.base) * SC_SUPER + (lane & 1) * SC_UNIT;
+                kind = 2;
+                if (gr < cur.G) {
+                    const int64_t lp = gr / a.rpp;
+                    slot = (int)(gr - lp * a.rpp);
+                    int64_t pp = lp;
+                    if (a.pt) pp = __ldg(a.pt + (int64_t)cur.b * a.pt_stride + lp);
+                    if (pp >= 0 && pp < a.n_pages) {
+                        kind = 1;
+                        page = (int)pp;
+                    } else {
+                        raise_status(a.status, CSA_ERR_DEVICE_BOUNDS);
+                    }
+                }
+            }
+            for (int j = 0; j < 32; ++j) {
+                const int kj = __shfl_sync(0xffffffffu, kind, j);
+                const int sj = __shfl_sync(0xffffffffu, slot, j);
+                const int pj = __shfl_sync(0xffffffffu, page, j);
+                if (kj == 0) {
+                    stop = true;
+                    break;
+                }
+                if (lane == 0) {
+                    const int64_t u = r * 32 + j;  // units issued by this CTA so far
                     const int s = (int)(u % SC_STAGES);
                     if (u >= SC_STAGES && !mbar_wait(smem_u32(&empty[s]), (uint32_t)(((u / SC_STAGES) - 1) & 1))) {
                         raise_status(a.status, CSA_ERR_TIMEOUT);
                         stop = true;
-                        break;
-                    }
-                    const int64_t gr = g0 + h * SC_UNIT;
-                    const uint32_t fb = smem_u32(&full[s]);
-                    int ok = 0;
-                    if (gr < cur.G) {
-                        const int64_t lp = gr / a.rpp;
-                        const int slot = (int)(gr - lp * a.rpp);
-                        int64_t pp = lp;
-                        if (a.pt) pp = __ldg(a.pt + (int64_t)cur.b * a.pt_stride + lp);
-                        if (pp >= 0 && pp < a.n_pages) {
-                            ok = 1;
+                    } else {
+                        const uint32_t fb = smem_u32(&full[s]);
+                        if (kj == 1) {
                             meta[s] = 1;
                             mbar_arrive_expect_tx(fb, (uint32_t)UB);
                             const uint32_t dst = smem_u32(stages + s * SC_STAGE_BYTES);
                             if constexpr (FP8) {
-                                tma_load_3d(dst, &kmap, 0, slot, (int)pp, fb);
+                                tma_load_3d(dst, &kmap, 0, sj, pj, fb);
                             } else {
-                                tma_load_3d(dst, &kmap, 0, slot, (int)pp, fb);
-                                tma_load_3d(dst + 2048u, &kmap, 64, slot, (int)pp, fb);
+                                tma_load_3d(dst, &kmap, 0, sj, pj, fb);
+                                tma_load_3d(dst + 2048u, &kmap, 64, sj, pj, fb);
                             }
                         } else {
-                            raise_status(a.status, CSA_ERR_DEVICE_BOUNDS);
+                            meta[s] = 0;
+                            mbar_arrive(fb);
                         }
                     }
-                    if (!ok) {
-                        meta[s] = 0;
-                        mbar_arrive(fb);
-                    }
                 }
+                stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
                 if (stop) break;
             }
         }
@@ -226,8 +248,10 @@ __global__ void __launch_bounds__(SC_THREADS, 2) score_kernel(const __grid_const
 
     // ---------------- consumers
     float4* qs = qs_all + warp * QF4;
+    const uint32_t qs_addr = smem_u32(qs);
     float* wsm = ws_all + warp * 16;
-    uint32_t* hist = hist_all + warp * kHistBins;
+    uint16_t* hist = hist_all + warp * kHistBins;
+    int hist_rows = 0;  // rows counted since the last flush (16-bit counters: flush before they can wrap)
     const int r = lane & 15;        // row within its unit
     const int hu = lane >> 4;       // which of the step's two units
     int qb = -1;
@@ -246,6 +270,7 @@ __global__ void __launch_bounds__(SC_THREADS, 2) score_kernel(const __grid_const
                 hist[bin] = 0;
             }
         }
+        hist_rows = 0;
         __syncwarp();
     };
     for (int64_t i = 0;; ++i) {
@@ -294,15 +319,17 @@ __global__ void __launch_bounds__(SC_THREADS, 2) score_kernel(const __grid_const
 #pragma unroll
             for (int ii = 0; ii < 8; ++ii) {
                 const uint64_t kk = pk2(kl[ii], kh[ii]);
+                const uint32_t qa = qs_addr + (uint32_t)((aa * 8 + ii) * (HI / 2)) * 16u;
 #pragma unroll
                 for (int hp = 0; hp < HI / 2; ++hp) {
-                    const float4 qv = qs[(aa * 8 + ii) * (HI / 2) + hp];
+                    uint64_t q0, q1;
+                    ld_qpairs(qa + hp * 16u, q0, q1);
                     if (ii == 0) {
-                        acc[2 * hp] = mul2(pk2(qv.x, qv.y), kk);
-                        acc[2 * hp + 1] = mul2(pk2(qv.z, qv.w), kk);
+                        acc[2 * hp] = mul2(q0, kk);
+                        acc[2 * hp + 1] = mul2(q1, kk);
                     } else {
-                        acc[2 * hp] = fma2(pk2(qv.x, qv.y), kk, acc[2 * hp]);
-                        acc[2 * hp + 1] = fma2(pk2(qv.z, qv.w), kk, acc[2 * hp + 1]);
+                        acc[2 * hp] = fma2(q0, kk, acc[2 * hp]);
+                        acc[2 * hp + 1] = fma2(q1, kk, acc[2 * hp + 1]);
                     }
                 }
             }
@@ -340,9 +367,11 @@ __global__ void __launch_bounds__(SC_THREADS, 2) score_kernel(const __grid_const
             const unsigned m = __ballot_sync(0xffffffffu, in);
             if (in) {
                 const unsigned peers = __match_any_sync(m, dg);
-                if (lane == __ffs(peers) - 1) hist[dg] += (uint32_t)__popc(peers);  // warp-private histogram
+                if (lane == __ffs(peers) - 1) hist[dg] = (uint16_t)(hist[dg] + __popc(peers));  // warp-private
             }
             __syncwarp();
+            hist_rows += 32;
+            if (hist_rows >= 65536 - 64) flush(qb);
         }
     }
     if (a.hist && qb >= 0) flush(qb);
@@ -388,7 +417,7 @@ static cudaError_t launch_score_t(const CUtensorMap& map, const ScoreArgs& a, in
     constexpr int QF4 = 8 * 8 * (HI / 2);
     constexpr size_t base = 1024 + (size_t)SC_STAGES * SC_STAGE_BYTES + SC_CONSUMERS * QF4 * 16 +
                             SC_CONSUMERS * 16 * 4 + 2 * SC_STAGES * 8 + (SC_STAGES + 4) * 4;
-    constexpr size_t with_hist = base + (size_t)SC_CONSUMERS * kHistBins * 4;
+    constexpr size_t with_hist = base + (size_t)SC_CONSUMERS * kHistBins * 2;
     const size_t smem = a.hist ? with_hist : base;
     static bool attr_set = false;
     if (!attr_set) {

@@ -8,16 +8,22 @@
 // lower index (a total order, so the selected set and its order are unique).
 //
 // One cluster of 8 CTAs per request; CTA r owns the contiguous index slice
-// [r*S, r*S+S).  Digits of the key: bits 31..21, 20..10, 9..0.  For each digit
-// every CTA builds a local histogram of the candidates that still match the
-// prefix, the 8 histograms are summed through distributed shared memory, and
-// every CTA finds the same bin that contains the k-th key.  Entries in higher
-// bins are selected; the matching bin's entries survive (kept in shared memory,
-// or re-read from L2 when more than CAP survive).  In the fused decode step the
-// first digit's histogram comes ready from the score kernel, so the first pass
-// is a single filtered scan.  After the last digit tau is exact; ties at tau are
-// taken lowest index first (slices are in index order across the cluster).  CTA
-// 0 gathers the k winners through DSMEM and sorts them (bitonic, shared memory).
+// [r*S, r*S+S).  Digits of the key: bits 31..21, 20..10, 9..0.
+//  1. First digit: its histogram over the whole request -- ready-made by the
+//     score kernel in the fused decode step, otherwise built per CTA and summed
+//     across the cluster through distributed shared memory -- gives the bin b0
+//     holding the k-th key.
+//  2. Each CTA scans its slice once (16 scores in flight per thread): keys in
+//     higher bins are winners, keys in b0 are survivors.
+//  3. Fast path (the survivors of all 8 CTAs fit CTA 0's gather buffer): every
+//     CTA copies its winners and survivors into CTA 0 through DSMEM and CTA 0
+//     finishes alone -- two more digits over the survivors, then the lowest-index
+//     ties at the exact threshold -- with no further cluster barrier.
+//     Otherwise every CTA keeps refining its survivors with cluster-reduced
+//     histograms (re-reading L2 when more than CAP survive) and the ties are
+//     taken lowest index first across the index-ordered slices.
+//  4. CTA 0 sorts the k winners by (key desc, index asc) with a bitonic network
+//     kept in registers (shuffles) except for strides of a warp or more.
 #include "common.cuh"
 #include "internal.h"
 
@@ -26,9 +32,10 @@ namespace csa {
 constexpr int TK_CL = 8;
 constexpr int TK_T = 1024;
 constexpr int TK_BINS = kHistBins;   // 2048: widest digit
-constexpr int TK_CAP = 12288;
+constexpr int TK_CAP = 10240;        // survivors kept per CTA
 constexpr int TK_KMAX = 2048;
-constexpr int TK_U = 4;              // independent loads in flight per thread in the scans
+constexpr int TK_GCAP = 6144;        // survivors CTA 0 can take from the whole cluster
+constexpr int TK_V = 16;             // scores per thread per scan iteration
 
 struct TopkArgs {
     const float* scores;
@@ -47,15 +54,18 @@ struct TopkArgs {
 
 struct TkSmem {
     uint32_t hist[2][TK_BINS];
-    uint32_t ckey[TK_CAP];
+    uint32_t ckey[TK_CAP];      // this CTA's survivors
     int32_t cidx[TK_CAP];
-    uint32_t skey[TK_KMAX];
+    uint32_t skey[TK_KMAX];     // this CTA's winners
     int32_t sidx[TK_KMAX];
-    uint32_t okey[TK_KMAX];
+    uint32_t okey[TK_KMAX];     // CTA 0: the cluster's winners
     int32_t oidx[TK_KMAX];
-    uint32_t xchg[4];
+    uint32_t gkey[TK_GCAP];     // CTA 0: the cluster's survivors (fast path)
+    int32_t gidx[TK_GCAP];
+    uint64_t sortbuf[2][1024];
+    uint32_t xchg[8];
     uint32_t wsum[32];
-    int n_cand, n_sel, n_new, overflow;
+    int n_cand, n_sel, n_new, overflow, n_out;
     uint32_t bin, above, cnt, taken;
 };
 
@@ -104,24 +114,35 @@ __device__ __forceinline__ uint32_t block_scan(TkSmem& sm, uint32_t v, uint32_t*
     return before + x - v;
 }
 
-// Total histogram (the global one from the score kernel, or the sum of the 8
-// CTAs' through DSMEM), then the bin holding the need-th largest key counted from
-// the top bin.  Writes sm.bin and sm.above (count in higher bins).
-__device__ __forceinline__ void reduce_and_find(TkSmem& sm, const uint32_t* ghist, int hb, int nbins,
-                                                uint32_t need) {
+enum { HIST_GLOBAL = 0, HIST_CLUSTER = 1, HIST_LOCAL = 2 };
+
+// The bin holding the need-th largest key counted from the top bin, from the
+// global histogram, the sum of the 8 CTAs' histograms (DSMEM) or this CTA's own.
+// Writes sm.bin and sm.above (count in higher bins).
+__device__ __forceinline__ void find_bin(TkSmem& sm, int mode, const uint32_t* ghist, int hb, int nbins,
+                                         uint32_t need) {
     const int t = threadIdx.x;
     const int bh = nbins - 1 - 2 * t, bl = nbins - 2 - 2 * t;  // this thread's two bins, high first
     uint32_t th = 0, tl = 0;
     if (bl >= 0) {
-        if (ghist) {
+        if (mode == HIST_GLOBAL) {
             th = __ldg(ghist + bh);
             tl = __ldg(ghist + bl);
+        } else if (mode == HIST_LOCAL) {
+            th = sm.hist[hb][bh];
+            tl = sm.hist[hb][bl];
         } else {
             const uint32_t ah = smem_u32(&sm.hist[hb][bh]), al = smem_u32(&sm.hist[hb][bl]);
+            uint32_t vh[TK_CL], vl[TK_CL];
 #pragma unroll
             for (int c = 0; c < TK_CL; ++c) {
-                th += ld_dsmem_u32(mapa(ah, c));
-                tl += ld_dsmem_u32(mapa(al, c));
+                vh[c] = ld_dsmem_u32(mapa(ah, c));
+                vl[c] = ld_dsmem_u32(mapa(al, c));
+            }
+#pragma unroll
+            for (int c = 0; c < TK_CL; ++c) {
+                th += vh[c];
+                tl += vl[c];
             }
         }
     }
@@ -139,8 +160,100 @@ __device__ __forceinline__ void reduce_and_find(TkSmem& sm, const uint32_t* ghis
     __syncthreads();
 }
 
+// Keys of TK_V scores of the slice for this thread: element j*4+q is index
+// base + 4*(tid + (j/1)*TK_T) + q (coalesced float4 loads when the slice is 16-byte aligned).
+__device__ __forceinline__ void load_keys(const float* sc, int64_t base, int64_t hi, bool vec, uint32_t (&key)[TK_V],
+                                          int64_t (&pos)[TK_V / 4]) {
+    const int tid = threadIdx.x;
+#pragma unroll
+    for (int j = 0; j < TK_V / 4; ++j) {
+        pos[j] = base + 4 * ((int64_t)tid + (int64_t)j * TK_T);
+        float v[4];
+        if (vec && pos[j] + 3 < hi) {
+            const float4 f = __ldg(reinterpret_cast<const float4*>(sc + pos[j]));
+            v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) v[q] = pos[j] + q < hi ? __ldg(sc + pos[j] + q) : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) key[j * 4 + q] = score_key(v[q]);
+    }
+}
+
 __device__ __forceinline__ bool kv_greater(uint32_t ka, int32_t ia, uint32_t kb, int32_t ib) {
     return ka > kb || (ka == kb && ia < ib);
+}
+
+// CTA 0: sort okey/oidx[0..total) by (key desc, index asc), write k outputs (-1 padding).
+__device__ void sort_and_write(TkSmem& sm, uint32_t total, int k, int32_t* out, uint32_t* kout) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    if (total > (uint32_t)TK_KMAX) total = TK_KMAX;
+    int n2 = 1;
+    while (n2 < (int)total) n2 <<= 1;
+    if (n2 <= 1024) {
+        // one element per thread, composite = key << 32 | (0x7FFFFFFF - idx): larger is better
+        const bool act = tid < n2;
+        uint64_t v = 0;
+        if (act && tid < (int)total) v = ((uint64_t)sm.okey[tid] << 32) | (uint32_t)(0x7FFFFFFF - sm.oidx[tid]);
+        int buf = 0;
+        for (int size = 2; size <= n2; size <<= 1) {
+            for (int j = size >> 1; j > 0; j >>= 1) {
+                uint64_t pv;
+                if (j >= 32) {
+                    if (act) sm.sortbuf[buf][tid] = v;
+                    __syncthreads();
+                    pv = act ? sm.sortbuf[buf][tid ^ j] : 0;
+                    buf ^= 1;
+                } else {
+                    pv = __shfl_xor_sync(0xffffffffu, v, j);
+                }
+                const bool up = (tid & size) == 0, lower = (tid & j) == 0;
+                const uint64_t mx = v > pv ? v : pv, mn = v > pv ? pv : v;
+                if (act) v = (up == lower) ? mx : mn;
+            }
+        }
+        if (tid < k) {
+            const bool ok = tid < (int)total;
+            out[tid] = ok ? (int32_t)(0x7FFFFFFF - (uint32_t)v) : -1;
+            if (kout) kout[tid] = ok ? (uint32_t)(v >> 32) : 0u;
+        }
+        for (int i = tid + TK_T; i < k; i += TK_T) {
+            out[i] = -1;
+            if (kout) kout[i] = 0u;
+        }
+        return;
+    }
+    // n2 = 2048: shared-memory bitonic network
+    for (int i = (int)total + tid; i < n2; i += TK_T) {
+        sm.okey[i] = 0u;
+        sm.oidx[i] = 0x7FFFFFFF;
+    }
+    __syncthreads();
+    for (int size = 2; size <= n2; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = tid; i < n2; i += TK_T) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    const uint32_t ki = sm.okey[i], kj = sm.okey[j];
+                    const int32_t ii = sm.oidx[i], ij = sm.oidx[j];
+                    const bool first_half = (i & size) == 0;
+                    const bool swap = first_half ? kv_greater(kj, ij, ki, ii) : kv_greater(ki, ii, kj, ij);
+                    if (swap) {
+                        sm.okey[i] = kj; sm.oidx[i] = ij;
+                        sm.okey[j] = ki; sm.oidx[j] = ii;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    for (int i = tid; i < k; i += TK_T) {
+        const bool ok = i < (int)total;
+        out[i] = ok ? sm.oidx[i] : -1;
+        if (kout) kout[i] = ok ? sm.okey[i] : 0u;
+    }
+    (void)lane;
 }
 
 __global__ void __launch_bounds__(TK_T, 1) topk_kernel(TopkArgs a) {
@@ -167,65 +280,185 @@ __global__ void __launch_bounds__(TK_T, 1) topk_kernel(TopkArgs a) {
     }
     if (G < 0) G = 0;
     const int k = a.k;
-    const int64_t slice = (G + TK_CL - 1) / TK_CL;
+    const int64_t slice = ((G + TK_CL - 1) / TK_CL + 3) & ~int64_t(3);
     const int64_t lo = min((int64_t)rank * slice, G), hi = min(lo + slice, G);
-    const uint32_t need_total = (uint32_t)min((int64_t)k, G);
+    const bool vec = (reinterpret_cast<uintptr_t>(sc + lo) & 15) == 0;
+    int32_t* out = a.idx_out + (int64_t)b * k;
+    uint32_t* kout = a.keys_out ? a.keys_out + (int64_t)b * k : nullptr;
 
     if (tid == 0) {
         sm.n_cand = 0;
         sm.n_sel = 0;
         sm.overflow = 0;
+        sm.n_out = 0;
     }
     __syncthreads();
 
     if (G > k) {
-        const int shifts[3] = {21, 10, 0};
-        const int widths[3] = {11, 11, 10};
-        uint32_t need = need_total;
-        uint32_t prefix = 0;
-        int prev_shift = 32;
-        for (int p = 0; p < 3; ++p) {
+        uint32_t need = (uint32_t)k;
+        // ---- 1. first digit (bits 31..21)
+        if (a.hist) {
+            find_bin(sm, HIST_GLOBAL, a.hist + (int64_t)b * kHistBins, 0, 2048, need);
+        } else {
+            for (int i = tid; i < TK_BINS; i += TK_T) sm.hist[0][i] = 0;
+            __syncthreads();
+            for (int64_t base = lo; base < hi; base += (int64_t)TK_T * TK_V) {
+                uint32_t key[TK_V];
+                int64_t pos[TK_V / 4];
+                load_keys(sc, base, hi, vec, key, pos);
+#pragma unroll
+                for (int e = 0; e < TK_V; ++e) hist_add(sm.hist[0], key[e] >> 21, pos[e / 4] + (e & 3) < hi);
+            }
+            cluster_sync();
+            find_bin(sm, HIST_CLUSTER, nullptr, 0, 2048, need);
+        }
+        const uint32_t b0 = sm.bin;
+        need -= sm.above;
+        // ---- 2. one scan of the slice: winners (digit > b0) and survivors (digit == b0)
+        for (int64_t base = lo; base < hi; base += (int64_t)TK_T * TK_V) {
+            uint32_t key[TK_V];
+            int64_t pos[TK_V / 4];
+            load_keys(sc, base, hi, vec, key, pos);
+            bool mine = false;
+#pragma unroll
+            for (int e = 0; e < TK_V; ++e) mine = mine || (pos[e / 4] + (e & 3) < hi && (key[e] >> 21) >= b0);
+            if (!__any_sync(0xffffffffu, mine)) continue;
+#pragma unroll
+            for (int e = 0; e < TK_V; ++e) {
+                const int64_t i = pos[e / 4] + (e & 3);
+                const bool in = i < hi;
+                const uint32_t d = key[e] >> 21;
+                const int s = warp_alloc(&sm.n_sel, in && d > b0);
+                if (s >= 0 && s < TK_KMAX) { sm.skey[s] = key[e]; sm.sidx[s] = (int32_t)i; }
+                const int c = warp_alloc(&sm.n_cand, in && d == b0);
+                if (c >= TK_CAP) sm.overflow = 1;
+                else if (c >= 0) { sm.ckey[c] = key[e]; sm.cidx[c] = (int32_t)i; }
+            }
+        }
+        __syncthreads();
+        if (tid == 0) {
+            sm.xchg[0] = (uint32_t)sm.n_sel;
+            sm.xchg[1] = sm.overflow ? 0xFFFFFFFFu : (uint32_t)sm.n_cand;
+        }
+        cluster_sync();
+        uint32_t off_sel = 0, tot_sel = 0, off_cand = 0, tot_cand = 0;
+        bool any_over = false;
+        for (uint32_t c = 0; c < TK_CL; ++c) {
+            const uint32_t ns = ld_dsmem_u32(mapa(smem_u32(&sm.xchg[0]), c));
+            const uint32_t nc = ld_dsmem_u32(mapa(smem_u32(&sm.xchg[1]), c));
+            if (nc == 0xFFFFFFFFu) any_over = true;
+            if (c < rank) { off_sel += ns; off_cand += nc; }
+            tot_sel += ns;
+            tot_cand += nc;
+        }
+        if (!any_over && tot_cand <= (uint32_t)TK_GCAP) {
+            // ---- 3a. fast path: gather into CTA 0, finish there
+            for (int i = tid; i < sm.n_sel; i += TK_T) {
+                st_dsmem_u32(mapa(smem_u32(&sm.okey[off_sel + i]), 0), sm.skey[i]);
+                st_dsmem_u32(mapa(smem_u32(&sm.oidx[off_sel + i]), 0), (uint32_t)sm.sidx[i]);
+            }
+            for (int i = tid; i < sm.n_cand; i += TK_T) {
+                st_dsmem_u32(mapa(smem_u32(&sm.gkey[off_cand + i]), 0), sm.ckey[i]);
+                st_dsmem_u32(mapa(smem_u32(&sm.gidx[off_cand + i]), 0), (uint32_t)sm.cidx[i]);
+            }
+            cluster_sync();
+            if (rank != 0) return;
+            if (tid == 0) sm.n_out = (int)tot_sel;
+            __syncthreads();
+            int n_list = (int)tot_cand;
+            const int shifts[2] = {10, 0};
+            const int widths[2] = {11, 10};
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+                const int shift = shifts[p];
+                const uint32_t mask = (1u << widths[p]) - 1u;
+                if ((uint32_t)n_list == need) break;  // every survivor is a winner
+                for (int i = tid; i < TK_BINS; i += TK_T) sm.hist[0][i] = 0;
+                __syncthreads();
+                for (int i0 = 0; i0 < n_list; i0 += TK_T) {
+                    const int i = i0 + tid;
+                    const bool in = i < n_list;
+                    hist_add(sm.hist[0], in ? (sm.gkey[i] >> shift) & mask : 0u, in);
+                }
+                __syncthreads();
+                find_bin(sm, HIST_LOCAL, nullptr, 0, 1 << widths[p], need);
+                const uint32_t bin = sm.bin;
+                need -= sm.above;
+                if (tid == 0) sm.n_new = 0;
+                __syncthreads();
+                for (int i0 = 0; i0 < n_list; i0 += TK_T) {
+                    const int i = i0 + tid;
+                    const bool in = i < n_list;
+                    const uint32_t key = in ? sm.gkey[i] : 0u;
+                    const int32_t idx = in ? sm.gidx[i] : 0;
+                    __syncthreads();  // chunk read by everyone before it is overwritten
+                    const uint32_t d = (key >> shift) & mask;
+                    const int s = warp_alloc(&sm.n_out, in && d > bin);
+                    if (s >= 0 && s < TK_KMAX) { sm.okey[s] = key; sm.oidx[s] = idx; }
+                    const int c = warp_alloc(&sm.n_new, in && d == bin);
+                    if (c >= 0) { sm.gkey[c] = key; sm.gidx[c] = idx; }
+                }
+                __syncthreads();
+                n_list = sm.n_new;
+            }
+            // survivors now share one key (or all of them are winners): keep the `need` lowest indices
+            if ((uint32_t)n_list == need) {
+                for (int i = tid; i < n_list; i += TK_T) {
+                    const int s = atomicAdd(&sm.n_out, 1);
+                    if (s < TK_KMAX) { sm.okey[s] = sm.gkey[i]; sm.oidx[s] = sm.gidx[i]; }
+                }
+            } else {
+                for (int i = tid; i < n_list; i += TK_T) {
+                    const int32_t my = sm.gidx[i];
+                    uint32_t rnk = 0;
+                    for (int j = 0; j < n_list; ++j) rnk += sm.gidx[j] < my ? 1u : 0u;
+                    if (rnk < need) {
+                        const int s = atomicAdd(&sm.n_out, 1);
+                        if (s < TK_KMAX) { sm.okey[s] = sm.gkey[i]; sm.oidx[s] = my; }
+                    }
+                }
+            }
+            __syncthreads();
+            sort_and_write(sm, (uint32_t)min(sm.n_out, k), k, out, kout);
+            return;
+        }
+        // ---- 3b. cluster-wide refinement (many survivors)
+        uint32_t prefix = b0;
+        int prev_shift = 21;
+        const int shifts[2] = {10, 0};
+        const int widths[2] = {11, 10};
+        for (int p = 0; p < 2; ++p) {
             const int shift = shifts[p];
             const uint32_t mask = (1u << widths[p]) - 1u;
             const int nbins = 1 << widths[p];
-            const int hb = p & 1;
-            const bool fused = p == 0 && a.hist != nullptr;
-            const uint32_t* gh = fused ? a.hist + (int64_t)b * kHistBins : nullptr;
-            if (!fused)
-                for (int i = tid; i < TK_BINS; i += TK_T) sm.hist[hb][i] = 0;
+            const int hb = (p + 1) & 1;
+            for (int i = tid; i < TK_BINS; i += TK_T) sm.hist[hb][i] = 0;
             __syncthreads();
-            const bool list_mode = p > 0 && !sm.overflow;
+            const bool list_mode = !sm.overflow;
             const int n_list = sm.n_cand;
-            // ---- histogram of the surviving candidates
-            if (!fused) {
-                if (list_mode) {
-                    for (int i0 = 0; i0 < n_list; i0 += TK_T) {
-                        const int i = i0 + tid;
-                        const bool in = i < n_list;
-                        const uint32_t key = in ? sm.ckey[i] : 0u;
-                        hist_add(sm.hist[hb], (key >> shift) & mask, in);
-                    }
-                } else {
-                    for (int64_t i0 = lo; i0 < hi; i0 += TK_U * TK_T) {
-                        uint32_t key[TK_U];
-                        bool in[TK_U];
+            if (list_mode) {
+                for (int i0 = 0; i0 < n_list; i0 += TK_T) {
+                    const int i = i0 + tid;
+                    const bool in = i < n_list;
+                    const uint32_t key = in ? sm.ckey[i] : 0u;
+                    hist_add(sm.hist[hb], (key >> shift) & mask, in);
+                }
+            } else {
+                for (int64_t base = lo; base < hi; base += (int64_t)TK_T * TK_V) {
+                    uint32_t key[TK_V];
+                    int64_t pos[TK_V / 4];
+                    load_keys(sc, base, hi, vec, key, pos);
 #pragma unroll
-                        for (int u = 0; u < TK_U; ++u) {
-                            const int64_t i = i0 + u * TK_T + tid;
-                            in[u] = i < hi;
-                            key[u] = in[u] ? score_key(__ldg(sc + i)) : 0u;
-                            if (prev_shift < 32) in[u] = in[u] && (key[u] >> prev_shift) == prefix;
-                        }
-#pragma unroll
-                        for (int u = 0; u < TK_U; ++u) hist_add(sm.hist[hb], (key[u] >> shift) & mask, in[u]);
+                    for (int e = 0; e < TK_V; ++e) {
+                        const bool in = pos[e / 4] + (e & 3) < hi && (key[e] >> prev_shift) == prefix;
+                        hist_add(sm.hist[hb], (key[e] >> shift) & mask, in);
                     }
                 }
-                cluster_sync();
             }
-            reduce_and_find(sm, gh, hb, nbins, need);
+            cluster_sync();
+            find_bin(sm, HIST_CLUSTER, nullptr, hb, nbins, need);
             const uint32_t bin = sm.bin;
             need -= sm.above;
-            // ---- select the higher bins, keep the matching bin
             if (list_mode) {
                 if (tid == 0) sm.n_new = 0;
                 __syncthreads();
@@ -246,36 +479,28 @@ __global__ void __launch_bounds__(TK_T, 1) topk_kernel(TopkArgs a) {
             } else {
                 if (tid == 0) { sm.n_cand = 0; sm.overflow = 0; }
                 __syncthreads();
-                for (int64_t i0 = lo; i0 < hi; i0 += TK_U * TK_T) {
-                    uint32_t key[TK_U], d[TK_U];
-                    bool in[TK_U];
-                    bool mine = false;
+                for (int64_t base = lo; base < hi; base += (int64_t)TK_T * TK_V) {
+                    uint32_t key[TK_V];
+                    int64_t pos[TK_V / 4];
+                    load_keys(sc, base, hi, vec, key, pos);
 #pragma unroll
-                    for (int u = 0; u < TK_U; ++u) {
-                        const int64_t i = i0 + u * TK_T + tid;
-                        in[u] = i < hi;
-                        key[u] = in[u] ? score_key(__ldg(sc + i)) : 0u;
-                        if (prev_shift < 32) in[u] = in[u] && (key[u] >> prev_shift) == prefix;
-                        d[u] = (key[u] >> shift) & mask;
-                        mine = mine || (in[u] && d[u] >= bin);
-                    }
-                    if (!__any_sync(0xffffffffu, mine)) continue;  // nothing at or above the bin here
-#pragma unroll
-                    for (int u = 0; u < TK_U; ++u) {
-                        const int32_t idx = (int32_t)(i0 + u * TK_T + tid);
-                        const int s = warp_alloc(&sm.n_sel, in[u] && d[u] > bin);
-                        if (s >= 0 && s < TK_KMAX) { sm.skey[s] = key[u]; sm.sidx[s] = idx; }
-                        const int c = warp_alloc(&sm.n_cand, in[u] && d[u] == bin);
+                    for (int e = 0; e < TK_V; ++e) {
+                        const int64_t i = pos[e / 4] + (e & 3);
+                        const bool in = i < hi && (key[e] >> prev_shift) == prefix;
+                        const uint32_t d = (key[e] >> shift) & mask;
+                        const int s = warp_alloc(&sm.n_sel, in && d > bin);
+                        if (s >= 0 && s < TK_KMAX) { sm.skey[s] = key[e]; sm.sidx[s] = (int32_t)i; }
+                        const int c = warp_alloc(&sm.n_cand, in && d == bin);
                         if (c >= TK_CAP) sm.overflow = 1;
-                        else if (c >= 0) { sm.ckey[c] = key[u]; sm.cidx[c] = idx; }
+                        else if (c >= 0) { sm.ckey[c] = key[e]; sm.cidx[c] = (int32_t)i; }
                     }
                 }
             }
             __syncthreads();
-            prefix = (prev_shift < 32 ? (prefix << widths[p]) : 0u) | bin;
+            prefix = (prefix << widths[p]) | bin;
             prev_shift = shift;
         }
-        // prefix == tau (full key); `need` ties at tau remain to be taken.
+        // prefix == tau (full key); `need` ties at tau remain to be taken, lowest index first.
         const uint32_t tau = prefix;
         const bool list_mode = !sm.overflow;
         if (!list_mode) {
@@ -292,10 +517,10 @@ __global__ void __launch_bounds__(TK_T, 1) topk_kernel(TopkArgs a) {
         }
         __syncthreads();
         const uint32_t c_r = sm.cnt;
-        if (tid == 0) sm.xchg[0] = c_r;
+        if (tid == 0) sm.xchg[2] = c_r;
         cluster_sync();
         uint32_t before = 0;
-        for (uint32_t c = 0; c < rank; ++c) before += ld_dsmem_u32(mapa(smem_u32(&sm.xchg[0]), c));
+        for (uint32_t c = 0; c < rank; ++c) before += ld_dsmem_u32(mapa(smem_u32(&sm.xchg[2]), c));
         const uint32_t take = need > before ? min(need - before, c_r) : 0u;
         if (take > 0) {
             if (take == c_r && list_mode) {
@@ -304,7 +529,6 @@ __global__ void __launch_bounds__(TK_T, 1) topk_kernel(TopkArgs a) {
                     if (s < TK_KMAX) { sm.skey[s] = tau; sm.sidx[s] = sm.cidx[i]; }
                 }
             } else if (list_mode && c_r <= (uint32_t)TK_T) {
-                // rank of each tie among this CTA's ties by index; keep the `take` lowest
                 if (tid < (int)c_r) {
                     const int32_t my = sm.cidx[tid];
                     uint32_t rnk = 0;
@@ -348,16 +572,16 @@ __global__ void __launch_bounds__(TK_T, 1) topk_kernel(TopkArgs a) {
         __syncthreads();
     }
 
-    // ---- gather the cluster's selections into CTA 0
+    // ---- gather the cluster's winners into CTA 0 (cluster-wide path)
     const uint32_t n_mine = (uint32_t)min(sm.n_sel, TK_KMAX);
     if (tid == 0) {
-        sm.xchg[1] = n_mine;
+        sm.xchg[3] = n_mine;
         if (sm.n_sel > TK_KMAX) raise_status(a.status, CSA_ERR_DEVICE_BOUNDS);
     }
     cluster_sync();
     uint32_t off = 0, total = 0;
     for (uint32_t c = 0; c < TK_CL; ++c) {
-        const uint32_t v = ld_dsmem_u32(mapa(smem_u32(&sm.xchg[1]), c));
+        const uint32_t v = ld_dsmem_u32(mapa(smem_u32(&sm.xchg[3]), c));
         if (c < rank) off += v;
         total += v;
     }
@@ -369,41 +593,7 @@ __global__ void __launch_bounds__(TK_T, 1) topk_kernel(TopkArgs a) {
     }
     cluster_sync();
     if (rank != 0) return;
-
-    // ---- CTA 0: bitonic sort of the winners by (key desc, index asc)
-    if (total > (uint32_t)TK_KMAX) total = TK_KMAX;
-    int n2 = 1;
-    while (n2 < (int)total) n2 <<= 1;
-    for (int i = (int)total + tid; i < n2; i += TK_T) {
-        sm.okey[i] = 0u;
-        sm.oidx[i] = 0x7FFFFFFF;
-    }
-    __syncthreads();
-    for (int size = 2; size <= n2; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int i = tid; i < n2; i += TK_T) {
-                const int j = i ^ stride;
-                if (j > i) {
-                    const uint32_t ki = sm.okey[i], kj = sm.okey[j];
-                    const int32_t ii = sm.oidx[i], ij = sm.oidx[j];
-                    const bool first_half = (i & size) == 0;  // this block is sorted "greater first"
-                    const bool swap = first_half ? kv_greater(kj, ij, ki, ii) : kv_greater(ki, ii, kj, ij);
-                    if (swap) {
-                        sm.okey[i] = kj; sm.oidx[i] = ij;
-                        sm.okey[j] = ki; sm.oidx[j] = ii;
-                    }
-                }
-            }
-            __syncthreads();
-        }
-    }
-    int32_t* out = a.idx_out + (int64_t)b * k;
-    uint32_t* kout = a.keys_out ? a.keys_out + (int64_t)b * k : nullptr;
-    for (int i = tid; i < k; i += TK_T) {
-        const bool v = i < (int)total;
-        out[i] = v ? sm.oidx[i] : -1;
-        if (kout) kout[i] = v ? sm.okey[i] : 0u;
-    }
+    sort_and_write(sm, total, k, out, kout);
 }
 
 cudaError_t launch_topk(const TopkLaunch& h, cudaStream_t s, bool pdl) {
