@@ -243,35 +243,41 @@ __global__ void __launch_bounds__(AT_T, 1) attn_kernel(AttnArgs a) {
         if (!mbar_wait(bar_o, (uint32_t)((it - 1) & 1))) ok = false;
         tc_fence_after();
         if (!ok && tid == 0) raise_status(a.status, CSA_ERR_TIMEOUT);
-        // ---- epilogue: this thread's O row (256 columns of its half)
+        // ---- epilogue: this thread's O row (256 columns of its half) goes TMEM -> registers ->
+        // shared memory (padded rows: conflict-free) -> one bulk async copy per row to global.
+        // Every MMA has completed, so the Q/K tiles' shared memory is free for staging.
         const bool direct = a.S == 1;
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        const uint32_t row_bytes = direct ? AT_DH * 2 : AT_DH * 4;  // bf16 output / fp32 partial
+        const uint32_t pitch = row_bytes + 16;
+        const uint32_t srow = sbase + SM_Q + (uint32_t)h * pitch;
         for (int c = 0; c < AT_DH; c += 32) {
             uint32_t o[32];
             tc_ld32(t_o + lane_off + c, o);
             tc_wait_ld();
-            if (h < H) {
-                const int col = half * AT_DH + c;
-                if (direct) {
-                    uint16_t* dst = a.out + ((int64_t)b * H + h) * D + col;
+            if (direct) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 8) {
-                        uint4 v;
-                        v.x = pack_bf16x2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
-                        v.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
-                        v.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
-                        v.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
-                        *reinterpret_cast<uint4*>(dst + e) = v;
-                    }
-                } else {
-                    float* dst = a.part_o + (((int64_t)b * a.S + split) * H + h) * D + col;
-#pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        *reinterpret_cast<float4*>(dst + e) =
-                            make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]), __uint_as_float(o[e + 2]),
-                                        __uint_as_float(o[e + 3]));
+                for (int e = 0; e < 32; e += 8) {
+                    uint4 v;
+                    v.x = pack_bf16x2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
+                    v.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+                    v.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+                    v.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
+                    st_shared_v4(srow + (uint32_t)(c + e) * 2u, v);
                 }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; e += 4)
+                    st_shared_v4(srow + (uint32_t)(c + e) * 4u, make_uint4(o[e], o[e + 1], o[e + 2], o[e + 3]));
             }
+        }
+        fence_proxy_async_smem();
+        if (h < H) {
+            void* dst = direct ? static_cast<void*>(a.out + ((int64_t)b * H + h) * D + half * AT_DH)
+                               : static_cast<void*>(a.part_o + (((int64_t)b * a.S + split) * H + h) * D + half * AT_DH);
+            bulk_s2g(dst, srow, row_bytes);
+            bulk_commit();
+            bulk_wait_read0();  // the staging rows must stay valid until the copy has read them
         }
         tc_fence_before();
         __syncthreads();

@@ -58,6 +58,14 @@ CSA_DEV void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t ba
         "l"(src), "r"(bytes), "r"(bar)
         : "memory");
 }
+// Bulk (non-tensor) copy of this CTA's shared memory to global, tracked by bulk groups.
+CSA_DEV void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
+}
+CSA_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every committed bulk group of this thread has finished reading its source.
+CSA_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 CSA_DEV void cp_async16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }

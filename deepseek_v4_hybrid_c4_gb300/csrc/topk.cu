@@ -80,6 +80,29 @@ __device__ __forceinline__ int warp_alloc(int* counter, bool pred) {
     return pred ? base + __popc(m & ((1u << lane) - 1u)) : -1;
 }
 
+// Slots for this thread's ns winners and nc survivors: one atomic per list per warp.
+__device__ __forceinline__ void warp_reserve(int* cs, int* cc, uint32_t ns, uint32_t nc, int& bs, int& bc) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t v = (ns << 16) | nc;
+    uint32_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    const uint32_t tot = __shfl_sync(0xffffffffu, x, 31);
+    int b_s = 0, b_c = 0;
+    if (lane == 31) {
+        b_s = atomicAdd(cs, (int)(tot >> 16));
+        b_c = atomicAdd(cc, (int)(tot & 0xFFFFu));
+    }
+    b_s = __shfl_sync(0xffffffffu, b_s, 31);
+    b_c = __shfl_sync(0xffffffffu, b_c, 31);
+    const uint32_t ex = x - v;
+    bs = b_s + (int)(ex >> 16);
+    bc = b_c + (int)(ex & 0xFFFFu);
+}
+
 __device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t digit, bool active) {
     const unsigned m = __ballot_sync(0xffffffffu, active);
     if (!active) return;
@@ -192,25 +215,29 @@ __device__ void sort_and_write(TkSmem& sm, uint32_t total, int k, int32_t* out, 
     int n2 = 1;
     while (n2 < (int)total) n2 <<= 1;
     if (n2 <= 1024) {
-        // one element per thread, composite = key << 32 | (0x7FFFFFFF - idx): larger is better
-        const bool act = tid < n2;
+        // one element per thread of the first max(n2, 32) threads; composite = key << 32 |
+        // (0x7FFFFFFF - idx) so that larger is better.  Strides below a warp use shuffles,
+        // larger ones exchange through shared memory behind a barrier of just these warps.
+        const int nt = n2 < 32 ? 32 : n2;
         uint64_t v = 0;
-        if (act && tid < (int)total) v = ((uint64_t)sm.okey[tid] << 32) | (uint32_t)(0x7FFFFFFF - sm.oidx[tid]);
-        int buf = 0;
-        for (int size = 2; size <= n2; size <<= 1) {
-            for (int j = size >> 1; j > 0; j >>= 1) {
-                uint64_t pv;
-                if (j >= 32) {
-                    if (act) sm.sortbuf[buf][tid] = v;
-                    __syncthreads();
-                    pv = act ? sm.sortbuf[buf][tid ^ j] : 0;
-                    buf ^= 1;
-                } else {
-                    pv = __shfl_xor_sync(0xffffffffu, v, j);
+        if (tid < nt) {
+            if (tid < (int)total) v = ((uint64_t)sm.okey[tid] << 32) | (uint32_t)(0x7FFFFFFF - sm.oidx[tid]);
+            int buf = 0;
+            for (int size = 2; size <= n2; size <<= 1) {
+                for (int j = size >> 1; j > 0; j >>= 1) {
+                    uint64_t pv;
+                    if (j >= 32) {
+                        sm.sortbuf[buf][tid] = v;
+                        asm volatile("bar.sync 2, %0;" ::"r"(nt) : "memory");
+                        pv = sm.sortbuf[buf][tid ^ j];
+                        buf ^= 1;
+                    } else {
+                        pv = __shfl_xor_sync(0xffffffffu, v, j);
+                    }
+                    const bool up = (tid & size) == 0, lower = (tid & j) == 0;
+                    const uint64_t mx = v > pv ? v : pv, mn = v > pv ? pv : v;
+                    v = (up == lower) ? mx : mn;
                 }
-                const bool up = (tid & size) == 0, lower = (tid & j) == 0;
-                const uint64_t mx = v > pv ? v : pv, mn = v > pv ? pv : v;
-                if (act) v = (up == lower) ? mx : mn;
             }
         }
         if (tid < k) {
@@ -319,110 +346,35 @@ __global__ void __launch_bounds__(TK_T, 1) topk_kernel(TopkArgs a) {
             uint32_t key[TK_V];
             int64_t pos[TK_V / 4];
             load_keys(sc, base, hi, vec, key, pos);
-            bool mine = false;
+            uint32_t ns = 0, nc = 0;
 #pragma unroll
-            for (int e = 0; e < TK_V; ++e) mine = mine || (pos[e / 4] + (e & 3) < hi && (key[e] >> 21) >= b0);
-            if (!__any_sync(0xffffffffu, mine)) continue;
+            for (int e = 0; e < TK_V; ++e) {
+                const bool in = pos[e / 4] + (e & 3) < hi;
+                const uint32_t d = key[e] >> 21;
+                ns += (in && d > b0) ? 1u : 0u;
+                nc += (in && d == b0) ? 1u : 0u;
+            }
+            if (!__any_sync(0xffffffffu, (ns | nc) != 0)) continue;
+            int bs, bc;
+            warp_reserve(&sm.n_sel, &sm.n_cand, ns, nc, bs, bc);
 #pragma unroll
             for (int e = 0; e < TK_V; ++e) {
                 const int64_t i = pos[e / 4] + (e & 3);
                 const bool in = i < hi;
                 const uint32_t d = key[e] >> 21;
-                const int s = warp_alloc(&sm.n_sel, in && d > b0);
-                if (s >= 0 && s < TK_KMAX) { sm.skey[s] = key[e]; sm.sidx[s] = (int32_t)i; }
-                const int c = warp_alloc(&sm.n_cand, in && d == b0);
-                if (c >= TK_CAP) sm.overflow = 1;
-                else if (c >= 0) { sm.ckey[c] = key[e]; sm.cidx[c] = (int32_t)i; }
+                if (in && d > b0) {
+                    if (bs < TK_KMAX) { sm.skey[bs] = key[e]; sm.sidx[bs] = (int32_t)i; }
+                    ++bs;
+                } else if (in && d == b0) {
+                    if (bc < TK_CAP) { sm.ckey[bc] = key[e]; sm.cidx[bc] = (int32_t)i; }
+                    else sm.overflow = 1;
+                    ++bc;
+                }
             }
         }
         __syncthreads();
-        if (tid == 0) {
-            sm.xchg[0] = (uint32_t)sm.n_sel;
-            sm.xchg[1] = sm.overflow ? 0xFFFFFFFFu : (uint32_t)sm.n_cand;
-        }
-        cluster_sync();
-        uint32_t off_sel = 0, tot_sel = 0, off_cand = 0, tot_cand = 0;
-        bool any_over = false;
-        for (uint32_t c = 0; c < TK_CL; ++c) {
-            const uint32_t ns = ld_dsmem_u32(mapa(smem_u32(&sm.xchg[0]), c));
-            const uint32_t nc = ld_dsmem_u32(mapa(smem_u32(&sm.xchg[1]), c));
-            if (nc == 0xFFFFFFFFu) any_over = true;
-            if (c < rank) { off_sel += ns; off_cand += nc; }
-            tot_sel += ns;
-            tot_cand += nc;
-        }
-        if (!any_over && tot_cand <= (uint32_t)TK_GCAP) {
-            // ---- 3a. fast path: gather into CTA 0, finish there
-            for (int i = tid; i < sm.n_sel; i += TK_T) {
-                st_dsmem_u32(mapa(smem_u32(&sm.okey[off_sel + i]), 0), sm.skey[i]);
-                st_dsmem_u32(mapa(smem_u32(&sm.oidx[off_sel + i]), 0), (uint32_t)sm.sidx[i]);
-            }
-            for (int i = tid; i < sm.n_cand; i += TK_T) {
-                st_dsmem_u32(mapa(smem_u32(&sm.gkey[off_cand + i]), 0), sm.ckey[i]);
-                st_dsmem_u32(mapa(smem_u32(&sm.gidx[off_cand + i]), 0), (uint32_t)sm.cidx[i]);
-            }
-            cluster_sync();
-            if (rank != 0) return;
-            if (tid == 0) sm.n_out = (int)tot_sel;
-            __syncthreads();
-            int n_list = (int)tot_cand;
-            const int shifts[2] = {10, 0};
-            const int widths[2] = {11, 10};
-#pragma unroll
-            for (int p = 0; p < 2; ++p) {
-                const int shift = shifts[p];
-                const uint32_t mask = (1u << widths[p]) - 1u;
-                if ((uint32_t)n_list == need) break;  // every survivor is a winner
-                for (int i = tid; i < TK_BINS; i += TK_T) sm.hist[0][i] = 0;
-                __syncthreads();
-                for (int i0 = 0; i0 < n_list; i0 += TK_T) {
-                    const int i = i0 + tid;
-                    const bool in = i < n_list;
-                    hist_add(sm.hist[0], in ? (sm.gkey[i] >> shift) & mask : 0u, in);
-                }
-                __syncthreads();
-                find_bin(sm, HIST_LOCAL, nullptr, 0, 1 << widths[p], need);
-                const uint32_t bin = sm.bin;
-                need -= sm.above;
-                if (tid == 0) sm.n_new = 0;
-                __syncthreads();
-                for (int i0 = 0; i0 < n_list; i0 += TK_T) {
-                    const int i = i0 + tid;
-                    const bool in = i < n_list;
-                    const uint32_t key = in ? sm.gkey[i] : 0u;
-                    const int32_t idx = in ? sm.gidx[i] : 0;
-                    __syncthreads();  // chunk read by everyone before it is overwritten
-                    const uint32_t d = (key >> shift) & mask;
-                    const int s = warp_alloc(&sm.n_out, in && d > bin);
-                    if (s >= 0 && s < TK_KMAX) { sm.okey[s] = key; sm.oidx[s] = idx; }
-                    const int c = warp_alloc(&sm.n_new, in && d == bin);
-                    if (c >= 0) { sm.gkey[c] = key; sm.gidx[c] = idx; }
-                }
-                __syncthreads();
-                n_list = sm.n_new;
-            }
-            // survivors now share one key (or all of them are winners): keep the `need` lowest indices
-            if ((uint32_t)n_list == need) {
-                for (int i = tid; i < n_list; i += TK_T) {
-                    const int s = atomicAdd(&sm.n_out, 1);
-                    if (s < TK_KMAX) { sm.okey[s] = sm.gkey[i]; sm.oidx[s] = sm.gidx[i]; }
-                }
-            } else {
-                for (int i = tid; i < n_list; i += TK_T) {
-                    const int32_t my = sm.gidx[i];
-                    uint32_t rnk = 0;
-                    for (int j = 0; j < n_list; ++j) rnk += sm.gidx[j] < my ? 1u : 0u;
-                    if (rnk < need) {
-                        const int s = atomicAdd(&sm.n_out, 1);
-                        if (s < TK_KMAX) { sm.okey[s] = sm.gkey[i]; sm.oidx[s] = my; }
-                    }
-                }
-            }
-            __syncthreads();
-            sort_and_write(sm, (uint32_t)min(sm.n_out, k), k, out, kout);
-            return;
-        }
-        // ---- 3b. cluster-wide refinement (many survivors)
+        // ---- 3. digits bits 20..10 and 9..0, refined across the cluster.  After the first of
+        //      them the survivors normally fit CTA 0, which then finishes alone.
         uint32_t prefix = b0;
         int prev_shift = 21;
         const int shifts[2] = {10, 0};
@@ -499,6 +451,81 @@ __global__ void __launch_bounds__(TK_T, 1) topk_kernel(TopkArgs a) {
             __syncthreads();
             prefix = (prefix << widths[p]) | bin;
             prev_shift = shift;
+            if (p != 0) continue;
+            // ---- exchange the counts; fast finish in CTA 0 when the survivors fit
+            if (tid == 0) {
+                sm.xchg[0] = (uint32_t)sm.n_sel;
+                sm.xchg[1] = sm.overflow ? 0xFFFFFFFFu : (uint32_t)sm.n_cand;
+            }
+            cluster_sync();
+            uint32_t off_sel = 0, tot_sel = 0, off_cand = 0, tot_cand = 0;
+            bool any_over = false;
+            for (uint32_t c = 0; c < TK_CL; ++c) {
+                const uint32_t ns = ld_dsmem_u32(mapa(smem_u32(&sm.xchg[0]), c));
+                const uint32_t nc = ld_dsmem_u32(mapa(smem_u32(&sm.xchg[1]), c));
+                if (nc == 0xFFFFFFFFu) any_over = true;
+                if (c < rank) { off_sel += ns; off_cand += nc; }
+                tot_sel += ns;
+                tot_cand += nc;
+            }
+            if (any_over || tot_cand > (uint32_t)TK_GCAP) continue;  // keep refining across the cluster
+            for (int i = tid; i < sm.n_sel; i += TK_T) {
+                st_dsmem_u32(mapa(smem_u32(&sm.okey[off_sel + i]), 0), sm.skey[i]);
+                st_dsmem_u32(mapa(smem_u32(&sm.oidx[off_sel + i]), 0), (uint32_t)sm.sidx[i]);
+            }
+            for (int i = tid; i < sm.n_cand; i += TK_T) {
+                st_dsmem_u32(mapa(smem_u32(&sm.gkey[off_cand + i]), 0), sm.ckey[i]);
+                st_dsmem_u32(mapa(smem_u32(&sm.gidx[off_cand + i]), 0), (uint32_t)sm.cidx[i]);
+            }
+            cluster_sync();
+            if (rank != 0) return;
+            if (tid == 0) sm.n_out = (int)tot_sel;
+            __syncthreads();
+            int n_list2 = (int)tot_cand;
+            if (n_list2 > TK_T && (uint32_t)n_list2 != need) {
+                // last digit (bits 9..0) locally, then the ties
+                for (int i = tid; i < TK_BINS; i += TK_T) sm.hist[0][i] = 0;
+                __syncthreads();
+                for (int i0 = 0; i0 < n_list2; i0 += TK_T) {
+                    const int i = i0 + tid;
+                    const bool in = i < n_list2;
+                    hist_add(sm.hist[0], in ? (sm.gkey[i] & 1023u) : 0u, in);
+                }
+                __syncthreads();
+                find_bin(sm, HIST_LOCAL, nullptr, 0, 1024, need);
+                const uint32_t lbin = sm.bin;
+                need -= sm.above;
+                if (tid == 0) sm.n_new = 0;
+                __syncthreads();
+                for (int i0 = 0; i0 < n_list2; i0 += TK_T) {
+                    const int i = i0 + tid;
+                    const bool in = i < n_list2;
+                    const uint32_t key = in ? sm.gkey[i] : 0u;
+                    const int32_t idx = in ? sm.gidx[i] : 0;
+                    __syncthreads();
+                    const uint32_t d = key & 1023u;
+                    const int so = warp_alloc(&sm.n_out, in && d > lbin);
+                    if (so >= 0 && so < TK_KMAX) { sm.okey[so] = key; sm.oidx[so] = idx; }
+                    const int c = warp_alloc(&sm.n_new, in && d == lbin);
+                    if (c >= 0) { sm.gkey[c] = key; sm.gidx[c] = idx; }
+                }
+                __syncthreads();
+                n_list2 = sm.n_new;
+            }
+            // the `need` best survivors by (key desc, index asc): rank each against all
+            for (int i = tid; i < n_list2; i += TK_T) {
+                const uint32_t myk = sm.gkey[i];
+                const int32_t myi = sm.gidx[i];
+                uint32_t rnk = 0;
+                for (int j = 0; j < n_list2; ++j) rnk += kv_greater(sm.gkey[j], sm.gidx[j], myk, myi) ? 1u : 0u;
+                if (rnk < need) {
+                    const int so = atomicAdd(&sm.n_out, 1);
+                    if (so < TK_KMAX) { sm.okey[so] = myk; sm.oidx[so] = myi; }
+                }
+            }
+            __syncthreads();
+            sort_and_write(sm, (uint32_t)min(sm.n_out, k), k, out, kout);
+            return;
         }
         // prefix == tau (full key); `need` ties at tau remain to be taken, lowest index first.
         const uint32_t tau = prefix;
