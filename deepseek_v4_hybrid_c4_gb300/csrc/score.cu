@@ -6,22 +6,28 @@
 //   S1[t] = P[t] + P[t+8]; S2 = S1[t] + S1[t+4]; S3 = S2[t] + S2[t+2]; dot = S3[0] + S3[1]
 //   acc = fma(w_h, ReLU(dot_h), acc) for h = 0..Hi-1, from acc = 0
 //
-// Layout: one candidate row per lane, so the whole fixed-order tree runs inside a
-// lane with no shuffles.  A lane walks the chunk pairs (a, a+8) in bit-reversed
-// order 0,4,2,6,1,5,3,7: each pair yields S1[a] with packed fma.rn.f32x2 (the two
-// halves are the P[a] and P[a+8] chains -- two IEEE fmas per instruction), and the
-// order makes every S2/S3 operand ready exactly when the tree needs it.  The
-// index query is staged per warp in shared memory as {q[8a+i], q[8a+64+i]} pairs
-// and read as broadcasts.
+// Layout: a warp takes a step of 32 rows (two 16-row units).  Lane (c, r), c = lane / 16,
+// r = lane % 16, holds rows r and r+16 and the chunk pairs (a, a+8) for a = {0,4,2,6} + c,
+// in that order: each pair yields S1[a] with packed fma.rn.f32x2 (the two halves are the
+// P[a] and P[a+8] chains -- two IEEE fmas per instruction), and the order makes every S2
+// and S3 operand ready when the tree needs it.  Half c ends with S3[c]; one shuffle
+// across the halves gives dot = S3[0] + S3[1] (IEEE addition is commutative, so both
+// halves agree bit for bit), and lane l finishes row l.  The index query is staged in
+// shared memory as {q[8a+i], q[8a+64+i]} pairs, two heads per 16-byte load, and each load
+// feeds both of the lane's rows.
 //
-// Memory path: a producer lane streams 16-row units with TMA tensor copies
-// (cp.async.bulk.tensor, 128-byte swizzle) into a ring of shared-memory stages
-// tracked by mbarriers.  The swizzle puts 16-byte chunk c of row r at position
-// c ^ (r & 7), so 32 lanes reading the same logical chunk of 32 different rows hit
-// distinct banks.  A consumer warp takes two units (32 rows) at a time.
-// Persistent grid, two CTAs per SM.
+// Memory path: each warp owns two 32-row slots in shared memory and fills them with TMA
+// tensor copies (cp.async.bulk.tensor, 128-byte swizzle), two units per step, completing
+// on the slot's mbarrier; it refills a slot as soon as every lane has read it, so a step
+// is always in flight behind the one being computed.  Page-table lookups are batched 16
+// steps ahead.  The swizzle puts 16-byte chunk c of row r at position c ^ (r & 7), so the
+// lanes' reads of one logical chunk of 16 rows spread over the banks.
 //
-// Optional fused epilogue: a per-warp (16-bit) histogram of the top 11 bits of each score's
+// Scheduling: CTAs of 6 warps, two per SM, one wave.  The work is cut into CTA-steps of 6
+// consecutive steps of one request (warp j takes step j), so all warps of a CTA work on the
+// same request at a time and share one staged query and one histogram.
+//
+// Optional fused epilogue: a per-CTA histogram of the top 11 bits of each score's
 // order-preserving key (the first digit of the top-k radix select), flushed per
 // request into a global [B][2048] histogram.
 #include <cuda.h>
@@ -34,12 +40,12 @@
 
 namespace csa {
 
-constexpr int SC_CONSUMERS = 4;              // consumer warps; each takes 32 rows (2 units) per step
-constexpr int SC_THREADS = (SC_CONSUMERS + 1) * 32;
+constexpr int SC_WARPS = 6;                  // warps per CTA; each takes 32 rows (2 units) per CTA-step
+constexpr int SC_THREADS = SC_WARPS * 32;
 constexpr int SC_UNIT = 16;                  // rows per unit (one TMA box height)
-constexpr int SC_SUPER = 32;                 // rows per consumer-warp step
-constexpr int SC_STAGES = 18;                // units in flight per CTA
-constexpr int SC_STAGE_BYTES = SC_UNIT * 256;  // bf16 unit (fp8 uses half)
+constexpr int SC_SUPER = 32;                 // rows per warp step
+constexpr int SC_STAGE_BYTES = SC_UNIT * 256;  // one unit (bf16; fp8 uses half)
+constexpr int SC_SLOT_BYTES = 2 * SC_STAGE_BYTES;  // one step
 
 struct ScoreArgs {
     const uint16_t* q_idx;
@@ -59,23 +65,27 @@ struct ScoreArgs {
     int32_t* status;
 };
 
-// Walks the concatenated space of 32-row steps of the batch (no step straddles two
-// requests): after seek(w), step w belongs to request b, with G candidates.
-struct StepCursor {
+// Walks the concatenated CTA-steps of the batch.  Request b has steps = ceil(G_b / 32)
+// steps of 32 rows, grouped into ceil(steps / SC_WARPS) CTA-steps of SC_WARPS consecutive
+// steps (warp j of the CTA takes step j), so a CTA-step never straddles two requests.
+// After seek(m), CTA-step m belongs to request b.  Calls must come with non-decreasing m.
+struct CtaStepCursor {
     int b = -1;
-    int64_t base = 0, steps = 0, G = 0;
+    int64_t base = 0, csteps = 0, steps = 0, G = 0;
     __device__ void load(const ScoreArgs& a) {
         G = a.n_tokens ? __ldg(a.n_tokens + b) / a.ratio : a.G;
         steps = (G + SC_SUPER - 1) / SC_SUPER;
+        csteps = (steps + SC_WARPS - 1) / SC_WARPS;
     }
-    __device__ bool seek(const ScoreArgs& a, int64_t w) {
+    __device__ bool seek(const ScoreArgs& a, int64_t m) {
         if (b < 0) {
             if (a.B <= 0) return false;
             b = 0;
             load(a);
         }
-        while (w >= base + steps) {
-            base += steps;
+        if (b >= a.B) return false;  // stays past the end once there
+        while (m >= base + csteps) {
+            base += csteps;
             if (++b >= a.B) return false;
             load(a);
         }
@@ -152,140 +162,130 @@ __device__ __forceinline__ void load_pair(const uint8_t* stage, int r, int a, fl
 }
 
 template <int HI, bool FP8>
-__global__ void __launch_bounds__(SC_THREADS, 2) score_kernel(const __grid_constant__ CUtensorMap kmap, ScoreArgs a) {
-    constexpr int UB = FP8 ? SC_UNIT * 128 : SC_UNIT * 256;   // bytes per unit
-    constexpr int QF4 = 8 * 8 * (HI / 2);                      // float4 entries of one warp's staged query
+__global__ void __launch_bounds__(SC_THREADS, HI >= 16 ? 1 : 2)
+    score_kernel(const __grid_constant__ CUtensorMap kmap, ScoreArgs a) {
+    constexpr int UB = FP8 ? SC_UNIT * 128 : SC_UNIT * 256;   // bytes per 16-row unit
+    constexpr int QF4 = 8 * 8 * (HI / 2);                      // float4 entries of the staged query
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* stages = smem;                                                     // SC_STAGES x 4 KiB, 1 KiB aligned
-    float4* qs_all = reinterpret_cast<float4*>(smem + SC_STAGES * SC_STAGE_BYTES);  // [warp][QF4]
-    float* ws_all = reinterpret_cast<float*>(qs_all + SC_CONSUMERS * QF4);        // [warp][16]
-    uint64_t* full = reinterpret_cast<uint64_t*>(ws_all + SC_CONSUMERS * 16);
-    uint64_t* empty = full + SC_STAGES;
-    int* meta = reinterpret_cast<int*>(empty + SC_STAGES);                     // page valid flag per stage
-    uint16_t* hist_all = reinterpret_cast<uint16_t*>(meta + SC_STAGES + 4);     // [warp][kHistBins], 16-bit
-
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // per warp: two 32-row slots; per CTA: the staged query, the weights, the histogram
+    uint8_t* slots = smem + warp * (2 * SC_SLOT_BYTES);
+    float4* qs = reinterpret_cast<float4*>(smem + SC_WARPS * 2 * SC_SLOT_BYTES);
+    float* wsm = reinterpret_cast<float*>(smem + SC_WARPS * 2 * SC_SLOT_BYTES + QF4 * 16);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + SC_WARPS * 2 * SC_SLOT_BYTES + QF4 * 16 + 64) + warp * 2;
+    uint32_t* hist = reinterpret_cast<uint32_t*>(smem + SC_WARPS * 2 * SC_SLOT_BYTES + QF4 * 16 + 64 +
+                                                 SC_WARPS * 16);
+    const uint32_t qs_addr = smem_u32(qs);
+
     pdl_launch_dependents();  // the top-k kernel may be scheduled now; it waits for this grid to finish
     if (a.hist)
-        for (int i = threadIdx.x; i < SC_CONSUMERS * kHistBins; i += SC_THREADS) hist_all[i] = 0;
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < SC_STAGES; ++s) {
-            mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&empty[s]), 1);
-        }
+        for (int i = threadIdx.x; i < kHistBins; i += SC_THREADS) hist[i] = 0;
+    if (lane == 0) {
+        mbar_init(smem_u32(&full[0]), 2);
+        mbar_init(smem_u32(&full[1]), 2);
         fence_mbar_init();
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kmap)) : "memory");
     }
-    __syncthreads();
+    __syncwarp();
 
-    if (warp == SC_CONSUMERS) {
-        // ---------------- producer warp: the 32 lanes look up the pages of 32 upcoming units
-        // at once (independent loads), then lane 0 issues their TMA copies in order.
-        if (lane == 0)
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kmap)) : "memory");
-        StepCursor cur;  // each lane walks the same step sequence (monotone seeks)
-        bool stop = false;
-        for (int64_t r = 0; !stop; ++r) {
-            // unit r*32 + lane of this CTA = half (lane & 1) of this CTA's step r*16 + lane/2
-            const int64_t i = r * 16 + (lane >> 1);
-            const int64_t w = blockIdx.x + i * gridDim.x;
-            int kind = 0;      // 0: past the end, 1: copy, 2: nothing to copy (beyond G / bad page)
-            int slot = 0, page = 0;
-            if (cur.seek(a, w)) {
-                const int64_t gr = (w - cur.base) * SC_SUPER + (lane & 1) * SC_UNIT;
-                kind = 2;
-                if (gr < cur.G) {
-                    const int64_t lp = gr / a.rpp;
-                    slot = (int)(gr - lp * a.rpp);
-                    int64_t pp = lp;
-                    if (a.pt) pp = __ldg(a.pt + (int64_t)cur.b * a.pt_stride + lp);
-                    if (pp >= 0 && pp < a.n_pages) {
-                        kind = 1;
-                        page = (int)pp;
-                    } else {
-                        raise_status(a.status, CSA_ERR_DEVICE_BOUNDS);
-                    }
+    // This CTA's CTA-steps: m = blockIdx.x + k * gridDim.x for k = 0, 1, ...; in each, warp j
+    // takes step j.  Page lookups run a window of 16 CTA-steps at a time: lane l holds unit
+    // (l & 1) of this warp's step in CTA-step k0 + (l >> 1), all 32 loads in flight together.
+    // Two register sets alternate (even / odd windows) and the next window is looked up as the
+    // current one starts, so the page-table latency stays off the copy path.
+    CtaStepCursor lc;  // this lane's lookup cursor
+    int wk[2] = {0, 0}, ws[2] = {0, 0}, wp[2] = {0, 0};  // per set: kind (0 past the end, 1 copy,
+                                                          // 2 nothing to copy), row in page, page
+    auto lookup_window = [&](int64_t k0, int& kind, int& slot, int& page) {
+        const int64_t k = k0 + (lane >> 1);
+        kind = 0;
+        slot = 0;
+        page = 0;
+        const int64_t m = blockIdx.x + k * gridDim.x;
+        if (lc.seek(a, m)) {
+            const int64_t gr = ((m - lc.base) * SC_WARPS + warp) * SC_SUPER + (lane & 1) * SC_UNIT;
+            kind = 2;
+            if (gr < lc.G) {
+                const int64_t lp = gr / a.rpp;
+                slot = (int)(gr - lp * a.rpp);
+                int64_t pp = lp;
+                if (a.pt) pp = __ldg(a.pt + (int64_t)lc.b * a.pt_stride + lp);
+                if (pp >= 0 && pp < a.n_pages) {
+                    kind = 1;
+                    page = (int)pp;
+                } else {
+                    raise_status(a.status, CSA_ERR_DEVICE_BOUNDS);
                 }
-            }
-            for (int j = 0; j < 32; ++j) {
-                const int kj = __shfl_sync(0xffffffffu, kind, j);
-                const int sj = __shfl_sync(0xffffffffu, slot, j);
-                const int pj = __shfl_sync(0xffffffffu, page, j);
-                if (kj == 0) {
-                    stop = true;
-                    break;
-                }
-                if (lane == 0) {
-                    const int64_t u = r * 32 + j;  // units issued by this CTA so far
-                    const int s = (int)(u % SC_STAGES);
-                    if (u >= SC_STAGES && !mbar_wait(smem_u32(&empty[s]), (uint32_t)(((u / SC_STAGES) - 1) & 1))) {
-                        raise_status(a.status, CSA_ERR_TIMEOUT);
-                        stop = true;
-                    } else {
-                        const uint32_t fb = smem_u32(&full[s]);
-                        if (kj == 1) {
-                            meta[s] = 1;
-                            mbar_arrive_expect_tx(fb, (uint32_t)UB);
-                            const uint32_t dst = smem_u32(stages + s * SC_STAGE_BYTES);
-                            if constexpr (FP8) {
-                                tma_load_3d(dst, &kmap, 0, sj, pj, fb);
-                            } else {
-                                tma_load_3d(dst, &kmap, 0, sj, pj, fb);
-                                tma_load_3d(dst + 2048u, &kmap, 64, sj, pj, fb);
-                            }
-                        } else {
-                            meta[s] = 0;
-                            mbar_arrive(fb);
-                        }
-                    }
-                }
-                stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
-                if (stop) break;
             }
         }
-        return;
-    }
+    };
+    // Fetch this warp's step of CTA-step k into slot k & 1: lanes 2i, 2i+1 (i = k mod 16) hold
+    // its two units.
+    auto issue = [&](int64_t k) {
+        const int set = (int)((k >> 4) & 1);
+        const int kind = set ? wk[1] : wk[0];
+        if ((lane >> 1) == (int)(k & 15) && kind != 0) {
+            const int sl = (int)(k & 1);
+            const uint32_t fb = smem_u32(&full[sl]);
+            if (kind == 1) {
+                const int slot = set ? ws[1] : ws[0], page = set ? wp[1] : wp[0];
+                mbar_arrive_expect_tx(fb, (uint32_t)UB);
+                const uint32_t dst = smem_u32(slots + sl * SC_SLOT_BYTES + (lane & 1) * SC_STAGE_BYTES);
+                if constexpr (FP8) {
+                    tma_load_3d(dst, &kmap, 0, slot, page, fb);
+                } else {
+                    tma_load_3d(dst, &kmap, 0, slot, page, fb);
+                    tma_load_3d(dst + 2048u, &kmap, 64, slot, page, fb);
+                }
+            } else {
+                mbar_arrive(fb);
+            }
+        }
+    };
+    lookup_window(0, wk[0], ws[0], wp[0]);
+    lookup_window(16, wk[1], ws[1], wp[1]);
+    issue(0);
+    issue(1);
 
-    // ---------------- consumers
-    float4* qs = qs_all + warp * QF4;
-    const uint32_t qs_addr = smem_u32(qs);
-    float* wsm = ws_all + warp * 16;
-    uint16_t* hist = hist_all + warp * kHistBins;
-    int hist_rows = 0;  // rows counted since the last flush (16-bit counters: flush before they can wrap)
-    const int r = lane & 15;        // row within its unit
-    const int hu = lane >> 4;       // which of the step's two units
     int qb = -1;
-    StepCursor cur;
-    int64_t u = 0;
+    bool dead = false;    // a copy never arrived: stop waiting and fetching, keep the CTA barriers
     bool waited = false;
-    auto flush = [&](int req) {
+    auto flush = [&](int req) {  // whole CTA
         if (!waited) {  // the global histogram is cleared by the preceding kernel of the step
             pdl_wait();
             waited = true;
         }
-        for (int bin = lane; bin < kHistBins; bin += 32) {
+        for (int bin = threadIdx.x; bin < kHistBins; bin += SC_THREADS) {
             const uint32_t c = hist[bin];
             if (c) {
                 atomicAdd(a.hist + (int64_t)req * kHistBins + bin, c);
                 hist[bin] = 0;
             }
         }
-        hist_rows = 0;
-        __syncwarp();
     };
-    for (int64_t i = 0;; ++i) {
-        const int64_t w = blockIdx.x + i * gridDim.x;
-        if (!cur.seek(a, w)) break;
-        const int64_t my_u = u;
-        u += 2;
-        if ((i % SC_CONSUMERS) != warp) continue;   // steps go round-robin over the consumer warps
-        if (cur.b != qb) {
+    const int r = lane & 15;        // row within its unit
+    const int hu = lane >> 4;       // chunk half (c)
+    CtaStepCursor cur;
+    for (int64_t k = 0;; ++k) {
+        const int64_t m = blockIdx.x + k * gridDim.x;
+        if (!cur.seek(a, m)) break;  // the same for every warp of the CTA
+        const int sl = (int)(k & 1);
+        if ((k & 15) == 0 && k > 0) {  // window k/16 starts: look up window k/16 + 1 into the freed set
+            if ((k >> 4) & 1) lookup_window(k + 16, wk[0], ws[0], wp[0]);
+            else lookup_window(k + 16, wk[1], ws[1], wp[1]);
+        }
+        if (cur.b != qb) {  // CTA-uniform: restage the query, flush the previous request's histogram
+            __syncthreads();
             if (a.hist && qb >= 0) flush(qb);
             qb = cur.b;
-            // stage this request's query as {q_h[8a+i], q_h[8a+64+i]} pairs, two heads per float4
+            // {q_h[8aa+i], q_h[8aa+64+i]} pairs of two heads per float4, at index
+            // ((nn * 8 + i) * HI/2 + head pair) * 2 + c for chunk pair aa = {0,4,2,6}[nn] + c
             const uint16_t* qp = a.q_idx + (int64_t)qb * a.Hi * DI;
-            for (int e = lane; e < QF4; e += 32) {
-                const int hp = e % (HI / 2), ii = (e / (HI / 2)) % 8, aa = e / (HI / 2) / 8;
+            for (int e = threadIdx.x; e < QF4; e += SC_THREADS) {
+                const int c = e & 1, rest = e >> 1;
+                const int hp = rest % (HI / 2), ii = (rest / (HI / 2)) % 8, nn = rest / (HI / 2) / 8;
+                const int aa = ((nn & 1) << 2) | (nn & 2) | c;
                 const int h0 = 2 * hp, h1 = 2 * hp + 1, d = 8 * aa + ii;
                 float4 v;
                 v.x = h0 < a.Hi ? bf16lo(qp[h0 * DI + d]) : 0.f;
@@ -294,67 +294,80 @@ __global__ void __launch_bounds__(SC_THREADS, 2) score_kernel(const __grid_const
                 v.w = h1 < a.Hi ? bf16lo(qp[h1 * DI + d + 64]) : 0.f;
                 qs[e] = v;
             }
-            if (lane < HI) wsm[lane] = lane < a.Hi ? __ldg(a.w_h + (int64_t)qb * a.Hi + lane) : 0.f;
-            __syncwarp();
+            if (threadIdx.x < HI) wsm[threadIdx.x] = threadIdx.x < a.Hi ? __ldg(a.w_h + (int64_t)qb * a.Hi + threadIdx.x) : 0.f;
+            __syncthreads();
         }
-        const int sA = (int)(my_u % SC_STAGES), sB = (int)((my_u + 1) % SC_STAGES);
-        const bool okA = mbar_wait(smem_u32(&full[sA]), (uint32_t)((my_u / SC_STAGES) & 1));
-        const bool okB = mbar_wait(smem_u32(&full[sB]), (uint32_t)(((my_u + 1) / SC_STAGES) & 1));
-        if (!okA || !okB) {
+        const int64_t st = (m - cur.base) * SC_WARPS + warp;  // this warp's step within the request
+        const int kind_me = __shfl_sync(0xffffffffu, ((k >> 4) & 1) ? wk[1] : wk[0], 2 * (int)(k & 15) + hu);
+        if (!dead && !mbar_wait(smem_u32(&full[sl]), (uint32_t)((k >> 1) & 1))) {
             raise_status(a.status, CSA_ERR_TIMEOUT);
-            break;
+            dead = true;
         }
-        const int s = hu ? sB : sA;
-        const int64_t g = (w - cur.base) * SC_SUPER + hu * SC_UNIT + r;
-        const bool valid = g < cur.G && meta[s] != 0;
-        const uint8_t* stage = stages + s * SC_STAGE_BYTES;
-
-        float t1[HI], t2[HI], t3[HI], dot[HI];
+        if (dead) continue;
+        if (st >= cur.steps) {  // the request's last CTA-step has fewer steps than warps
+            issue(k + 2);
+            continue;
+        }
+        const int64_t g = st * SC_SUPER + lane;
+        const bool valid = g < cur.G && kind_me == 1;
+        // lane (c, r): rows r and r+16 of the step (units 0 and 1, in-unit row r), chunk pairs
+        // aa = {0,4,2,6} + c; the two halves meet at dot = S3[0] + S3[1]
+        const uint8_t* st0 = slots + sl * SC_SLOT_BYTES;
+        const uint8_t* st1 = st0 + SC_STAGE_BYTES;
+        float t1[2][HI], t2[2][HI], s3[2][HI];
 #pragma unroll
-        for (int n = 0; n < 8; ++n) {
-            const int aa = ((n & 1) << 2) | (n & 2) | ((n >> 2) & 1);  // 0,4,2,6,1,5,3,7
-            float kl[8], kh[8];
-            load_pair<FP8>(stage, r, aa, kl, kh);
-            uint64_t acc[HI];
+        for (int nn = 0; nn < 4; ++nn) {
+            const int aa = ((nn & 1) << 2) | (nn & 2) | hu;
+            float kl0[8], kh0[8], kl1[8], kh1[8];
+            load_pair<FP8>(st0, r, aa, kl0, kh0);
+            load_pair<FP8>(st1, r, aa, kl1, kh1);
+            uint64_t acc0[HI], acc1[HI];
 #pragma unroll
             for (int ii = 0; ii < 8; ++ii) {
-                const uint64_t kk = pk2(kl[ii], kh[ii]);
-                const uint32_t qa = qs_addr + (uint32_t)((aa * 8 + ii) * (HI / 2)) * 16u;
+                const uint64_t kk0 = pk2(kl0[ii], kh0[ii]);
+                const uint64_t kk1 = pk2(kl1[ii], kh1[ii]);
+                const uint32_t qa = qs_addr + (uint32_t)(((nn * 8 + ii) * (HI / 2)) * 2 + hu) * 16u;
 #pragma unroll
                 for (int hp = 0; hp < HI / 2; ++hp) {
                     uint64_t q0, q1;
-                    ld_qpairs(qa + hp * 16u, q0, q1);
+                    ld_qpairs(qa + hp * 32u, q0, q1);
                     if (ii == 0) {
-                        acc[2 * hp] = mul2(q0, kk);
-                        acc[2 * hp + 1] = mul2(q1, kk);
+                        acc0[2 * hp] = mul2(q0, kk0);
+                        acc0[2 * hp + 1] = mul2(q1, kk0);
+                        acc1[2 * hp] = mul2(q0, kk1);
+                        acc1[2 * hp + 1] = mul2(q1, kk1);
                     } else {
-                        acc[2 * hp] = fma2(q0, kk, acc[2 * hp]);
-                        acc[2 * hp + 1] = fma2(q1, kk, acc[2 * hp + 1]);
+                        acc0[2 * hp] = fma2(q0, kk0, acc0[2 * hp]);
+                        acc0[2 * hp + 1] = fma2(q1, kk0, acc0[2 * hp + 1]);
+                        acc1[2 * hp] = fma2(q0, kk1, acc1[2 * hp]);
+                        acc1[2 * hp + 1] = fma2(q1, kk1, acc1[2 * hp + 1]);
                     }
                 }
             }
 #pragma unroll
             for (int h = 0; h < HI; ++h) {
-                const float s1 = lo2(acc[h]) + hi2(acc[h]);       // S1[aa] = P[aa] + P[aa+8]
-                if ((n & 1) == 0) {
-                    t1[h] = s1;
+                const float u0 = lo2(acc0[h]) + hi2(acc0[h]);   // S1[aa] = P[aa] + P[aa+8]
+                const float u1 = lo2(acc1[h]) + hi2(acc1[h]);
+                if (nn == 0 || nn == 2) {
+                    t1[0][h] = u0;
+                    t1[1][h] = u1;
+                } else if (nn == 1) {
+                    t2[0][h] = t1[0][h] + u0;                    // S2 = S1[a] + S1[a+4]
+                    t2[1][h] = t1[1][h] + u1;
                 } else {
-                    const float s2 = t1[h] + s1;                   // S2[aa-4] = S1[aa-4] + S1[aa]
-                    if ((n & 3) == 1) {
-                        t2[h] = s2;
-                    } else {
-                        const float s3 = t2[h] + s2;               // S3 = S2[t] + S2[t+2]
-                        if (n == 3) t3[h] = s3;
-                        else dot[h] = t3[h] + s3;                  // dot = S3[0] + S3[1]
-                    }
+                    s3[0][h] = t2[0][h] + (t1[0][h] + u0);      // S3 = S2[a] + S2[a+2]
+                    s3[1][h] = t2[1][h] + (t1[1][h] + u1);
                 }
             }
         }
-        // every lane has read its row: release both stages
+        // every lane has read the slot: refill it with the CTA-step after next
         __syncwarp();
-        if (lane == 0) {
-            mbar_arrive(smem_u32(&empty[sA]));
-            mbar_arrive(smem_u32(&empty[sB]));
+        issue(k + 2);
+        float dot[HI];
+#pragma unroll
+        for (int h = 0; h < HI; ++h) {
+            const float other = __shfl_xor_sync(0xffffffffu, hu ? s3[0][h] : s3[1][h], 16);
+            dot[h] = (hu ? s3[1][h] : s3[0][h]) + other;          // dot = S3[0] + S3[1]
         }
         float sc = 0.f;
 #pragma unroll
@@ -364,17 +377,17 @@ __global__ void __launch_bounds__(SC_THREADS, 2) score_kernel(const __grid_const
         if (a.hist) {
             const bool in = g < cur.G;
             const uint32_t dg = score_key(sc) >> 21;
-            const unsigned m = __ballot_sync(0xffffffffu, in);
+            const unsigned mk = __ballot_sync(0xffffffffu, in);
             if (in) {
-                const unsigned peers = __match_any_sync(m, dg);
-                if (lane == __ffs(peers) - 1) hist[dg] = (uint16_t)(hist[dg] + __popc(peers));  // warp-private
+                const unsigned peers = __match_any_sync(mk, dg);
+                if (lane == __ffs(peers) - 1) atomicAdd(&hist[dg], (uint32_t)__popc(peers));
             }
-            __syncwarp();
-            hist_rows += 32;
-            if (hist_rows >= 65536 - 64) flush(qb);
         }
     }
+    __syncthreads();
     if (a.hist && qb >= 0) flush(qb);
+    // Nothing is in flight here on a normal exit: the two CTA-steps looked up last lie past
+    // the end, so no copy was issued for them.
 }
 
 // ------------------------------------------------------------------ host side
@@ -415,9 +428,8 @@ template <int HI, bool FP8>
 static cudaError_t launch_score_t(const CUtensorMap& map, const ScoreArgs& a, int64_t total_steps_bound,
                                   cudaStream_t s, bool pdl) {
     constexpr int QF4 = 8 * 8 * (HI / 2);
-    constexpr size_t base = 1024 + (size_t)SC_STAGES * SC_STAGE_BYTES + SC_CONSUMERS * QF4 * 16 +
-                            SC_CONSUMERS * 16 * 4 + 2 * SC_STAGES * 8 + (SC_STAGES + 4) * 4;
-    constexpr size_t with_hist = base + (size_t)SC_CONSUMERS * kHistBins * 2;
+    constexpr size_t base = 1024 + (size_t)SC_WARPS * 2 * SC_SLOT_BYTES + (size_t)QF4 * 16 + 64 + SC_WARPS * 16;
+    constexpr size_t with_hist = base + (size_t)kHistBins * 4;
     const size_t smem = a.hist ? with_hist : base;
     static bool attr_set = false;
     if (!attr_set) {
@@ -432,7 +444,7 @@ static cudaError_t launch_score_t(const CUtensorMap& map, const ScoreArgs& a, in
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     }
-    int64_t grid = 2LL * sms;
+    int64_t grid = (HI >= 16 ? 1LL : 2LL) * sms;  // one wave of resident CTAs
     if (total_steps_bound < grid) grid = total_steps_bound < 1 ? 1 : total_steps_bound;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -474,7 +486,7 @@ cudaError_t launch_score(const ScoreLaunch& h, cudaStream_t s, bool pdl) {
     a.n_pages = n_pages;
     CUtensorMap map;
     if (!make_kmap(&map, h.kidx, h.fp8, rpp, n_pages)) return cudaErrorInvalidValue;
-    const int64_t steps = (int64_t)h.B * ((h.max_G + SC_SUPER - 1) / SC_SUPER);
+    const int64_t steps = (int64_t)h.B * (((h.max_G + SC_SUPER - 1) / SC_SUPER + SC_WARPS - 1) / SC_WARPS);
     const int hi = h.Hi <= 4 ? 4 : (h.Hi <= 8 ? 8 : 16);
     if (h.fp8) {
         if (hi == 4) return launch_score_t<4, true>(map, a, steps, s, pdl);
