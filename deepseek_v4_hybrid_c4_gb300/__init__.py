@@ -58,8 +58,10 @@ def lib() -> ctypes.CDLL:
         vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
         L.csa_compress.argtypes = [csa_paged, i64, i32, vp, vp, i64, i64, csa_paged, vp]
         L.csa_index_score.argtypes = [vp, vp, i32, csa_paged, i32, i64, vp, vp]
-        L.csa_topk.argtypes = [vp, i64, i32, vp, vp, vp]
-        L.csa_topk_batched.argtypes = [vp, vp, i32, i64, i32, vp, vp, vp]
+        L.csa_topk.argtypes = [vp, i64, i32, vp, vp, vp, sz, vp]
+        L.csa_topk_batched.argtypes = [vp, vp, i32, i64, i32, vp, vp, vp, sz, vp]
+        L.csa_topk_workspace_size.argtypes = [i32]
+        L.csa_topk_workspace_size.restype = sz
         L.csa_sparse_attn.argtypes = [vp, i32, f32, csa_paged, vp, i32, csa_paged, i64, i32, vp, vp, vp, sz, vp]
         L.csa_sparse_attn_workspace_size.argtypes = [i32, i32, i32]
         L.csa_sparse_attn_workspace_size.restype = sz
@@ -134,13 +136,32 @@ def csa_index_score(q_idx, w_h, Hi: int, k_idx: csa_paged, k_dtype: int, G: int,
            "csa_index_score")
 
 
-def csa_topk(scores, G: int, k: int, idx_out, keys_out=None, stream=None) -> None:
-    _check(lib().csa_topk(_ptr(scores), G, k, _ptr(idx_out), _ptr(keys_out), _stream(stream)), "csa_topk")
+def csa_topk_workspace_size(B: int) -> int:
+    return int(lib().csa_topk_workspace_size(B))
 
 
-def csa_topk_batched(scores, offsets, B: int, max_G: int, k: int, idx_out, keys_out=None, stream=None) -> None:
+def _scratch(nbytes: int, like):
+    import torch
+    return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=like.device if hasattr(like, "device") else "cuda")
+
+
+def csa_topk(scores, G: int, k: int, idx_out, keys_out=None, workspace=None, ws_bytes: int = 0,
+             stream=None) -> None:
+    """workspace None: a scratch tensor of csa_topk_workspace_size(1) bytes is allocated."""
+    if workspace is None:
+        ws_bytes = csa_topk_workspace_size(1)
+        workspace = _scratch(ws_bytes, scores)
+    _check(lib().csa_topk(_ptr(scores), G, k, _ptr(idx_out), _ptr(keys_out), _ptr(workspace), ws_bytes,
+                          _stream(stream)), "csa_topk")
+
+
+def csa_topk_batched(scores, offsets, B: int, max_G: int, k: int, idx_out, keys_out=None, workspace=None,
+                     ws_bytes: int = 0, stream=None) -> None:
+    if workspace is None:
+        ws_bytes = csa_topk_workspace_size(B)
+        workspace = _scratch(ws_bytes, scores)
     _check(lib().csa_topk_batched(_ptr(scores), _ptr(offsets), B, max_G, k, _ptr(idx_out), _ptr(keys_out),
-                                  _stream(stream)), "csa_topk_batched")
+                                  _ptr(workspace), ws_bytes, _stream(stream)), "csa_topk_batched")
 
 
 def csa_sparse_attn_workspace_size(H: int, n_sel: int, swa: int) -> int:

@@ -152,18 +152,36 @@ csa_status csa_index_score(const void* q_idx, const float* w_h, int32_t Hi, csa_
     return from_cuda(launch_score(l, static_cast<cudaStream_t>(stream), false));
 }
 
+static size_t topk_ws_layout(int32_t B, size_t* lists_off) {
+    const size_t hist = align256((size_t)B * kHistBlock * sizeof(uint32_t));
+    if (lists_off) *lists_off = hist;
+    return hist + align256(topk_lists_bytes(B));
+}
+
+size_t csa_topk_workspace_size(int32_t B) {
+    if (B < 1 || B > 65535) return 0;
+    return topk_ws_layout(B, nullptr);
+}
+
 static csa_status topk_common(const float* scores, const int64_t* offsets, int32_t B, int64_t G, int32_t k,
-                              int32_t* idx_out, uint32_t* keys_out, void* stream) {
+                              int32_t* idx_out, uint32_t* keys_out, void* workspace, size_t ws_bytes,
+                              void* stream) {
     if (k < 1 || k > 2048) return CSA_ERR_UNSUPPORTED;
     if (!scores || !al4(scores) || !idx_out || !al4(idx_out)) return CSA_ERR_INVALID_ARG;
     if (keys_out && !al4(keys_out)) return CSA_ERR_INVALID_ARG;
     if (B < 1 || B > 65535 || G < 0 || G > 0x7FFFFFFFLL) return CSA_ERR_INVALID_ARG;
+    size_t lists_off = 0;
+    const size_t need = topk_ws_layout(B, &lists_off);
+    if (!workspace || ws_bytes < need || !al16(workspace)) return CSA_ERR_WORKSPACE;
     int32_t* st = status_ptr();
     if (!st) return CSA_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
     TopkLaunch t;
     t.scores = scores;
     t.B = B;
     t.G = G;
+    t.max_G = G;
     t.offsets = offsets;
     t.n_tokens = nullptr;
     t.ratio = 1;
@@ -171,19 +189,26 @@ static csa_status topk_common(const float* scores, const int64_t* offsets, int32
     t.k = k;
     t.idx_out = idx_out;
     t.keys_out = keys_out;
-    t.hist = nullptr;
+    t.hist = reinterpret_cast<uint32_t*>(ws);
+    t.lists = ws + lists_off;
     t.status = st;
-    return from_cuda(launch_topk(t, static_cast<cudaStream_t>(stream), false));
+    // clear the histograms and control words, count the first digit, select
+    cudaError_t e = cudaMemsetAsync(ws, 0, (size_t)B * kHistBlock * sizeof(uint32_t), s);
+    if (e == cudaSuccess) e = launch_topk_hist(t, s);
+    if (e == cudaSuccess) e = launch_topk(t, s, true);
+    return from_cuda(e);
 }
 
-csa_status csa_topk(const float* scores, int64_t G, int32_t k, int32_t* idx_out, uint32_t* keys_out, void* stream) {
-    return topk_common(scores, nullptr, 1, G, k, idx_out, keys_out, stream);
+csa_status csa_topk(const float* scores, int64_t G, int32_t k, int32_t* idx_out, uint32_t* keys_out,
+                    void* workspace, size_t ws_bytes, void* stream) {
+    return topk_common(scores, nullptr, 1, G, k, idx_out, keys_out, workspace, ws_bytes, stream);
 }
 
 csa_status csa_topk_batched(const float* scores, const int64_t* offsets, int32_t B, int64_t max_G, int32_t k,
-                            int32_t* idx_out, uint32_t* keys_out, void* stream) {
+                            int32_t* idx_out, uint32_t* keys_out, void* workspace, size_t ws_bytes,
+                            void* stream) {
     if (!offsets) return CSA_ERR_INVALID_ARG;
-    return topk_common(scores, offsets, B, max_G, k, idx_out, keys_out, stream);
+    return topk_common(scores, offsets, B, max_G, k, idx_out, keys_out, workspace, ws_bytes, stream);
 }
 
 size_t csa_sparse_attn_workspace_size(int32_t H, int32_t n_sel, int32_t swa) {
@@ -230,7 +255,7 @@ csa_status csa_sparse_attn(const void* q, int32_t H, float scale, csa_paged kv_c
 
 // ------------------------------------------------------------------ fused decode
 struct DecodeLayout {
-    size_t scores, hist, sel, attn, total;
+    size_t scores, hist, lists, sel, attn, total;
     int64_t score_stride;
 };
 
@@ -271,7 +296,9 @@ static DecodeLayout decode_layout(const csa_decode_params* p) {
     L.scores = off;
     if (p->ratio == 4) off += align256((size_t)p->B * L.score_stride * sizeof(float));
     L.hist = off;
-    if (p->ratio == 4) off += align256((size_t)p->B * kHistBins * sizeof(uint32_t));
+    if (p->ratio == 4) off += align256((size_t)p->B * kHistBlock * sizeof(uint32_t));
+    L.lists = off;
+    if (p->ratio == 4) off += align256(topk_lists_bytes(p->B));
     L.sel = off;
     if (p->ratio == 4 && !p->sel) off += align256((size_t)p->B * p->k * sizeof(int32_t));
     L.attn = off;
@@ -370,6 +397,7 @@ csa_status csa_decode_timed(const csa_decode_params* p, void* workspace, size_t 
         t.scores = l.scores;
         t.B = p->B;
         t.G = 0;
+        t.max_G = max_G;
         t.offsets = nullptr;
         t.n_tokens = p->n_tokens;
         t.ratio = p->ratio;
@@ -378,6 +406,7 @@ csa_status csa_decode_timed(const csa_decode_params* p, void* workspace, size_t 
         t.idx_out = sel_out;
         t.keys_out = nullptr;
         t.hist = hist;
+        t.lists = ws + L.lists;
         t.status = st;
         e = launch_topk(t, s, ev == nullptr);
         if (e != cudaSuccess) return CSA_ERR_CUDA;

@@ -39,7 +39,7 @@ __device__ __forceinline__ void group_range(const CompressArgs& a, int b, int64_
 
 __device__ __forceinline__ void zero_hist(const CompressArgs& a, int b) {
     if (a.hist_zero && blockIdx.x == 0)
-        for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) a.hist_zero[(int64_t)b * kHistBins + i] = 0u;
+        for (int i = threadIdx.x; i < kHistBlock; i += blockDim.x) a.hist_zero[(int64_t)b * kHistBlock + i] = 0u;
 }
 
 // lane's 16 dims of a bf16 row -> fp32

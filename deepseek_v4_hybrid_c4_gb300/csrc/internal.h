@@ -9,6 +9,9 @@ namespace csa {
 
 constexpr int kLatentRowBytes = 1024;  // one bf16 latent row (512 dims)
 constexpr int kHistBins = 2048;        // first top-k digit: key >> 21
+// Per-request top-k control block in the workspace: the first digit's histogram
+// (kHistBins counters) then the select's control words; cleared before every step.
+constexpr int kHistBlock = kHistBins + 32;
 
 struct HPaged {            // host copy of a paged buffer description (see csa_paged)
     const void* base;
@@ -21,7 +24,7 @@ struct HPaged {            // host copy of a paged buffer description (see csa_p
 
 // Stage 1.  Single mode (n_tokens == nullptr): groups [first, first + count) of one
 // sequence.  Batched mode: request b = blockIdx.y compresses [n_done[b], n_tokens[b]/ratio).
-// hist_zero (nullable): [B][kHistBins] counters cleared by block (0, b) for stage 2.
+// hist_zero (nullable): [B][kHistBlock] words cleared by block (0, b) for stages 2 and 3.
 struct CompressLaunch {
     HPaged raw, out;
     const float* w_gate;
@@ -51,18 +54,20 @@ struct ScoreLaunch {
     int ratio;
     int64_t G;             // single mode
     int64_t max_G;         // host bound (grid sizing)
-    uint32_t* hist;        // fused first-digit histogram [B][kHistBins] (zeroed beforehand) or nullptr
+    uint32_t* hist;        // fused first-digit histogram, [B][kHistBlock] (zeroed beforehand), or nullptr
     int32_t* status;
 };
 cudaError_t launch_score(const ScoreLaunch& a, cudaStream_t s, bool pdl);
 
 // Stage 3.  Request b's scores: single: [0, G); offsets mode: [offsets[b], offsets[b+1]);
-// decode mode: b * score_stride + [0, n_tokens[b] / ratio).  hist (nullable): the
-// first digit's histogram from stage 2.
+// decode mode: b * score_stride + [0, n_tokens[b] / ratio).  hist: [B][kHistBlock] words,
+// zeroed before the step; the first digit's histogram is either fused into stage 2 or
+// built by launch_topk_hist.  lists: topk_lists_bytes(B) of scratch.
 struct TopkLaunch {
     const float* scores;
     int B;
     int64_t G;                 // single mode
+    int64_t max_G;             // host bound on every request's length (grid sizing)
     const int64_t* offsets;    // offsets mode
     const int64_t* n_tokens;   // decode mode
     int ratio;
@@ -70,9 +75,12 @@ struct TopkLaunch {
     int k;
     int32_t* idx_out;          // [B, k]
     uint32_t* keys_out;        // [B, k] or nullptr
-    const uint32_t* hist;
+    uint32_t* hist;
+    void* lists;
     int32_t* status;
 };
+size_t topk_lists_bytes(int B);
+cudaError_t launch_topk_hist(const TopkLaunch& a, cudaStream_t s);
 cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t s, bool pdl);
 
 // Stage 4 (+ log-sum-exp merge).  Per request b: keys = sel rows of kv_c (n_sel of

@@ -61,7 +61,7 @@ struct ScoreArgs {
     const int64_t* n_tokens;
     int ratio;
     int64_t G;
-    uint32_t* hist;          // [B][kHistBins] or nullptr
+    uint32_t* hist;          // [B][kHistBlock] (the first kHistBins words) or nullptr
     int32_t* status;
 };
 
@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(SC_THREADS, HI >= 16 ? 1 : 2)
         for (int bin = threadIdx.x; bin < kHistBins; bin += SC_THREADS) {
             const uint32_t c = hist[bin];
             if (c) {
-                atomicAdd(a.hist + (int64_t)req * kHistBins + bin, c);
+                atomicAdd(a.hist + (int64_t)req * kHistBlock + bin, c);
                 hist[bin] = 0;
             }
         }

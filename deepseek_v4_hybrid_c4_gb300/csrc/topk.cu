@@ -1,41 +1,39 @@
-// Stage 3: exact top-k of the index scores by cluster radix select (the pages'
-// "Lightning TopK": per-CTA histograms over N/8 candidates reduced inside a
-// cluster of 8 to a threshold tau, then a local scatter of the entries above
-// tau -- "SGLang 如何为 DeepSeek V4 打造「Day-0」推理加速", sec. "创新 2";
-// "DeepSeek-V4 本地部署，SGLang 把活做絕了", sec. "Kernel 層一堆狠活").
+// Stage 3: exact top-k of the index scores by radix select ("SGLang 如何为 DeepSeek V4
+// 打造「Day-0」推理加速", sec. "创新 2", Lightning TopK: per-CTA histograms reduced
+// to a threshold tau, then a scatter of the entries above tau; "DeepSeek-V4 本地部署，
+// SGLang 把活做絕了", sec. "Kernel 層一堆狠活").
 //
-// Order: descending order-preserving 32-bit key of the fp32 score, ties to the
-// lower index (a total order, so the selected set and its order are unique).
+// Order: descending order-preserving 32-bit key of the fp32 score, ties to the lower
+// index.  Equivalently, descending 63-bit composite V = key << 31 | (2^31 - 1 - index),
+// which is unique per element, so the selected set and its order are unique.  Digits
+// of V, high to low: key bits 31..21 | 20..10 | 9..0, then inverted-index bits
+// 30..20 | 19..10 | 9..0.
 //
-// One cluster of 8 CTAs per request; CTA r owns the contiguous index slice
-// [r*S, r*S+S).  Digits of the key: bits 31..21, 20..10, 9..0.
-//  1. First digit: its histogram over the whole request -- ready-made by the
-//     score kernel in the fused decode step, otherwise built per CTA and summed
-//     across the cluster through distributed shared memory -- gives the bin b0
-//     holding the k-th key.
-//  2. Each CTA scans its slice once (16 scores in flight per thread): keys in
-//     higher bins are winners, keys in b0 are survivors.
-//  3. Fast path (the survivors of all 8 CTAs fit CTA 0's gather buffer): every
-//     CTA copies its winners and survivors into CTA 0 through DSMEM and CTA 0
-//     finishes alone -- two more digits over the survivors, then the lowest-index
-//     ties at the exact threshold -- with no further cluster barrier.
-//     Otherwise every CTA keeps refining its survivors with cluster-reduced
-//     histograms (re-reading L2 when more than CAP survive) and the ties are
-//     taken lowest index first across the index-ordered slices.
-//  4. CTA 0 sorts the k winners by (key desc, index asc) with a bitonic network
-//     kept in registers (shuffles) except for strides of a warp or more.
+// Wide select, two phases in one launch with grid (C, B):
+//  A. Every CTA of request b reads the first digit's histogram of the whole request
+//     (fused into the score kernel in the decode step; built by topk_hist_kernel for
+//     the standalone call, per-CTA histograms summed inside a cluster of 8 through
+//     distributed shared memory) and finds the bin b0 holding the k-th key.  It scans
+//     its slice of the scores once: keys above b0 are winners, keys in b0 survivors,
+//     both appended to global lists with one atomic per warp.
+//  B. The last CTA of the request to finish (a completion counter; no CTA waits for
+//     another) loads both lists into shared memory and refines the survivors digit by
+//     digit (histogram, bin of the remaining need, compaction) until winners plus
+//     survivors fit one sort; then a bitonic sort by V gives the k outputs in order.
+//     If more survivors arrive than the list holds, the digits run over the scores in
+//     global memory until the candidates fit.
 #include "common.cuh"
 #include "internal.h"
 
 namespace csa {
 
-constexpr int TK_CL = 8;
-constexpr int TK_T = 1024;
+constexpr int TK_T = 1024;           // threads per CTA
 constexpr int TK_BINS = kHistBins;   // 2048: widest digit
-constexpr int TK_CAP = 10240;        // survivors kept per CTA
-constexpr int TK_KMAX = 2048;
-constexpr int TK_GCAP = 6144;        // survivors CTA 0 can take from the whole cluster
-constexpr int TK_V = 16;             // scores per thread per scan iteration
+constexpr int TK_KMAX = 2048;        // largest k; winners list capacity
+constexpr int TK_SCAP = 16384;       // survivors list capacity (global and shared)
+constexpr int TK_CHUNK = 4 * TK_T;   // scores per CTA in phase A (one float4 per thread)
+constexpr int TK_HCL = 8;            // cluster size of the standalone histogram kernel
+constexpr int TK_HCHUNK = 8 * TK_T;  // scores per CTA of the histogram kernel
 
 struct TopkArgs {
     const float* scores;
@@ -48,26 +46,38 @@ struct TopkArgs {
     int k;
     int32_t* idx_out;
     uint32_t* keys_out;
-    const uint32_t* hist;
+    uint32_t* hist;   // [B][kHistBlock]: first-digit histogram, then the control words
+    uint2* wlist;     // [B][TK_KMAX] winners {key, index}
+    uint2* slist;     // [B][TK_SCAP] survivors
     int32_t* status;
 };
 
 struct TkSmem {
-    uint32_t hist[2][TK_BINS];
-    uint32_t ckey[TK_CAP];      // this CTA's survivors
-    int32_t cidx[TK_CAP];
-    uint32_t skey[TK_KMAX];     // this CTA's winners
-    int32_t sidx[TK_KMAX];
-    uint32_t okey[TK_KMAX];     // CTA 0: the cluster's winners
+    uint32_t hist[TK_BINS];
+    uint32_t okey[TK_KMAX];     // winners, then the union to sort
     int32_t oidx[TK_KMAX];
-    uint32_t gkey[TK_GCAP];     // CTA 0: the cluster's survivors (fast path)
-    int32_t gidx[TK_GCAP];
+    uint32_t ckey[TK_SCAP];     // survivors
+    int32_t cidx[TK_SCAP];
     uint64_t sortbuf[2][1024];
-    uint32_t xchg[8];
     uint32_t wsum[32];
-    int n_cand, n_sel, n_new, overflow, n_out;
-    uint32_t bin, above, cnt, taken;
+    int n_sel, n_cand, n_new;
+    uint32_t bin, above, cnt, last;
 };
+
+__device__ __forceinline__ void request_span(const TopkArgs& a, int b, const float*& sc, int64_t& G) {
+    if (a.offsets) {
+        const int64_t o0 = a.offsets[b], o1 = a.offsets[b + 1];
+        sc = a.scores + o0;
+        G = o1 - o0;
+    } else if (a.n_tokens) {
+        sc = a.scores + (int64_t)b * a.score_stride;
+        G = a.n_tokens[b] / a.ratio;
+    } else {
+        sc = a.scores;
+        G = a.G;
+    }
+    if (G < 0) G = 0;
+}
 
 __device__ __forceinline__ int warp_alloc(int* counter, bool pred) {
     const unsigned m = __ballot_sync(0xffffffffu, pred);
@@ -80,7 +90,8 @@ __device__ __forceinline__ int warp_alloc(int* counter, bool pred) {
     return pred ? base + __popc(m & ((1u << lane) - 1u)) : -1;
 }
 
-// Slots for this thread's ns winners and nc survivors: one atomic per list per warp.
+// Slots for this thread's ns winners and nc survivors (each < 2^16 per warp): one atomic
+// per non-empty list per warp.
 __device__ __forceinline__ void warp_reserve(int* cs, int* cc, uint32_t ns, uint32_t nc, int& bs, int& bc) {
     const int lane = threadIdx.x & 31;
     const uint32_t v = (ns << 16) | nc;
@@ -93,8 +104,8 @@ __device__ __forceinline__ void warp_reserve(int* cs, int* cc, uint32_t ns, uint
     const uint32_t tot = __shfl_sync(0xffffffffu, x, 31);
     int b_s = 0, b_c = 0;
     if (lane == 31) {
-        b_s = atomicAdd(cs, (int)(tot >> 16));
-        b_c = atomicAdd(cc, (int)(tot & 0xFFFFu));
+        if (tot >> 16) b_s = atomicAdd(cs, (int)(tot >> 16));
+        if (tot & 0xFFFFu) b_c = atomicAdd(cc, (int)(tot & 0xFFFFu));
     }
     b_s = __shfl_sync(0xffffffffu, b_s, 31);
     b_c = __shfl_sync(0xffffffffu, b_c, 31);
@@ -137,13 +148,12 @@ __device__ __forceinline__ uint32_t block_scan(TkSmem& sm, uint32_t v, uint32_t*
     return before + x - v;
 }
 
-enum { HIST_GLOBAL = 0, HIST_CLUSTER = 1, HIST_LOCAL = 2 };
+enum { HIST_GLOBAL = 0, HIST_LOCAL = 1 };
 
-// The bin holding the need-th largest key counted from the top bin, from the
-// global histogram, the sum of the 8 CTAs' histograms (DSMEM) or this CTA's own.
-// Writes sm.bin and sm.above (count in higher bins).
-__device__ __forceinline__ void find_bin(TkSmem& sm, int mode, const uint32_t* ghist, int hb, int nbins,
-                                         uint32_t need) {
+// The bin holding the need-th largest element counted from the top bin, from a
+// global histogram (written by an earlier kernel) or this CTA's sm.hist.  Writes
+// sm.bin, sm.above (count in higher bins) and sm.cnt (count in the bin).
+__device__ __forceinline__ void find_bin(TkSmem& sm, int mode, const uint32_t* ghist, int nbins, uint32_t need) {
     const int t = threadIdx.x;
     const int bh = nbins - 1 - 2 * t, bl = nbins - 2 - 2 * t;  // this thread's two bins, high first
     uint32_t th = 0, tl = 0;
@@ -151,23 +161,15 @@ __device__ __forceinline__ void find_bin(TkSmem& sm, int mode, const uint32_t* g
         if (mode == HIST_GLOBAL) {
             th = __ldg(ghist + bh);
             tl = __ldg(ghist + bl);
-        } else if (mode == HIST_LOCAL) {
-            th = sm.hist[hb][bh];
-            tl = sm.hist[hb][bl];
         } else {
-            const uint32_t ah = smem_u32(&sm.hist[hb][bh]), al = smem_u32(&sm.hist[hb][bl]);
-            uint32_t vh[TK_CL], vl[TK_CL];
-#pragma unroll
-            for (int c = 0; c < TK_CL; ++c) {
-                vh[c] = ld_dsmem_u32(mapa(ah, c));
-                vl[c] = ld_dsmem_u32(mapa(al, c));
-            }
-#pragma unroll
-            for (int c = 0; c < TK_CL; ++c) {
-                th += vh[c];
-                tl += vl[c];
-            }
+            th = sm.hist[bh];
+            tl = sm.hist[bl];
         }
+    }
+    if (t == 0) {
+        sm.bin = 0;
+        sm.above = 0;
+        sm.cnt = 0;
     }
     uint32_t total;
     const uint32_t excl = block_scan(sm, th + tl, &total);
@@ -175,40 +177,36 @@ __device__ __forceinline__ void find_bin(TkSmem& sm, int mode, const uint32_t* g
         if (th > 0 && excl < need && need <= excl + th) {
             sm.bin = (uint32_t)bh;
             sm.above = excl;
+            sm.cnt = th;
         } else if (tl > 0 && excl + th < need && need <= excl + th + tl) {
             sm.bin = (uint32_t)bl;
             sm.above = excl + th;
+            sm.cnt = tl;
         }
     }
     __syncthreads();
 }
 
-// Keys of TK_V scores of the slice for this thread: element j*4+q is index
-// base + 4*(tid + (j/1)*TK_T) + q (coalesced float4 loads when the slice is 16-byte aligned).
-__device__ __forceinline__ void load_keys(const float* sc, int64_t base, int64_t hi, bool vec, uint32_t (&key)[TK_V],
-                                          int64_t (&pos)[TK_V / 4]) {
-    const int tid = threadIdx.x;
+// The keys of 4 consecutive scores pos .. pos+3 (a float4 load when the whole group is
+// in range and 16-byte aligned); out-of-range entries read as key 0.
+__device__ __forceinline__ void load4(const float* sc, int64_t pos, int64_t hi, bool vec, uint32_t (&key)[4]) {
+    float v[4];
+    if (vec && pos + 3 < hi) {
+        const float4 f = __ldcg(reinterpret_cast<const float4*>(sc + pos));
+        v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+    } else {
 #pragma unroll
-    for (int j = 0; j < TK_V / 4; ++j) {
-        pos[j] = base + 4 * ((int64_t)tid + (int64_t)j * TK_T);
-        float v[4];
-        if (vec && pos[j] + 3 < hi) {
-            const float4 f = __ldg(reinterpret_cast<const float4*>(sc + pos[j]));
-            v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
-        } else {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) v[q] = pos[j] + q < hi ? __ldg(sc + pos[j] + q) : 0.f;
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) key[j * 4 + q] = score_key(v[q]);
+        for (int q = 0; q < 4; ++q) v[q] = pos + q < hi ? __ldcg(sc + pos + q) : 0.f;
     }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) key[q] = score_key(v[q]);
 }
 
 __device__ __forceinline__ bool kv_greater(uint32_t ka, int32_t ia, uint32_t kb, int32_t ib) {
     return ka > kb || (ka == kb && ia < ib);
 }
 
-// CTA 0: sort okey/oidx[0..total) by (key desc, index asc), write k outputs (-1 padding).
+// Sort okey/oidx[0..total) by (key desc, index asc) and write k outputs (-1 padding).
 __device__ void sort_and_write(TkSmem& sm, uint32_t total, int k, int32_t* out, uint32_t* kout) {
     const int tid = threadIdx.x, lane = tid & 31;
     if (total > (uint32_t)TK_KMAX) total = TK_KMAX;
@@ -283,347 +281,248 @@ __device__ void sort_and_write(TkSmem& sm, uint32_t total, int k, int32_t* out, 
     (void)lane;
 }
 
-__global__ void __launch_bounds__(TK_T, 1) topk_kernel(TopkArgs a) {
+// Digit d (1..5) of the composite V of (key, index); see the header.
+__device__ __forceinline__ uint32_t digit_of(int d, uint32_t key, int32_t idx) {
+    const uint32_t inv = 0x7FFFFFFFu - (uint32_t)idx;
+    switch (d) {
+        case 1: return (key >> 10) & 2047u;
+        case 2: return key & 1023u;
+        case 3: return (inv >> 20) & 2047u;
+        case 4: return (inv >> 10) & 1023u;
+        default: return inv & 1023u;
+    }
+}
+__device__ __forceinline__ int digit_bins(int d) { return (d == 1 || d == 3) ? 2048 : 1024; }
+
+// Standalone first digit: the histogram of key >> 21 over every request's scores.  Each
+// CTA counts its slice in shared memory; the cluster's rank-0 CTA sums the 8 CTAs'
+// histograms through distributed shared memory and adds the non-zero bins to the global
+// histogram (zeroed beforehand).
+__global__ void __launch_bounds__(TK_T, 1) topk_hist_kernel(TopkArgs a) {
+    __shared__ uint32_t h[TK_BINS];
+    const int tid = threadIdx.x;
+    const int b = blockIdx.y;
+    const float* sc;
+    int64_t G;
+    request_span(a, b, sc, G);
+    for (int i = tid; i < TK_BINS; i += TK_T) h[i] = 0;
+    __syncthreads();
+    const int64_t lo = min((int64_t)blockIdx.x * TK_HCHUNK, G), hi = min(lo + TK_HCHUNK, G);
+    const bool vec = (reinterpret_cast<uintptr_t>(sc) & 15) == 0;
+    for (int64_t base = lo; base < hi; base += 4 * TK_T) {  // the same trip count for every thread
+        const int64_t pos = base + 4 * tid;
+        uint32_t key[4];
+        load4(sc, pos, hi, vec, key);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) hist_add(h, key[q] >> 21, pos + q < hi);
+    }
+    cluster_sync();
+    if (cluster_ctarank() == 0) {
+        uint32_t* gh = a.hist + (int64_t)b * kHistBlock;
+        for (int i = tid; i < TK_BINS; i += TK_T) {
+            const uint32_t ai = smem_u32(&h[i]);
+            uint32_t v = 0;
+#pragma unroll
+            for (int c = 0; c < TK_HCL; ++c) v += ld_dsmem_u32(mapa(ai, c));
+            if (v) atomicAdd(gh + i, v);
+        }
+    }
+    cluster_sync();  // the other CTAs' shared memory stays alive until it has been read
+}
+
+__global__ void __launch_bounds__(TK_T, 1) topk_select_kernel(TopkArgs a) {
     extern __shared__ __align__(16) uint8_t tk_raw[];
     TkSmem& sm = *reinterpret_cast<TkSmem*>(tk_raw);
     const int tid = threadIdx.x;
     pdl_wait();               // scores (and the fused histogram) come from the preceding kernel
     pdl_launch_dependents();
-    const uint32_t rank = cluster_ctarank();
-    const int b = blockIdx.x / TK_CL;
-
+    const int b = blockIdx.y;
     const float* sc;
     int64_t G;
-    if (a.offsets) {
-        const int64_t o0 = a.offsets[b], o1 = a.offsets[b + 1];
-        sc = a.scores + o0;
-        G = o1 - o0;
-    } else if (a.n_tokens) {
-        sc = a.scores + (int64_t)b * a.score_stride;
-        G = a.n_tokens[b] / a.ratio;
-    } else {
-        sc = a.scores;
-        G = a.G;
-    }
-    if (G < 0) G = 0;
+    request_span(a, b, sc, G);
     const int k = a.k;
-    const int64_t slice = ((G + TK_CL - 1) / TK_CL + 3) & ~int64_t(3);
-    const int64_t lo = min((int64_t)rank * slice, G), hi = min(lo + slice, G);
-    const bool vec = (reinterpret_cast<uintptr_t>(sc + lo) & 15) == 0;
+    uint32_t* ghist = a.hist + (int64_t)b * kHistBlock;
+    uint32_t* ctl = ghist + kHistBins;  // [0] winners, [1] survivors, [2] finished CTAs
+    uint2* wl = a.wlist + (int64_t)b * TK_KMAX;
+    uint2* sl = a.slist + (int64_t)b * TK_SCAP;
     int32_t* out = a.idx_out + (int64_t)b * k;
     uint32_t* kout = a.keys_out ? a.keys_out + (int64_t)b * k : nullptr;
+    const bool all_in = G <= k;  // every candidate is selected
+    const bool vec = (reinterpret_cast<uintptr_t>(sc) & 15) == 0;
 
+    // ---- A. first digit from the request's histogram; one scan of this CTA's slice
+    uint32_t b0 = 0;
+    if (!all_in) {
+        find_bin(sm, HIST_GLOBAL, ghist, TK_BINS, (uint32_t)k);
+        b0 = sm.bin;
+    }
+    const int64_t chunk = (((G + gridDim.x - 1) / gridDim.x) + 3) & ~int64_t(3);
+    const int64_t lo = min((int64_t)blockIdx.x * chunk, G), hi = min(lo + chunk, G);
+    for (int64_t base = lo; base < hi; base += TK_CHUNK) {
+        const int64_t pos = base + 4 * tid;
+        uint32_t key[4];
+        load4(sc, pos, hi, vec, key);
+        uint32_t ns = 0, nc = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const bool in = pos + q < hi;
+            const uint32_t d = key[q] >> 21;
+            ns += (in && (all_in || d > b0)) ? 1u : 0u;
+            nc += (in && !all_in && d == b0) ? 1u : 0u;
+        }
+        if (!__any_sync(0xffffffffu, (ns | nc) != 0)) continue;
+        int bs, bc;
+        warp_reserve(reinterpret_cast<int*>(&ctl[0]), reinterpret_cast<int*>(&ctl[1]), ns, nc, bs, bc);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const bool in = pos + q < hi;
+            const uint32_t d = key[q] >> 21;
+            if (in && (all_in || d > b0)) {
+                if (bs < TK_KMAX) wl[bs] = make_uint2(key[q], (uint32_t)(pos + q));
+                else raise_status(a.status, CSA_ERR_DEVICE_BOUNDS);
+                ++bs;
+            } else if (in && !all_in && d == b0) {
+                if (bc < TK_SCAP) sl[bc] = make_uint2(key[q], (uint32_t)(pos + q));
+                ++bc;
+            }
+        }
+    }
+    // ---- the last CTA of the request to finish goes on
+    __syncthreads();
     if (tid == 0) {
-        sm.n_cand = 0;
-        sm.n_sel = 0;
-        sm.overflow = 0;
-        sm.n_out = 0;
+        __threadfence();
+        sm.last = atomicAdd(&ctl[2], 1u) == gridDim.x - 1 ? 1u : 0u;
     }
     __syncthreads();
+    if (!sm.last) return;
+    __threadfence();
 
-    if (G > k) {
-        uint32_t need = (uint32_t)k;
-        // ---- 1. first digit (bits 31..21)
-        if (a.hist) {
-            find_bin(sm, HIST_GLOBAL, a.hist + (int64_t)b * kHistBins, 0, 2048, need);
-        } else {
-            for (int i = tid; i < TK_BINS; i += TK_T) sm.hist[0][i] = 0;
-            __syncthreads();
-            for (int64_t base = lo; base < hi; base += (int64_t)TK_T * TK_V) {
-                uint32_t key[TK_V];
-                int64_t pos[TK_V / 4];
-                load_keys(sc, base, hi, vec, key, pos);
-#pragma unroll
-                for (int e = 0; e < TK_V; ++e) hist_add(sm.hist[0], key[e] >> 21, pos[e / 4] + (e & 3) < hi);
-            }
-            cluster_sync();
-            find_bin(sm, HIST_CLUSTER, nullptr, 0, 2048, need);
-        }
-        const uint32_t b0 = sm.bin;
-        need -= sm.above;
-        // ---- 2. one scan of the slice: winners (digit > b0) and survivors (digit == b0)
-        for (int64_t base = lo; base < hi; base += (int64_t)TK_T * TK_V) {
-            uint32_t key[TK_V];
-            int64_t pos[TK_V / 4];
-            load_keys(sc, base, hi, vec, key, pos);
-            uint32_t ns = 0, nc = 0;
-#pragma unroll
-            for (int e = 0; e < TK_V; ++e) {
-                const bool in = pos[e / 4] + (e & 3) < hi;
-                const uint32_t d = key[e] >> 21;
-                ns += (in && d > b0) ? 1u : 0u;
-                nc += (in && d == b0) ? 1u : 0u;
-            }
-            if (!__any_sync(0xffffffffu, (ns | nc) != 0)) continue;
-            int bs, bc;
-            warp_reserve(&sm.n_sel, &sm.n_cand, ns, nc, bs, bc);
-#pragma unroll
-            for (int e = 0; e < TK_V; ++e) {
-                const int64_t i = pos[e / 4] + (e & 3);
-                const bool in = i < hi;
-                const uint32_t d = key[e] >> 21;
-                if (in && d > b0) {
-                    if (bs < TK_KMAX) { sm.skey[bs] = key[e]; sm.sidx[bs] = (int32_t)i; }
-                    ++bs;
-                } else if (in && d == b0) {
-                    if (bc < TK_CAP) { sm.ckey[bc] = key[e]; sm.cidx[bc] = (int32_t)i; }
-                    else sm.overflow = 1;
-                    ++bc;
-                }
-            }
-        }
-        __syncthreads();
-        // ---- 3. digits bits 20..10 and 9..0, refined across the cluster.  After the first of
-        //      them the survivors normally fit CTA 0, which then finishes alone.
-        uint32_t prefix = b0;
-        int prev_shift = 21;
-        const int shifts[2] = {10, 0};
-        const int widths[2] = {11, 10};
-        for (int p = 0; p < 2; ++p) {
-            const int shift = shifts[p];
-            const uint32_t mask = (1u << widths[p]) - 1u;
-            const int nbins = 1 << widths[p];
-            const int hb = (p + 1) & 1;
-            for (int i = tid; i < TK_BINS; i += TK_T) sm.hist[hb][i] = 0;
-            __syncthreads();
-            const bool list_mode = !sm.overflow;
-            const int n_list = sm.n_cand;
-            if (list_mode) {
-                for (int i0 = 0; i0 < n_list; i0 += TK_T) {
-                    const int i = i0 + tid;
-                    const bool in = i < n_list;
-                    const uint32_t key = in ? sm.ckey[i] : 0u;
-                    hist_add(sm.hist[hb], (key >> shift) & mask, in);
-                }
-            } else {
-                for (int64_t base = lo; base < hi; base += (int64_t)TK_T * TK_V) {
-                    uint32_t key[TK_V];
-                    int64_t pos[TK_V / 4];
-                    load_keys(sc, base, hi, vec, key, pos);
-#pragma unroll
-                    for (int e = 0; e < TK_V; ++e) {
-                        const bool in = pos[e / 4] + (e & 3) < hi && (key[e] >> prev_shift) == prefix;
-                        hist_add(sm.hist[hb], (key[e] >> shift) & mask, in);
-                    }
-                }
-            }
-            cluster_sync();
-            find_bin(sm, HIST_CLUSTER, nullptr, hb, nbins, need);
-            const uint32_t bin = sm.bin;
-            need -= sm.above;
-            if (list_mode) {
-                if (tid == 0) sm.n_new = 0;
-                __syncthreads();
-                for (int i0 = 0; i0 < n_list; i0 += TK_T) {
-                    const int i = i0 + tid;
-                    const bool in = i < n_list;
-                    const uint32_t key = in ? sm.ckey[i] : 0u;
-                    const int32_t idx = in ? sm.cidx[i] : 0;
-                    __syncthreads();  // chunk read by everyone before it is overwritten
-                    const uint32_t d = (key >> shift) & mask;
-                    const int s = warp_alloc(&sm.n_sel, in && d > bin);
-                    if (s >= 0 && s < TK_KMAX) { sm.skey[s] = key; sm.sidx[s] = idx; }
-                    const int c = warp_alloc(&sm.n_new, in && d == bin);
-                    if (c >= 0) { sm.ckey[c] = key; sm.cidx[c] = idx; }
-                }
-                __syncthreads();
-                if (tid == 0) sm.n_cand = sm.n_new;
-            } else {
-                if (tid == 0) { sm.n_cand = 0; sm.overflow = 0; }
-                __syncthreads();
-                for (int64_t base = lo; base < hi; base += (int64_t)TK_T * TK_V) {
-                    uint32_t key[TK_V];
-                    int64_t pos[TK_V / 4];
-                    load_keys(sc, base, hi, vec, key, pos);
-#pragma unroll
-                    for (int e = 0; e < TK_V; ++e) {
-                        const int64_t i = pos[e / 4] + (e & 3);
-                        const bool in = i < hi && (key[e] >> prev_shift) == prefix;
-                        const uint32_t d = (key[e] >> shift) & mask;
-                        const int s = warp_alloc(&sm.n_sel, in && d > bin);
-                        if (s >= 0 && s < TK_KMAX) { sm.skey[s] = key[e]; sm.sidx[s] = (int32_t)i; }
-                        const int c = warp_alloc(&sm.n_cand, in && d == bin);
-                        if (c >= TK_CAP) sm.overflow = 1;
-                        else if (c >= 0) { sm.ckey[c] = key[e]; sm.cidx[c] = (int32_t)i; }
-                    }
-                }
-            }
-            __syncthreads();
-            prefix = (prefix << widths[p]) | bin;
-            prev_shift = shift;
-            if (p != 0) continue;
-            // ---- exchange the counts; fast finish in CTA 0 when the survivors fit
-            if (tid == 0) {
-                sm.xchg[0] = (uint32_t)sm.n_sel;
-                sm.xchg[1] = sm.overflow ? 0xFFFFFFFFu : (uint32_t)sm.n_cand;
-            }
-            cluster_sync();
-            uint32_t off_sel = 0, tot_sel = 0, off_cand = 0, tot_cand = 0;
-            bool any_over = false;
-            for (uint32_t c = 0; c < TK_CL; ++c) {
-                const uint32_t ns = ld_dsmem_u32(mapa(smem_u32(&sm.xchg[0]), c));
-                const uint32_t nc = ld_dsmem_u32(mapa(smem_u32(&sm.xchg[1]), c));
-                if (nc == 0xFFFFFFFFu) any_over = true;
-                if (c < rank) { off_sel += ns; off_cand += nc; }
-                tot_sel += ns;
-                tot_cand += nc;
-            }
-            if (any_over || tot_cand > (uint32_t)TK_GCAP) continue;  // keep refining across the cluster
-            for (int i = tid; i < sm.n_sel; i += TK_T) {
-                st_dsmem_u32(mapa(smem_u32(&sm.okey[off_sel + i]), 0), sm.skey[i]);
-                st_dsmem_u32(mapa(smem_u32(&sm.oidx[off_sel + i]), 0), (uint32_t)sm.sidx[i]);
-            }
-            for (int i = tid; i < sm.n_cand; i += TK_T) {
-                st_dsmem_u32(mapa(smem_u32(&sm.gkey[off_cand + i]), 0), sm.ckey[i]);
-                st_dsmem_u32(mapa(smem_u32(&sm.gidx[off_cand + i]), 0), (uint32_t)sm.cidx[i]);
-            }
-            cluster_sync();
-            if (rank != 0) return;
-            if (tid == 0) sm.n_out = (int)tot_sel;
-            __syncthreads();
-            int n_list2 = (int)tot_cand;
-            if (n_list2 > TK_T && (uint32_t)n_list2 != need) {
-                // last digit (bits 9..0) locally, then the ties
-                for (int i = tid; i < TK_BINS; i += TK_T) sm.hist[0][i] = 0;
-                __syncthreads();
-                for (int i0 = 0; i0 < n_list2; i0 += TK_T) {
-                    const int i = i0 + tid;
-                    const bool in = i < n_list2;
-                    hist_add(sm.hist[0], in ? (sm.gkey[i] & 1023u) : 0u, in);
-                }
-                __syncthreads();
-                find_bin(sm, HIST_LOCAL, nullptr, 0, 1024, need);
-                const uint32_t lbin = sm.bin;
-                need -= sm.above;
-                if (tid == 0) sm.n_new = 0;
-                __syncthreads();
-                for (int i0 = 0; i0 < n_list2; i0 += TK_T) {
-                    const int i = i0 + tid;
-                    const bool in = i < n_list2;
-                    const uint32_t key = in ? sm.gkey[i] : 0u;
-                    const int32_t idx = in ? sm.gidx[i] : 0;
-                    __syncthreads();
-                    const uint32_t d = key & 1023u;
-                    const int so = warp_alloc(&sm.n_out, in && d > lbin);
-                    if (so >= 0 && so < TK_KMAX) { sm.okey[so] = key; sm.oidx[so] = idx; }
-                    const int c = warp_alloc(&sm.n_new, in && d == lbin);
-                    if (c >= 0) { sm.gkey[c] = key; sm.gidx[c] = idx; }
-                }
-                __syncthreads();
-                n_list2 = sm.n_new;
-            }
-            // the `need` best survivors by (key desc, index asc): rank each against all
-            for (int i = tid; i < n_list2; i += TK_T) {
-                const uint32_t myk = sm.gkey[i];
-                const int32_t myi = sm.gidx[i];
-                uint32_t rnk = 0;
-                for (int j = 0; j < n_list2; ++j) rnk += kv_greater(sm.gkey[j], sm.gidx[j], myk, myi) ? 1u : 0u;
-                if (rnk < need) {
-                    const int so = atomicAdd(&sm.n_out, 1);
-                    if (so < TK_KMAX) { sm.okey[so] = myk; sm.oidx[so] = myi; }
-                }
-            }
-            __syncthreads();
-            sort_and_write(sm, (uint32_t)min(sm.n_out, k), k, out, kout);
-            return;
-        }
-        // prefix == tau (full key); `need` ties at tau remain to be taken, lowest index first.
-        const uint32_t tau = prefix;
-        const bool list_mode = !sm.overflow;
-        if (!list_mode) {
-            if (tid == 0) sm.cnt = 0;
-            __syncthreads();
-            for (int64_t i0 = lo; i0 < hi; i0 += TK_T) {
-                const int64_t i = i0 + tid;
-                const bool f = i < hi && score_key(__ldg(sc + i)) == tau;
-                warp_alloc(reinterpret_cast<int*>(&sm.cnt), f);
-            }
-            __syncthreads();
-        } else if (tid == 0) {
-            sm.cnt = (uint32_t)sm.n_cand;
-        }
-        __syncthreads();
-        const uint32_t c_r = sm.cnt;
-        if (tid == 0) sm.xchg[2] = c_r;
-        cluster_sync();
-        uint32_t before = 0;
-        for (uint32_t c = 0; c < rank; ++c) before += ld_dsmem_u32(mapa(smem_u32(&sm.xchg[2]), c));
-        const uint32_t take = need > before ? min(need - before, c_r) : 0u;
-        if (take > 0) {
-            if (take == c_r && list_mode) {
-                for (int i = tid; i < (int)c_r; i += TK_T) {
-                    const int s = atomicAdd(&sm.n_sel, 1);
-                    if (s < TK_KMAX) { sm.skey[s] = tau; sm.sidx[s] = sm.cidx[i]; }
-                }
-            } else if (list_mode && c_r <= (uint32_t)TK_T) {
-                if (tid < (int)c_r) {
-                    const int32_t my = sm.cidx[tid];
-                    uint32_t rnk = 0;
-                    for (uint32_t j = 0; j < c_r; ++j) rnk += sm.cidx[j] < my ? 1u : 0u;
-                    if (rnk < take) {
-                        const int s = atomicAdd(&sm.n_sel, 1);
-                        if (s < TK_KMAX) { sm.skey[s] = tau; sm.sidx[s] = my; }
-                    }
-                }
-            } else {
-                // ordered scan of the slice: the first `take` ties in index order
-                if (tid == 0) sm.taken = 0;
-                __syncthreads();
-                for (int64_t i0 = lo; i0 < hi; i0 += TK_T) {
-                    const int64_t i = i0 + tid;
-                    const bool f = i < hi && score_key(__ldg(sc + i)) == tau;
-                    uint32_t tot;
-                    const uint32_t ex = block_scan(sm, f ? 1u : 0u, &tot);
-                    const uint32_t base = sm.taken;
-                    if (f && base + ex < take) {
-                        const int s = atomicAdd(&sm.n_sel, 1);
-                        if (s < TK_KMAX) { sm.skey[s] = tau; sm.sidx[s] = (int32_t)i; }
-                    }
-                    __syncthreads();
-                    if (tid == 0) sm.taken = base + tot;
-                    __syncthreads();
-                    if (sm.taken >= take) break;
-                }
-            }
-        }
-        __syncthreads();
-    } else {
-        // every candidate is selected
-        for (int64_t i0 = lo; i0 < hi; i0 += TK_T) {
-            const int64_t i = i0 + tid;
-            const bool in = i < hi;
-            const uint32_t key = in ? score_key(__ldg(sc + i)) : 0u;
-            const int s = warp_alloc(&sm.n_sel, in);
-            if (s >= 0 && s < TK_KMAX) { sm.skey[s] = key; sm.sidx[s] = (int32_t)i; }
-        }
-        __syncthreads();
-    }
-
-    // ---- gather the cluster's winners into CTA 0 (cluster-wide path)
-    const uint32_t n_mine = (uint32_t)min(sm.n_sel, TK_KMAX);
+    // ---- B. refine the survivors
     if (tid == 0) {
-        sm.xchg[3] = n_mine;
-        if (sm.n_sel > TK_KMAX) raise_status(a.status, CSA_ERR_DEVICE_BOUNDS);
+        const uint32_t nw = __ldcg(&ctl[0]);
+        sm.n_sel = (int)min(nw, (uint32_t)TK_KMAX);
+        sm.n_cand = (int)__ldcg(&ctl[1]);
     }
-    cluster_sync();
-    uint32_t off = 0, total = 0;
-    for (uint32_t c = 0; c < TK_CL; ++c) {
-        const uint32_t v = ld_dsmem_u32(mapa(smem_u32(&sm.xchg[3]), c));
-        if (c < rank) off += v;
-        total += v;
+    __syncthreads();
+    const int n_w0 = sm.n_sel;
+    bool implicit = sm.n_cand > TK_SCAP;  // survivors list incomplete: the digits run over the scores
+    for (int i = tid; i < n_w0; i += TK_T) {
+        const uint2 v = __ldcg(wl + i);
+        sm.okey[i] = v.x;
+        sm.oidx[i] = (int32_t)v.y;
     }
-    for (uint32_t i = tid; i < n_mine; i += TK_T) {
-        if (off + i < (uint32_t)TK_KMAX) {
-            st_dsmem_u32(mapa(smem_u32(&sm.okey[off + i]), 0), sm.skey[i]);
-            st_dsmem_u32(mapa(smem_u32(&sm.oidx[off + i]), 0), (uint32_t)sm.sidx[i]);
+    if (!implicit)
+        for (int i = tid; i < sm.n_cand; i += TK_T) {
+            const uint2 v = __ldcg(sl + i);
+            sm.ckey[i] = v.x;
+            sm.cidx[i] = (int32_t)v.y;
         }
+    __syncthreads();
+    uint32_t need = all_in ? 0u : (uint32_t)k - (uint32_t)n_w0;
+    const int sort_max = k <= 1024 ? 1024 : TK_KMAX;
+    uint32_t bins[6] = {b0, 0, 0, 0, 0, 0};
+    // prefix match of (key, index) on digits 0 .. d-1 (implicit mode)
+    auto matches = [&](int d, uint32_t key, int32_t idx) {
+        if ((key >> 21) != bins[0]) return false;
+        for (int e = 1; e < d; ++e)
+            if (digit_of(e, key, idx) != bins[e]) return false;
+        return true;
+    };
+    for (int d = 1; d <= 5 && sm.n_sel + sm.n_cand > sort_max; ++d) {
+        const int nb = digit_bins(d);
+        for (int i = tid; i < TK_BINS; i += TK_T) sm.hist[i] = 0;
+        __syncthreads();
+        if (!implicit) {
+            const int n = sm.n_cand;
+            for (int i0 = 0; i0 < n; i0 += TK_T) {
+                const int i = i0 + tid;
+                const bool in = i < n;
+                hist_add(sm.hist, in ? digit_of(d, sm.ckey[i], sm.cidx[i]) : 0u, in);
+            }
+        } else {
+            for (int64_t p0 = 0; p0 < G; p0 += 4 * TK_T) {
+                uint32_t key[4];
+                const int64_t pos = p0 + 4 * tid;
+                load4(sc, pos, G, vec, key);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int32_t idx = (int32_t)(pos + q);
+                    const bool in = pos + q < G && matches(d, key[q], idx);
+                    hist_add(sm.hist, in ? digit_of(d, key[q], idx) : 0u, in);
+                }
+            }
+        }
+        __syncthreads();
+        find_bin(sm, HIST_LOCAL, nullptr, nb, need);
+        const uint32_t bin = sm.bin, n_bin = sm.cnt;
+        need -= sm.above;
+        bins[d] = bin;
+        if (!implicit) {
+            // in-place compaction: a chunk is read by everyone before any of it is overwritten
+            const int n = sm.n_cand;
+            if (tid == 0) sm.n_new = 0;
+            __syncthreads();
+            for (int i0 = 0; i0 < n; i0 += TK_T) {
+                const int i = i0 + tid;
+                const bool in = i < n;
+                const uint32_t key = in ? sm.ckey[i] : 0u;
+                const int32_t idx = in ? sm.cidx[i] : 0;
+                __syncthreads();
+                const uint32_t dv = digit_of(d, key, idx);
+                const int so = warp_alloc(&sm.n_sel, in && dv > bin);
+                if (so >= 0 && so < TK_KMAX) { sm.okey[so] = key; sm.oidx[so] = idx; }
+                const int c = warp_alloc(&sm.n_new, in && dv == bin);
+                if (c >= 0) { sm.ckey[c] = key; sm.cidx[c] = idx; }
+            }
+            __syncthreads();
+            if (tid == 0) sm.n_cand = sm.n_new;
+        } else {
+            const bool gather = n_bin <= (uint32_t)TK_SCAP;
+            if (tid == 0) sm.n_cand = 0;
+            __syncthreads();
+            for (int64_t p0 = 0; p0 < G; p0 += 4 * TK_T) {
+                uint32_t key[4];
+                const int64_t pos = p0 + 4 * tid;
+                load4(sc, pos, G, vec, key);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int32_t idx = (int32_t)(pos + q);
+                    const bool in = pos + q < G && matches(d, key[q], idx);
+                    const uint32_t dv = digit_of(d, key[q], idx);
+                    const int so = warp_alloc(&sm.n_sel, in && dv > bin);
+                    if (so >= 0 && so < TK_KMAX) { sm.okey[so] = key[q]; sm.oidx[so] = idx; }
+                    const int c = warp_alloc(&sm.n_cand, gather && in && dv == bin);
+                    if (c >= 0 && c < TK_SCAP) { sm.ckey[c] = key[q]; sm.cidx[c] = idx; }
+                }
+            }
+            __syncthreads();
+            if (tid == 0 && !gather) sm.n_cand = (int)n_bin;
+            implicit = !gather;
+        }
+        __syncthreads();
     }
-    cluster_sync();
-    if (rank != 0) return;
-    sort_and_write(sm, total, k, out, kout);
+    // ---- the union of winners and survivors fits one sort
+    const int n_w = sm.n_sel, n_c = implicit ? 0 : sm.n_cand;
+    if (tid == 0 && n_w + n_c > TK_KMAX) raise_status(a.status, CSA_ERR_DEVICE_BOUNDS);
+    for (int i = tid; i < n_c && n_w + i < TK_KMAX; i += TK_T) {
+        sm.okey[n_w + i] = sm.ckey[i];
+        sm.oidx[n_w + i] = sm.cidx[i];
+    }
+    __syncthreads();
+    sort_and_write(sm, (uint32_t)min(n_w + n_c, TK_KMAX), k, out, kout);
 }
 
-cudaError_t launch_topk(const TopkLaunch& h, cudaStream_t s, bool pdl) {
+static int g_sms = 0;
+static int sm_count() {
+    if (!g_sms) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
+    }
+    return g_sms;
+}
+
+static TopkArgs topk_args(const TopkLaunch& h) {
     TopkArgs a;
     a.scores = h.scores;
     a.B = h.B;
@@ -636,29 +535,60 @@ cudaError_t launch_topk(const TopkLaunch& h, cudaStream_t s, bool pdl) {
     a.idx_out = h.idx_out;
     a.keys_out = h.keys_out;
     a.hist = h.hist;
+    a.wlist = reinterpret_cast<uint2*>(h.lists);
+    a.slist = reinterpret_cast<uint2*>(h.lists) + (size_t)h.B * TK_KMAX;
     a.status = h.status;
+    return a;
+}
+
+size_t topk_lists_bytes(int B) { return (size_t)B * (TK_KMAX + TK_SCAP) * sizeof(uint2); }
+
+cudaError_t launch_topk_hist(const TopkLaunch& h, cudaStream_t s) {
+    const TopkArgs a = topk_args(h);
+    int64_t per = (h.max_G + TK_HCHUNK - 1) / TK_HCHUNK;
+    per = (per + TK_HCL - 1) / TK_HCL * TK_HCL;
+    if (per < TK_HCL) per = TK_HCL;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = TK_HCL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3((unsigned)per, (unsigned)h.B, 1);
+    cfg.blockDim = dim3(TK_T, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    return cudaLaunchKernelEx(&cfg, topk_hist_kernel, a);
+}
+
+cudaError_t launch_topk(const TopkLaunch& h, cudaStream_t s, bool pdl) {
+    const TopkArgs a = topk_args(h);
     const size_t smem = sizeof(TkSmem);
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e =
+            cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
+    // slices of about TK_CHUNK scores, at most one wave of CTAs over the batch
+    int64_t per = (h.max_G + TK_CHUNK - 1) / TK_CHUNK;
+    const int64_t cap = (sm_count() + h.B - 1) / h.B;
+    if (per > cap) per = cap;
+    if (per < 1) per = 1;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = TK_CL;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 2 : 1;
-    cfg.gridDim = dim3((unsigned)(TK_CL * h.B), 1, 1);
+    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.gridDim = dim3((unsigned)per, (unsigned)h.B, 1);
     cfg.blockDim = dim3(TK_T, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    return cudaLaunchKernelEx(&cfg, topk_kernel, a);
+    return cudaLaunchKernelEx(&cfg, topk_select_kernel, a);
 }
 
 }  // namespace csa
