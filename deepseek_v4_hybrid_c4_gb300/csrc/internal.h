@@ -10,8 +10,9 @@ namespace csa {
 constexpr int kLatentRowBytes = 1024;  // one bf16 latent row (512 dims)
 constexpr int kHistBins = 2048;        // first top-k digit: key >> 21
 // Per-request top-k control block in the workspace: the first digit's histogram
-// (kHistBins counters) then the select's control words; cleared before every step.
-constexpr int kHistBlock = kHistBins + 32;
+// (kHistBins counters), the survivors' second-digit histogram (kHistBins), then the
+// select's control words and per-CTA counts; cleared before every step.
+constexpr int kHistBlock = 2 * kHistBins + 256;
 
 struct HPaged {            // host copy of a paged buffer description (see csa_paged)
     const void* base;
@@ -62,7 +63,7 @@ cudaError_t launch_score(const ScoreLaunch& a, cudaStream_t s, bool pdl);
 // Stage 3.  Request b's scores: single: [0, G); offsets mode: [offsets[b], offsets[b+1]);
 // decode mode: b * score_stride + [0, n_tokens[b] / ratio).  hist: [B][kHistBlock] words,
 // zeroed before the step; the first digit's histogram is either fused into stage 2 or
-// built by launch_topk_hist.  lists: topk_lists_bytes(B) of scratch.
+// built by launch_topk_hist.  lists: topk_lists_bytes(B, max_G) of scratch.
 struct TopkLaunch {
     const float* scores;
     int B;
@@ -79,7 +80,7 @@ struct TopkLaunch {
     void* lists;
     int32_t* status;
 };
-size_t topk_lists_bytes(int B);
+size_t topk_lists_bytes(int B, int64_t max_G);
 cudaError_t launch_topk_hist(const TopkLaunch& a, cudaStream_t s);
 cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t s, bool pdl);
 

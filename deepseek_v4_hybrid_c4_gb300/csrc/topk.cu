@@ -30,7 +30,8 @@ namespace csa {
 constexpr int TK_T = 1024;           // threads per CTA
 constexpr int TK_BINS = kHistBins;   // 2048: widest digit
 constexpr int TK_KMAX = 2048;        // largest k; winners list capacity
-constexpr int TK_SCAP = 16384;       // survivors list capacity (global and shared)
+constexpr int TK_SCAP = 16384;       // survivors held in shared memory
+constexpr int TK_MAXC = 64;          // most select CTAs per request
 constexpr int TK_CHUNK = 4 * TK_T;   // scores per CTA in phase A (one float4 per thread)
 constexpr int TK_HCL = 8;            // cluster size of the standalone histogram kernel
 constexpr int TK_HCHUNK = 8 * TK_T;  // scores per CTA of the histogram kernel
@@ -46,9 +47,10 @@ struct TopkArgs {
     int k;
     int32_t* idx_out;
     uint32_t* keys_out;
-    uint32_t* hist;   // [B][kHistBlock]: first-digit histogram, then the control words
-    uint2* wlist;     // [B][TK_KMAX] winners {key, index}
-    uint2* slist;     // [B][TK_SCAP] survivors
+    uint32_t* hist;   // [B][kHistBlock]: digit histograms, control words, per-CTA counts
+    uint2* wlist;     // [B][C][capw] winners {key, index}, one region per CTA
+    uint2* slist;     // [B][C][caps] survivors
+    int64_t capw, caps;
     int32_t* status;
 };
 
@@ -58,8 +60,10 @@ struct TkSmem {
     int32_t oidx[TK_KMAX];
     uint32_t ckey[TK_SCAP];     // survivors
     int32_t cidx[TK_SCAP];
-    uint64_t sortbuf[2][1024];
+    uint64_t sortbuf[TK_KMAX];
     uint32_t wsum[32];
+    uint32_t xoff[32];
+    uint32_t pw[TK_MAXC + 1], ps[TK_MAXC + 1];  // per-CTA list offsets (phase B)
     int n_sel, n_cand, n_new;
     uint32_t bin, above, cnt, last;
 };
@@ -88,30 +92,6 @@ __device__ __forceinline__ int warp_alloc(int* counter, bool pred) {
     if (lane == leader) base = atomicAdd(counter, __popc(m));
     base = __shfl_sync(0xffffffffu, base, leader);
     return pred ? base + __popc(m & ((1u << lane) - 1u)) : -1;
-}
-
-// Slots for this thread's ns winners and nc survivors (each < 2^16 per warp): one atomic
-// per non-empty list per warp.
-__device__ __forceinline__ void warp_reserve(int* cs, int* cc, uint32_t ns, uint32_t nc, int& bs, int& bc) {
-    const int lane = threadIdx.x & 31;
-    const uint32_t v = (ns << 16) | nc;
-    uint32_t x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-    }
-    const uint32_t tot = __shfl_sync(0xffffffffu, x, 31);
-    int b_s = 0, b_c = 0;
-    if (lane == 31) {
-        if (tot >> 16) b_s = atomicAdd(cs, (int)(tot >> 16));
-        if (tot & 0xFFFFu) b_c = atomicAdd(cc, (int)(tot & 0xFFFFu));
-    }
-    b_s = __shfl_sync(0xffffffffu, b_s, 31);
-    b_c = __shfl_sync(0xffffffffu, b_c, 31);
-    const uint32_t ex = x - v;
-    bs = b_s + (int)(ex >> 16);
-    bc = b_c + (int)(ex & 0xFFFFu);
 }
 
 __device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t digit, bool active) {
@@ -148,24 +128,12 @@ __device__ __forceinline__ uint32_t block_scan(TkSmem& sm, uint32_t v, uint32_t*
     return before + x - v;
 }
 
-enum { HIST_GLOBAL = 0, HIST_LOCAL = 1 };
-
-// The bin holding the need-th largest element counted from the top bin, from a
-// global histogram (written by an earlier kernel) or this CTA's sm.hist.  Writes
-// sm.bin, sm.above (count in higher bins) and sm.cnt (count in the bin).
-__device__ __forceinline__ void find_bin(TkSmem& sm, int mode, const uint32_t* ghist, int nbins, uint32_t need) {
+// The bin holding the need-th largest element counted from the top bin, given this
+// thread's two bins' counts (bins nbins-1-2t and nbins-2-2t, high first).  Writes sm.bin,
+// sm.above (count in higher bins) and sm.cnt (count in the bin).
+__device__ __forceinline__ void find_bin_vals(TkSmem& sm, uint32_t th, uint32_t tl, int nbins, uint32_t need) {
     const int t = threadIdx.x;
-    const int bh = nbins - 1 - 2 * t, bl = nbins - 2 - 2 * t;  // this thread's two bins, high first
-    uint32_t th = 0, tl = 0;
-    if (bl >= 0) {
-        if (mode == HIST_GLOBAL) {
-            th = __ldg(ghist + bh);
-            tl = __ldg(ghist + bl);
-        } else {
-            th = sm.hist[bh];
-            tl = sm.hist[bl];
-        }
-    }
+    const int bh = nbins - 1 - 2 * t, bl = nbins - 2 - 2 * t;
     if (t == 0) {
         sm.bin = 0;
         sm.above = 0;
@@ -186,6 +154,18 @@ __device__ __forceinline__ void find_bin(TkSmem& sm, int mode, const uint32_t* g
     }
     __syncthreads();
 }
+// From a histogram in global memory written by an earlier kernel (read-only path).
+__device__ __forceinline__ void find_bin_global(TkSmem& sm, const uint32_t* gh, int nbins, uint32_t need) {
+    const int bh = nbins - 1 - 2 * (int)threadIdx.x, bl = bh - 1;
+    const uint32_t th = bl >= 0 ? __ldg(gh + bh) : 0u, tl = bl >= 0 ? __ldg(gh + bl) : 0u;
+    find_bin_vals(sm, th, tl, nbins, need);
+}
+// From this CTA's sm.hist.
+__device__ __forceinline__ void find_bin_local(TkSmem& sm, int nbins, uint32_t need) {
+    const int bh = nbins - 1 - 2 * (int)threadIdx.x, bl = bh - 1;
+    const uint32_t th = bl >= 0 ? sm.hist[bh] : 0u, tl = bl >= 0 ? sm.hist[bl] : 0u;
+    find_bin_vals(sm, th, tl, nbins, need);
+}
 
 // The keys of 4 consecutive scores pos .. pos+3 (a float4 load when the whole group is
 // in range and 16-byte aligned); out-of-range entries read as key 0.
@@ -202,83 +182,83 @@ __device__ __forceinline__ void load4(const float* sc, int64_t pos, int64_t hi, 
     for (int q = 0; q < 4; ++q) key[q] = score_key(v[q]);
 }
 
-__device__ __forceinline__ bool kv_greater(uint32_t ka, int32_t ia, uint32_t kb, int32_t ib) {
-    return ka > kb || (ka == kb && ia < ib);
+// Bitonic sort of the 64 composites of a warp, two per lane (element 2*lane + r), larger
+// first: the stride-1 stages stay in the lane, the others use shuffles.
+__device__ __forceinline__ void warp_sort64(uint64_t (&v)[2]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int size = 2; size <= 64; size <<= 1) {
+#pragma unroll
+        for (int j = size >> 1; j > 0; j >>= 1) {
+            if (j == 1) {
+                const bool desc = ((2 * lane) & size) == 0;
+                const uint64_t mx = v[0] > v[1] ? v[0] : v[1], mn = v[0] > v[1] ? v[1] : v[0];
+                v[0] = desc ? mx : mn;
+                v[1] = desc ? mn : mx;
+            } else {
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const uint64_t pv = __shfl_xor_sync(0xffffffffu, v[r], j >> 1);
+                    const int i = 2 * lane + r;
+                    const bool lower = (i & j) == 0, desc = (i & size) == 0;
+                    const uint64_t mx = v[r] > pv ? v[r] : pv, mn = v[r] > pv ? pv : v[r];
+                    v[r] = (desc == lower) ? mx : mn;
+                }
+            }
+        }
+    }
 }
 
-// Sort okey/oidx[0..total) by (key desc, index asc) and write k outputs (-1 padding).
-__device__ void sort_and_write(TkSmem& sm, uint32_t total, int k, int32_t* out, uint32_t* kout) {
-    const int tid = threadIdx.x, lane = tid & 31;
-    if (total > (uint32_t)TK_KMAX) total = TK_KMAX;
-    int n2 = 1;
-    while (n2 < (int)total) n2 <<= 1;
-    if (n2 <= 1024) {
-        // one element per thread of the first max(n2, 32) threads; composite = key << 32 |
-        // (0x7FFFFFFF - idx) so that larger is better.  Strides below a warp use shuffles,
-        // larger ones exchange through shared memory behind a barrier of just these warps.
-        const int nt = n2 < 32 ? 32 : n2;
-        uint64_t v = 0;
-        if (tid < nt) {
-            if (tid < (int)total) v = ((uint64_t)sm.okey[tid] << 32) | (uint32_t)(0x7FFFFFFF - sm.oidx[tid]);
-            int buf = 0;
-            for (int size = 2; size <= n2; size <<= 1) {
-                for (int j = size >> 1; j > 0; j >>= 1) {
-                    uint64_t pv;
-                    if (j >= 32) {
-                        sm.sortbuf[buf][tid] = v;
-                        asm volatile("bar.sync 2, %0;" ::"r"(nt) : "memory");
-                        pv = sm.sortbuf[buf][tid ^ j];
-                        buf ^= 1;
-                    } else {
-                        pv = __shfl_xor_sync(0xffffffffu, v, j);
-                    }
-                    const bool up = (tid & size) == 0, lower = (tid & j) == 0;
-                    const uint64_t mx = v > pv ? v : pv, mn = v > pv ? pv : v;
-                    v = (up == lower) ? mx : mn;
-                }
-            }
+// Order okey/oidx[0..total) (total <= TK_KMAX) by (key desc, index asc) and write the
+// first k (then -1 padding).  Warp w sorts elements [64w, 64w+64) into a run; an
+// element's output position is its place in its own run plus, for every other run, the
+// number of that run's elements above it (binary search).  Composites are unique and
+// the zero padding sits below every element, so the positions are exact.
+__device__ void rank_scatter(TkSmem& sm, int total, int k, int32_t* out, uint32_t* kout) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (total > TK_KMAX) total = TK_KMAX;
+    const int nruns = (total + 63) / 64;
+    uint64_t v[2] = {0ull, 0ull};
+    uint64_t* runs = sm.sortbuf;
+    if (warp < nruns) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int i = 64 * warp + 2 * lane + r;
+            // composite: key << 32 | (2^31 - 1 - index); 0 = padding
+            v[r] = i < total ? ((uint64_t)sm.okey[i] << 32) | (uint32_t)(0x7FFFFFFF - sm.oidx[i]) : 0ull;
         }
-        if (tid < k) {
-            const bool ok = tid < (int)total;
-            out[tid] = ok ? (int32_t)(0x7FFFFFFF - (uint32_t)v) : -1;
-            if (kout) kout[tid] = ok ? (uint32_t)(v >> 32) : 0u;
-        }
-        for (int i = tid + TK_T; i < k; i += TK_T) {
-            out[i] = -1;
-            if (kout) kout[i] = 0u;
-        }
-        return;
-    }
-    // n2 = 2048: shared-memory bitonic network
-    for (int i = (int)total + tid; i < n2; i += TK_T) {
-        sm.okey[i] = 0u;
-        sm.oidx[i] = 0x7FFFFFFF;
+        warp_sort64(v);
+        runs[64 * warp + 2 * lane] = v[0];
+        runs[64 * warp + 2 * lane + 1] = v[1];
     }
     __syncthreads();
-    for (int size = 2; size <= n2; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int i = tid; i < n2; i += TK_T) {
-                const int j = i ^ stride;
-                if (j > i) {
-                    const uint32_t ki = sm.okey[i], kj = sm.okey[j];
-                    const int32_t ii = sm.oidx[i], ij = sm.oidx[j];
-                    const bool first_half = (i & size) == 0;
-                    const bool swap = first_half ? kv_greater(kj, ij, ki, ii) : kv_greater(ki, ii, kj, ij);
-                    if (swap) {
-                        sm.okey[i] = kj; sm.oidx[i] = ij;
-                        sm.okey[j] = ki; sm.oidx[j] = ii;
-                    }
-                }
+    if (warp < nruns) {
+        int rank[2] = {2 * lane, 2 * lane + 1};
+        for (int o = 0; o < nruns; ++o) {
+            if (o == warp) continue;
+            const uint64_t* run = runs + 64 * o;
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                int lo = 0;  // elements of run o above v[r]: the run is sorted larger first
+#pragma unroll
+                for (int step = 32; step > 0; step >>= 1)
+                    if (run[lo + step - 1] > v[r]) lo += step;
+                if (lo == 63 && run[63] > v[r]) lo = 64;
+                rank[r] += lo;
             }
-            __syncthreads();
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            if (v[r] != 0ull && rank[r] < k) {
+                out[rank[r]] = (int32_t)(0x7FFFFFFF - (uint32_t)v[r]);
+                if (kout) kout[rank[r]] = (uint32_t)(v[r] >> 32);
+            }
         }
     }
-    for (int i = tid; i < k; i += TK_T) {
-        const bool ok = i < (int)total;
-        out[i] = ok ? sm.oidx[i] : -1;
-        if (kout) kout[i] = ok ? sm.okey[i] : 0u;
+    for (int i = total + tid; i < k; i += TK_T) {
+        out[i] = -1;
+        if (kout) kout[i] = 0u;
     }
-    (void)lane;
 }
 
 // Digit d (1..5) of the composite V of (key, index); see the header.
@@ -330,38 +310,55 @@ __global__ void __launch_bounds__(TK_T, 1) topk_hist_kernel(TopkArgs a) {
     cluster_sync();  // the other CTAs' shared memory stays alive until it has been read
 }
 
+// prefix match of (key, index) on digits 0 .. d-1
+__device__ __forceinline__ bool prefix_match(const uint32_t (&bins)[6], int d, uint32_t key, int32_t idx) {
+    if ((key >> 21) != bins[0]) return false;
+    for (int e = 1; e < d; ++e)
+        if (digit_of(e, key, idx) != bins[e]) return false;
+    return true;
+}
+
 __global__ void __launch_bounds__(TK_T, 1) topk_select_kernel(TopkArgs a) {
     extern __shared__ __align__(16) uint8_t tk_raw[];
     TkSmem& sm = *reinterpret_cast<TkSmem*>(tk_raw);
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_wait();               // scores (and the fused histogram) come from the preceding kernel
     pdl_launch_dependents();
     const int b = blockIdx.y;
+    const int C = (int)gridDim.x;
     const float* sc;
     int64_t G;
     request_span(a, b, sc, G);
     const int k = a.k;
-    uint32_t* ghist = a.hist + (int64_t)b * kHistBlock;
-    uint32_t* ctl = ghist + kHistBins;  // [0] winners, [1] survivors, [2] finished CTAs
-    uint2* wl = a.wlist + (int64_t)b * TK_KMAX;
-    uint2* sl = a.slist + (int64_t)b * TK_SCAP;
+    uint32_t* ghist = a.hist + (int64_t)b * kHistBlock;   // first digit (key bits 31..21)
+    uint32_t* ghist1 = ghist + kHistBins;                 // second digit of the survivors
+    uint32_t* ctl = ghist + 2 * kHistBins;                // [0] finished CTAs
+    uint32_t* table = ctl + 32;                           // [c] = {winners, survivors} of CTA c
     int32_t* out = a.idx_out + (int64_t)b * k;
     uint32_t* kout = a.keys_out ? a.keys_out + (int64_t)b * k : nullptr;
     const bool all_in = G <= k;  // every candidate is selected
     const bool vec = (reinterpret_cast<uintptr_t>(sc) & 15) == 0;
 
-    // ---- A. first digit from the request's histogram; one scan of this CTA's slice
+    // ---- A. one scan of this CTA's slice: winners (first digit above b0) and survivors
+    //      (= b0) compacted, in index order, into this CTA's own list regions
+    const int64_t chunk = (((G + C - 1) / C) + 3) & ~int64_t(3);
+    const int64_t lo = min((int64_t)blockIdx.x * chunk, G), hi = min(lo + chunk, G);
+    uint2* wl = a.wlist + ((int64_t)b * C + blockIdx.x) * a.capw;
+    uint2* sl = a.slist + ((int64_t)b * C + blockIdx.x) * a.caps;
+    uint32_t key[4];
+    load4(sc, lo + 4 * tid, hi, vec, key);  // in flight while the threshold bin is found
+    for (int i = tid; i < TK_BINS; i += TK_T) sm.hist[i] = 0;
     uint32_t b0 = 0;
     if (!all_in) {
-        find_bin(sm, HIST_GLOBAL, ghist, TK_BINS, (uint32_t)k);
+        find_bin_global(sm, ghist, TK_BINS, (uint32_t)k);
         b0 = sm.bin;
+    } else {
+        __syncthreads();
     }
-    const int64_t chunk = (((G + gridDim.x - 1) / gridDim.x) + 3) & ~int64_t(3);
-    const int64_t lo = min((int64_t)blockIdx.x * chunk, G), hi = min(lo + chunk, G);
+    uint32_t run_w = 0, run_s = 0;  // this CTA's list lengths so far
     for (int64_t base = lo; base < hi; base += TK_CHUNK) {
         const int64_t pos = base + 4 * tid;
-        uint32_t key[4];
-        load4(sc, pos, hi, vec, key);
+        if (base != lo) load4(sc, pos, hi, vec, key);
         uint32_t ns = 0, nc = 0;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -370,93 +367,162 @@ __global__ void __launch_bounds__(TK_T, 1) topk_select_kernel(TopkArgs a) {
             ns += (in && (all_in || d > b0)) ? 1u : 0u;
             nc += (in && !all_in && d == b0) ? 1u : 0u;
         }
-        if (!__any_sync(0xffffffffu, (ns | nc) != 0)) continue;
-        int bs, bc;
-        warp_reserve(reinterpret_cast<int*>(&ctl[0]), reinterpret_cast<int*>(&ctl[1]), ns, nc, bs, bc);
+        // CTA-wide exclusive offsets (16-bit halves: at most TK_CHUNK per pass)
+        const uint32_t v = (ns << 16) | nc;
+        uint32_t x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) sm.wsum[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            const uint32_t w = sm.wsum[lane];
+            uint32_t wx = w;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, wx, o);
+                if (lane >= o) wx += y;
+            }
+            sm.xoff[lane] = wx - w;
+            if (lane == 31) sm.cnt = wx;
+        }
+        __syncthreads();
+        const uint32_t ex = sm.xoff[warp] + (x - v), tot = sm.cnt;
+        uint32_t bs = run_w + (ex >> 16), bc = run_s + (ex & 0xFFFFu);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const bool in = pos + q < hi;
             const uint32_t d = key[q] >> 21;
-            if (in && (all_in || d > b0)) {
-                if (bs < TK_KMAX) wl[bs] = make_uint2(key[q], (uint32_t)(pos + q));
+            const bool win = in && (all_in || d > b0), sur = in && !all_in && d == b0;
+            if (win) {
+                if (bs < (uint32_t)a.capw) wl[bs] = make_uint2(key[q], (uint32_t)(pos + q));
                 else raise_status(a.status, CSA_ERR_DEVICE_BOUNDS);
                 ++bs;
-            } else if (in && !all_in && d == b0) {
-                if (bc < TK_SCAP) sl[bc] = make_uint2(key[q], (uint32_t)(pos + q));
+            } else if (sur) {
+                sl[bc] = make_uint2(key[q], (uint32_t)(pos + q));  // capacity: the slice length
                 ++bc;
             }
+            hist_add(sm.hist, (key[q] >> 10) & 2047u, sur);  // the survivors' second digit
         }
+        run_w += tot >> 16;
+        run_s += tot & 0xFFFFu;
+        __syncthreads();
     }
-    // ---- the last CTA of the request to finish goes on
-    __syncthreads();
     if (tid == 0) {
-        __threadfence();
-        sm.last = atomicAdd(&ctl[2], 1u) == gridDim.x - 1 ? 1u : 0u;
+        table[2 * blockIdx.x] = min(run_w, (uint32_t)a.capw);
+        table[2 * blockIdx.x + 1] = run_s;
     }
+    for (int i = tid; i < TK_BINS; i += TK_T) {
+        const uint32_t c = sm.hist[i];
+        if (c) atomicAdd(ghist1 + i, c);
+    }
+    // ---- the last CTA of the request to finish goes on (every thread's list entries and
+    //      counts are made visible before the CTA counts itself finished)
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) sm.last = atomicAdd(&ctl[0], 1u) == (uint32_t)C - 1 ? 1u : 0u;
     __syncthreads();
     if (!sm.last) return;
     __threadfence();
 
-    // ---- B. refine the survivors
-    if (tid == 0) {
-        const uint32_t nw = __ldcg(&ctl[0]);
-        sm.n_sel = (int)min(nw, (uint32_t)TK_KMAX);
-        sm.n_cand = (int)__ldcg(&ctl[1]);
+    // ---- B. gather the lists, refine the survivors digit by digit, rank the union
+    // the second digit's histogram bins of this thread, loaded early (L2: written by this grid)
+    const int bh = TK_BINS - 1 - 2 * tid, bl = bh - 1;
+    const uint32_t h1h = __ldcg(ghist1 + bh), h1l = __ldcg(ghist1 + bl);
+    if (warp == 0) {  // per-CTA list offsets: exclusive prefix over the table
+        uint32_t cw = 0, cs = 0;
+        for (int c0 = 0; c0 < C; c0 += 32) {
+            const int c = c0 + lane;
+            const uint32_t tw = c < C ? __ldcg(table + 2 * c) : 0u, ts = c < C ? __ldcg(table + 2 * c + 1) : 0u;
+            uint32_t xw = tw, xs = ts;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t yw = __shfl_up_sync(0xffffffffu, xw, o), ys = __shfl_up_sync(0xffffffffu, xs, o);
+                if (lane >= o) { xw += yw; xs += ys; }
+            }
+            if (c < C) {
+                sm.pw[c] = cw + xw - tw;
+                sm.ps[c] = cs + xs - ts;
+            }
+            cw += __shfl_sync(0xffffffffu, xw, 31);
+            cs += __shfl_sync(0xffffffffu, xs, 31);
+        }
+        if (lane == 0) {
+            sm.pw[C] = cw;
+            sm.ps[C] = cs;
+        }
     }
     __syncthreads();
-    const int n_w0 = sm.n_sel;
-    bool implicit = sm.n_cand > TK_SCAP;  // survivors list incomplete: the digits run over the scores
-    for (int i = tid; i < n_w0; i += TK_T) {
-        const uint2 v = __ldcg(wl + i);
-        sm.okey[i] = v.x;
-        sm.oidx[i] = (int32_t)v.y;
+    const int n_w0 = (int)min(sm.pw[C], (uint32_t)TK_KMAX), n_s0 = (int)sm.ps[C];
+    // element j of the concatenated lists: its CTA by binary search over the prefixes
+    auto region = [&](const uint32_t* pre, uint32_t j) {
+        int r = 0;
+        for (int step = TK_MAXC / 2; step > 0; step >>= 1)
+            if (r + step <= C - 1 && pre[r + step] <= j) r += step;
+        return r;
+    };
+    const uint2* wl0 = a.wlist + (int64_t)b * C * a.capw;
+    const uint2* sl0 = a.slist + (int64_t)b * C * a.caps;
+    for (int j = tid; j < n_w0; j += TK_T) {
+        const int r = region(sm.pw, (uint32_t)j);
+        const uint2 e = __ldcg(wl0 + (int64_t)r * a.capw + (j - (int)sm.pw[r]));
+        sm.okey[j] = e.x;
+        sm.oidx[j] = (int32_t)e.y;
     }
-    if (!implicit)
-        for (int i = tid; i < sm.n_cand; i += TK_T) {
-            const uint2 v = __ldcg(sl + i);
-            sm.ckey[i] = v.x;
-            sm.cidx[i] = (int32_t)v.y;
+    const bool s_fit = n_s0 <= TK_SCAP;
+    if (!all_in && s_fit) {
+#pragma unroll 4
+        for (int j = tid; j < n_s0; j += TK_T) {
+            const int r = region(sm.ps, (uint32_t)j);
+            const uint2 e = __ldcg(sl0 + (int64_t)r * a.caps + (j - (int)sm.ps[r]));
+            sm.ckey[j] = e.x;
+            sm.cidx[j] = (int32_t)e.y;
         }
+    }
+    if (tid == 0) {
+        sm.n_sel = n_w0;
+        sm.n_cand = all_in ? 0 : n_s0;
+    }
     __syncthreads();
     uint32_t need = all_in ? 0u : (uint32_t)k - (uint32_t)n_w0;
-    const int sort_max = k <= 1024 ? 1024 : TK_KMAX;
+    const int rank_max = k <= 1024 ? 1024 : TK_KMAX;
     uint32_t bins[6] = {b0, 0, 0, 0, 0, 0};
-    // prefix match of (key, index) on digits 0 .. d-1 (implicit mode)
-    auto matches = [&](int d, uint32_t key, int32_t idx) {
-        if ((key >> 21) != bins[0]) return false;
-        for (int e = 1; e < d; ++e)
-            if (digit_of(e, key, idx) != bins[e]) return false;
-        return true;
-    };
-    for (int d = 1; d <= 5 && sm.n_sel + sm.n_cand > sort_max; ++d) {
+    bool implicit = !all_in && !s_fit;  // survivors not in shared memory: the digits scan the scores
+    for (int d = 1; d <= 5 && sm.n_sel + sm.n_cand > rank_max; ++d) {
         const int nb = digit_bins(d);
-        for (int i = tid; i < TK_BINS; i += TK_T) sm.hist[i] = 0;
-        __syncthreads();
-        if (!implicit) {
-            const int n = sm.n_cand;
-            for (int i0 = 0; i0 < n; i0 += TK_T) {
-                const int i = i0 + tid;
-                const bool in = i < n;
-                hist_add(sm.hist, in ? digit_of(d, sm.ckey[i], sm.cidx[i]) : 0u, in);
-            }
+        if (d == 1) {
+            find_bin_vals(sm, h1h, h1l, TK_BINS, need);  // counted by phase A
         } else {
-            for (int64_t p0 = 0; p0 < G; p0 += 4 * TK_T) {
-                uint32_t key[4];
-                const int64_t pos = p0 + 4 * tid;
-                load4(sc, pos, G, vec, key);
+            for (int i = tid; i < TK_BINS; i += TK_T) sm.hist[i] = 0;
+            __syncthreads();
+            if (!implicit) {
+                const int n = sm.n_cand;
+                for (int i0 = 0; i0 < n; i0 += TK_T) {
+                    const int i = i0 + tid;
+                    const bool in = i < n;
+                    hist_add(sm.hist, in ? digit_of(d, sm.ckey[i], sm.cidx[i]) : 0u, in);
+                }
+            } else {
+                for (int64_t p0 = 0; p0 < G; p0 += 4 * TK_T) {
+                    uint32_t kk[4];
+                    const int64_t pos = p0 + 4 * tid;
+                    load4(sc, pos, G, vec, kk);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int32_t idx = (int32_t)(pos + q);
-                    const bool in = pos + q < G && matches(d, key[q], idx);
-                    hist_add(sm.hist, in ? digit_of(d, key[q], idx) : 0u, in);
+                    for (int q = 0; q < 4; ++q) {
+                        const int32_t idx = (int32_t)(pos + q);
+                        const bool in = pos + q < G && prefix_match(bins, d, kk[q], idx);
+                        hist_add(sm.hist, in ? digit_of(d, kk[q], idx) : 0u, in);
+                    }
                 }
             }
+            __syncthreads();
+            find_bin_local(sm, nb, need);
         }
-        __syncthreads();
-        find_bin(sm, HIST_LOCAL, nullptr, nb, need);
-        const uint32_t bin = sm.bin, n_bin = sm.cnt;
+        const uint32_t dbin = sm.bin, d_n = sm.cnt;
         need -= sm.above;
-        bins[d] = bin;
+        bins[d] = dbin;
         if (!implicit) {
             // in-place compaction: a chunk is read by everyone before any of it is overwritten
             const int n = sm.n_cand;
@@ -465,43 +531,43 @@ __global__ void __launch_bounds__(TK_T, 1) topk_select_kernel(TopkArgs a) {
             for (int i0 = 0; i0 < n; i0 += TK_T) {
                 const int i = i0 + tid;
                 const bool in = i < n;
-                const uint32_t key = in ? sm.ckey[i] : 0u;
+                const uint32_t kk = in ? sm.ckey[i] : 0u;
                 const int32_t idx = in ? sm.cidx[i] : 0;
                 __syncthreads();
-                const uint32_t dv = digit_of(d, key, idx);
-                const int so = warp_alloc(&sm.n_sel, in && dv > bin);
-                if (so >= 0 && so < TK_KMAX) { sm.okey[so] = key; sm.oidx[so] = idx; }
-                const int c = warp_alloc(&sm.n_new, in && dv == bin);
-                if (c >= 0) { sm.ckey[c] = key; sm.cidx[c] = idx; }
+                const uint32_t dv = digit_of(d, kk, idx);
+                const int so = warp_alloc(&sm.n_sel, in && dv > dbin);
+                if (so >= 0 && so < TK_KMAX) { sm.okey[so] = kk; sm.oidx[so] = idx; }
+                const int c = warp_alloc(&sm.n_new, in && dv == dbin);
+                if (c >= 0) { sm.ckey[c] = kk; sm.cidx[c] = idx; }
             }
             __syncthreads();
             if (tid == 0) sm.n_cand = sm.n_new;
         } else {
-            const bool gather = n_bin <= (uint32_t)TK_SCAP;
+            const bool g2 = d_n <= (uint32_t)TK_SCAP;
             if (tid == 0) sm.n_cand = 0;
             __syncthreads();
             for (int64_t p0 = 0; p0 < G; p0 += 4 * TK_T) {
-                uint32_t key[4];
+                uint32_t kk[4];
                 const int64_t pos = p0 + 4 * tid;
-                load4(sc, pos, G, vec, key);
+                load4(sc, pos, G, vec, kk);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int32_t idx = (int32_t)(pos + q);
-                    const bool in = pos + q < G && matches(d, key[q], idx);
-                    const uint32_t dv = digit_of(d, key[q], idx);
-                    const int so = warp_alloc(&sm.n_sel, in && dv > bin);
-                    if (so >= 0 && so < TK_KMAX) { sm.okey[so] = key[q]; sm.oidx[so] = idx; }
-                    const int c = warp_alloc(&sm.n_cand, gather && in && dv == bin);
-                    if (c >= 0 && c < TK_SCAP) { sm.ckey[c] = key[q]; sm.cidx[c] = idx; }
+                    const bool in = pos + q < G && prefix_match(bins, d, kk[q], idx);
+                    const uint32_t dv = digit_of(d, kk[q], idx);
+                    const int so = warp_alloc(&sm.n_sel, in && dv > dbin);
+                    if (so >= 0 && so < TK_KMAX) { sm.okey[so] = kk[q]; sm.oidx[so] = idx; }
+                    const int c = warp_alloc(&sm.n_cand, g2 && in && dv == dbin);
+                    if (c >= 0 && c < TK_SCAP) { sm.ckey[c] = kk[q]; sm.cidx[c] = idx; }
                 }
             }
             __syncthreads();
-            if (tid == 0 && !gather) sm.n_cand = (int)n_bin;
-            implicit = !gather;
+            if (tid == 0 && !g2) sm.n_cand = (int)d_n;
+            implicit = !g2;
         }
         __syncthreads();
     }
-    // ---- the union of winners and survivors fits one sort
+    // ---- the union of winners and survivors fits one ranking
     const int n_w = sm.n_sel, n_c = implicit ? 0 : sm.n_cand;
     if (tid == 0 && n_w + n_c > TK_KMAX) raise_status(a.status, CSA_ERR_DEVICE_BOUNDS);
     for (int i = tid; i < n_c && n_w + i < TK_KMAX; i += TK_T) {
@@ -509,20 +575,34 @@ __global__ void __launch_bounds__(TK_T, 1) topk_select_kernel(TopkArgs a) {
         sm.oidx[n_w + i] = sm.cidx[i];
     }
     __syncthreads();
-    sort_and_write(sm, (uint32_t)min(n_w + n_c, TK_KMAX), k, out, kout);
+    rank_scatter(sm, min(n_w + n_c, TK_KMAX), k, out, kout);
+    if (tid == 0) ctl[0] = 0u;  // the counter is ready for the next call on this workspace
 }
 
-static int g_sms = 0;
-static int sm_count() {
-    if (!g_sms) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
-    }
-    return g_sms;
+// Phase-A CTAs per request and the per-CTA list capacities for a batch bound max_G.
+struct TopkGeometry {
+    int C;
+    int64_t capw, caps;
+};
+static TopkGeometry topk_geometry(int64_t max_G) {
+    TopkGeometry g;
+    int64_t c = (max_G + TK_CHUNK - 1) / TK_CHUNK;
+    if (c > TK_MAXC) c = TK_MAXC;
+    if (c < 1) c = 1;
+    g.C = (int)c;
+    g.caps = ((((max_G + c - 1) / c) + 3) & ~int64_t(3));
+    if (g.caps < 4) g.caps = 4;
+    g.capw = g.caps < TK_KMAX ? g.caps : TK_KMAX;
+    return g;
+}
+
+size_t topk_lists_bytes(int B, int64_t max_G) {
+    const TopkGeometry g = topk_geometry(max_G);
+    return (size_t)B * g.C * (size_t)(g.capw + g.caps) * sizeof(uint2);
 }
 
 static TopkArgs topk_args(const TopkLaunch& h) {
+    const TopkGeometry g = topk_geometry(h.max_G);
     TopkArgs a;
     a.scores = h.scores;
     a.B = h.B;
@@ -535,13 +615,13 @@ static TopkArgs topk_args(const TopkLaunch& h) {
     a.idx_out = h.idx_out;
     a.keys_out = h.keys_out;
     a.hist = h.hist;
+    a.capw = g.capw;
+    a.caps = g.caps;
     a.wlist = reinterpret_cast<uint2*>(h.lists);
-    a.slist = reinterpret_cast<uint2*>(h.lists) + (size_t)h.B * TK_KMAX;
+    a.slist = reinterpret_cast<uint2*>(h.lists) + (size_t)h.B * g.C * g.capw;
     a.status = h.status;
     return a;
 }
-
-size_t topk_lists_bytes(int B) { return (size_t)B * (TK_KMAX + TK_SCAP) * sizeof(uint2); }
 
 cudaError_t launch_topk_hist(const TopkLaunch& h, cudaStream_t s) {
     const TopkArgs a = topk_args(h);
@@ -573,18 +653,13 @@ cudaError_t launch_topk(const TopkLaunch& h, cudaStream_t s, bool pdl) {
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    // slices of about TK_CHUNK scores, at most one wave of CTAs over the batch
-    int64_t per = (h.max_G + TK_CHUNK - 1) / TK_CHUNK;
-    const int64_t cap = (sm_count() + h.B - 1) / h.B;
-    if (per > cap) per = cap;
-    if (per < 1) per = 1;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    cfg.gridDim = dim3((unsigned)per, (unsigned)h.B, 1);
+    cfg.gridDim = dim3((unsigned)topk_geometry(h.max_G).C, (unsigned)h.B, 1);
     cfg.blockDim = dim3(TK_T, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;

@@ -113,11 +113,11 @@ csa_status csa_index_score(const void* q_idx, const float* w_h, int32_t Hi, csa_
  * Radix select over the key's digits: the first digit's histogram is built by CTAs
  * whose shared-memory histograms are summed inside a cluster of 8 (distributed shared
  * memory); the select then runs wide over the scores and finishes in one CTA.
- * workspace: device, 16-byte aligned, at least csa_topk_workspace_size(1) bytes,
+ * workspace: device, 16-byte aligned, at least csa_topk_workspace_size(1, G) bytes,
  * owned by the caller, its contents overwritten (no state is kept between calls).
  * 1 <= k <= 2048, G <= 2^31 - 1.  CSA_ERR_WORKSPACE when it is missing or small.
  */
-size_t csa_topk_workspace_size(int32_t B);
+size_t csa_topk_workspace_size(int32_t B, int64_t max_G);
 csa_status csa_topk(const float* scores, int64_t G, int32_t k, int32_t* idx_out, uint32_t* keys_out,
                     void* workspace, size_t ws_bytes, void* stream);
 
@@ -125,7 +125,7 @@ csa_status csa_topk(const float* scores, int64_t G, int32_t k, int32_t* idx_out,
  * Batched stage 3 over a ragged batch: request b owns scores[offsets[b] .. offsets[b+1])
  * (offsets: device int64 [B+1]), writes idx_out[b*k .. b*k+k) (indices local to
  * the request).  max_G: host-side bound on every request's length.  workspace:
- * csa_topk_workspace_size(B) bytes.
+ * csa_topk_workspace_size(B, max_G) bytes.
  */
 csa_status csa_topk_batched(const float* scores, const int64_t* offsets, int32_t B, int64_t max_G, int32_t k,
                             int32_t* idx_out, uint32_t* keys_out, void* workspace, size_t ws_bytes,

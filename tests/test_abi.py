@@ -46,8 +46,9 @@ def test_library_loads_and_answers_host_queries(libpath):
     # argument validation is synchronous and touches no device memory
     assert L.csa_topk(None, 10, 4, None, None, None, 0, None) == csa.CSA_ERR_INVALID_ARG
     assert L.csa_topk(None, 10, 0, None, None, None, 0, None) == csa.CSA_ERR_UNSUPPORTED
-    assert csa.csa_topk_workspace_size(1) > 0 and csa.csa_topk_workspace_size(0) == 0
-    assert csa.csa_topk_workspace_size(32) > csa.csa_topk_workspace_size(1)
+    assert csa.csa_topk_workspace_size(1, 1000) > 0 and csa.csa_topk_workspace_size(0, 1000) == 0
+    assert csa.csa_topk_workspace_size(32, 1000) > csa.csa_topk_workspace_size(1, 1000)
+    assert csa.csa_topk_workspace_size(1, 262144) > csa.csa_topk_workspace_size(1, 1000)
     p = csa.csa_decode_params()
     assert L.csa_decode(ctypes.byref(p), None, 0, None) == csa.CSA_ERR_UNSUPPORTED
     assert csa.csa_decode_workspace_size(p) == 0
