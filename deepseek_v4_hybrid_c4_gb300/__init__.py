@@ -60,7 +60,7 @@ def lib() -> ctypes.CDLL:
         L.csa_index_score.argtypes = [vp, vp, i32, csa_paged, i32, i64, vp, vp]
         L.csa_topk.argtypes = [vp, i64, i32, vp, vp, vp, sz, vp]
         L.csa_topk_batched.argtypes = [vp, vp, i32, i64, i32, vp, vp, vp, sz, vp]
-        L.csa_topk_workspace_size.argtypes = [i32, i64]
+        L.csa_topk_workspace_size.argtypes = [i32, i64, i32]
         L.csa_topk_workspace_size.restype = sz
         L.csa_sparse_attn.argtypes = [vp, i32, f32, csa_paged, vp, i32, csa_paged, i64, i32, vp, vp, vp, sz, vp]
         L.csa_sparse_attn_workspace_size.argtypes = [i32, i32, i32]
@@ -136,8 +136,8 @@ def csa_index_score(q_idx, w_h, Hi: int, k_idx: csa_paged, k_dtype: int, G: int,
            "csa_index_score")
 
 
-def csa_topk_workspace_size(B: int, max_G: int) -> int:
-    return int(lib().csa_topk_workspace_size(B, max_G))
+def csa_topk_workspace_size(B: int, max_G: int, k: int) -> int:
+    return int(lib().csa_topk_workspace_size(B, max_G, k))
 
 
 def _scratch(nbytes: int, like):
@@ -147,9 +147,9 @@ def _scratch(nbytes: int, like):
 
 def csa_topk(scores, G: int, k: int, idx_out, keys_out=None, workspace=None, ws_bytes: int = 0,
              stream=None) -> None:
-    """workspace None: a scratch tensor of csa_topk_workspace_size(1, G) bytes is allocated."""
+    """workspace None: a scratch tensor of csa_topk_workspace_size(1, G, k) bytes is allocated."""
     if workspace is None:
-        ws_bytes = csa_topk_workspace_size(1, G)
+        ws_bytes = csa_topk_workspace_size(1, G, k)
         workspace = _scratch(ws_bytes, scores)
     _check(lib().csa_topk(_ptr(scores), G, k, _ptr(idx_out), _ptr(keys_out), _ptr(workspace), ws_bytes,
                           _stream(stream)), "csa_topk")
@@ -158,7 +158,7 @@ def csa_topk(scores, G: int, k: int, idx_out, keys_out=None, workspace=None, ws_
 def csa_topk_batched(scores, offsets, B: int, max_G: int, k: int, idx_out, keys_out=None, workspace=None,
                      ws_bytes: int = 0, stream=None) -> None:
     if workspace is None:
-        ws_bytes = csa_topk_workspace_size(B, max_G)
+        ws_bytes = csa_topk_workspace_size(B, max_G, k)
         workspace = _scratch(ws_bytes, scores)
     _check(lib().csa_topk_batched(_ptr(scores), _ptr(offsets), B, max_G, k, _ptr(idx_out), _ptr(keys_out),
                                   _ptr(workspace), ws_bytes, _stream(stream)), "csa_topk_batched")
@@ -192,7 +192,7 @@ def csa_decode_timed(p: csa_decode_params, workspace, ws_bytes: int, stream=None
 
 
 def csa_decode_noalloc(p: csa_decode_params, stream=None) -> None:
-    """csa_decode with the library's own fixed 16 MiB scratch (for callers that cannot allocate)."""
+    """csa_decode with the library's own fixed 32 MiB scratch (for callers that cannot allocate)."""
     _check(lib().csa_decode_noalloc(ctypes.byref(p), _stream(stream)), "csa_decode_noalloc")
 
 

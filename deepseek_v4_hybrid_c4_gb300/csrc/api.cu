@@ -152,15 +152,15 @@ csa_status csa_index_score(const void* q_idx, const float* w_h, int32_t Hi, csa_
     return from_cuda(launch_score(l, static_cast<cudaStream_t>(stream), false));
 }
 
-static size_t topk_ws_layout(int32_t B, int64_t max_G, size_t* lists_off) {
+static size_t topk_ws_layout(int32_t B, int64_t max_G, int32_t k, size_t* lists_off) {
     const size_t hist = align256((size_t)B * kHistBlock * sizeof(uint32_t));
     if (lists_off) *lists_off = hist;
-    return hist + align256(topk_lists_bytes(B, max_G));
+    return hist + align256(topk_lists_bytes(B, max_G, k));
 }
 
-size_t csa_topk_workspace_size(int32_t B, int64_t max_G) {
-    if (B < 1 || B > 65535 || max_G < 0 || max_G > 0x7FFFFFFFLL) return 0;
-    return topk_ws_layout(B, max_G, nullptr);
+size_t csa_topk_workspace_size(int32_t B, int64_t max_G, int32_t k) {
+    if (B < 1 || B > 65535 || max_G < 0 || max_G > 0x7FFFFFFFLL || k < 1 || k > 2048) return 0;
+    return topk_ws_layout(B, max_G, k, nullptr);
 }
 
 static csa_status topk_common(const float* scores, const int64_t* offsets, int32_t B, int64_t G, int32_t k,
@@ -171,7 +171,7 @@ static csa_status topk_common(const float* scores, const int64_t* offsets, int32
     if (keys_out && !al4(keys_out)) return CSA_ERR_INVALID_ARG;
     if (B < 1 || B > 65535 || G < 0 || G > 0x7FFFFFFFLL) return CSA_ERR_INVALID_ARG;
     size_t lists_off = 0;
-    const size_t need = topk_ws_layout(B, G, &lists_off);
+    const size_t need = topk_ws_layout(B, G, k, &lists_off);
     if (!workspace || ws_bytes < need || !al16(workspace)) return CSA_ERR_WORKSPACE;
     int32_t* st = status_ptr();
     if (!st) return CSA_ERR_CUDA;
@@ -298,7 +298,7 @@ static DecodeLayout decode_layout(const csa_decode_params* p) {
     L.hist = off;
     if (p->ratio == 4) off += align256((size_t)p->B * kHistBlock * sizeof(uint32_t));
     L.lists = off;
-    if (p->ratio == 4) off += align256(topk_lists_bytes(p->B, max_G));
+    if (p->ratio == 4) off += align256(topk_lists_bytes(p->B, max_G, p->k));
     L.sel = off;
     if (p->ratio == 4 && !p->sel) off += align256((size_t)p->B * p->k * sizeof(int32_t));
     L.attn = off;

@@ -63,7 +63,7 @@ cudaError_t launch_score(const ScoreLaunch& a, cudaStream_t s, bool pdl);
 // Stage 3.  Request b's scores: single: [0, G); offsets mode: [offsets[b], offsets[b+1]);
 // decode mode: b * score_stride + [0, n_tokens[b] / ratio).  hist: [B][kHistBlock] words,
 // zeroed before the step; the first digit's histogram is either fused into stage 2 or
-// built by launch_topk_hist.  lists: topk_lists_bytes(B, max_G) of scratch.
+// built by launch_topk_hist.  lists: topk_lists_bytes(B, max_G, k) of scratch.
 struct TopkLaunch {
     const float* scores;
     int B;
@@ -80,7 +80,7 @@ struct TopkLaunch {
     void* lists;
     int32_t* status;
 };
-size_t topk_lists_bytes(int B, int64_t max_G);
+size_t topk_lists_bytes(int B, int64_t max_G, int k);
 cudaError_t launch_topk_hist(const TopkLaunch& a, cudaStream_t s);
 cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t s, bool pdl);
 

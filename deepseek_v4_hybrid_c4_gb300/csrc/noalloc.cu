@@ -16,7 +16,7 @@ namespace csa {
 
 // Largest workspace a call may need, in bytes.  Every device that loads the
 // library holds this array until the process exits.
-constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 

@@ -401,8 +401,8 @@ __global__ void __launch_bounds__(TK_T, 1) topk_select_kernel(TopkArgs a) {
                 else raise_status(a.status, CSA_ERR_DEVICE_BOUNDS);
                 ++bs;
             } else if (sur) {
-                sl[bc] = make_uint2(key[q], (uint32_t)(pos + q));  // capacity: the slice length
-                ++bc;
+                if (bc < (uint32_t)a.caps) sl[bc] = make_uint2(key[q], (uint32_t)(pos + q));
+                ++bc;  // past the capacity only counted: phase B then scans the scores instead
             }
             hist_add(sm.hist, (key[q] >> 10) & 2047u, sur);  // the survivors' second digit
         }
@@ -433,9 +433,11 @@ __global__ void __launch_bounds__(TK_T, 1) topk_select_kernel(TopkArgs a) {
     const uint32_t h1h = __ldcg(ghist1 + bh), h1l = __ldcg(ghist1 + bl);
     if (warp == 0) {  // per-CTA list offsets: exclusive prefix over the table
         uint32_t cw = 0, cs = 0;
+        bool over = false;
         for (int c0 = 0; c0 < C; c0 += 32) {
             const int c = c0 + lane;
             const uint32_t tw = c < C ? __ldcg(table + 2 * c) : 0u, ts = c < C ? __ldcg(table + 2 * c + 1) : 0u;
+            over |= __any_sync(0xffffffffu, ts > (uint32_t)a.caps);
             uint32_t xw = tw, xs = ts;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -452,6 +454,7 @@ __global__ void __launch_bounds__(TK_T, 1) topk_select_kernel(TopkArgs a) {
         if (lane == 0) {
             sm.pw[C] = cw;
             sm.ps[C] = cs;
+            sm.n_new = over ? 1 : 0;  // a CTA's survivors overflowed its region
         }
     }
     __syncthreads();
@@ -471,7 +474,7 @@ __global__ void __launch_bounds__(TK_T, 1) topk_select_kernel(TopkArgs a) {
         sm.okey[j] = e.x;
         sm.oidx[j] = (int32_t)e.y;
     }
-    const bool s_fit = n_s0 <= TK_SCAP;
+    const bool s_fit = n_s0 <= TK_SCAP && sm.n_new == 0;
     if (!all_in && s_fit) {
 #pragma unroll 4
         for (int j = tid; j < n_s0; j += TK_T) {
@@ -580,29 +583,36 @@ __global__ void __launch_bounds__(TK_T, 1) topk_select_kernel(TopkArgs a) {
 }
 
 // Phase-A CTAs per request and the per-CTA list capacities for a batch bound max_G.
+// Winners: a CTA never holds more than min(slice, k).  Survivors: an even share of what
+// phase B can hold in shared memory (at least 256); a CTA with more only counts them and
+// phase B then works from the scores.
 struct TopkGeometry {
     int C;
     int64_t capw, caps;
 };
-static TopkGeometry topk_geometry(int64_t max_G) {
+static TopkGeometry topk_geometry(int64_t max_G, int k) {
     TopkGeometry g;
     int64_t c = (max_G + TK_CHUNK - 1) / TK_CHUNK;
     if (c > TK_MAXC) c = TK_MAXC;
     if (c < 1) c = 1;
     g.C = (int)c;
-    g.caps = ((((max_G + c - 1) / c) + 3) & ~int64_t(3));
+    const int64_t slice = ((((max_G + c - 1) / c) + 3) & ~int64_t(3));
+    int64_t share = TK_SCAP / c;
+    if (share < 256) share = 256;
+    g.caps = slice < share ? slice : share;
     if (g.caps < 4) g.caps = 4;
-    g.capw = g.caps < TK_KMAX ? g.caps : TK_KMAX;
+    g.capw = slice < k ? slice : k;
+    if (g.capw < 4) g.capw = 4;
     return g;
 }
 
-size_t topk_lists_bytes(int B, int64_t max_G) {
-    const TopkGeometry g = topk_geometry(max_G);
+size_t topk_lists_bytes(int B, int64_t max_G, int k) {
+    const TopkGeometry g = topk_geometry(max_G, k);
     return (size_t)B * g.C * (size_t)(g.capw + g.caps) * sizeof(uint2);
 }
 
 static TopkArgs topk_args(const TopkLaunch& h) {
-    const TopkGeometry g = topk_geometry(h.max_G);
+    const TopkGeometry g = topk_geometry(h.max_G, h.k);
     TopkArgs a;
     a.scores = h.scores;
     a.B = h.B;
@@ -659,7 +669,7 @@ cudaError_t launch_topk(const TopkLaunch& h, cudaStream_t s, bool pdl) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    cfg.gridDim = dim3((unsigned)topk_geometry(h.max_G).C, (unsigned)h.B, 1);
+    cfg.gridDim = dim3((unsigned)topk_geometry(h.max_G, h.k).C, (unsigned)h.B, 1);
     cfg.blockDim = dim3(TK_T, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;

@@ -113,11 +113,11 @@ csa_status csa_index_score(const void* q_idx, const float* w_h, int32_t Hi, csa_
  * Radix select over the key's digits: the first digit's histogram is built by CTAs
  * whose shared-memory histograms are summed inside a cluster of 8 (distributed shared
  * memory); the select then runs wide over the scores and finishes in one CTA.
- * workspace: device, 16-byte aligned, at least csa_topk_workspace_size(1, G) bytes,
+ * workspace: device, 16-byte aligned, at least csa_topk_workspace_size(1, G, k) bytes,
  * owned by the caller, its contents overwritten (no state is kept between calls).
  * 1 <= k <= 2048, G <= 2^31 - 1.  CSA_ERR_WORKSPACE when it is missing or small.
  */
-size_t csa_topk_workspace_size(int32_t B, int64_t max_G);
+size_t csa_topk_workspace_size(int32_t B, int64_t max_G, int32_t k);
 csa_status csa_topk(const float* scores, int64_t G, int32_t k, int32_t* idx_out, uint32_t* keys_out,
                     void* workspace, size_t ws_bytes, void* stream);
 
@@ -125,7 +125,7 @@ csa_status csa_topk(const float* scores, int64_t G, int32_t k, int32_t* idx_out,
  * Batched stage 3 over a ragged batch: request b owns scores[offsets[b] .. offsets[b+1])
  * (offsets: device int64 [B+1]), writes idx_out[b*k .. b*k+k) (indices local to
  * the request).  max_G: host-side bound on every request's length.  workspace:
- * csa_topk_workspace_size(B, max_G) bytes.
+ * csa_topk_workspace_size(B, max_G, k) bytes.
  */
 csa_status csa_topk_batched(const float* scores, const int64_t* offsets, int32_t B, int64_t max_G, int32_t k,
                             int32_t* idx_out, uint32_t* keys_out, void* workspace, size_t ws_bytes,
@@ -219,9 +219,9 @@ csa_status csa_decode_timed(const csa_decode_params* p, void* workspace, size_t 
  * only hands the library its input and output buffers, or a runtime that forbids
  * cudaMalloc once it has started.  (The pages have no counterpart: this is a
  * packaging of csa_decode, not part of the method.)
- * The scratch comes from a fixed 16 MiB array in libcsa's own device memory, which
+ * The scratch comes from a fixed 32 MiB array in libcsa's own device memory, which
  * every GPU that loads the library holds until the process exits; a call whose
- * csa_decode_workspace_size() exceeds 16 MiB returns CSA_ERR_WORKSPACE and enqueues
+ * csa_decode_workspace_size() exceeds 32 MiB returns CSA_ERR_WORKSPACE and enqueues
  * nothing.  Nothing is allocated and no scratch contents need to start at zero.
  * The first call on a device looks up the array's device address (with that device
  * current); make that first call before any stream capture.  Every call shares the

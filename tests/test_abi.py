@@ -46,9 +46,10 @@ def test_library_loads_and_answers_host_queries(libpath):
     # argument validation is synchronous and touches no device memory
     assert L.csa_topk(None, 10, 4, None, None, None, 0, None) == csa.CSA_ERR_INVALID_ARG
     assert L.csa_topk(None, 10, 0, None, None, None, 0, None) == csa.CSA_ERR_UNSUPPORTED
-    assert csa.csa_topk_workspace_size(1, 1000) > 0 and csa.csa_topk_workspace_size(0, 1000) == 0
-    assert csa.csa_topk_workspace_size(32, 1000) > csa.csa_topk_workspace_size(1, 1000)
-    assert csa.csa_topk_workspace_size(1, 262144) > csa.csa_topk_workspace_size(1, 1000)
+    assert csa.csa_topk_workspace_size(1, 1000, 512) > 0 and csa.csa_topk_workspace_size(0, 1000, 512) == 0
+    assert csa.csa_topk_workspace_size(1, 1000, 0) == 0 and csa.csa_topk_workspace_size(1, 1000, 2049) == 0
+    assert csa.csa_topk_workspace_size(32, 1000, 512) > csa.csa_topk_workspace_size(1, 1000, 512)
+    assert csa.csa_topk_workspace_size(1, 262144, 512) > csa.csa_topk_workspace_size(1, 1000, 512)
     p = csa.csa_decode_params()
     assert L.csa_decode(ctypes.byref(p), None, 0, None) == csa.CSA_ERR_UNSUPPORTED
     assert csa.csa_decode_workspace_size(p) == 0
@@ -70,3 +71,25 @@ def test_product_path_does_not_reach_the_oracle():
                 src = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+(oracle|synth)\b", src, re.M), f
                 assert "liboracle" not in src and "orc_" not in src, f
+
+
+def test_every_workload_fits_the_noalloc_scratch(libpath):
+    """csa_decode_noalloc serves each of the five synthetic workloads at full size: the
+    workspace each needs (a host-side computation, no device) fits its fixed 32 MiB array."""
+    import synth
+    import deepseek_v4_hybrid_c4_gb300 as csa
+    for i in range(5):
+        c = synth.config(i)
+        p = csa.csa_decode_params()
+        p.B, p.ratio, p.H, p.Hi, p.k, p.swa = len(c.requests), c.ratio, c.H, c.Hi, c.k, c.swa
+        p.scale = 0.04
+        p.k_dtype = csa.CSA_BF16 if c.kdtype == "bf16" else csa.CSA_FP8_E4M3
+        p.max_tokens = max(r.n_tokens for r in c.requests)
+        for f in ("n_tokens", "n_groups_done", "kv_raw", "kv_c", "k_idx", "w_gate", "b_pos", "q", "q_idx", "w_h",
+                  "out", "lse", "sel", "page_table", "c_page_table"):
+            setattr(p, f, 4096)  # never dereferenced by the size query
+        p.raw_rows_per_page, p.raw_page_stride, p.n_pages = c.rows_per_page, c.rows_per_page * 1024, 1 << 20
+        p.c_rows_per_page, p.c_page_stride, p.c_n_pages = 16, 16 * 1024, 1 << 20
+        p.kidx_page_stride = 16 * 256
+        need = csa.csa_decode_workspace_size(p)
+        assert 0 < need <= 32 << 20, (i, need)
