@@ -305,7 +305,7 @@ static DecodeLayout decode_layout(const csa_decode_params* p) {
     const int64_t W = p->max_tokens < p->swa ? p->max_tokens : p->swa;
     const int64_t max_keys = (p->ratio == 4 ? p->k : max_G) + W;
     off += align256(attn_workspace_bytes(p->B, p->H, max_keys));
-    L.total = off;
+    L.total = off > 256 ? off : 256;  // never 0: a size of 0 means the parameters were rejected
     return L;
 }
 

@@ -16,8 +16,14 @@
 //   by more than 2^8, then O is rescaled in TMEM); P (bf16) goes to shared memory;
 //   O += P V with tcgen05.mma (M=128, N=256, K=64) where the same K tile is read
 //   as an MN-major B operand.
-// S uses TMEM columns [256, 320), the O half [0, 256).  Splits are merged by a
-// log-sum-exp kernel (or written directly when a request has one split).
+// S uses TMEM columns [256, 320), the O half [0, 256).
+//
+// With one split per request the CTA writes the bf16 output directly.  Otherwise each
+// split writes its rows normalised by their own sum (O_s / l_s as fp16: |values| <=
+// max |V|, relative rounding 2^-11) and its (max, sum) to the workspace with coalesced
+// stores (staged through shared memory), and a merge kernel (one CTA per head and
+// request, chained by programmatic dependent launch) computes
+// O = sum_s (l_s 2^(m_s - M) / L) (O_s / l_s) with every split's row loaded at once.
 #include "common.cuh"
 #include "internal.h"
 
@@ -35,6 +41,9 @@ constexpr uint32_t SM_TMEM = SM_BAR + 16;
 constexpr uint32_t SM_KPTR = SM_BAR + 64;          // 64 row pointers
 constexpr uint32_t SM_KOK = SM_KPTR + 64 * 8;      // 64-bit valid mask
 constexpr uint32_t AT_SMEM = SM_KOK + 64 + 1024;   // + alignment slack
+constexpr uint32_t R_PITCH = AT_DH * 2 + 16;       // staged fp16 row of one half (padded)
+constexpr uint32_t SM_STG = 0;                     // this split's [128] staged rows (the Q tile's space)
+constexpr int AT_MAX_SPLITS = 16;                  // splits per request (the merge holds them in registers)
 constexpr uint32_t Q_SLAB = AT_M * 128;
 constexpr uint32_t K_SLAB = AT_KT * 128;
 constexpr float LOG2E = 1.4426950408889634f;
@@ -54,12 +63,20 @@ struct AttnArgs {
     int64_t N;
     int swa;
     int tps, S;
-    float* part_o;             // [B][S][H][512]
-    float* part_ml;            // [B][S][H][2]  (max in log2 units, sum)
+    __half* part_o;            // [B][S][H][512] normalised partial rows (fp16)
+    float2* part_ml;           // [B][2 halves][S][H] {max (log2 units), sum}
     uint16_t* out;
     float* lse;
     int32_t* status;
 };
+
+// 2^x with the hardware's approximate exponential (ex2.approx.ftz: relative error below
+// 2^-22, 2^-inf = +0); the softmax weights are graded by tolerance.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk) {  // byte offset inside a 128-B-row slab
     return row * 128u + ((chunk ^ (row & 7u)) << 4);
@@ -85,6 +102,7 @@ __global__ void __launch_bounds__(AT_T, 1) attn_kernel(AttnArgs a) {
     const int H = a.H;
     const int h = tid;  // head row owned by this thread
 
+    const int S = a.S;
     float m_run = -INFINITY, l_run = 0.f;
     if (t0 >= t1) {
         pdl_wait();
@@ -190,7 +208,7 @@ __global__ void __launch_bounds__(AT_T, 1) attn_kernel(AttnArgs a) {
                 if (m_run == -INFINITY) {
                     m_run = mt;
                 } else if (mt > m_run + RESCALE_THRESHOLD) {
-                    alpha = exp2f(m_run - mt);
+                    alpha = ex2(m_run - mt);
                     m_run = mt;
                 }
             }
@@ -212,8 +230,8 @@ __global__ void __launch_bounds__(AT_T, 1) attn_kernel(AttnArgs a) {
             uint32_t pk[32];
 #pragma unroll
             for (int j = 0; j < 64; j += 2) {
-                const float p0 = m_run == -INFINITY ? 0.f : exp2f(x[j] - m_run);
-                const float p1 = m_run == -INFINITY ? 0.f : exp2f(x[j + 1] - m_run);
+                const float p0 = m_run == -INFINITY ? 0.f : ex2(x[j] - m_run);
+                const float p1 = m_run == -INFINITY ? 0.f : ex2(x[j + 1] - m_run);
                 const uint32_t w = pack_bf16x2(p0, p1);
                 pk[j >> 1] = w;
                 lsum += bf16lo(w) + bf16hi(w);
@@ -243,108 +261,99 @@ __global__ void __launch_bounds__(AT_T, 1) attn_kernel(AttnArgs a) {
         if (!mbar_wait(bar_o, (uint32_t)((it - 1) & 1))) ok = false;
         tc_fence_after();
         if (!ok && tid == 0) raise_status(a.status, CSA_ERR_TIMEOUT);
-        // ---- epilogue: this thread's O row (256 columns of its half) goes TMEM -> registers ->
-        // shared memory (padded rows: conflict-free) -> one bulk async copy per row to global.
-        // Every MMA has completed, so the Q/K tiles' shared memory is free for staging.
-        const bool direct = a.S == 1;
+    }
+    // ---- this split's rows, normalised (fp16 partial, or the bf16 output when S == 1), into
+    //      shared memory (every MMA has completed, so the Q/K tiles' space is free), then
+    //      coalesced to global memory
+    const bool direct = S == 1;
+    if (t0 < t1) {
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-        const uint32_t row_bytes = direct ? AT_DH * 2 : AT_DH * 4;  // bf16 output / fp32 partial
-        const uint32_t pitch = row_bytes + 16;
-        const uint32_t srow = sbase + SM_Q + (uint32_t)h * pitch;
+        const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + SM_TMEM);
+        const uint32_t srow = sbase + SM_STG + (uint32_t)h * R_PITCH;
         for (int c = 0; c < AT_DH; c += 32) {
             uint32_t o[32];
-            tc_ld32(t_o + lane_off + c, o);
+            tc_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, o);
             tc_wait_ld();
-            if (direct) {
 #pragma unroll
-                for (int e = 0; e < 32; e += 8) {
-                    uint4 v;
-                    v.x = pack_bf16x2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
-                    v.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
-                    v.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
-                    v.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
-                    st_shared_v4(srow + (uint32_t)(c + e) * 2u, v);
+            for (int e = 0; e < 32; e += 8) {
+                uint32_t w4[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float f0 = __uint_as_float(o[e + 2 * q]) * inv, f1 = __uint_as_float(o[e + 2 * q + 1]) * inv;
+                    if (direct) {
+                        w4[q] = pack_bf16x2(f0, f1);
+                    } else {
+                        const __half2 hv = __floats2half2_rn(f0, f1);
+                        w4[q] = *reinterpret_cast<const uint32_t*>(&hv);
+                    }
                 }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 32; e += 4)
-                    st_shared_v4(srow + (uint32_t)(c + e) * 4u, make_uint4(o[e], o[e + 1], o[e + 2], o[e + 3]));
+                st_shared_v4(srow + (uint32_t)(c + e) * 2u, make_uint4(w4[0], w4[1], w4[2], w4[3]));
             }
-        }
-        fence_proxy_async_smem();
-        if (h < H) {
-            void* dst = direct ? static_cast<void*>(a.out + ((int64_t)b * H + h) * D + half * AT_DH)
-                               : static_cast<void*>(a.part_o + (((int64_t)b * a.S + split) * H + h) * D + half * AT_DH);
-            bulk_s2g(dst, srow, row_bytes);
-            bulk_commit();
-            bulk_wait_read0();  // the staging rows must stay valid until the copy has read them
         }
         tc_fence_before();
         __syncthreads();
         if (warp == 0) tmem_dealloc(tmem, 512);
-    }
-    if (h < H && half == 0) {
-        if (a.S == 1) {
-            if (a.lse) a.lse[(int64_t)b * H + h] = l_run > 0.f ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
-        } else {
-            float* ml = a.part_ml + (((int64_t)b * a.S + split) * H + h) * 2;
-            ml[0] = m_run;
-            ml[1] = l_run;
+        // warp w copies rows w, w + 4, ...: one 512-byte row per warp instruction
+        uint16_t* dst = direct ? a.out + (int64_t)b * H * D + half * AT_DH
+                               : reinterpret_cast<uint16_t*>(a.part_o + ((int64_t)b * S + split) * H * D + half * AT_DH);
+        for (int r = warp; r < H; r += AT_T / 32) {
+            const uint4 v = ld_shared_v4(sbase + SM_STG + (uint32_t)r * R_PITCH + (uint32_t)lane * 16u);
+            *reinterpret_cast<uint4*>(dst + (int64_t)r * D + lane * 8) = v;
         }
+    } else if (direct) {  // no keys at all
+        for (int r = warp; r < H; r += AT_T / 32)
+            *reinterpret_cast<uint4*>(a.out + ((int64_t)b * H + r) * D + half * AT_DH + lane * 8) = make_uint4(0, 0, 0, 0);
+    }
+    if (h < H) {
+        const float l = t0 < t1 ? l_run : 0.f;
+        if (!direct)
+            a.part_ml[(((int64_t)b * 2 + half) * S + split) * H + h] = make_float2(m_run, l);
+        else if (half == 0 && a.lse)
+            a.lse[(int64_t)b * H + h] = l > 0.f ? (m_run + log2f(l)) * LN2 : -INFINITY;
     }
 }
 
-// Log-sum-exp merge of the splits: one CTA per (head, request), 4 columns per thread.
+// Log-sum-exp merge of the splits: one CTA per (head, request); thread t owns columns
+// 4t .. 4t+3 (half t / 64).  Every split's (max, sum) and row piece are loaded at once.
 __global__ void __launch_bounds__(128) attn_merge_kernel(AttnArgs a) {
     pdl_wait();
-    const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
-    const int H = a.H, S = a.S;
-    const float* ml = a.part_ml + ((int64_t)b * S * H) * 2;
-    const float* po = a.part_o + ((int64_t)b * S * H + h) * D + tid * 4;
+    const int h = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
+    const int H = a.H, S = a.S, half = t >> 6;
+    const float2* mlb = a.part_ml + ((int64_t)b * 2 + half) * S * H + h;
+    const __half* pb = a.part_o + ((int64_t)b * S * H + h) * D + t * 4;
+    float2 ml[AT_MAX_SPLITS];
+    uint2 x[AT_MAX_SPLITS];
+#pragma unroll
+    for (int s = 0; s < AT_MAX_SPLITS; ++s) {
+        if (s < S) {
+            ml[s] = __ldcg(mlb + (int64_t)s * H);
+            x[s] = __ldcg(reinterpret_cast<const uint2*>(pb + (int64_t)s * H * D));
+        }
+    }
     float M = -INFINITY;
-    for (int s = 0; s < S; ++s) {
-        const float2 v = *reinterpret_cast<const float2*>(ml + ((int64_t)s * H + h) * 2);
-        if (v.y > 0.f) M = fmaxf(M, v.x);
-    }
-    float L = 0.f;
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    int s = 0;
-    for (; s + 4 <= S; s += 4) {  // four splits' loads in flight at once
-        float2 v[4];
-        float4 x[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            v[u] = *reinterpret_cast<const float2*>(ml + ((int64_t)(s + u) * H + h) * 2);
-            x[u] = *reinterpret_cast<const float4*>(po + (int64_t)(s + u) * H * D);
-        }
+    for (int s = 0; s < AT_MAX_SPLITS; ++s)
+        if (s < S && ml[s].y > 0.f) M = fmaxf(M, ml[s].x);
+    float L = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            if (!(v[u].y > 0.f)) continue;
-            const float w = exp2f(v[u].x - M);
-            L = fmaf(w, v[u].y, L);
-            o.x = fmaf(w, x[u].x, o.x);
-            o.y = fmaf(w, x[u].y, o.y);
-            o.z = fmaf(w, x[u].z, o.z);
-            o.w = fmaf(w, x[u].w, o.w);
+    for (int s = 0; s < AT_MAX_SPLITS; ++s) {
+        if (s < S && ml[s].y > 0.f) {
+            const float w = ml[s].y * ex2(ml[s].x - M);
+            const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&x[s].x));
+            const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&x[s].y));
+            L += w;
+            o0 = fmaf(w, f01.x, o0);
+            o1 = fmaf(w, f01.y, o1);
+            o2 = fmaf(w, f23.x, o2);
+            o3 = fmaf(w, f23.y, o3);
         }
-    }
-    for (; s < S; ++s) {
-        const float2 v = *reinterpret_cast<const float2*>(ml + ((int64_t)s * H + h) * 2);
-        if (!(v.y > 0.f)) continue;
-        const float4 x = *reinterpret_cast<const float4*>(po + (int64_t)s * H * D);
-        const float w = exp2f(v.x - M);
-        L = fmaf(w, v.y, L);
-        o.x = fmaf(w, x.x, o.x);
-        o.y = fmaf(w, x.y, o.y);
-        o.z = fmaf(w, x.z, o.z);
-        o.w = fmaf(w, x.w, o.w);
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     uint2 r;
-    r.x = pack_bf16x2(o.x * inv, o.y * inv);
-    r.y = pack_bf16x2(o.z * inv, o.w * inv);
-    *reinterpret_cast<uint2*>(a.out + ((int64_t)b * H + h) * D + tid * 4) = r;
-    if (tid == 0 && a.lse) a.lse[(int64_t)b * H + h] = L > 0.f ? (M + log2f(L)) * LN2 : -INFINITY;
+    r.x = pack_bf16x2(o0 * inv, o1 * inv);
+    r.y = pack_bf16x2(o2 * inv, o3 * inv);
+    *reinterpret_cast<uint2*>(a.out + ((int64_t)b * H + h) * D + t * 4) = r;
+    if (t == 0 && a.lse) a.lse[(int64_t)b * H + h] = L > 0.f ? (M + log2f(L)) * LN2 : -INFINITY;
 }
 
 // Split heuristic (device independent so workspace sizes are stable): about one
@@ -353,6 +362,7 @@ static void plan_splits(int B, int64_t max_keys, int* tps, int* S) {
     const int64_t T = (max_keys + AT_KT - 1) / AT_KT;
     int64_t s = 76 / (B > 0 ? B : 1);
     if (s < 1) s = 1;
+    if (s > AT_MAX_SPLITS) s = AT_MAX_SPLITS;
     if (s > T) s = T;
     if (s < 1) s = 1;
     int64_t t = (T + s - 1) / s;
@@ -366,9 +376,8 @@ static void plan_splits(int B, int64_t max_keys, int* tps, int* S) {
 size_t attn_workspace_bytes(int B, int H, int64_t max_keys) {
     int tps, S;
     plan_splits(B, max_keys, &tps, &S);
-    if (S == 1) return 0;
-    const size_t po = (size_t)B * S * H * D * sizeof(float);
-    const size_t pm = (size_t)B * S * H * 2 * sizeof(float);
+    const size_t po = (size_t)B * S * H * D * sizeof(__half);
+    const size_t pm = (size_t)B * 2 * S * H * sizeof(float2);
     return ((po + 255) & ~size_t(255)) + pm;
 }
 
@@ -398,9 +407,9 @@ cudaError_t launch_attn(const AttnLaunch& h, cudaStream_t s, bool pdl) {
     a.N = h.N;
     a.swa = h.swa;
     plan_splits(h.B, h.max_keys, &a.tps, &a.S);
-    const size_t po = (size_t)h.B * a.S * h.H * D * sizeof(float);
-    a.part_o = static_cast<float*>(h.ws);
-    a.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(h.ws) + ((po + 255) & ~size_t(255)));
+    const size_t po = (size_t)h.B * a.S * h.H * D * sizeof(__half);
+    a.part_o = static_cast<__half*>(h.ws);
+    a.part_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(h.ws) + ((po + 255) & ~size_t(255)));
     a.out = static_cast<uint16_t*>(h.out);
     a.lse = h.lse;
     a.status = h.status;
@@ -422,6 +431,7 @@ cudaError_t launch_attn(const AttnLaunch& h, cudaStream_t s, bool pdl) {
     cfg.stream = s;
     cudaError_t e = cudaLaunchKernelEx(&cfg, attn_kernel, a);
     if (e != cudaSuccess || a.S == 1) return e;
+    cfg.numAttrs = 1;  // the merge waits for the attention grid (griddepcontrol.wait)
     cfg.gridDim = dim3((unsigned)h.H, (unsigned)h.B, 1);
     cfg.blockDim = dim3(128, 1, 1);
     cfg.dynamicSmemBytes = 0;

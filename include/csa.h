@@ -201,6 +201,9 @@ typedef struct {
     int32_t* sel;                /* int32 [B, k], nullable (ratio 4): the selected candidates */
 } csa_decode_params;
 
+/* workspace: device, 16-byte aligned, caller-owned, at least csa_decode_workspace_size(p)
+ * bytes; its contents need not start at zero and are overwritten.  The size query returns
+ * 0 only when the parameters are rejected (csa_decode then returns the reason). */
 csa_status csa_decode(const csa_decode_params* p, void* workspace, size_t ws_bytes, void* stream);
 size_t csa_decode_workspace_size(const csa_decode_params* p);
 
