@@ -189,6 +189,7 @@ static csa_status topk_common(const float* scores, const int64_t* offsets, int32
     t.k = k;
     t.idx_out = idx_out;
     t.keys_out = keys_out;
+    t.sorted = true;
     t.hist = reinterpret_cast<uint32_t*>(ws);
     t.lists = ws + lists_off;
     t.status = st;
@@ -405,6 +406,7 @@ csa_status csa_decode_timed(const csa_decode_params* p, void* workspace, size_t 
         t.k = p->k;
         t.idx_out = sel_out;
         t.keys_out = nullptr;
+        t.sorted = false;  // attention takes the set; a fixed order keeps the step deterministic
         t.hist = hist;
         t.lists = ws + L.lists;
         t.status = st;

@@ -76,6 +76,7 @@ struct TopkLaunch {
     int k;
     int32_t* idx_out;          // [B, k]
     uint32_t* keys_out;        // [B, k] or nullptr
+    bool sorted;               // true: by (score desc, index asc); false: the set in a fixed order
     uint32_t* hist;
     void* lists;
     int32_t* status;

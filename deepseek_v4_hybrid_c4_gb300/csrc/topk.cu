@@ -47,6 +47,7 @@ struct TopkArgs {
     int k;
     int32_t* idx_out;
     uint32_t* keys_out;
+    int sorted;       // 1: output ordered by (score desc, index asc); 0: the set, in a fixed order
     uint32_t* hist;   // [B][kHistBlock]: digit histograms, control words, per-CTA counts
     uint2* wlist;     // [B][C][capw] winners {key, index}, one region per CTA
     uint2* slist;     // [B][C][caps] survivors
@@ -83,17 +84,6 @@ __device__ __forceinline__ void request_span(const TopkArgs& a, int b, const flo
     if (G < 0) G = 0;
 }
 
-__device__ __forceinline__ int warp_alloc(int* counter, bool pred) {
-    const unsigned m = __ballot_sync(0xffffffffu, pred);
-    if (m == 0) return -1;
-    const int lane = threadIdx.x & 31;
-    const int leader = __ffs(m) - 1;
-    int base = 0;
-    if (lane == leader) base = atomicAdd(counter, __popc(m));
-    base = __shfl_sync(0xffffffffu, base, leader);
-    return pred ? base + __popc(m & ((1u << lane) - 1u)) : -1;
-}
-
 __device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t digit, bool active) {
     const unsigned m = __ballot_sync(0xffffffffu, active);
     if (!active) return;
@@ -126,6 +116,22 @@ __device__ __forceinline__ uint32_t block_scan(TkSmem& sm, uint32_t v, uint32_t*
     *total = sm.wsum[31];
     __syncthreads();
     return before + x - v;
+}
+
+// Order-preserving split of one chunk (one element per thread): `win` elements are
+// appended to the winners (sm.n_sel), `stay` elements to the survivors at *n_stay, both
+// in thread order.  Returns this thread's slots (-1 when not taken).  Every thread calls it.
+__device__ __forceinline__ void ordered_split(TkSmem& sm, bool win, bool stay, int* n_stay, int& so, int& sc) {
+    uint32_t tot;
+    const uint32_t ex = block_scan(sm, (win ? 0x10000u : 0u) | (stay ? 1u : 0u), &tot);
+    so = win ? sm.n_sel + (int)(ex >> 16) : -1;
+    sc = stay ? *n_stay + (int)(ex & 0xFFFFu) : -1;
+    __syncthreads();  // every thread has read the counters
+    if (threadIdx.x == 0) {
+        sm.n_sel += (int)(tot >> 16);
+        *n_stay += (int)(tot & 0xFFFFu);
+    }
+    __syncthreads();
 }
 
 // The bin holding the need-th largest element counted from the top bin, given this
@@ -490,7 +496,9 @@ __global__ void __launch_bounds__(TK_T, 1) topk_select_kernel(TopkArgs a) {
     }
     __syncthreads();
     uint32_t need = all_in ? 0u : (uint32_t)k - (uint32_t)n_w0;
-    const int rank_max = k <= 1024 ? 1024 : TK_KMAX;
+    // refine until winners plus survivors fit one ranking (sorted output) or are exactly the
+    // k selected (set output: the survivors left are then exactly the ones needed)
+    const int rank_max = a.sorted ? (k <= 1024 ? 1024 : TK_KMAX) : k;
     uint32_t bins[6] = {b0, 0, 0, 0, 0, 0};
     bool implicit = !all_in && !s_fit;  // survivors not in shared memory: the digits scan the scores
     for (int d = 1; d <= 5 && sm.n_sel + sm.n_cand > rank_max; ++d) {
@@ -538,9 +546,9 @@ __global__ void __launch_bounds__(TK_T, 1) topk_select_kernel(TopkArgs a) {
                 const int32_t idx = in ? sm.cidx[i] : 0;
                 __syncthreads();
                 const uint32_t dv = digit_of(d, kk, idx);
-                const int so = warp_alloc(&sm.n_sel, in && dv > dbin);
+                int so, c;
+                ordered_split(sm, in && dv > dbin, in && dv == dbin, &sm.n_new, so, c);
                 if (so >= 0 && so < TK_KMAX) { sm.okey[so] = kk; sm.oidx[so] = idx; }
-                const int c = warp_alloc(&sm.n_new, in && dv == dbin);
                 if (c >= 0) { sm.ckey[c] = kk; sm.cidx[c] = idx; }
             }
             __syncthreads();
@@ -554,13 +562,13 @@ __global__ void __launch_bounds__(TK_T, 1) topk_select_kernel(TopkArgs a) {
                 const int64_t pos = p0 + 4 * tid;
                 load4(sc, pos, G, vec, kk);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < 4; ++q) {  // a fixed order: element q of every thread, by thread
                     const int32_t idx = (int32_t)(pos + q);
                     const bool in = pos + q < G && prefix_match(bins, d, kk[q], idx);
                     const uint32_t dv = digit_of(d, kk[q], idx);
-                    const int so = warp_alloc(&sm.n_sel, in && dv > dbin);
+                    int so, c;
+                    ordered_split(sm, in && dv > dbin, g2 && in && dv == dbin, &sm.n_cand, so, c);
                     if (so >= 0 && so < TK_KMAX) { sm.okey[so] = kk[q]; sm.oidx[so] = idx; }
-                    const int c = warp_alloc(&sm.n_cand, g2 && in && dv == dbin);
                     if (c >= 0 && c < TK_SCAP) { sm.ckey[c] = kk[q]; sm.cidx[c] = idx; }
                 }
             }
@@ -578,7 +586,15 @@ __global__ void __launch_bounds__(TK_T, 1) topk_select_kernel(TopkArgs a) {
         sm.oidx[n_w + i] = sm.cidx[i];
     }
     __syncthreads();
-    rank_scatter(sm, min(n_w + n_c, TK_KMAX), k, out, kout);
+    if (a.sorted) {
+        rank_scatter(sm, min(n_w + n_c, TK_KMAX), k, out, kout);
+    } else {  // the set in its fixed order: winners by round, then the last survivors
+        const int tot = min(n_w + n_c, k);
+        for (int i = tid; i < k; i += TK_T) {
+            out[i] = i < tot ? sm.oidx[i] : -1;
+            if (kout) kout[i] = i < tot ? sm.okey[i] : 0u;
+        }
+    }
     if (tid == 0) ctl[0] = 0u;  // the counter is ready for the next call on this workspace
 }
 
@@ -624,6 +640,7 @@ static TopkArgs topk_args(const TopkLaunch& h) {
     a.k = h.k;
     a.idx_out = h.idx_out;
     a.keys_out = h.keys_out;
+    a.sorted = h.sorted ? 1 : 0;
     a.hist = h.hist;
     a.capw = g.capw;
     a.caps = g.caps;

@@ -198,7 +198,10 @@ typedef struct {
     /* outputs */
     void* out;                   /* bf16 [B, H, 512] */
     float* lse;                  /* fp32 [B, H], nullable */
-    int32_t* sel;                /* int32 [B, k], nullable (ratio 4): the selected candidates */
+    int32_t* sel;                /* int32 [B, k], nullable (ratio 4): the selected candidates as a
+                                    set (the same set as csa_topk, -1 padding at the end), in a
+                                    fixed order that is not the score order: the same inputs give
+                                    the same order and the same output bits */
 } csa_decode_params;
 
 /* workspace: device, 16-byte aligned, caller-owned, at least csa_decode_workspace_size(p)

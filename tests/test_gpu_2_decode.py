@@ -34,8 +34,11 @@ def run_and_check(entry, case):
     c_rpp = case.c_rows_per_page()
     for b, (r, ref) in enumerate(zip(case.requests, refs)):
         if case.ratio == 4:
+            # the step's selection is the top-k set (csa_topk's order is tested in the stage tests)
             got_sel = batch.sel[b].cpu().numpy()
-            assert np.array_equal(got_sel, ref["sel"]), f"request {b}: top-k differs"
+            n = int((ref["sel"] >= 0).sum())
+            assert (got_sel[n:] == -1).all(), f"request {b}: padding"
+            assert np.array_equal(np.sort(got_sel[:n]), np.sort(ref["sel"][:n])), f"request {b}: top-k set differs"
         assert_close(out[b], ref["out_f64"], f"{case.name} request {b} output")
         assert np.abs(lse[b] - ref["lse"]).max() <= 1e-3 * max(1.0, np.abs(ref["lse"]).max())
         # the pending groups were compressed into the pool
@@ -84,8 +87,25 @@ def test_decode_graph_capture_replay(entry):
     g.replay()
     torch.cuda.synchronize()
     ref = oracle.decode_case(case)[0]
-    assert np.array_equal(batch.sel[0].cpu().numpy(), ref["sel"])
+    assert np.array_equal(np.sort(batch.sel[0].cpu().numpy()), np.sort(ref["sel"]))
     assert_close(batch.out[0].float().cpu().numpy(), ref["out_f64"], "graph replay")
+
+
+def test_decode_is_deterministic(entry):
+    """Two runs of the same step give the same selection order and the same output bits."""
+    case = synth.config(3, scale_down=16)
+    batch = entry.case_to_batch(case)
+    batch.run()
+    torch.cuda.synchronize()
+    sel, out, lse = batch.sel.clone(), batch.out.clone(), batch.lse.clone()
+    for _ in range(2):
+        batch.sel.fill_(-7)
+        batch.out.zero_()
+        batch.run()
+        torch.cuda.synchronize()
+        assert torch.equal(batch.sel, sel)
+        assert torch.equal(batch.out, out)
+        assert torch.equal(batch.lse, lse)
 
 
 @pytest.mark.parametrize("cfg", [1, 2, 3, 4])
