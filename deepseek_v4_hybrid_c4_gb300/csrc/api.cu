@@ -152,15 +152,9 @@ csa_status csa_index_score(const void* q_idx, const float* w_h, int32_t Hi, csa_
     return from_cuda(launch_score(l, static_cast<cudaStream_t>(stream), false));
 }
 
-static size_t topk_ws_layout(int32_t B, int64_t max_G, int32_t k, size_t* lists_off) {
-    const size_t hist = align256((size_t)B * kHistBlock * sizeof(uint32_t));
-    if (lists_off) *lists_off = hist;
-    return hist + align256(topk_lists_bytes(B, max_G, k));
-}
-
 size_t csa_topk_workspace_size(int32_t B, int64_t max_G, int32_t k) {
     if (B < 1 || B > 65535 || max_G < 0 || max_G > 0x7FFFFFFFLL || k < 1 || k > 2048) return 0;
-    return topk_ws_layout(B, max_G, k, nullptr);
+    return align256((size_t)B * kHistBlock * sizeof(uint32_t));  // one histogram per radix digit
 }
 
 static csa_status topk_common(const float* scores, const int64_t* offsets, int32_t B, int64_t G, int32_t k,
@@ -170,13 +164,9 @@ static csa_status topk_common(const float* scores, const int64_t* offsets, int32
     if (!scores || !al4(scores) || !idx_out || !al4(idx_out)) return CSA_ERR_INVALID_ARG;
     if (keys_out && !al4(keys_out)) return CSA_ERR_INVALID_ARG;
     if (B < 1 || B > 65535 || G < 0 || G > 0x7FFFFFFFLL) return CSA_ERR_INVALID_ARG;
-    size_t lists_off = 0;
-    const size_t need = topk_ws_layout(B, G, k, &lists_off);
-    if (!workspace || ws_bytes < need || !al16(workspace)) return CSA_ERR_WORKSPACE;
+    if (!workspace || ws_bytes < csa_topk_workspace_size(B, G, k) || !al16(workspace)) return CSA_ERR_WORKSPACE;
     int32_t* st = status_ptr();
     if (!st) return CSA_ERR_CUDA;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
     TopkLaunch t;
     t.scores = scores;
     t.B = B;
@@ -190,13 +180,12 @@ static csa_status topk_common(const float* scores, const int64_t* offsets, int32
     t.idx_out = idx_out;
     t.keys_out = keys_out;
     t.sorted = true;
-    t.hist = reinterpret_cast<uint32_t*>(ws);
-    t.lists = ws + lists_off;
+    t.hist_fused = false;
+    t.hist = static_cast<uint32_t*>(workspace);
     t.status = st;
-    // clear the histograms and control words, count the first digit, select
-    cudaError_t e = cudaMemsetAsync(ws, 0, (size_t)B * kHistBlock * sizeof(uint32_t), s);
-    if (e == cudaSuccess) e = launch_topk_hist(t, s);
-    if (e == cudaSuccess) e = launch_topk(t, s, true);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(workspace, 0, (size_t)B * kHistBlock * sizeof(uint32_t), s);
+    if (e == cudaSuccess) e = launch_topk(t, s, false);
     return from_cuda(e);
 }
 
@@ -407,8 +396,8 @@ csa_status csa_decode_timed(const csa_decode_params* p, void* workspace, size_t 
         t.idx_out = sel_out;
         t.keys_out = nullptr;
         t.sorted = false;  // attention takes the set; a fixed order keeps the step deterministic
+        t.hist_fused = true;
         t.hist = hist;
-        t.lists = ws + L.lists;
         t.status = st;
         e = launch_topk(t, s, ev == nullptr);
         if (e != cudaSuccess) return CSA_ERR_CUDA;

@@ -9,10 +9,9 @@ namespace csa {
 
 constexpr int kLatentRowBytes = 1024;  // one bf16 latent row (512 dims)
 constexpr int kHistBins = 2048;        // first top-k digit: key >> 21
-// Per-request top-k control block in the workspace: the first digit's histogram
-// (kHistBins counters), the survivors' second-digit histogram (kHistBins), then the
-// select's control words and per-CTA counts; cleared before every step.
-constexpr int kHistBlock = 2 * kHistBins + 256;
+// Per-request top-k block in the workspace: one histogram per radix digit (six of
+// kHistBins counters; digit 0 first); cleared before every step.
+constexpr int kHistBlock = 6 * kHistBins;
 
 struct HPaged {            // host copy of a paged buffer description (see csa_paged)
     const void* base;
@@ -61,9 +60,9 @@ struct ScoreLaunch {
 cudaError_t launch_score(const ScoreLaunch& a, cudaStream_t s, bool pdl);
 
 // Stage 3.  Request b's scores: single: [0, G); offsets mode: [offsets[b], offsets[b+1]);
-// decode mode: b * score_stride + [0, n_tokens[b] / ratio).  hist: [B][kHistBlock] words,
-// zeroed before the step; the first digit's histogram is either fused into stage 2 or
-// built by launch_topk_hist.  lists: topk_lists_bytes(B, max_G, k) of scratch.
+// decode mode: b * score_stride + [0, n_tokens[b] / ratio).  hist: [B][kHistBlock], zeroed
+// before the launch; with hist_fused its first kHistBins words hold digit 0's histogram
+// from stage 2, otherwise the select counts digit 0 itself.
 struct TopkLaunch {
     const float* scores;
     int B;
@@ -77,12 +76,11 @@ struct TopkLaunch {
     int32_t* idx_out;          // [B, k]
     uint32_t* keys_out;        // [B, k] or nullptr
     bool sorted;               // true: by (score desc, index asc); false: the set in a fixed order
+    bool hist_fused;
     uint32_t* hist;
-    void* lists;
     int32_t* status;
 };
 size_t topk_lists_bytes(int B, int64_t max_G, int k);
-cudaError_t launch_topk_hist(const TopkLaunch& a, cudaStream_t s);
 cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t s, bool pdl);
 
 // Stage 4 (+ log-sum-exp merge).  Per request b: keys = sel rows of kv_c (n_sel of
