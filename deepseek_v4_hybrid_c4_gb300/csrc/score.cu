@@ -2,19 +2,18 @@
 // 把活做絕了", sec. "Kernel 層一堆狠活": 256K candidates at 1M context feed the top-512).
 //
 //   score[g] = sum_h w_h * ReLU(q_idx[h] . k_idx[g])     fp32, bit-exact fixed order:
-//   P[t]  = q[8t]*k[8t], then fma over dims 8t+1..8t+7   (chunk t = 0..15)
-//   S1[t] = P[t] + P[t+8]; S2 = S1[t] + S1[t+4]; S3 = S2[t] + S2[t+2]; dot = S3[0] + S3[1]
-//   acc = fma(w_h, ReLU(dot_h), acc) for h = 0..Hi-1, from acc = 0
+//   Q[j]  = q[32j]*k[32j], then fma over dims 32j+1..32j+31   (chain j = 0..3)
+//   dot   = (Q[0] + Q[2]) + (Q[1] + Q[3])
+//   acc   = fma(w_h, ReLU(dot_h), acc) for h = 0..Hi-1, from acc = 0
 //
 // Layout: a warp takes a step of 32 rows (two 16-row units).  Lane (c, r), c = lane / 16,
-// r = lane % 16, holds rows r and r+16 and the chunk pairs (a, a+8) for a = {0,4,2,6} + c,
-// in that order: each pair yields S1[a] with packed fma.rn.f32x2 (the two halves are the
-// P[a] and P[a+8] chains -- two IEEE fmas per instruction), and the order makes every S2
-// and S3 operand ready when the tree needs it.  Half c ends with S3[c]; one shuffle
-// across the halves gives dot = S3[0] + S3[1] (IEEE addition is commutative, so both
-// halves agree bit for bit), and lane l finishes row l.  The index query is staged in
-// shared memory as {q[8a+i], q[8a+64+i]} pairs, two heads per 16-byte load, and each load
-// feeds both of the lane's rows.
+// r = lane % 16, holds rows r and r+16 and runs chains c and c+2 of both rows together with
+// packed fma.rn.f32x2 (the two halves of a 64-bit accumulator are the Q[c] and Q[c+2]
+// chains -- two IEEE fmas per instruction, dims 32c+i and 64+32c+i).  Half c ends with
+// Q[c] + Q[c+2]; one shuffle across the halves gives the dot (IEEE addition is
+// commutative, so both halves agree bit for bit), and lane l finishes row l.  The index
+// query is staged in shared memory as {q[32c+i], q[64+32c+i]} pairs, two heads per
+// 16-byte load, and each load feeds both of the lane's rows.
 //
 // Memory path: each warp owns two 32-row slots in shared memory and fills them with TMA
 // tensor copies (cp.async.bulk.tensor, 128-byte swizzle), two units per step, completing
@@ -165,7 +164,7 @@ template <int HI, bool FP8>
 __global__ void __launch_bounds__(SC_THREADS, HI >= 16 ? 1 : 2)
     score_kernel(const __grid_constant__ CUtensorMap kmap, ScoreArgs a) {
     constexpr int UB = FP8 ? SC_UNIT * 128 : SC_UNIT * 256;   // bytes per 16-row unit
-    constexpr int QF4 = 8 * 8 * (HI / 2);                      // float4 entries of the staged query
+    constexpr int QF4 = 32 * (HI / 2) * 2;                     // float4 entries of the staged query
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -279,14 +278,13 @@ __global__ void __launch_bounds__(SC_THREADS, HI >= 16 ? 1 : 2)
             __syncthreads();
             if (a.hist && qb >= 0) flush(qb);
             qb = cur.b;
-            // {q_h[8aa+i], q_h[8aa+64+i]} pairs of two heads per float4, at index
-            // ((nn * 8 + i) * HI/2 + head pair) * 2 + c for chunk pair aa = {0,4,2,6}[nn] + c
+            // {q_h[32c+i], q_h[64+32c+i]} pairs of two heads per float4, at index
+            // (i * HI/2 + head pair) * 2 + c, i = 0..31
             const uint16_t* qp = a.q_idx + (int64_t)qb * a.Hi * DI;
             for (int e = threadIdx.x; e < QF4; e += SC_THREADS) {
                 const int c = e & 1, rest = e >> 1;
-                const int hp = rest % (HI / 2), ii = (rest / (HI / 2)) % 8, nn = rest / (HI / 2) / 8;
-                const int aa = ((nn & 1) << 2) | (nn & 2) | c;
-                const int h0 = 2 * hp, h1 = 2 * hp + 1, d = 8 * aa + ii;
+                const int hp = rest % (HI / 2), ii = rest / (HI / 2);
+                const int h0 = 2 * hp, h1 = 2 * hp + 1, d = 32 * c + ii;
                 float4 v;
                 v.x = h0 < a.Hi ? bf16lo(qp[h0 * DI + d]) : 0.f;
                 v.y = h0 < a.Hi ? bf16lo(qp[h0 * DI + d + 64]) : 0.f;
@@ -310,28 +308,27 @@ __global__ void __launch_bounds__(SC_THREADS, HI >= 16 ? 1 : 2)
         }
         const int64_t g = st * SC_SUPER + lane;
         const bool valid = g < cur.G && kind_me == 1;
-        // lane (c, r): rows r and r+16 of the step (units 0 and 1, in-unit row r), chunk pairs
-        // aa = {0,4,2,6} + c; the two halves meet at dot = S3[0] + S3[1]
+        // lane (c, r): rows r and r+16 of the step (units 0 and 1, in-unit row r); chains c
+        // and c+2: dims 32c + 8g + ii (low halves) and 64 + 32c + 8g + ii (high halves)
         const uint8_t* st0 = slots + sl * SC_SLOT_BYTES;
         const uint8_t* st1 = st0 + SC_STAGE_BYTES;
-        float t1[2][HI], t2[2][HI], s3[2][HI];
+        uint64_t acc0[HI], acc1[HI];
 #pragma unroll
-        for (int nn = 0; nn < 4; ++nn) {
-            const int aa = ((nn & 1) << 2) | (nn & 2) | hu;
+        for (int gq = 0; gq < 4; ++gq) {
+            const int ch = 4 * hu + gq;  // 8-dim chunk of each half row
             float kl0[8], kh0[8], kl1[8], kh1[8];
-            load_pair<FP8>(st0, r, aa, kl0, kh0);
-            load_pair<FP8>(st1, r, aa, kl1, kh1);
-            uint64_t acc0[HI], acc1[HI];
+            load_pair<FP8>(st0, r, ch, kl0, kh0);
+            load_pair<FP8>(st1, r, ch, kl1, kh1);
 #pragma unroll
             for (int ii = 0; ii < 8; ++ii) {
                 const uint64_t kk0 = pk2(kl0[ii], kh0[ii]);
                 const uint64_t kk1 = pk2(kl1[ii], kh1[ii]);
-                const uint32_t qa = qs_addr + (uint32_t)(((nn * 8 + ii) * (HI / 2)) * 2 + hu) * 16u;
+                const uint32_t qa = qs_addr + (uint32_t)(((gq * 8 + ii) * (HI / 2)) * 2 + hu) * 16u;
 #pragma unroll
                 for (int hp = 0; hp < HI / 2; ++hp) {
                     uint64_t q0, q1;
                     ld_qpairs(qa + hp * 32u, q0, q1);
-                    if (ii == 0) {
+                    if (gq == 0 && ii == 0) {
                         acc0[2 * hp] = mul2(q0, kk0);
                         acc0[2 * hp + 1] = mul2(q1, kk0);
                         acc1[2 * hp] = mul2(q0, kk1);
@@ -344,21 +341,6 @@ __global__ void __launch_bounds__(SC_THREADS, HI >= 16 ? 1 : 2)
                     }
                 }
             }
-#pragma unroll
-            for (int h = 0; h < HI; ++h) {
-                const float u0 = lo2(acc0[h]) + hi2(acc0[h]);   // S1[aa] = P[aa] + P[aa+8]
-                const float u1 = lo2(acc1[h]) + hi2(acc1[h]);
-                if (nn == 0 || nn == 2) {
-                    t1[0][h] = u0;
-                    t1[1][h] = u1;
-                } else if (nn == 1) {
-                    t2[0][h] = t1[0][h] + u0;                    // S2 = S1[a] + S1[a+4]
-                    t2[1][h] = t1[1][h] + u1;
-                } else {
-                    s3[0][h] = t2[0][h] + (t1[0][h] + u0);      // S3 = S2[a] + S2[a+2]
-                    s3[1][h] = t2[1][h] + (t1[1][h] + u1);
-                }
-            }
         }
         // every lane has read the slot: refill it with the CTA-step after next
         __syncwarp();
@@ -366,8 +348,10 @@ __global__ void __launch_bounds__(SC_THREADS, HI >= 16 ? 1 : 2)
         float dot[HI];
 #pragma unroll
         for (int h = 0; h < HI; ++h) {
-            const float other = __shfl_xor_sync(0xffffffffu, hu ? s3[0][h] : s3[1][h], 16);
-            dot[h] = (hu ? s3[1][h] : s3[0][h]) + other;          // dot = S3[0] + S3[1]
+            const float r0 = lo2(acc0[h]) + hi2(acc0[h]);  // row r:    Q[c] + Q[c+2]
+            const float r1 = lo2(acc1[h]) + hi2(acc1[h]);  // row r+16
+            const float other = __shfl_xor_sync(0xffffffffu, hu ? r0 : r1, 16);
+            dot[h] = (hu ? r1 : r0) + other;               // (Q[0] + Q[2]) + (Q[1] + Q[3])
         }
         float sc = 0.f;
 #pragma unroll

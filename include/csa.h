@@ -96,8 +96,8 @@ csa_status csa_compress(csa_paged kv_raw, int64_t n_tokens, int32_t ratio, const
  * q_idx bf16 [Hi, 128] (contiguous), w_h fp32 [Hi], k_idx rows ([G, 128], bf16 or
  * fp8-e4m3 per k_dtype; paged tables need rows_per_page % 16 == 0), scores fp32 [G].
  * Bit-exact fixed order:
- *   P[t] = q[8t]*k[8t], then P[t] = fma(q[8t+i], k[8t+i], P[t]) for i = 1..7  (t = 0..15)
- *   S1[t] = P[t] + P[t+8]; S2[t] = S1[t] + S1[t+4]; S3[t] = S2[t] + S2[t+2]; dot = S3[0] + S3[1]
+ *   Q[j] = q[32j]*k[32j], then Q[j] = fma(q[32j+i], k[32j+i], Q[j]) for i = 1..31  (j = 0..3)
+ *   dot = (Q[0] + Q[2]) + (Q[1] + Q[3])
  *   acc = 0; acc = fma(w_h, dot > 0 ? dot : +0, acc) for h = 0..Hi-1
  */
 csa_status csa_index_score(const void* q_idx, const float* w_h, int32_t Hi, csa_paged k_idx, csa_dtype k_dtype,

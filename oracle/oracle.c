@@ -139,14 +139,14 @@ int orc_compress(const uint16_t* x, int64_t n_tokens, int ratio, const float* w_
  * 層一堆狠活": the indexer picks top-512 of 256K candidates at 1M context).
  *   score[g] = sum_h w_h * ReLU(q_idx[h] . k_idx[g])
  * fp32, fixed order (bit-exact contract shared with the GPU):
- *   chunk t = dims 8t..8t+7:  P[t] = q[8t]*k[8t];  P[t] = fmaf(q[8t+i], k[8t+i], P[t]) for i = 1..7
- *   S1[t] = P[t] + P[t+8] (t<8);  S2[t] = S1[t] + S1[t+4] (t<4);
- *   S3[t] = S2[t] + S2[t+2] (t<2);  dot_h = S3[0] + S3[1]
+ *   chain j = dims 32j..32j+31 (j = 0..3):  Q[j] = q[32j]*k[32j];
+ *                                         Q[j] = fmaf(q[32j+i], k[32j+i], Q[j]) for i = 1..31
+ *   dot_h = (Q[0] + Q[2]) + (Q[1] + Q[3])
  *   acc = 0;  acc = fmaf(w_h, ReLU(dot_h), acc) for h = 0..Hi-1, ReLU(x) = x > 0 ? x : +0
  * q_idx bf16 [Hi,128]; k_idx bf16 or e4m3 [G,128] (logical row order).
  * Pinned by: exact small-integer cases; fp64 error bound for Hi = 1; ReLU of
  * all-negative dots; exact doubling under w -> 2w; hand-computed golden case
- * in which the chunk order decides the rounding.
+ * in which the chain order decides the rounding.
  * ------------------------------------------------------------------------- */
 void orc_index_score(const uint16_t* q_idx, const float* w_h, int Hi, const void* k_idx, int k_fp8, int64_t G,
                      float* scores) {
@@ -160,16 +160,13 @@ void orc_index_score(const uint16_t* q_idx, const float* w_h, int Hi, const void
                          : orc_bf16_to_f32(((const uint16_t*)k_idx)[g * D_INDEX + d]);
         float acc = 0.0f;
         for (int h = 0; h < Hi; ++h) {
-            float P[16], S1[8], S2[4], S3[2];
-            for (int t = 0; t < 16; ++t) {
-                float p = q[h][8 * t] * k[8 * t];
-                for (int i = 1; i < 8; ++i) p = fmaf(q[h][8 * t + i], k[8 * t + i], p);
-                P[t] = p;
+            float Q[4];
+            for (int j = 0; j < 4; ++j) {
+                float p = q[h][32 * j] * k[32 * j];
+                for (int i = 1; i < 32; ++i) p = fmaf(q[h][32 * j + i], k[32 * j + i], p);
+                Q[j] = p;
             }
-            for (int t = 0; t < 8; ++t) S1[t] = P[t] + P[t + 8];
-            for (int t = 0; t < 4; ++t) S2[t] = S1[t] + S1[t + 4];
-            for (int t = 0; t < 2; ++t) S3[t] = S2[t] + S2[t + 2];
-            float dot = S3[0] + S3[1];
+            float dot = (Q[0] + Q[2]) + (Q[1] + Q[3]);
             float r = dot > 0.0f ? dot : 0.0f;
             acc = fmaf(w_h[h], r, acc);
         }
