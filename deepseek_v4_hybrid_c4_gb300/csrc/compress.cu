@@ -38,8 +38,10 @@ __device__ __forceinline__ void group_range(const CompressArgs& a, int b, int64_
 }
 
 __device__ __forceinline__ void zero_hist(const CompressArgs& a, int b) {
-    if (a.hist_zero && blockIdx.x == 0)
-        for (int i = threadIdx.x; i < kHistBlock; i += blockDim.x) a.hist_zero[(int64_t)b * kHistBlock + i] = 0u;
+    if (a.hist_zero && blockIdx.x == 0) {  // 16-byte stores: the block is 16-byte aligned
+        uint4* z = reinterpret_cast<uint4*>(a.hist_zero + (int64_t)b * kHistBlock);
+        for (int i = threadIdx.x; i < kHistBlock / 4; i += blockDim.x) z[i] = make_uint4(0, 0, 0, 0);
+    }
 }
 
 // lane's 16 dims of a bf16 row -> fp32
@@ -101,7 +103,8 @@ __global__ void __launch_bounds__(256) compress_r4_kernel(CompressArgs a) {
     }
     const float bp0 = __ldg(a.b_pos + 0), bp1 = __ldg(a.b_pos + 1), bp2 = __ldg(a.b_pos + 2),
                 bp3 = __ldg(a.b_pos + 3);
-    for (int64_t gi = (int64_t)blockIdx.x * 8 + warp; gi < count; gi += (int64_t)gridDim.x * 8) {
+    const int wpb = blockDim.x >> 5;  // warps per block
+    for (int64_t gi = (int64_t)blockIdx.x * wpb + warp; gi < count; gi += (int64_t)gridDim.x * wpb) {
         const int64_t g = first + gi;
         uint4 v[4][2];
 #pragma unroll
@@ -247,10 +250,14 @@ cudaError_t launch_compress(const CompressLaunch& h, cudaStream_t s, bool pdl) {
     cfg.stream = s;
     cfg.blockDim = dim3(256, 1, 1);
     int64_t gx;
-    if (h.n_tokens)
+    if (h.n_tokens) {
         gx = 1;  // decode: one block per request loops over its pending groups
-    else
+        // C4: a single warp, small enough to share an SM with the index-score kernel's CTAs
+        // (which start right behind it and fill every SM)
+        if (h.ratio == 4) cfg.blockDim = dim3(32, 1, 1);
+    } else {
         gx = h.ratio == 4 ? (h.count + 7) / 8 : h.count;
+    }
     if (gx < 1) gx = 1;
     if (gx > 0x7FFFFFFFLL) gx = 0x7FFFFFFFLL;
     cfg.gridDim = dim3((unsigned)gx, (unsigned)h.B, 1);
