@@ -242,6 +242,48 @@ __global__ void __launch_bounds__(SC_THREADS, HI >= 16 ? 1 : 2)
             }
         }
     };
+    // The index query of a request: thread t holds 16-byte chunks t and t + SC_THREADS of the
+    // [Hi][128] bf16 rows (chunk j = head j / 16, dims 8 (j % 16) ..), and thread t < HI the
+    // head weight.  A request's query is fetched one CTA-step before it is staged, so its
+    // loads never queue behind the bulk copies; the first one is fetched before any copy.
+    constexpr int QCH = HI * DI / 8;  // 16-byte chunks of the query, HI <= 16 -> <= 256
+    uint4 qv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+    float wv = 0.f;
+    int qf_b = -1;  // request whose query the registers hold (CTA-uniform)
+    auto q_fetch = [&](int b) {
+        const uint4* src = reinterpret_cast<const uint4*>(a.q_idx + (int64_t)b * a.Hi * DI);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int j = threadIdx.x + i * SC_THREADS;
+            qv[i] = (j < QCH && j / 16 < a.Hi) ? __ldg(src + j) : make_uint4(0, 0, 0, 0);
+        }
+        wv = threadIdx.x < a.Hi ? __ldg(a.w_h + (int64_t)b * a.Hi + threadIdx.x) : 0.f;
+        qf_b = b;
+    };
+    // Staged layout: float4 (i * HI/2 + head pair) * 2 + c holds {q_h0[32c+i], q_h0[64+32c+i],
+    // q_h1[32c+i], q_h1[64+32c+i]}, i = 0..31.
+    auto q_store = [&]() {
+        float* qf = reinterpret_cast<float*>(qs);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int j = threadIdx.x + i * SC_THREADS;
+            if (j < QCH) {
+                const int h = j >> 4, d0 = (j & 15) * 8;
+                const uint32_t wd[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int d = d0 + e, dd = d & 63;
+                    const int idx = (((dd & 31) * (HI / 2) + (h >> 1)) * 2 + (dd >> 5)) * 4 + (h & 1) * 2 + (d >> 6);
+                    qf[idx] = (e & 1) ? bf16hi(wd[e >> 1]) : bf16lo(wd[e >> 1]);
+                }
+            }
+        }
+        if (threadIdx.x < HI) wsm[threadIdx.x] = wv;
+    };
+    {
+        CtaStepCursor c0;
+        if (c0.seek(a, blockIdx.x)) q_fetch(c0.b);
+    }
     lookup_window(0, wk[0], ws[0], wp[0]);
     lookup_window(16, wk[1], ws[1], wp[1]);
     issue(0);
@@ -275,25 +317,16 @@ __global__ void __launch_bounds__(SC_THREADS, HI >= 16 ? 1 : 2)
             else lookup_window(k + 16, wk[1], ws[1], wp[1]);
         }
         if (cur.b != qb) {  // CTA-uniform: restage the query, flush the previous request's histogram
+            if (qf_b != cur.b) q_fetch(cur.b);
             __syncthreads();
             if (a.hist && qb >= 0) flush(qb);
             qb = cur.b;
-            // {q_h[32c+i], q_h[64+32c+i]} pairs of two heads per float4, at index
-            // (i * HI/2 + head pair) * 2 + c, i = 0..31
-            const uint16_t* qp = a.q_idx + (int64_t)qb * a.Hi * DI;
-            for (int e = threadIdx.x; e < QF4; e += SC_THREADS) {
-                const int c = e & 1, rest = e >> 1;
-                const int hp = rest % (HI / 2), ii = rest / (HI / 2);
-                const int h0 = 2 * hp, h1 = 2 * hp + 1, d = 32 * c + ii;
-                float4 v;
-                v.x = h0 < a.Hi ? bf16lo(qp[h0 * DI + d]) : 0.f;
-                v.y = h0 < a.Hi ? bf16lo(qp[h0 * DI + d + 64]) : 0.f;
-                v.z = h1 < a.Hi ? bf16lo(qp[h1 * DI + d]) : 0.f;
-                v.w = h1 < a.Hi ? bf16lo(qp[h1 * DI + d + 64]) : 0.f;
-                qs[e] = v;
-            }
-            if (threadIdx.x < HI) wsm[threadIdx.x] = threadIdx.x < a.Hi ? __ldg(a.w_h + (int64_t)qb * a.Hi + threadIdx.x) : 0.f;
+            q_store();
             __syncthreads();
+        }
+        {  // the CTA's next CTA-step starts another request: fetch its query now
+            CtaStepCursor nx = cur;
+            if (nx.seek(a, m + gridDim.x) && nx.b != qb && nx.b != qf_b) q_fetch(nx.b);
         }
         const int64_t st = (m - cur.base) * SC_WARPS + warp;  // this warp's step within the request
         const int kind_me = __shfl_sync(0xffffffffu, ((k >> 4) & 1) ? wk[1] : wk[0], 2 * (int)(k & 15) + hu);
@@ -328,16 +361,17 @@ __global__ void __launch_bounds__(SC_THREADS, HI >= 16 ? 1 : 2)
                 for (int hp = 0; hp < HI / 2; ++hp) {
                     uint64_t q0, q1;
                     ld_qpairs(qa + hp * 32u, q0, q1);
+                    // each pair of consecutive instructions shares one multiplicand
                     if (gq == 0 && ii == 0) {
                         acc0[2 * hp] = mul2(q0, kk0);
-                        acc0[2 * hp + 1] = mul2(q1, kk0);
                         acc1[2 * hp] = mul2(q0, kk1);
                         acc1[2 * hp + 1] = mul2(q1, kk1);
+                        acc0[2 * hp + 1] = mul2(q1, kk0);
                     } else {
                         acc0[2 * hp] = fma2(q0, kk0, acc0[2 * hp]);
-                        acc0[2 * hp + 1] = fma2(q1, kk0, acc0[2 * hp + 1]);
                         acc1[2 * hp] = fma2(q0, kk1, acc1[2 * hp]);
                         acc1[2 * hp + 1] = fma2(q1, kk1, acc1[2 * hp + 1]);
+                        acc0[2 * hp + 1] = fma2(q1, kk0, acc0[2 * hp + 1]);
                     }
                 }
             }
