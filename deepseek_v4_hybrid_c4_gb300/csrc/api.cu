@@ -288,7 +288,9 @@ static DecodeLayout decode_layout(const csa_decode_params* p) {
     L.hist = off;
     if (p->ratio == 4) off += align256((size_t)p->B * kHistBlock * sizeof(uint32_t));
     L.lists = off;
-    if (p->ratio == 4) off += align256(topk_lists_bytes(p->B, max_G, p->k));
+    if (p->ratio == 4)
+        off += align256(select_set_supported(max_G, p->k) ? select_set_lists_bytes(p->B, max_G)
+                                                          : topk_lists_bytes(p->B, max_G, p->k));
     L.sel = off;
     if (p->ratio == 4 && !p->sel) off += align256((size_t)p->B * p->k * sizeof(int32_t));
     L.attn = off;
@@ -383,23 +385,39 @@ csa_status csa_decode_timed(const csa_decode_params* p, void* workspace, size_t 
         mark(2);
         // 3. top-k per request
         int32_t* sel_out = p->sel ? p->sel : reinterpret_cast<int32_t*>(ws + L.sel);
-        TopkLaunch t;
-        t.scores = l.scores;
-        t.B = p->B;
-        t.G = 0;
-        t.max_G = max_G;
-        t.offsets = nullptr;
-        t.n_tokens = p->n_tokens;
-        t.ratio = p->ratio;
-        t.score_stride = L.score_stride;
-        t.k = p->k;
-        t.idx_out = sel_out;
-        t.keys_out = nullptr;
-        t.sorted = false;  // attention takes the set; a fixed order keeps the step deterministic
-        t.hist_fused = true;
-        t.hist = hist;
-        t.status = st;
-        e = launch_topk(t, s, ev == nullptr);
+        if (select_set_supported(max_G, p->k)) {
+            SelectSetLaunch t;
+            t.scores = l.scores;
+            t.score_stride = L.score_stride;
+            t.B = p->B;
+            t.max_G = max_G;
+            t.n_tokens = p->n_tokens;
+            t.ratio = p->ratio;
+            t.k = p->k;
+            t.idx_out = sel_out;
+            t.hist = hist;
+            t.lists = ws + L.lists;
+            t.status = st;
+            e = launch_select_set(t, s, ev == nullptr);
+        } else {
+            TopkLaunch t;
+            t.scores = l.scores;
+            t.B = p->B;
+            t.G = 0;
+            t.max_G = max_G;
+            t.offsets = nullptr;
+            t.n_tokens = p->n_tokens;
+            t.ratio = p->ratio;
+            t.score_stride = L.score_stride;
+            t.k = p->k;
+            t.idx_out = sel_out;
+            t.keys_out = nullptr;
+            t.sorted = false;  // attention takes the set; a fixed order keeps the step deterministic
+            t.hist_fused = true;
+            t.hist = hist;
+            t.status = st;
+            e = launch_topk(t, s, ev == nullptr);
+        }
         if (e != cudaSuccess) return CSA_ERR_CUDA;
         mark(3);
         sel = sel_out;

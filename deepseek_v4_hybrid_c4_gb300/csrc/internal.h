@@ -10,8 +10,12 @@ namespace csa {
 constexpr int kLatentRowBytes = 1024;  // one bf16 latent row (512 dims)
 constexpr int kHistBins = 2048;        // first top-k digit: key >> 21
 // Per-request top-k block in the workspace: one histogram per radix digit (six of
-// kHistBins counters; digit 0 first); cleared before every step.
-constexpr int kHistBlock = 6 * kHistBins;
+// kHistBins counters; digit 0 first), then the decode select's completion counter and
+// padding to 16 bytes; cleared before every step.
+constexpr int kHistDone = 6 * kHistBins;
+constexpr int kHistBlock = 6 * kHistBins + 4;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct HPaged {            // host copy of a paged buffer description (see csa_paged)
     const void* base;
@@ -82,6 +86,27 @@ struct TopkLaunch {
 };
 size_t topk_lists_bytes(int B, int64_t max_G, int k);
 cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t s, bool pdl);
+
+// Stage 3 in the decode step: the top-k set of request b's scores b * score_stride +
+// [0, n_tokens[b] / ratio), with the first digit's histogram from stage 2 in hist ([B]
+// [kHistBlock], zeroed before stage 2).  lists: select_set_lists_bytes(B, max_G) bytes of
+// workspace.  Only where select_set_supported(max_G, k).
+struct SelectSetLaunch {
+    const float* scores;
+    int64_t score_stride;      // a multiple of 4
+    int B;
+    int64_t max_G;
+    const int64_t* n_tokens;
+    int ratio;
+    int k;
+    int32_t* idx_out;          // [B, k]
+    uint32_t* hist;
+    void* lists;
+    int32_t* status;
+};
+bool select_set_supported(int64_t max_G, int k);
+size_t select_set_lists_bytes(int B, int64_t max_G);
+cudaError_t launch_select_set(const SelectSetLaunch& a, cudaStream_t s, bool pdl);
 
 // Stage 4 (+ log-sum-exp merge).  Per request b: keys = sel rows of kv_c (n_sel of
 // them, -1 = padding; sel == nullptr: rows 0..n_c-1 with n_c = n_tokens/ratio in

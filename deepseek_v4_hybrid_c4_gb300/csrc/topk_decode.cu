@@ -1,0 +1,466 @@
+// Stage 3 of the decode step: the exact top-k set of every request's index scores ("SGLang
+// 如何为 DeepSeek V4 打造「Day-0」推理加速", sec. "创新 2", Lightning TopK: histograms give a
+// threshold bin, then a scatter of the entries above it), laid out for a one-token decode
+// step where the whole select sits on the critical path between the score kernel and the
+// attention.
+//
+// Order, as in the cluster select: descending order-preserving key of the fp32 score, ties
+// to the lower index -- descending composite V = key << 31 | (2^31 - 1 - index), digits
+// key 31..21 | 20..10 | 9..0, then inverted index 30..20 | 19..10 | 9..0.
+//
+// A wide grid instead of one cluster: request b gets C CTAs of SW_T threads, CTA c owning
+// the SW_SLICE scores [c SW_SLICE, (c+1) SW_SLICE), four per thread (one 16-byte load), so
+// the 1 MB of scores of a 262,144-candidate request is read by 128 SMs at once.
+//  1. Every CTA reads the first digit's histogram, which the score kernel built, and finds
+//     the bin b0 holding the k-th key.
+//  2. Its keys above b0 are winners, keys in b0 candidates.  Both lists go, in index order,
+//     to the CTA's own region of the workspace (winners first); the candidates' second
+//     digit is counted into a global histogram; the CTA publishes its two counts.
+//  3. The last CTA to finish (a counter in the request's histogram block) takes prefix
+//     sums of the published counts, writes the winners to the output, loads the
+//     candidates (index order; into shared memory when they fit) and refines them digit
+//     by digit -- the second digit from the global histogram, the others counted in shared
+//     memory -- appending each round's winners in index order until the threshold bin
+//     holds exactly the number still needed.
+// Output: the k indices as a set in a fixed order (first-digit winners, then each round's
+// winners, each in index order); -1 pads when the request has fewer than k candidates.
+#include "common.cuh"
+#include "internal.h"
+
+namespace csa {
+
+constexpr int SW_T = 512;                 // threads per CTA
+constexpr int SW_PER = 4;                 // scores per thread
+constexpr int SW_SLICE = SW_T * SW_PER;   // scores per CTA
+constexpr int SW_CAP = 8192;              // candidates the last CTA keeps in shared memory
+constexpr int SW_CMAX = 2048;             // CTAs per request
+constexpr int SW_BINS = kHistBins;        // 2048: widest digit
+
+struct SelArgs {
+    const float* scores;     // request b at b * score_stride (a multiple of 4)
+    int64_t score_stride;
+    const int64_t* n_tokens;
+    int ratio;
+    int C;                   // CTAs per request
+    int k;
+    int32_t* out;            // [B][k]
+    uint32_t* hist;          // [B][kHistBlock]: digit 0 from the score kernel; digit 1 and the counter here
+    uint64_t* lists;         // [B][C * SW_SLICE]: per CTA, winners then candidates, key << 32 | index
+    uint32_t* counts;        // [B][C]: winners << 16 | candidates
+    int32_t* status;
+};
+
+struct SwSmem {
+    uint2 cand[SW_CAP];      // candidates (last CTA): {key, index}
+    uint32_t hist[SW_BINS];
+    uint32_t wpre[SW_CMAX + 1];  // exclusive prefix of the CTAs' winners (wpre[C] = total)
+    uint32_t cpre[SW_CMAX + 1];  // ... and of their candidates
+    uint32_t wsum[SW_T / 32];
+    uint64_t wsum64[SW_T / 32];
+    uint32_t bin, above, cnt;
+    int last;
+};
+
+// Exclusive prefix of v over the CTA's threads; *total = the sum.  Every thread calls it.
+__device__ __forceinline__ uint32_t sw_scan(SwSmem& sm, uint32_t v, uint32_t* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) sm.wsum[warp] = x;
+    __syncthreads();
+    uint32_t before = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < SW_T / 32; ++w) {
+        const uint32_t s = sm.wsum[w];
+        before += w < warp ? s : 0u;
+        tot += s;
+    }
+    __syncthreads();  // wsum is free again
+    *total = tot;
+    return before + x - v;
+}
+
+// The same over 64-bit values.
+__device__ __forceinline__ uint64_t sw_scan64(SwSmem& sm, uint64_t v, uint64_t* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint64_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) sm.wsum64[warp] = x;
+    __syncthreads();
+    uint64_t before = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < SW_T / 32; ++w) {
+        const uint64_t s = sm.wsum64[w];
+        before += w < warp ? s : 0ull;
+        tot += s;
+    }
+    __syncthreads();
+    *total = tot;
+    return before + x - v;
+}
+
+// The bin holding the need-th largest element, counting from the top bin, given thread t's
+// four bins 2047 - 4t - j (j = 0..3, high first).  Sets sm.bin (~0 when the counts hold
+// fewer than need), sm.above (elements in higher bins) and sm.cnt (elements in the bin).
+__device__ __forceinline__ void sw_find_bin(SwSmem& sm, const uint32_t (&h)[4], uint32_t need) {
+    if (threadIdx.x == 0) {
+        sm.bin = ~0u;
+        sm.above = 0;
+        sm.cnt = 0;
+    }
+    uint32_t tot;
+    uint32_t acc = sw_scan(sm, h[0] + h[1] + h[2] + h[3], &tot);  // its barriers order the reset
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if (h[j] > 0 && acc < need && need <= acc + h[j]) {
+            sm.bin = (uint32_t)(SW_BINS - 1 - 4 * (int)threadIdx.x - j);
+            sm.above = acc;
+            sm.cnt = h[j];
+        }
+        acc += h[j];
+    }
+    __syncthreads();
+}
+
+// Digit d (1..5) of the composite of (key, index).
+__device__ __forceinline__ uint32_t sw_digit(int d, uint32_t key, int32_t idx) {
+    const uint32_t inv = 0x7FFFFFFFu - (uint32_t)idx;
+    switch (d) {
+        case 1: return (key >> 10) & 2047u;
+        case 2: return key & 1023u;
+        case 3: return (inv >> 20) & 2047u;
+        case 4: return (inv >> 10) & 1023u;
+        default: return inv & 1023u;
+    }
+}
+
+// Largest c in [0, C) with pre[c] <= x (pre non-decreasing, pre[0] = 0).
+__device__ __forceinline__ int sw_owner(const uint32_t* pre, int C, uint32_t x) {
+    int lo = 0, n = C;
+    while (n > 1) {
+        const int h = n >> 1;
+        if (pre[lo + h] <= x) lo += h;
+        n -= h;
+    }
+    return lo;
+}
+
+__global__ void __launch_bounds__(SW_T, 1) select_set_kernel(SelArgs a) {
+    extern __shared__ __align__(16) uint8_t sw_raw[];
+    SwSmem& sm = *reinterpret_cast<SwSmem*>(sw_raw);
+    const int tid = threadIdx.x;
+    const int c = blockIdx.x, b = blockIdx.y, C = a.C, k = a.k;
+    int64_t G = __ldg(a.n_tokens + b) / a.ratio;
+    if (G < 0) G = 0;
+    const float* sc = a.scores + (int64_t)b * a.score_stride;
+    uint32_t* hb = a.hist + (int64_t)b * kHistBlock;
+    uint64_t* lb = a.lists + (int64_t)b * C * SW_SLICE;
+    uint32_t* cb = a.counts + (int64_t)b * C;
+    int32_t* out = a.out + (int64_t)b * k;
+    const bool all_in = G <= k;
+    pdl_wait();  // the scores and the first digit's histogram come from the score kernel
+    pdl_launch_dependents();  // the attention's prologue touches none of this kernel's output
+
+    // ---- 1. this thread's four keys, and the first digit's bin
+    const int64_t pos = (int64_t)c * SW_SLICE + SW_PER * tid;
+    uint32_t key[SW_PER];
+    if (pos + SW_PER - 1 < G) {
+        const float4 f = __ldcg(reinterpret_cast<const float4*>(sc + pos));
+        key[0] = score_key(f.x);
+        key[1] = score_key(f.y);
+        key[2] = score_key(f.z);
+        key[3] = score_key(f.w);
+    } else {
+#pragma unroll
+        for (int q = 0; q < SW_PER; ++q) key[q] = pos + q < G ? score_key(__ldcg(sc + pos + q)) : 0u;
+    }
+    uint32_t b0 = 0;
+    if (!all_in) {
+        const uint4 hv = __ldcg(reinterpret_cast<const uint4*>(hb + (SW_BINS - 4 - 4 * tid)));
+        const uint32_t h[4] = {hv.w, hv.z, hv.y, hv.x};
+        sw_find_bin(sm, h, (uint32_t)k);
+        b0 = sm.bin;  // ~0u (inconsistent histogram): no winners, no candidates; caught below
+    }
+
+    // ---- 2. winners and candidates of the slice, in index order, to this CTA's region
+    bool win[SW_PER], cand[SW_PER];
+    uint32_t nw = 0, nc = 0;
+#pragma unroll
+    for (int q = 0; q < SW_PER; ++q) {
+        const bool in = pos + q < G;
+        const uint32_t d0 = key[q] >> 21;
+        win[q] = in && (all_in || d0 > b0);
+        cand[q] = in && !all_in && d0 == b0;
+        nw += win[q] ? 1u : 0u;
+        nc += cand[q] ? 1u : 0u;
+    }
+    uint32_t tot;
+    const uint32_t ex = sw_scan(sm, (nw << 16) | nc, &tot);
+    const uint32_t tw = tot >> 16, tc = tot & 0xFFFFu;
+    uint32_t ow = ex >> 16, oc = tw + (ex & 0xFFFFu);
+    uint64_t* lc = lb + (int64_t)c * SW_SLICE;
+#pragma unroll
+    for (int q = 0; q < SW_PER; ++q) {
+        const uint64_t v = ((uint64_t)key[q] << 32) | (uint32_t)(pos + q);
+        if (win[q]) {
+            lc[ow++] = v;
+        } else if (cand[q]) {
+            lc[oc++] = v;
+            atomicAdd(hb + SW_BINS + ((key[q] >> 10) & 2047u), 1u);
+        }
+    }
+    if (tid == 0) cb[c] = (tw << 16) | tc;
+
+    // ---- 3. the request's last CTA to get here finishes it (one fence per CTA on each side
+    //      of the counter, after the barrier that orders the CTA's writes before it)
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        sm.last = atomicAdd(hb + kHistDone, 1u) == (uint32_t)(C - 1);
+        __threadfence();
+    }
+    __syncthreads();
+    if (!sm.last) return;
+
+    // offsets of every CTA's lists: thread t owns CTAs [t g, t g + g)
+    const int g = (C + SW_T - 1) / SW_T;  // <= 4
+    uint32_t cw[4], cn[4], sw_ = 0, sc_ = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int cj = tid * g + j;
+        const uint32_t v = (j < g && cj < C) ? __ldcg(cb + cj) : 0u;
+        cw[j] = v >> 16;
+        cn[j] = v & 0xFFFFu;
+        sw_ += cw[j];
+        sc_ += cn[j];
+    }
+    uint32_t h1[4] = {0u, 0u, 0u, 0u};  // the candidates' second digit, counted by every CTA
+    if (!all_in) {
+        const uint4 hv = __ldcg(reinterpret_cast<const uint4*>(hb + SW_BINS + (SW_BINS - 4 - 4 * tid)));
+        h1[0] = hv.w;
+        h1[1] = hv.z;
+        h1[2] = hv.y;
+        h1[3] = hv.x;
+    }
+    uint64_t tot64;
+    const uint64_t x64 = sw_scan64(sm, ((uint64_t)sw_ << 32) | sc_, &tot64);  // winners high, candidates low
+    const uint32_t W0 = (uint32_t)(tot64 >> 32), Cn = (uint32_t)tot64;
+    uint32_t xw = (uint32_t)(x64 >> 32), xc = (uint32_t)x64;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int cj = tid * g + j;
+        if (j < g && cj < C) {
+            sm.wpre[cj] = xw;
+            sm.cpre[cj] = xc;
+            xw += cw[j];
+            xc += cn[j];
+        }
+    }
+    if (tid == 0) {
+        sm.wpre[C] = W0;
+        sm.cpre[C] = Cn;
+    }
+    __syncthreads();
+    const bool ok = all_in ? W0 == (uint32_t)G : (b0 != ~0u && W0 < (uint32_t)k && W0 + Cn >= (uint32_t)k);
+    if (!ok) {  // the histogram does not match the scores (not cleared, or written by another step)
+        if (tid == 0) raise_status(a.status, CSA_ERR_DEVICE_BOUNDS);
+        for (int i = tid; i < k; i += SW_T) out[i] = -1;
+        return;
+    }
+    // first-digit winner o lies in the region of the CTA whose range of winners holds it;
+    // candidate j (index order) after the winners of the CTA whose range of candidates holds it
+    auto winner_src = [&](uint32_t o) {
+        const int cj = sw_owner(sm.wpre, C, o);
+        return lb + (int64_t)cj * SW_SLICE + (o - sm.wpre[cj]);
+    };
+    auto cand_src = [&](uint32_t j) {
+        const int cj = sw_owner(sm.cpre, C, j);
+        return lb + (int64_t)cj * SW_SLICE + (sm.wpre[cj + 1] - sm.wpre[cj]) + (j - sm.cpre[cj]);
+    };
+    auto cand_global = [&](uint32_t j, uint32_t& kk, int32_t& ii) {
+        const uint64_t v = __ldcg(cand_src(j));
+        kk = (uint32_t)(v >> 32);
+        ii = (int32_t)(uint32_t)v;
+    };
+    if (all_in) {
+        for (uint32_t o = tid; o < W0; o += SW_T) out[o] = (int32_t)(uint32_t)__ldcg(winner_src(o));
+        for (int i = (int)W0 + tid; i < k; i += SW_T) out[i] = -1;
+        return;
+    }
+    uint32_t need = (uint32_t)k - W0, base = W0;
+    // the second digit's bin needs only the global histogram: found before any list is read
+    sw_find_bin(sm, h1, need);
+    const uint32_t bd1 = sm.bin, above1 = sm.above, cnt1 = sm.cnt;
+    // every CTA region at once: warp w copies regions w, w + 16, ... (eight in flight per
+    // lane), winners straight to the output, candidates to shared memory when they fit
+    const bool held = Cn <= (uint32_t)SW_CAP;
+    const int lane = tid & 31, warp = tid >> 5;
+    constexpr int NW = SW_T / 32;
+    for (int cb0 = warp; cb0 < C; cb0 += 8 * NW) {
+        uint32_t wo[8], co[8], nw8[8], n8[8], nmax = 0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int cj = cb0 + u * NW;
+            wo[u] = 0u;
+            co[u] = 0u;
+            nw8[u] = 0u;
+            n8[u] = 0u;
+            if (cj < C) {
+                wo[u] = sm.wpre[cj];
+                nw8[u] = sm.wpre[cj + 1] - wo[u];
+                co[u] = sm.cpre[cj];
+                n8[u] = nw8[u] + (held ? sm.cpre[cj + 1] - co[u] : 0u);
+            }
+            nmax = max(nmax, n8[u]);
+        }
+        for (uint32_t i0 = 0; i0 < nmax; i0 += 32) {
+            const uint32_t i = i0 + lane;
+            uint64_t v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (i < n8[u]) v[u] = __ldcg(lb + (int64_t)(cb0 + u * NW) * SW_SLICE + i);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (i < nw8[u])
+                    out[wo[u] + i] = (int32_t)(uint32_t)v[u];
+                else if (i < n8[u])
+                    sm.cand[co[u] + i - nw8[u]] = make_uint2((uint32_t)(v[u] >> 32), (uint32_t)v[u]);
+            }
+        }
+    }
+    __syncthreads();
+    auto cand_at = [&](uint32_t j, uint32_t& kk, int32_t& ii) {
+        if (held) {
+            const uint2 e = sm.cand[j];
+            kk = e.x;
+            ii = (int32_t)e.y;
+        } else {
+            cand_global(j, kk, ii);
+        }
+    };
+
+    // ---- rounds over digits 1..5 on the candidates (each thread a contiguous range)
+    const uint32_t per = (Cn + SW_T - 1) / SW_T;
+    const uint32_t j0 = min((uint32_t)tid * per, Cn), j1 = min(j0 + per, Cn);
+    uint32_t bins[6] = {b0, 0u, 0u, 0u, 0u, 0u};
+    for (int d = 1; d <= 5; ++d) {
+        uint32_t bd = bd1, above = above1, cnt = cnt1;
+        if (d > 1) {
+            uint32_t h[4];
+            for (int i = tid; i < SW_BINS; i += SW_T) sm.hist[i] = 0u;
+            __syncthreads();
+            for (uint32_t j = j0; j < j1; ++j) {
+                uint32_t kk;
+                int32_t ii;
+                cand_at(j, kk, ii);
+                bool m = true;
+                for (int e = 1; e < d; ++e) m = m && sw_digit(e, kk, ii) == bins[e];
+                if (m) atomicAdd(&sm.hist[sw_digit(d, kk, ii)], 1u);
+            }
+            __syncthreads();
+#pragma unroll
+            for (int j = 0; j < 4; ++j) h[j] = sm.hist[SW_BINS - 1 - 4 * tid - j];
+            sw_find_bin(sm, h, need);
+            bd = sm.bin;
+            above = sm.above;
+            cnt = sm.cnt;
+        }
+        if (bd == ~0u) {  // cannot happen: the candidates hold at least `need` elements
+            if (tid == 0) raise_status(a.status, CSA_ERR_DEVICE_BOUNDS);
+            for (int i = (int)base + tid; i < k; i += SW_T) out[i] = -1;
+            return;
+        }
+        bins[d] = bd;
+        const bool last_round = cnt == need - above;  // the whole bin is taken
+        // this round's winners in index order: digit above bd (or the whole bin, last round)
+        auto takes = [&](uint32_t kk, int32_t ii) {
+            if (d == 1) {  // every candidate is in the first digit's bin
+                const uint32_t dv = (kk >> 10) & 2047u;
+                return dv > bd || (last_round && dv == bd);
+            }
+            for (int e = 1; e < d; ++e)
+                if (sw_digit(e, kk, ii) != bins[e]) return false;
+            const uint32_t dv = sw_digit(d, kk, ii);
+            return dv > bd || (last_round && dv == bd);
+        };
+        uint32_t n = 0;
+        for (uint32_t j = j0; j < j1; ++j) {
+            uint32_t kk;
+            int32_t ii;
+            cand_at(j, kk, ii);
+            n += takes(kk, ii) ? 1u : 0u;
+        }
+        uint32_t rt;
+        uint32_t o = base + sw_scan(sm, n, &rt);
+        for (uint32_t j = j0; j < j1; ++j) {
+            uint32_t kk;
+            int32_t ii;
+            cand_at(j, kk, ii);
+            if (takes(kk, ii)) {
+                if (o < (uint32_t)k) out[o] = ii;
+                ++o;
+            }
+        }
+        base += rt;
+        if (last_round) break;
+        need -= above;
+    }
+    if (base != (uint32_t)k && tid == 0) raise_status(a.status, CSA_ERR_DEVICE_BOUNDS);
+}
+
+// ------------------------------------------------------------------ host side
+static int64_t select_set_ctas(int64_t max_G) { return max_G <= 0 ? 1 : (max_G + SW_SLICE - 1) / SW_SLICE; }
+
+bool select_set_supported(int64_t max_G, int k) {
+    return select_set_ctas(max_G) <= SW_CMAX && k >= 1 && k <= 2048;
+}
+
+size_t select_set_lists_bytes(int B, int64_t max_G) {
+    if (!select_set_supported(max_G, 1)) return 0;
+    const int64_t C = select_set_ctas(max_G);
+    return align_up((size_t)B * C * SW_SLICE * sizeof(uint64_t), 256) + align_up((size_t)B * C * sizeof(uint32_t), 256);
+}
+
+cudaError_t launch_select_set(const SelectSetLaunch& h, cudaStream_t s, bool pdl) {
+    SelArgs a;
+    a.scores = h.scores;
+    a.score_stride = h.score_stride;
+    a.n_tokens = h.n_tokens;
+    a.ratio = h.ratio;
+    a.C = (int)select_set_ctas(h.max_G);
+    a.k = h.k;
+    a.out = h.idx_out;
+    a.hist = h.hist;
+    a.lists = reinterpret_cast<uint64_t*>(h.lists);
+    a.counts = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(h.lists) +
+                                           align_up((size_t)h.B * a.C * SW_SLICE * sizeof(uint64_t), 256));
+    a.status = h.status;
+    const size_t smem = sizeof(SwSmem);
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(select_set_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.gridDim = dim3((unsigned)a.C, (unsigned)h.B, 1);
+    cfg.blockDim = dim3(SW_T, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    return cudaLaunchKernelEx(&cfg, select_set_kernel, a);
+}
+
+}  // namespace csa

@@ -103,6 +103,19 @@ class DecodeBatch:
         self.params = p
         self.ws_bytes = csa_decode_workspace_size(p)  # 0 also when the parameters are rejected: run() reports why
         self.ws = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
+        self._shape = dict(ratio=ratio, H=H, Hi=Hi, k=k, swa=swa, scale=scale, kdtype=kdtype,
+                           rows_per_page=rows_per_page, n_pages=n_pages, max_tokens=max_tokens,
+                           c_rows_per_page=c_rows_per_page, c_n_pages=c_n_pages, device=device)
+
+    def clone(self) -> "DecodeBatch":
+        """The same step over copies of every device buffer (same values, other addresses):
+        e.g. the next layer of a model whose layers hold identical synthetic caches."""
+        c = lambda t: None if t is None else t.clone()
+        return DecodeBatch(raw_pool=c(self.raw_pool), c_pool=c(self.c_pool), kidx_pool=c(self.kidx_pool),
+                           page_table=c(self.page_table), n_tokens=c(self.n_tokens),
+                           n_groups_done=c(self.n_groups_done), q=c(self.q), q_idx=c(self.q_idx) if self.Hi else None,
+                           w_h=c(self.w_h) if self.Hi else None, w_gate=c(self.w_gate), b_pos=c(self.b_pos),
+                           c_page_table=c(self.c_page_table), **self._shape)
 
     def run(self, stream=None, events=None) -> None:
         if events is None:
