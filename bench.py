@@ -163,6 +163,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=LAYERS,
+                    help="layers cycled by the timed steps (1: a small run for profiler captures)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
@@ -186,7 +188,8 @@ def main():
     # LAYERS layers of the same shape, each with its own copy of every buffer; consecutive steps
     # run consecutive layers, so a step's inputs were last touched LAYERS - 1 steps earlier and
     # the LAYERS * ~68 MB read per round (> 129 MB L2) has evicted them by then
-    layers = [batch] + [batch.clone() for _ in range(LAYERS - 1)]
+    n_layers = max(1, args.layers)
+    layers = [batch] + [batch.clone() for _ in range(n_layers - 1)]
     stream = torch.cuda.Stream()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     flush_rd = torch.ones(256 << 20, dtype=torch.uint8, device="cuda")
@@ -223,8 +226,8 @@ def main():
             lb.run(stream)
         graphs.append(g)
     with torch.cuda.stream(stream):
-        for i in range(max(3, args.warmup) * LAYERS):
-            graphs[i % LAYERS].replay()
+        for i in range(max(3, args.warmup) * n_layers):
+            graphs[i % n_layers].replay()
     barrier()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     clk_path = os.path.join(ROOT, "gpurun_out", "bench_clocks.csv") if os.path.isdir(
@@ -235,7 +238,7 @@ def main():
         with torch.cuda.stream(stream):
             for i in range(args.steps):
                 ev[i][0].record(stream)
-                graphs[i % LAYERS].replay()
+                graphs[i % n_layers].replay()
                 ev[i][1].record(stream)
         barrier()
     step_ms = [a.elapsed_time(b) for a, b in ev]
@@ -248,7 +251,7 @@ def main():
         for i in range(args.steps):
             flush_l2()
             evf[i][0].record(stream)
-            graphs[i % LAYERS].replay()
+            graphs[i % n_layers].replay()
             evf[i][1].record(stream)
     barrier()
     ms_flushed = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in evf))
@@ -261,7 +264,7 @@ def main():
     barrier()
     with torch.cuda.stream(stream):
         for i in range(args.steps):
-            layers[i % LAYERS].run(stream, sev[i])
+            layers[i % n_layers].run(stream, sev[i])
     barrier()
     stage_ms = [[sev[i][j].elapsed_time(sev[i][j + 1]) for i in range(args.steps)] for j in range(4)]
     eager_ms = statistics.mean(sev[i][0].elapsed_time(sev[i][4]) for i in range(args.steps))
@@ -288,7 +291,7 @@ def main():
     barrier()
     with torch.cuda.stream(stream):
         for i in range(args.steps):
-            lb = layers[i % LAYERS]
+            lb = layers[i % n_layers]
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             lb.q.copy_(hq, non_blocking=True)
@@ -296,7 +299,7 @@ def main():
             lb.w_h.copy_(hwh, non_blocking=True)
             lb.raw_pool[row0: row0 + n_new].copy_(hraw, non_blocking=True)
             lb.kidx_pool[krow: krow + 1].copy_(hkidx, non_blocking=True)
-            graphs[i % LAYERS].replay()
+            graphs[i % n_layers].replay()
             hout.copy_(lb.out, non_blocking=True)
             hlse.copy_(lb.lse, non_blocking=True)
             e1.record(stream)
@@ -327,8 +330,8 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (fp32 accumulate; fp32 fixed-order index score)",
         "data": "synthetic (seeded Philox4x32-10 generators; shapes of the 1M-context workload)",
-        "config": {"workload": WORKLOAD, "l2": f"inputs larger than L2: {LAYERS} layers with their own buffers, stepped in turn "
-                               f"({LAYERS} x {ab['total'] / 1e6:.0f} MB per round > 129 MB L2; no flush)",
+        "config": {"workload": WORKLOAD, "l2": f"inputs larger than L2: {n_layers} layers with their own buffers, stepped in turn "
+                               f"({n_layers} x {ab['total'] / 1e6:.0f} MB per round vs 129 MB L2; no flush)",
                    "launch": "one CUDA graph per step",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "value_l2_flushed": round(ms_flushed * 1e3 / world, 3),
