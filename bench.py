@@ -4,14 +4,16 @@ One step = the fused decode of one C4 layer at 1M context, bs = 1 (N = 1,048,576
 tokens -> 262,144 candidates -> top-512, plus SWA 128; 128 query heads, 8 index heads,
 64-token pages under a random page-table permutation; one pending group compressed).
 Prints one JSON line.  Inputs are synthetic (seeded generators) and resident in HBM
-before timing.  The timed steps run the layers of a 6-layer stack in turn, each layer with
-its own copy of every buffer, so a step's ~68 MB of inputs were last touched five steps
-earlier and 340 MB of other layers' traffic (> 129 MB L2) has evicted them: data cold, code
-warm, as in a model's decode loop.  The same steps are also timed after an explicit L2
-flush (a 256 MiB write, then a 256 MiB read of a second buffer), which leaves the code cold
-too ("value_l2_flushed").  Each step is one CUDA graph replay; an eager pass records CUDA
-events between the stages for the per-stage breakdown and the roofline of the dominant
-kernel.
+before timing.  The timed region is exactly K steps back to back between two CUDA events,
+running the layers of a 6-layer stack in turn, each layer with its own copy of every buffer:
+a step's ~68 MB of inputs were last touched five steps earlier and 340 MB of other layers'
+traffic (> 129 MB L2) has evicted them -- data cold, code warm.  As a model captures its
+decode loop, one CUDA graph holds the six layers' steps (K // 6 replays, then K mod 6
+one-layer graphs), so a graph launch (about 4 us on the GPU) is paid once per six steps.
+Two more timings go alongside: each one-layer graph alone between its own events
+("value_step_alone"), and the same after an explicit L2 flush (a 256 MiB write, then a
+256 MiB read of a second buffer; "value_l2_flushed").  An eager pass records CUDA events
+between the stages for the per-stage breakdown and the roofline of the dominant kernel.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
 
@@ -76,7 +78,7 @@ class ClockSampler:
             dev = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0]
             sel = [f"--id={dev}"] if dev.isdigit() else []
             self.proc = subprocess.Popen(["nvidia-smi"] + sel + [f"--query-gpu={q}", "--format=csv,noheader",
-                                                                 "-lms", "100"], stdout=self.f,
+                                                                 "-lms", "20"], stdout=self.f,
                                          stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except Exception:
@@ -159,7 +161,7 @@ def _score_source_sha():
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -225,36 +227,60 @@ def main():
         with torch.cuda.graph(g, stream=stream):
             lb.run(stream)
         graphs.append(g)
+    # and one graph over the whole stack, as a model captures its decode loop
+    stack = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(stack, stream=stream):
+        for lb in layers:
+            lb.run(stream)
+
+    def run_steps(K):  # exactly K layer-steps: K // n_layers stack replays, then single layers
+        full, rem = divmod(K, n_layers)
+        for _ in range(full):
+            stack.replay()
+        for i in range(rem):
+            graphs[i].replay()
+
     with torch.cuda.stream(stream):
         for i in range(max(3, args.warmup) * n_layers):
             graphs[i % n_layers].replay()
+        for _ in range(max(3, args.warmup)):
+            stack.replay()
     barrier()
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     clk_path = os.path.join(ROOT, "gpurun_out", "bench_clocks.csv") if os.path.isdir(
         os.path.join(ROOT, "gpurun_out")) else "/tmp/bench_clocks.csv"
     clocks = ClockSampler(clk_path)
     barrier()
     with clocks:
+        # the timed region: exactly K steps back to back, as a model's layer loop runs them
+        with torch.cuda.stream(stream):
+            e_start.record(stream)
+            run_steps(args.steps)
+            e_end.record(stream)
+        barrier()
+        ms = max_over_ranks(e_start.elapsed_time(e_end) / args.steps)
+        assert csa.csa_read_device_status(stream) == 0
+        # each step alone between two events (its own launch latency inside)
         with torch.cuda.stream(stream):
             for i in range(args.steps):
                 ev[i][0].record(stream)
                 graphs[i % n_layers].replay()
                 ev[i][1].record(stream)
         barrier()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    ms = max_over_ranks(statistics.mean(step_ms))
-    assert csa.csa_read_device_status(stream) == 0
-    # the same steps after an explicit flush of L2 (256 MiB write, then 256 MiB read of a second
-    # buffer): data and code both cold
-    evf = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    with torch.cuda.stream(stream):
-        for i in range(args.steps):
-            flush_l2()
-            evf[i][0].record(stream)
-            graphs[i % n_layers].replay()
-            evf[i][1].record(stream)
-    barrier()
-    ms_flushed = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in evf))
+        ms_alone = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev))
+        # each step alone after an explicit flush of L2 (256 MiB write, then 256 MiB read of a
+        # second buffer): data and code both cold
+        evf = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                flush_l2()
+                evf[i][0].record(stream)
+                graphs[i % n_layers].replay()
+                evf[i][1].record(stream)
+        barrier()
+        ms_flushed = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in evf))
 
     # ---- eager pass with events between the stages (breakdown + dominant-kernel roofline)
     sev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
@@ -332,8 +358,12 @@ def main():
         "data": "synthetic (seeded Philox4x32-10 generators; shapes of the 1M-context workload)",
         "config": {"workload": WORKLOAD, "l2": f"inputs larger than L2: {n_layers} layers with their own buffers, stepped in turn "
                                f"({n_layers} x {ab['total'] / 1e6:.0f} MB per round vs 129 MB L2; no flush)",
-                   "launch": "one CUDA graph per step",
+                   "launch": f"one CUDA graph over the {n_layers} layers' steps, replayed K // {n_layers} "
+                             f"times, then K mod {n_layers} one-layer graphs; K steps back to back between "
+                             "two events (value_step_alone: each one-layer graph between its own events; "
+                             "value_l2_flushed: the same after an explicit L2 flush)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "value_step_alone": round(ms_alone * 1e3 / world, 3),
         "value_l2_flushed": round(ms_flushed * 1e3 / world, 3),
         "stages_us_eager": {n: round(statistics.mean(v) * 1e3, 3) for n, v in
                             zip(["compress", "score", "topk", "attn"], stage_ms)},
