@@ -10,10 +10,8 @@ namespace csa {
 constexpr int kLatentRowBytes = 1024;  // one bf16 latent row (512 dims)
 constexpr int kHistBins = 2048;        // first top-k digit: key >> 21
 // Per-request top-k block in the workspace: one histogram per radix digit (six of
-// kHistBins counters; digit 0 first), then the decode select's completion counter and
-// padding to 16 bytes; cleared before every step.
-constexpr int kHistDone = 6 * kHistBins;
-constexpr int kHistBlock = 6 * kHistBins + 4;
+// kHistBins counters; digit 0 first); cleared before every step.
+constexpr int kHistBlock = 6 * kHistBins;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

@@ -10,18 +10,22 @@
 //
 // A wide grid instead of one cluster: request b gets C CTAs of SW_T threads, CTA c owning
 // the SW_SLICE scores [c SW_SLICE, (c+1) SW_SLICE), four per thread (one 16-byte load), so
-// the 1 MB of scores of a 262,144-candidate request is read by 128 SMs at once.
-//  1. Every CTA reads the first digit's histogram, which the score kernel built, and finds
-//     the bin b0 holding the k-th key.
-//  2. Its keys above b0 are winners, keys in b0 candidates.  Both lists go, in index order,
-//     to the CTA's own region of the workspace (winners first); the candidates' second
-//     digit is counted into a global histogram; the CTA publishes its two counts.
-//  3. The last CTA to finish (a counter in the request's histogram block) takes prefix
-//     sums of the published counts, writes the winners to the output, loads the
-//     candidates (index order; into shared memory when they fit) and refines them digit
-//     by digit -- the second digit from the global histogram, the others counted in shared
-//     memory -- appending each round's winners in index order until the threshold bin
-//     holds exactly the number still needed.
+// the 1 MB of scores of a 262,144-candidate request is read by 128 SMs at once.  Two
+// kernels, chained by programmatic dependent launch:
+//  scan:   every CTA reads the first digit's histogram, which the score kernel built, and
+//          finds the bin b0 holding the k-th key.  Its keys above b0 are winners, keys in b0
+//          candidates; both lists go, in index order, to the CTA's own region of the
+//          workspace (winners first), the candidates' second digit is counted into a global
+//          histogram, and the CTA publishes its two counts.
+//  finish: every CTA takes the prefix sums of the published counts and writes its own
+//          region's winners.  Every CTA also finds the second digit's bin b1 in the global
+//          histogram.  When taking all of b1 completes the set (the usual case), every CTA
+//          counts each region's candidates with a second digit >= b1, warp by warp with
+//          ballots, and writes its own region's at the prefix of those counts -- no CTA waits
+//          for another.  Otherwise CTA 0 loads all candidates (index order; into shared memory
+//          when they fit) and refines them digit by digit -- the others counted in shared
+//          memory -- appending each round's winners in index order until the threshold bin
+//          holds exactly the number still needed.
 // Output: the k indices as a set in a fixed order (first-digit winners, then each round's
 // winners, each in index order); -1 pads when the request has fewer than k candidates.
 #include "common.cuh"
@@ -50,19 +54,23 @@ struct SelArgs {
     int32_t* status;
 };
 
-struct SwSmem {
-    uint2 cand[SW_CAP];      // candidates (last CTA): {key, index}
-    uint32_t hist[SW_BINS];
-    uint32_t wpre[SW_CMAX + 1];  // exclusive prefix of the CTAs' winners (wpre[C] = total)
-    uint32_t cpre[SW_CMAX + 1];  // ... and of their candidates
+struct SwCore {              // scans and bin searches
     uint32_t wsum[SW_T / 32];
     uint64_t wsum64[SW_T / 32];
     uint32_t bin, above, cnt;
-    int last;
+};
+
+struct SwFinSmem {           // finish kernel
+    SwCore core;
+    uint32_t wpre[SW_CMAX + 1];  // exclusive prefix of the CTAs' winners (wpre[C] = total)
+    uint32_t cpre[SW_CMAX + 1];  // ... and of their candidates
+    uint32_t spre[SW_CMAX + 1];  // per region: candidates taken in the second digit, then their prefix
+    uint32_t hist[SW_BINS];
+    uint2 cand[SW_CAP];      // candidates (slow path, CTA 0): {key, index}
 };
 
 // Exclusive prefix of v over the CTA's threads; *total = the sum.  Every thread calls it.
-__device__ __forceinline__ uint32_t sw_scan(SwSmem& sm, uint32_t v, uint32_t* total) {
+__device__ __forceinline__ uint32_t sw_scan(SwCore& sm, uint32_t v, uint32_t* total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint32_t x = v;
 #pragma unroll
@@ -85,7 +93,7 @@ __device__ __forceinline__ uint32_t sw_scan(SwSmem& sm, uint32_t v, uint32_t* to
 }
 
 // The same over 64-bit values.
-__device__ __forceinline__ uint64_t sw_scan64(SwSmem& sm, uint64_t v, uint64_t* total) {
+__device__ __forceinline__ uint64_t sw_scan64(SwCore& sm, uint64_t v, uint64_t* total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint64_t x = v;
 #pragma unroll
@@ -110,7 +118,7 @@ __device__ __forceinline__ uint64_t sw_scan64(SwSmem& sm, uint64_t v, uint64_t* 
 // The bin holding the need-th largest element, counting from the top bin, given thread t's
 // four bins 2047 - 4t - j (j = 0..3, high first).  Sets sm.bin (~0 when the counts hold
 // fewer than need), sm.above (elements in higher bins) and sm.cnt (elements in the bin).
-__device__ __forceinline__ void sw_find_bin(SwSmem& sm, const uint32_t (&h)[4], uint32_t need) {
+__device__ __forceinline__ void sw_find_bin(SwCore& sm, const uint32_t (&h)[4], uint32_t need) {
     if (threadIdx.x == 0) {
         sm.bin = ~0u;
         sm.above = 0;
@@ -153,23 +161,20 @@ __device__ __forceinline__ int sw_owner(const uint32_t* pre, int C, uint32_t x) 
     return lo;
 }
 
-__global__ void __launch_bounds__(SW_T, 1) select_set_kernel(SelArgs a) {
-    extern __shared__ __align__(16) uint8_t sw_raw[];
-    SwSmem& sm = *reinterpret_cast<SwSmem*>(sw_raw);
+__global__ void __launch_bounds__(SW_T) select_scan_kernel(SelArgs a) {
+    __shared__ SwCore sm;
     const int tid = threadIdx.x;
     const int c = blockIdx.x, b = blockIdx.y, C = a.C, k = a.k;
     int64_t G = __ldg(a.n_tokens + b) / a.ratio;
     if (G < 0) G = 0;
     const float* sc = a.scores + (int64_t)b * a.score_stride;
     uint32_t* hb = a.hist + (int64_t)b * kHistBlock;
-    uint64_t* lb = a.lists + (int64_t)b * C * SW_SLICE;
-    uint32_t* cb = a.counts + (int64_t)b * C;
-    int32_t* out = a.out + (int64_t)b * k;
+    uint64_t* lc = a.lists + ((int64_t)b * C + c) * SW_SLICE;
     const bool all_in = G <= k;
     pdl_wait();  // the scores and the first digit's histogram come from the score kernel
-    pdl_launch_dependents();  // the attention's prologue touches none of this kernel's output
+    pdl_launch_dependents();
 
-    // ---- 1. this thread's four keys, and the first digit's bin
+    // ---- this thread's four keys, and the first digit's bin
     const int64_t pos = (int64_t)c * SW_SLICE + SW_PER * tid;
     uint32_t key[SW_PER];
     if (pos + SW_PER - 1 < G) {
@@ -187,10 +192,10 @@ __global__ void __launch_bounds__(SW_T, 1) select_set_kernel(SelArgs a) {
         const uint4 hv = __ldcg(reinterpret_cast<const uint4*>(hb + (SW_BINS - 4 - 4 * tid)));
         const uint32_t h[4] = {hv.w, hv.z, hv.y, hv.x};
         sw_find_bin(sm, h, (uint32_t)k);
-        b0 = sm.bin;  // ~0u (inconsistent histogram): no winners, no candidates; caught below
+        b0 = sm.bin;  // ~0u (inconsistent histogram): no winners, no candidates; the finish reports it
     }
 
-    // ---- 2. winners and candidates of the slice, in index order, to this CTA's region
+    // ---- winners and candidates of the slice, in index order, to this CTA's region
     bool win[SW_PER], cand[SW_PER];
     uint32_t nw = 0, nc = 0;
 #pragma unroll
@@ -206,7 +211,6 @@ __global__ void __launch_bounds__(SW_T, 1) select_set_kernel(SelArgs a) {
     const uint32_t ex = sw_scan(sm, (nw << 16) | nc, &tot);
     const uint32_t tw = tot >> 16, tc = tot & 0xFFFFu;
     uint32_t ow = ex >> 16, oc = tw + (ex & 0xFFFFu);
-    uint64_t* lc = lb + (int64_t)c * SW_SLICE;
 #pragma unroll
     for (int q = 0; q < SW_PER; ++q) {
         const uint64_t v = ((uint64_t)key[q] << 32) | (uint32_t)(pos + q);
@@ -217,20 +221,29 @@ __global__ void __launch_bounds__(SW_T, 1) select_set_kernel(SelArgs a) {
             atomicAdd(hb + SW_BINS + ((key[q] >> 10) & 2047u), 1u);
         }
     }
-    if (tid == 0) cb[c] = (tw << 16) | tc;
+    if (tid == 0) a.counts[(int64_t)b * C + c] = (tw << 16) | tc;
+}
 
-    // ---- 3. the request's last CTA to get here finishes it (one fence per CTA on each side
-    //      of the counter, after the barrier that orders the CTA's writes before it)
-    __syncthreads();
-    if (tid == 0) {
-        __threadfence();
-        sm.last = atomicAdd(hb + kHistDone, 1u) == (uint32_t)(C - 1);
-        __threadfence();
-    }
-    __syncthreads();
-    if (!sm.last) return;
+__global__ void __launch_bounds__(SW_T, 1) select_finish_kernel(SelArgs a) {
+    extern __shared__ __align__(16) uint8_t sw_raw[];
+    SwFinSmem& fs = *reinterpret_cast<SwFinSmem*>(sw_raw);
+    SwCore& sm = fs.core;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int NW = SW_T / 32;
+    const int c = blockIdx.x, b = blockIdx.y, C = a.C, k = a.k;
+    int64_t G = __ldg(a.n_tokens + b) / a.ratio;
+    if (G < 0) G = 0;
+    const uint32_t* hb = a.hist + (int64_t)b * kHistBlock;
+    const uint64_t* lb = a.lists + (int64_t)b * C * SW_SLICE;
+    const uint32_t* cb = a.counts + (int64_t)b * C;
+    int32_t* out = a.out + (int64_t)b * k;
+    const bool all_in = G <= k;
+    // The attention may be scheduled at once: its prologue reads only the step's inputs, and it
+    // waits for this grid to complete before it reads the selection.
+    pdl_launch_dependents();
+    pdl_wait();  // the lists, their counts and the second digit's histogram come from the scan
 
-    // offsets of every CTA's lists: thread t owns CTAs [t g, t g + g)
+    // ---- offsets of every CTA's lists: thread t owns CTAs [t g, t g + g)
     const int g = (C + SW_T - 1) / SW_T;  // <= 4
     uint32_t cw[4], cn[4], sw_ = 0, sc_ = 0;
 #pragma unroll
@@ -242,7 +255,7 @@ __global__ void __launch_bounds__(SW_T, 1) select_set_kernel(SelArgs a) {
         sw_ += cw[j];
         sc_ += cn[j];
     }
-    uint32_t h1[4] = {0u, 0u, 0u, 0u};  // the candidates' second digit, counted by every CTA
+    uint32_t h1[4] = {0u, 0u, 0u, 0u};  // the candidates' second digit, counted by every scan CTA
     if (!all_in) {
         const uint4 hv = __ldcg(reinterpret_cast<const uint4*>(hb + SW_BINS + (SW_BINS - 4 - 4 * tid)));
         h1[0] = hv.w;
@@ -258,104 +271,165 @@ __global__ void __launch_bounds__(SW_T, 1) select_set_kernel(SelArgs a) {
     for (int j = 0; j < 4; ++j) {
         const int cj = tid * g + j;
         if (j < g && cj < C) {
-            sm.wpre[cj] = xw;
-            sm.cpre[cj] = xc;
+            fs.wpre[cj] = xw;
+            fs.cpre[cj] = xc;
             xw += cw[j];
             xc += cn[j];
         }
     }
     if (tid == 0) {
-        sm.wpre[C] = W0;
-        sm.cpre[C] = Cn;
+        fs.wpre[C] = W0;
+        fs.cpre[C] = Cn;
     }
     __syncthreads();
-    const bool ok = all_in ? W0 == (uint32_t)G : (b0 != ~0u && W0 < (uint32_t)k && W0 + Cn >= (uint32_t)k);
+    const bool ok = all_in ? W0 == (uint32_t)G : (W0 < (uint32_t)k && W0 + Cn >= (uint32_t)k);
     if (!ok) {  // the histogram does not match the scores (not cleared, or written by another step)
-        if (tid == 0) raise_status(a.status, CSA_ERR_DEVICE_BOUNDS);
-        for (int i = tid; i < k; i += SW_T) out[i] = -1;
+        if (c == 0) {
+            if (tid == 0) raise_status(a.status, CSA_ERR_DEVICE_BOUNDS);
+            for (int i = tid; i < k; i += SW_T) out[i] = -1;
+        }
         return;
     }
-    // first-digit winner o lies in the region of the CTA whose range of winners holds it;
-    // candidate j (index order) after the winners of the CTA whose range of candidates holds it
-    auto winner_src = [&](uint32_t o) {
-        const int cj = sw_owner(sm.wpre, C, o);
-        return lb + (int64_t)cj * SW_SLICE + (o - sm.wpre[cj]);
-    };
-    auto cand_src = [&](uint32_t j) {
-        const int cj = sw_owner(sm.cpre, C, j);
-        return lb + (int64_t)cj * SW_SLICE + (sm.wpre[cj + 1] - sm.wpre[cj]) + (j - sm.cpre[cj]);
-    };
-    auto cand_global = [&](uint32_t j, uint32_t& kk, int32_t& ii) {
-        const uint64_t v = __ldcg(cand_src(j));
-        kk = (uint32_t)(v >> 32);
-        ii = (int32_t)(uint32_t)v;
-    };
+    // ---- this CTA's first-digit winners
+    const uint64_t* lc = lb + (int64_t)c * SW_SLICE;
+    const uint32_t my_w = fs.wpre[c + 1] - fs.wpre[c];
+    for (uint32_t i = tid; i < my_w; i += SW_T) out[fs.wpre[c] + i] = (int32_t)(uint32_t)__ldcg(lc + i);
     if (all_in) {
-        for (uint32_t o = tid; o < W0; o += SW_T) out[o] = (int32_t)(uint32_t)__ldcg(winner_src(o));
-        for (int i = (int)W0 + tid; i < k; i += SW_T) out[i] = -1;
+        if (c == 0)
+            for (int i = (int)W0 + tid; i < k; i += SW_T) out[i] = -1;
         return;
     }
     uint32_t need = (uint32_t)k - W0, base = W0;
-    // the second digit's bin needs only the global histogram: found before any list is read
     sw_find_bin(sm, h1, need);
     const uint32_t bd1 = sm.bin, above1 = sm.above, cnt1 = sm.cnt;
-    // every CTA region at once: warp w copies regions w, w + 16, ... (eight in flight per
-    // lane), winners straight to the output, candidates to shared memory when they fit
-    const bool held = Cn <= (uint32_t)SW_CAP;
-    const int lane = tid & 31, warp = tid >> 5;
-    constexpr int NW = SW_T / 32;
-    for (int cb0 = warp; cb0 < C; cb0 += 8 * NW) {
-        uint32_t wo[8], co[8], nw8[8], n8[8], nmax = 0;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int cj = cb0 + u * NW;
-            wo[u] = 0u;
-            co[u] = 0u;
-            nw8[u] = 0u;
-            n8[u] = 0u;
-            if (cj < C) {
-                wo[u] = sm.wpre[cj];
-                nw8[u] = sm.wpre[cj + 1] - wo[u];
-                co[u] = sm.cpre[cj];
-                n8[u] = nw8[u] + (held ? sm.cpre[cj + 1] - co[u] : 0u);
-            }
-            nmax = max(nmax, n8[u]);
+    if (bd1 == ~0u) {  // cannot happen: the candidates hold at least `need` elements
+        if (c == 0) {
+            if (tid == 0) raise_status(a.status, CSA_ERR_DEVICE_BOUNDS);
+            for (int i = (int)base + tid; i < k; i += SW_T) out[i] = -1;
         }
-        for (uint32_t i0 = 0; i0 < nmax; i0 += 32) {
-            const uint32_t i = i0 + lane;
-            uint64_t v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (i < n8[u]) v[u] = __ldcg(lb + (int64_t)(cb0 + u * NW) * SW_SLICE + i);
+        return;
+    }
+
+    if (cnt1 == need - above1) {
+        // ---- fast path: the candidates whose second digit is >= bd1 complete the set.  Count
+        //      them per region (warp w: regions w, w + 16, ..., eight in flight per lane) ...
+        for (int cb0 = warp; cb0 < C; cb0 += 8 * NW) {
+            uint32_t off8[8], n8[8], t8[8], nmax = 0;
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                if (i < nw8[u])
-                    out[wo[u] + i] = (int32_t)(uint32_t)v[u];
-                else if (i < n8[u])
-                    sm.cand[co[u] + i - nw8[u]] = make_uint2((uint32_t)(v[u] >> 32), (uint32_t)v[u]);
+                const int cj = cb0 + u * NW;
+                off8[u] = cj < C ? fs.wpre[cj + 1] - fs.wpre[cj] : 0u;
+                n8[u] = cj < C ? fs.cpre[cj + 1] - fs.cpre[cj] : 0u;
+                t8[u] = 0u;
+                nmax = max(nmax, n8[u]);
+            }
+            for (uint32_t i0 = 0; i0 < nmax; i0 += 32) {
+                const uint32_t i = i0 + lane;
+                uint64_t v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (i < n8[u]) v[u] = __ldcg(lb + (int64_t)(cb0 + u * NW) * SW_SLICE + off8[u] + i);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const bool t = i < n8[u] && ((uint32_t)(v[u] >> 42) & 2047u) >= bd1;
+                    t8[u] += (uint32_t)__popc(__ballot_sync(0xffffffffu, t));
+                }
+            }
+            if (lane == 0)
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (cb0 + u * NW < C) fs.spre[cb0 + u * NW] = t8[u];
+        }
+        __syncthreads();
+        // ... their prefix over the regions ...
+        uint32_t st[4], ss = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int cj = tid * g + j;
+            st[j] = (j < g && cj < C) ? fs.spre[cj] : 0u;
+            ss += st[j];
+        }
+        uint32_t taken;
+        uint32_t xs = sw_scan(sm, ss, &taken);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int cj = tid * g + j;
+            if (j < g && cj < C) {
+                fs.spre[cj] = xs;
+                xs += st[j];
             }
         }
+        __syncthreads();
+        if (c == 0 && tid == 0 && taken != need) raise_status(a.status, CSA_ERR_DEVICE_BOUNDS);
+        // ... and this CTA's own, in index order after every earlier region's
+        if (warp == 0) {
+            const uint32_t off = my_w, n = fs.cpre[c + 1] - fs.cpre[c];
+            uint32_t o = base + fs.spre[c];
+            for (uint32_t i0 = 0; i0 < n; i0 += 32) {
+                const uint32_t i = i0 + lane;
+                const uint64_t v = i < n ? __ldcg(lc + off + i) : 0ull;
+                const bool t = i < n && ((uint32_t)(v >> 42) & 2047u) >= bd1;
+                const unsigned m = __ballot_sync(0xffffffffu, t);
+                const uint32_t r = o + (uint32_t)__popc(m & ((1u << lane) - 1u));
+                if (t && r < (uint32_t)k) out[r] = (int32_t)(uint32_t)v;
+                o += (uint32_t)__popc(m);
+            }
+        }
+        return;
     }
-    __syncthreads();
+
+    // ---- general path (ties at the threshold, wide bins): CTA 0 refines every candidate
+    if (c != 0) return;
+    const bool held = Cn <= (uint32_t)SW_CAP;
+    auto cand_src = [&](uint32_t j) {
+        const int cj = sw_owner(fs.cpre, C, j);
+        return lb + (int64_t)cj * SW_SLICE + (fs.wpre[cj + 1] - fs.wpre[cj]) + (j - fs.cpre[cj]);
+    };
+    if (held) {  // every region at once: warp w copies regions w, w + 16, ... (eight in flight per lane)
+        for (int cb0 = warp; cb0 < C; cb0 += 8 * NW) {
+            uint32_t off8[8], co8[8], n8[8], nmax = 0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int cj = cb0 + u * NW;
+                off8[u] = cj < C ? fs.wpre[cj + 1] - fs.wpre[cj] : 0u;
+                co8[u] = cj < C ? fs.cpre[cj] : 0u;
+                n8[u] = cj < C ? fs.cpre[cj + 1] - co8[u] : 0u;
+                nmax = max(nmax, n8[u]);
+            }
+            for (uint32_t i0 = 0; i0 < nmax; i0 += 32) {
+                const uint32_t i = i0 + lane;
+                uint64_t v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (i < n8[u]) v[u] = __ldcg(lb + (int64_t)(cb0 + u * NW) * SW_SLICE + off8[u] + i);
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (i < n8[u]) fs.cand[co8[u] + i] = make_uint2((uint32_t)(v[u] >> 32), (uint32_t)v[u]);
+            }
+        }
+        __syncthreads();
+    }
     auto cand_at = [&](uint32_t j, uint32_t& kk, int32_t& ii) {
         if (held) {
-            const uint2 e = sm.cand[j];
+            const uint2 e = fs.cand[j];
             kk = e.x;
             ii = (int32_t)e.y;
         } else {
-            cand_global(j, kk, ii);
+            const uint64_t v = __ldcg(cand_src(j));
+            kk = (uint32_t)(v >> 32);
+            ii = (int32_t)(uint32_t)v;
         }
     };
 
-    // ---- rounds over digits 1..5 on the candidates (each thread a contiguous range)
+    // rounds over digits 1..5 on the candidates (each thread a contiguous range)
     const uint32_t per = (Cn + SW_T - 1) / SW_T;
     const uint32_t j0 = min((uint32_t)tid * per, Cn), j1 = min(j0 + per, Cn);
-    uint32_t bins[6] = {b0, 0u, 0u, 0u, 0u, 0u};
+    uint32_t bins[6] = {0u, 0u, 0u, 0u, 0u, 0u};
     for (int d = 1; d <= 5; ++d) {
         uint32_t bd = bd1, above = above1, cnt = cnt1;
         if (d > 1) {
             uint32_t h[4];
-            for (int i = tid; i < SW_BINS; i += SW_T) sm.hist[i] = 0u;
+            for (int i = tid; i < SW_BINS; i += SW_T) fs.hist[i] = 0u;
             __syncthreads();
             for (uint32_t j = j0; j < j1; ++j) {
                 uint32_t kk;
@@ -363,11 +437,11 @@ __global__ void __launch_bounds__(SW_T, 1) select_set_kernel(SelArgs a) {
                 cand_at(j, kk, ii);
                 bool m = true;
                 for (int e = 1; e < d; ++e) m = m && sw_digit(e, kk, ii) == bins[e];
-                if (m) atomicAdd(&sm.hist[sw_digit(d, kk, ii)], 1u);
+                if (m) atomicAdd(&fs.hist[sw_digit(d, kk, ii)], 1u);
             }
             __syncthreads();
 #pragma unroll
-            for (int j = 0; j < 4; ++j) h[j] = sm.hist[SW_BINS - 1 - 4 * tid - j];
+            for (int j = 0; j < 4; ++j) h[j] = fs.hist[SW_BINS - 1 - 4 * tid - j];
             sw_find_bin(sm, h, need);
             bd = sm.bin;
             above = sm.above;
@@ -382,10 +456,6 @@ __global__ void __launch_bounds__(SW_T, 1) select_set_kernel(SelArgs a) {
         const bool last_round = cnt == need - above;  // the whole bin is taken
         // this round's winners in index order: digit above bd (or the whole bin, last round)
         auto takes = [&](uint32_t kk, int32_t ii) {
-            if (d == 1) {  // every candidate is in the first digit's bin
-                const uint32_t dv = (kk >> 10) & 2047u;
-                return dv > bd || (last_round && dv == bd);
-            }
             for (int e = 1; e < d; ++e)
                 if (sw_digit(e, kk, ii) != bins[e]) return false;
             const uint32_t dv = sw_digit(d, kk, ii);
@@ -443,10 +513,11 @@ cudaError_t launch_select_set(const SelectSetLaunch& h, cudaStream_t s, bool pdl
     a.counts = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(h.lists) +
                                            align_up((size_t)h.B * a.C * SW_SLICE * sizeof(uint64_t), 256));
     a.status = h.status;
-    const size_t smem = sizeof(SwSmem);
+    const size_t smem = sizeof(SwFinSmem);
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(select_set_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e =
+            cudaFuncSetAttribute(select_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -458,9 +529,12 @@ cudaError_t launch_select_set(const SelectSetLaunch& h, cudaStream_t s, bool pdl
     cfg.numAttrs = pdl ? 1 : 0;
     cfg.gridDim = dim3((unsigned)a.C, (unsigned)h.B, 1);
     cfg.blockDim = dim3(SW_T, 1, 1);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
-    return cudaLaunchKernelEx(&cfg, select_set_kernel, a);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, select_scan_kernel, a);
+    if (e != cudaSuccess) return e;
+    cfg.dynamicSmemBytes = smem;
+    return cudaLaunchKernelEx(&cfg, select_finish_kernel, a);
 }
 
 }  // namespace csa
