@@ -39,6 +39,10 @@ constexpr int SW_SLICE = SW_T * SW_PER;   // scores per CTA
 constexpr int SW_CAP = 8192;              // candidates the last CTA keeps in shared memory
 constexpr int SW_CMAX = 2048;             // CTAs per request
 constexpr int SW_BINS = kHistBins;        // 2048: widest digit
+// Shared memory the scan kernel reserves without using it: more than half an SM's, so the
+// scan CTAs spread one per SM (each then has an SM's load slots for its 2,048 scores) and
+// still leave room for a finish CTA waiting on the same SM.
+constexpr size_t SW_SCAN_SPREAD_SMEM = 116 * 1024;
 
 struct SelArgs {
     const float* scores;     // request b at b * score_stride (a multiple of 4)
@@ -238,10 +242,12 @@ __global__ void __launch_bounds__(SW_T, 1) select_finish_kernel(SelArgs a) {
     const uint32_t* cb = a.counts + (int64_t)b * C;
     int32_t* out = a.out + (int64_t)b * k;
     const bool all_in = G <= k;
-    // The attention may be scheduled at once: its prologue reads only the step's inputs, and it
-    // waits for this grid to complete before it reads the selection.
-    pdl_launch_dependents();
     pdl_wait();  // the lists, their counts and the second digit's histogram come from the scan
+    pdl_launch_dependents();
+    // entry tid of this CTA's own region, read with the counts: it holds the region's winners
+    // and candidates whenever they number at most SW_T (the other entries go unused)
+    const uint64_t* lc = lb + (int64_t)c * SW_SLICE;
+    const uint64_t mine = __ldcg(lc + tid);
 
     // ---- offsets of every CTA's lists: thread t owns CTAs [t g, t g + g)
     const int g = (C + SW_T - 1) / SW_T;  // <= 4
@@ -291,9 +297,9 @@ __global__ void __launch_bounds__(SW_T, 1) select_finish_kernel(SelArgs a) {
         return;
     }
     // ---- this CTA's first-digit winners
-    const uint64_t* lc = lb + (int64_t)c * SW_SLICE;
-    const uint32_t my_w = fs.wpre[c + 1] - fs.wpre[c];
-    for (uint32_t i = tid; i < my_w; i += SW_T) out[fs.wpre[c] + i] = (int32_t)(uint32_t)__ldcg(lc + i);
+    const uint32_t my_w = fs.wpre[c + 1] - fs.wpre[c], my_c = fs.cpre[c + 1] - fs.cpre[c];
+    if ((uint32_t)tid < my_w) out[fs.wpre[c] + tid] = (int32_t)(uint32_t)mine;
+    for (uint32_t i = SW_T + tid; i < my_w; i += SW_T) out[fs.wpre[c] + i] = (int32_t)(uint32_t)__ldcg(lc + i);
     if (all_in) {
         if (c == 0)
             for (int i = (int)W0 + tid; i < k; i += SW_T) out[i] = -1;
@@ -362,13 +368,19 @@ __global__ void __launch_bounds__(SW_T, 1) select_finish_kernel(SelArgs a) {
         __syncthreads();
         if (c == 0 && tid == 0 && taken != need) raise_status(a.status, CSA_ERR_DEVICE_BOUNDS);
         // ... and this CTA's own, in index order after every earlier region's
-        if (warp == 0) {
-            const uint32_t off = my_w, n = fs.cpre[c + 1] - fs.cpre[c];
-            uint32_t o = base + fs.spre[c];
-            for (uint32_t i0 = 0; i0 < n; i0 += 32) {
+        const uint32_t o0 = base + fs.spre[c];
+        if (my_w + my_c <= (uint32_t)SW_T) {  // they sit in `mine` of threads my_w .. my_w + my_c - 1
+            const bool t = (uint32_t)tid >= my_w && (uint32_t)tid < my_w + my_c &&
+                           ((uint32_t)(mine >> 42) & 2047u) >= bd1;
+            uint32_t tt;
+            const uint32_t r = o0 + sw_scan(sm, t ? 1u : 0u, &tt);
+            if (t && r < (uint32_t)k) out[r] = (int32_t)(uint32_t)mine;
+        } else if (warp == 0) {
+            uint32_t o = o0;
+            for (uint32_t i0 = 0; i0 < my_c; i0 += 32) {
                 const uint32_t i = i0 + lane;
-                const uint64_t v = i < n ? __ldcg(lc + off + i) : 0ull;
-                const bool t = i < n && ((uint32_t)(v >> 42) & 2047u) >= bd1;
+                const uint64_t v = i < my_c ? __ldcg(lc + my_w + i) : 0ull;
+                const bool t = i < my_c && ((uint32_t)(v >> 42) & 2047u) >= bd1;
                 const unsigned m = __ballot_sync(0xffffffffu, t);
                 const uint32_t r = o + (uint32_t)__popc(m & ((1u << lane) - 1u));
                 if (t && r < (uint32_t)k) out[r] = (int32_t)(uint32_t)v;
@@ -514,10 +526,14 @@ cudaError_t launch_select_set(const SelectSetLaunch& h, cudaStream_t s, bool pdl
                                            align_up((size_t)h.B * a.C * SW_SLICE * sizeof(uint64_t), 256));
     a.status = h.status;
     const size_t smem = sizeof(SwFinSmem);
+    static_assert(sizeof(SwFinSmem) + SW_SCAN_SPREAD_SMEM + 2 * 1024 <= 228 * 1024, "a scan and a finish CTA share an SM");
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e =
             cudaFuncSetAttribute(select_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(select_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)SW_SCAN_SPREAD_SMEM);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -529,7 +545,7 @@ cudaError_t launch_select_set(const SelectSetLaunch& h, cudaStream_t s, bool pdl
     cfg.numAttrs = pdl ? 1 : 0;
     cfg.gridDim = dim3((unsigned)a.C, (unsigned)h.B, 1);
     cfg.blockDim = dim3(SW_T, 1, 1);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = SW_SCAN_SPREAD_SMEM;
     cfg.stream = s;
     cudaError_t e = cudaLaunchKernelEx(&cfg, select_scan_kernel, a);
     if (e != cudaSuccess) return e;
