@@ -270,25 +270,30 @@ __global__ void __launch_bounds__(AT_T, 1) attn_kernel(AttnArgs a) {
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
         const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + SM_TMEM);
         const uint32_t srow = sbase + SM_STG + (uint32_t)h * R_PITCH;
-        for (int c = 0; c < AT_DH; c += 32) {
-            uint32_t o[32];
-            tc_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, o);
+        for (int c0 = 0; c0 < AT_DH; c0 += 128) {  // four TMEM loads in flight, one wait
+            uint32_t o[4][32];
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq)
+                tc_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c0 + 32 * qq), o[qq]);
             tc_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; e += 8) {
-                uint32_t w4[4];
+            for (int qq = 0; qq < 4; ++qq)
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float f0 = __uint_as_float(o[e + 2 * q]) * inv, f1 = __uint_as_float(o[e + 2 * q + 1]) * inv;
-                    if (direct) {
-                        w4[q] = pack_bf16x2(f0, f1);
-                    } else {
-                        const __half2 hv = __floats2half2_rn(f0, f1);
-                        w4[q] = *reinterpret_cast<const uint32_t*>(&hv);
+                for (int e = 0; e < 32; e += 8) {
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float f0 = __uint_as_float(o[qq][e + 2 * q]) * inv;
+                        const float f1 = __uint_as_float(o[qq][e + 2 * q + 1]) * inv;
+                        if (direct) {
+                            w4[q] = pack_bf16x2(f0, f1);
+                        } else {
+                            const __half2 hv = __floats2half2_rn(f0, f1);
+                            w4[q] = *reinterpret_cast<const uint32_t*>(&hv);
+                        }
                     }
+                    st_shared_v4(srow + (uint32_t)(c0 + 32 * qq + e) * 2u, make_uint4(w4[0], w4[1], w4[2], w4[3]));
                 }
-                st_shared_v4(srow + (uint32_t)(c + e) * 2u, make_uint4(w4[0], w4[1], w4[2], w4[3]));
-            }
         }
         tc_fence_before();
         __syncthreads();
@@ -296,9 +301,19 @@ __global__ void __launch_bounds__(AT_T, 1) attn_kernel(AttnArgs a) {
         // warp w copies rows w, w + 4, ...: one 512-byte row per warp instruction
         uint16_t* dst = direct ? a.out + (int64_t)b * H * D + half * AT_DH
                                : reinterpret_cast<uint16_t*>(a.part_o + ((int64_t)b * S + split) * H * D + half * AT_DH);
-        for (int r = warp; r < H; r += AT_T / 32) {
-            const uint4 v = ld_shared_v4(sbase + SM_STG + (uint32_t)r * R_PITCH + (uint32_t)lane * 16u);
-            *reinterpret_cast<uint4*>(dst + (int64_t)r * D + lane * 8) = v;
+        constexpr int NWA = AT_T / 32;
+        for (int r0 = warp; r0 < H; r0 += 8 * NWA) {  // eight rows per warp in flight
+            uint4 v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int r = r0 + j * NWA;
+                if (r < H) v[j] = ld_shared_v4(sbase + SM_STG + (uint32_t)r * R_PITCH + (uint32_t)lane * 16u);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int r = r0 + j * NWA;
+                if (r < H) *reinterpret_cast<uint4*>(dst + (int64_t)r * D + lane * 8) = v[j];
+            }
         }
     } else if (direct) {  // no keys at all
         for (int r = warp; r < H; r += AT_T / 32)
