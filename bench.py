@@ -295,12 +295,12 @@ def main():
     stage_ms = [[sev[i][j].elapsed_time(sev[i][j + 1]) for i in range(args.steps)] for j in range(4)]
     eager_ms = statistics.mean(sev[i][0].elapsed_time(sev[i][4]) for i in range(args.steps))
 
-    # ---- end to end through host buffers: the new token's state goes up, the output comes back
-    hq = batch.q.cpu().pin_memory()
-    hqi = batch.q_idx.cpu().pin_memory()
-    hwh = batch.w_h.cpu().pin_memory()
-    hout = torch.empty(batch.out.shape, dtype=batch.out.dtype).pin_memory()
-    hlse = torch.empty(batch.lse.shape, dtype=batch.lse.dtype).pin_memory()
+    # ---- end to end through host buffers: the new token's state goes up, the output comes back.
+    #      Per layer one CUDA graph holds the step with its copies: the packed per-step inputs
+    #      (q | q_idx | w_h), the completed group's raw rows and its index row up from pinned
+    #      host memory, and the packed outputs (out | lse) back down.
+    h_in = batch.step_in.cpu().pin_memory()
+    h_out = torch.empty(batch.step_out.shape, dtype=batch.step_out.dtype).pin_memory()
     r0 = case.requests[0]
     G = r0.n_tokens // case.ratio
     t0 = r0.n_groups_done * case.ratio
@@ -310,28 +310,33 @@ def main():
     c_rpp = case.c_rows_per_page()
     krow = int(r0.pages[(G - 1) // c_rpp]) * c_rpp + (G - 1) % c_rpp
     hkidx = batch.kidx_pool[krow: krow + 1].cpu().pin_memory()
-    h2d = (hq.numel() * 2 + hqi.numel() * 2 + hwh.numel() * 4 + hraw.numel() * 2 +
-           hkidx.numel() * hkidx.element_size())
-    d2h = hout.numel() * 2 + hlse.numel() * 4
-    e2e_ms = []
-    barrier()
-    with torch.cuda.stream(stream):
-        for i in range(args.steps):
-            lb = layers[i % n_layers]
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            lb.q.copy_(hq, non_blocking=True)
-            lb.q_idx.copy_(hqi, non_blocking=True)
-            lb.w_h.copy_(hwh, non_blocking=True)
+    h2d = h_in.numel() + hraw.numel() * 2 + hkidx.numel() * hkidx.element_size()
+    d2h = h_out.numel()
+    e2e_graphs = []
+    for lb in layers:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            lb.step_in.copy_(h_in, non_blocking=True)
             lb.raw_pool[row0: row0 + n_new].copy_(hraw, non_blocking=True)
             lb.kidx_pool[krow: krow + 1].copy_(hkidx, non_blocking=True)
-            graphs[i % n_layers].replay()
-            hout.copy_(lb.out, non_blocking=True)
-            hlse.copy_(lb.lse, non_blocking=True)
+            lb.run(stream)
+            h_out.copy_(lb.step_out, non_blocking=True)
+        e2e_graphs.append(g)
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup) * n_layers):
+            e2e_graphs[i % n_layers].replay()
+    barrier()
+    e2e_ms = []
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            e2e_graphs[i % n_layers].replay()
             e1.record(stream)
-            e1.synchronize()
+            e1.synchronize()  # the host holds the step's output before the next step goes up
             e2e_ms.append(e0.elapsed_time(e1))
     barrier()
+    assert csa.csa_read_device_status(stream) == 0
     e2e = max_over_ranks(statistics.mean(e2e_ms))
 
     if rank != 0:

@@ -32,6 +32,22 @@ def _bits(x, dev):
     return torch.from_numpy(a).to(dev)
 
 
+def _pack(dev, parts):
+    """One device buffer holding every tensor of `parts`, each at a 256-byte boundary, and a
+    view of the buffer for each (the data copied in), so that the group moves in one copy."""
+    offs, total = [], 0
+    for t in parts:
+        offs.append(total)
+        total = (total + t.numel() * t.element_size() + 255) // 256 * 256
+    buf = torch.zeros(max(total, 256), dtype=torch.uint8, device=dev)
+    views = []
+    for t, o in zip(parts, offs):
+        v = buf[o: o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+        v.copy_(t)
+        views.append(v)
+    return buf, views
+
+
 class DecodeBatch:
     """One fused decode step over B requests.
 
@@ -42,6 +58,8 @@ class DecodeBatch:
       kidx_pool  [n_pages * c_rpp, 128] bf16 / fp8        index keys (C4 only)
     page_table [B, P] int32, n_tokens / n_groups_done [B] int64, q [B, H, 512] bf16,
     q_idx [B, Hi, 128] bf16, w_h [B, Hi] fp32, w_gate [512] fp32, b_pos [ratio] fp32.
+    The per-step inputs q, q_idx and w_h are views of one device buffer (`step_in`), and the
+    outputs out and lse of another (`step_out`), so each group moves in a single copy.
     """
 
     def __init__(self, *, ratio, H, Hi, k, swa, scale, kdtype, rows_per_page, raw_pool, c_pool, kidx_pool,
@@ -57,14 +75,16 @@ class DecodeBatch:
         self.c_page_table = None if c_page_table is None else _dev(c_page_table, i32, dev)
         self.n_tokens = _dev(n_tokens, i64, dev)
         self.n_groups_done = _dev(n_groups_done, i64, dev)
-        self.q = _bits(q, dev)
         self.B = int(self.n_tokens.shape[0])
-        self.q_idx = _bits(q_idx, dev) if Hi else torch.zeros(8, dtype=torch.int16, device=dev)
-        self.w_h = _dev(w_h, f32, dev) if Hi else torch.zeros(4, dtype=f32, device=dev)
+        self.step_in, (self.q, self.q_idx, self.w_h) = _pack(dev, [
+            _bits(q, dev),
+            _bits(q_idx, dev) if Hi else torch.zeros(8, dtype=torch.int16, device=dev),
+            _dev(w_h, f32, dev) if Hi else torch.zeros(4, dtype=f32, device=dev)])
         self.w_gate = _dev(w_gate, f32, dev)
         self.b_pos = _dev(b_pos, f32, dev)
-        self.out = torch.zeros((self.B, H, 512), dtype=torch.bfloat16, device=dev)
-        self.lse = torch.zeros((self.B, H), dtype=f32, device=dev)
+        self.step_out, (self.out, self.lse) = _pack(dev, [
+            torch.zeros((self.B, H, 512), dtype=torch.bfloat16, device=dev),
+            torch.zeros((self.B, H), dtype=f32, device=dev)])
         self.sel = torch.zeros((self.B, max(k, 1)), dtype=i32, device=dev) if ratio == 4 else None
         if max_tokens is None:
             max_tokens = int(torch.as_tensor(n_tokens).max())
