@@ -73,6 +73,19 @@ def test_decode_ragged_with_short_requests(entry):
     run_and_check(entry, case)
 
 
+@pytest.mark.parametrize("G", [6000, 10240])
+def test_decode_select_all_scores_equal(entry, G):
+    """Every index key equal, so every score ties: the select refines down to the index digits
+    (its general path; above 8,192 candidates it rereads them from L2 each round).  Ties go to
+    the lower index, so the set is candidates 0 .. k-1 -- checked in closed form besides the
+    oracle."""
+    case = synth.make_decode_case("eq", 13, [4 * G], H=16, Hi=4, k=512)
+    for r in case.requests:
+        r.kidx[:] = r.kidx[0]
+    batch = run_and_check(entry, case)
+    assert np.array_equal(np.sort(batch.sel[0].cpu().numpy()), np.arange(512))
+
+
 def test_decode_graph_capture_replay(entry):
     """The step enqueues only device work: it can be captured once and replayed."""
     case = synth.config(0)
