@@ -382,7 +382,7 @@ def main():
                      "peak_source": f"{peak_kind} (burst copy)"},
         "e2e": {"value": round(e2e * 1e3 / world, 3), "unit": "µs/layer-step", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": args.steps * (4 + (1 if _attn_splits(case) > 1 else 0)),
+        "gpu_launches": args.steps * (5 + (1 if _attn_splits(case) > 1 else 0)),  # compress, score, select scan + finish, attention (+ merge)
         "clocks": clocks.summary(),
     }
     if not args.no_cpu_baseline:
