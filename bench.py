@@ -50,15 +50,21 @@ def peaks():
 
 
 def algorithmic_bytes(case):
-    """Bytes the step must move through HBM (scores stay in L2 and are not counted)."""
-    r = case.requests[0]
-    G = r.n_tokens // case.ratio
-    kidx = G * 128 * (2 if case.kdtype == "bf16" else 1)
-    pages = (r.n_tokens + case.rows_per_page - 1) // case.rows_per_page * 4  # page table (int32)
-    gather = case.k * 1024 + min(case.swa, r.n_tokens) * 1024
-    q = case.H * 512 * 2 + case.Hi * 128 * 2 + case.Hi * 4
-    out = case.H * 512 * 2 + case.H * 4
-    comp = (G - r.n_groups_done) * (case.ratio * 1024 + 1024)
+    """Bytes the step must move through HBM, summed over the batch's requests (scores, lists and
+    partials stay in L2 and are not counted)."""
+    kidx = pages = gather = q = out = comp = 0
+    for r in case.requests:
+        G = r.n_tokens // case.ratio
+        if case.ratio == 4:  # index keys streamed, then k selected rows gathered
+            kidx += G * 128 * (2 if case.kdtype == "bf16" else 1)
+            gather += min(case.k, G) * 1024
+        else:                # dense: every compressed row
+            gather += G * 1024
+        gather += min(case.swa, r.n_tokens) * 1024
+        pages += (r.n_tokens + case.rows_per_page - 1) // case.rows_per_page * 4  # page table (int32)
+        q += case.H * 512 * 2 + case.Hi * 128 * 2 + case.Hi * 4
+        out += case.H * 512 * 2 + case.H * 4
+        comp += (G - r.n_groups_done) * (case.ratio * 1024 + 1024)
     return dict(total=kidx + pages + gather + q + out + comp, score_kernel=kidx)
 
 
@@ -147,6 +153,103 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
+def other_workloads(torch, csa, entry, synth, stream, flush_l2, peak):
+    """The other measured rows: the top-512 select alone over the 1M workload's 262,144 scores;
+    the ragged fp8 batch and the C128 dense batch as decode steps; the prefill compressors
+    (C128 over 8 x 524,288 tokens, C4 over 1,048,576) as bandwidth.  Each step or call is timed
+    alone between CUDA events after an L2 flush (write then read); medians over the runs."""
+    res = {}
+
+    def timed(fn, n, flush=True):
+        ts = []
+        for _ in range(n):
+            with torch.cuda.stream(stream):
+                if flush:
+                    flush_l2()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        return statistics.median(ts), sorted(ts)[int(0.9 * (len(ts) - 1))]
+
+    # ---- the select alone: csa_topk (sorted output) on the 1M workload's scores
+    case2 = synth.config(2)
+    b2 = entry.case_to_batch(case2)
+    r2 = case2.requests[0]
+    G2 = r2.n_tokens // case2.ratio
+    c_rpp = case2.c_rows_per_page()
+    kp = csa.paged(b2.kidx_pool, c_rpp, 256, page_table=b2.page_table[0], n_pages=case2.n_pages)
+    scores = torch.empty(G2, dtype=torch.float32, device="cuda")
+    idx = torch.empty(case2.k, dtype=torch.int32, device="cuda")
+    ws_bytes = csa.csa_topk_workspace_size(1, G2, case2.k)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
+    with torch.cuda.stream(stream):
+        csa.csa_index_score(b2.q_idx, b2.w_h, case2.Hi, kp, csa.CSA_BF16, G2, scores, stream.cuda_stream)
+    torch.cuda.synchronize()
+    topk = lambda: csa.csa_topk(scores, G2, case2.k, idx, None, ws, ws_bytes, stream.cuda_stream)
+    warm, warm90 = timed(topk, 50, flush=False)
+    cold, cold90 = timed(topk, 50, flush=True)
+    with torch.cuda.stream(stream):  # 200 calls back to back: per-call launch latency pipelined
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(200):
+            topk()
+        e1.record(stream)
+    e1.synchronize()
+    res["topk_262144_to_512"] = {"us_per_call_back_to_back": round(e0.elapsed_time(e1) * 1e3 / 200, 2),
+                                 "us_alone_scores_in_l2": round(warm, 2), "us_p90_alone_scores_in_l2": round(warm90, 2),
+                                 "us_alone_l2_flushed": round(cold, 2), "us_p90_alone_l2_flushed": round(cold90, 2),
+                                 "output": "sorted by (score desc, index asc); each call zeroes its histograms "
+                                           "(one memset) and runs four kernels"}
+    # ---- C4 prefill compressor over the 1M workload's raw pool
+    rp = csa.paged(b2.raw_pool, case2.rows_per_page, 1024, page_table=b2.page_table[0], n_pages=case2.n_pages)
+    cout = torch.empty((G2, 512), dtype=torch.int16, device="cuda")
+    cp = csa.paged(cout, G2, 1024)
+    comp4 = lambda: csa.csa_compress(rp, r2.n_tokens, 4, b2.w_gate, b2.b_pos, 0, G2, cp, stream.cuda_stream)
+    t, t90 = timed(comp4, 10)
+    by = r2.n_tokens * 1024 + G2 * 1024
+    res["c4_prefill_compress_1M"] = {"us": round(t, 1), "GB_s": round(by / t / 1e3, 1),
+                                     "frac_of_peak": round(by / t / 1e3 / peak, 4), "bytes": by}
+    del b2, cout, scores
+    torch.cuda.empty_cache()
+    # ---- decode steps of the ragged fp8 batch and of the C128 dense batch
+    for cfg, name in [(3, "ragged32_fp8_decode"), (4, "c128_dense_bs8_decode")]:
+        case = synth.config(cfg)
+        b = entry.case_to_batch(case)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                b.run(stream)
+        torch.cuda.synchronize()
+        assert csa.csa_read_device_status(stream) == 0
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            b.run(stream)
+        t, t90 = timed(g.replay, 30)
+        by = algorithmic_bytes(case)["total"]
+        res[name] = {"us_per_step": round(t, 2), "us_p90": round(t90, 2), "algorithmic_bytes": by,
+                     "GB_s": round(by / t / 1e3, 1), "frac_of_peak": round(by / t / 1e3 / peak, 4),
+                     "requests": len(case.requests)}
+        if cfg == 4:  # ---- C128 prefill compressor over the same 8 x 524,288 tokens
+            outs = [torch.empty((r.n_tokens // 128, 512), dtype=torch.int16, device="cuda") for r in case.requests]
+            descs = [(csa.paged(b.raw_pool, case.rows_per_page, 1024, page_table=b.page_table[i], n_pages=case.n_pages),
+                      csa.paged(o, o.shape[0], 1024), r.n_tokens) for i, (r, o) in enumerate(zip(case.requests, outs))]
+
+            def comp128():
+                for rp_, op_, n_ in descs:
+                    csa.csa_compress(rp_, n_, 128, b.w_gate, b.b_pos, 0, n_ // 128, op_, stream.cuda_stream)
+            t, t90 = timed(comp128, 10)
+            by = sum(r.n_tokens * 1024 + (r.n_tokens // 128) * 1024 for r in case.requests)
+            res["c128_prefill_compress_8x512K"] = {"us": round(t, 1), "GB_s": round(by / t / 1e3, 1),
+                                                   "frac_of_peak": round(by / t / 1e3 / peak, 4), "bytes": by}
+            del outs, descs
+        del g, b
+        torch.cuda.empty_cache()
+    assert csa.csa_read_device_status(stream) == 0
+    return res
+
+
 def _attn_splits(case):
     """Key splits of the attention launch (a merge kernel follows when there are several)."""
     T = (case.k + case.swa + 63) // 64
@@ -165,6 +268,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip the other measured rows (select alone, ragged and C128 batches, prefill compressors)")
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="layers cycled by the timed steps (1: a small run for profiler captures)")
     args = ap.parse_args()
@@ -385,6 +490,11 @@ def main():
         "gpu_launches": args.steps * (5 + (1 if _attn_splits(case) > 1 else 0)),  # compress, score, select scan + finish, attention (+ merge)
         "clocks": clocks.summary(),
     }
+    if not args.no_other_workloads:
+        del graphs, stack, e2e_graphs
+        layers = layers[:1]
+        torch.cuda.empty_cache()
+        line["other_workloads"] = other_workloads(torch, csa, __graft_entry__, synth, stream, flush_l2, peak)
     if not args.no_cpu_baseline:
         times = oracle_step_times(case, 3, 15.0)
         line["cpu_baseline"] = {"value": round(statistics.median(times) * 1e6, 1), "unit": "µs/layer-step",

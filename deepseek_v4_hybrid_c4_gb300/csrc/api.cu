@@ -154,7 +154,9 @@ csa_status csa_index_score(const void* q_idx, const float* w_h, int32_t Hi, csa_
 
 size_t csa_topk_workspace_size(int32_t B, int64_t max_G, int32_t k) {
     if (B < 1 || B > 65535 || max_G < 0 || max_G > 0x7FFFFFFFLL || k < 1 || k > 2048) return 0;
-    return align256((size_t)B * kHistBlock * sizeof(uint32_t));  // one histogram per radix digit
+    // one histogram per radix digit, then (wide select) every scan CTA's lists and counts
+    return align256((size_t)B * kHistBlock * sizeof(uint32_t)) +
+           (select_set_supported(max_G, k) ? select_set_lists_bytes(B, max_G) : 0);
 }
 
 static csa_status topk_common(const float* scores, const int64_t* offsets, int32_t B, int64_t G, int32_t k,
@@ -185,7 +187,28 @@ static csa_status topk_common(const float* scores, const int64_t* offsets, int32
     t.status = st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemsetAsync(workspace, 0, (size_t)B * kHistBlock * sizeof(uint32_t), s);
-    if (e == cudaSuccess) e = launch_topk(t, s, false);
+    if (e != cudaSuccess) return from_cuda(e);
+    if (select_set_supported(G, k)) {  // wide select (first digit, scan, finish), then the sort
+        SelectSetLaunch w;
+        w.scores = scores;
+        w.score_stride = 0;
+        w.B = B;
+        w.max_G = G;
+        w.n_tokens = nullptr;
+        w.ratio = 1;
+        w.k = k;
+        w.idx_out = idx_out;
+        w.hist = static_cast<uint32_t*>(workspace);
+        w.lists = static_cast<uint8_t*>(workspace) + align256((size_t)B * kHistBlock * sizeof(uint32_t));
+        w.status = st;
+        w.offsets = offsets;
+        w.G = G;
+        w.standalone = true;
+        w.keys_out = keys_out;
+        e = launch_select_set(w, s, true);
+    } else {
+        e = launch_topk(t, s, false);
+    }
     return from_cuda(e);
 }
 

@@ -94,13 +94,19 @@ struct SelectSetLaunch {
     int64_t score_stride;      // a multiple of 4
     int B;
     int64_t max_G;
-    const int64_t* n_tokens;
+    const int64_t* n_tokens;   // decode mode; else offsets mode (offsets) or single (G)
     int ratio;
     int k;
     int32_t* idx_out;          // [B, k]
     uint32_t* hist;
     void* lists;
     int32_t* status;
+    const int64_t* offsets = nullptr;
+    int64_t G = 0;
+    // standalone: the first digit's histogram is counted here (hist zeroed beforehand) and
+    // the set is sorted by (score desc, index asc) at the end, keys to keys_out when given
+    bool standalone = false;
+    uint32_t* keys_out = nullptr;
 };
 bool select_set_supported(int64_t max_G, int k);
 size_t select_set_lists_bytes(int B, int64_t max_G);

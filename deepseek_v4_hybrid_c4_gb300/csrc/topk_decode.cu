@@ -45,10 +45,14 @@ constexpr int SW_BINS = kHistBins;        // 2048: widest digit
 constexpr size_t SW_SCAN_SPREAD_SMEM = 116 * 1024;
 
 struct SelArgs {
-    const float* scores;     // request b at b * score_stride (a multiple of 4)
+    // request b's scores: decode mode (n_tokens): scores + b * score_stride, n_tokens[b] / ratio
+    // of them; offsets mode: [offsets[b], offsets[b+1]); single: [0, G)
+    const float* scores;
     int64_t score_stride;
     const int64_t* n_tokens;
     int ratio;
+    const int64_t* offsets;
+    int64_t G;
     int C;                   // CTAs per request
     int k;
     int32_t* out;            // [B][k]
@@ -72,6 +76,36 @@ struct SwFinSmem {           // finish kernel
     uint32_t hist[SW_BINS];
     uint2 cand[SW_CAP];      // candidates (slow path, CTA 0): {key, index}
 };
+
+__device__ __forceinline__ void sel_span(const SelArgs& a, int b, const float*& sc, int64_t& G) {
+    if (a.n_tokens) {
+        sc = a.scores + (int64_t)b * a.score_stride;
+        G = __ldg(a.n_tokens + b) / a.ratio;
+    } else if (a.offsets) {
+        const int64_t o0 = __ldg(a.offsets + b), o1 = __ldg(a.offsets + b + 1);
+        sc = a.scores + o0;
+        G = o1 - o0;
+    } else {
+        sc = a.scores;
+        G = a.G;
+    }
+    if (G < 0) G = 0;
+}
+
+// Keys of the four scores pos .. pos + 3 (one 16-byte load when aligned and in range); key 0
+// past the end.
+__device__ __forceinline__ void sel_load4(const float* sc, int64_t pos, int64_t G, uint32_t (&key)[SW_PER]) {
+    if (pos + SW_PER - 1 < G && (reinterpret_cast<uintptr_t>(sc + pos) & 15) == 0) {
+        const float4 f = __ldcg(reinterpret_cast<const float4*>(sc + pos));
+        key[0] = score_key(f.x);
+        key[1] = score_key(f.y);
+        key[2] = score_key(f.z);
+        key[3] = score_key(f.w);
+    } else {
+#pragma unroll
+        for (int q = 0; q < SW_PER; ++q) key[q] = pos + q < G ? score_key(__ldcg(sc + pos + q)) : 0u;
+    }
+}
 
 // Exclusive prefix of v over the CTA's threads; *total = the sum.  Every thread calls it.
 __device__ __forceinline__ uint32_t sw_scan(SwCore& sm, uint32_t v, uint32_t* total) {
@@ -169,9 +203,9 @@ __global__ void __launch_bounds__(SW_T) select_scan_kernel(SelArgs a) {
     __shared__ SwCore sm;
     const int tid = threadIdx.x;
     const int c = blockIdx.x, b = blockIdx.y, C = a.C, k = a.k;
-    int64_t G = __ldg(a.n_tokens + b) / a.ratio;
-    if (G < 0) G = 0;
-    const float* sc = a.scores + (int64_t)b * a.score_stride;
+    const float* sc;
+    int64_t G;
+    sel_span(a, b, sc, G);
     uint32_t* hb = a.hist + (int64_t)b * kHistBlock;
     uint64_t* lc = a.lists + ((int64_t)b * C + c) * SW_SLICE;
     const bool all_in = G <= k;
@@ -181,16 +215,7 @@ __global__ void __launch_bounds__(SW_T) select_scan_kernel(SelArgs a) {
     // ---- this thread's four keys, and the first digit's bin
     const int64_t pos = (int64_t)c * SW_SLICE + SW_PER * tid;
     uint32_t key[SW_PER];
-    if (pos + SW_PER - 1 < G) {
-        const float4 f = __ldcg(reinterpret_cast<const float4*>(sc + pos));
-        key[0] = score_key(f.x);
-        key[1] = score_key(f.y);
-        key[2] = score_key(f.z);
-        key[3] = score_key(f.w);
-    } else {
-#pragma unroll
-        for (int q = 0; q < SW_PER; ++q) key[q] = pos + q < G ? score_key(__ldcg(sc + pos + q)) : 0u;
-    }
+    sel_load4(sc, pos, G, key);
     uint32_t b0 = 0;
     if (!all_in) {
         const uint4 hv = __ldcg(reinterpret_cast<const uint4*>(hb + (SW_BINS - 4 - 4 * tid)));
@@ -235,8 +260,9 @@ __global__ void __launch_bounds__(SW_T, 1) select_finish_kernel(SelArgs a) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int NW = SW_T / 32;
     const int c = blockIdx.x, b = blockIdx.y, C = a.C, k = a.k;
-    int64_t G = __ldg(a.n_tokens + b) / a.ratio;
-    if (G < 0) G = 0;
+    const float* sc_unused;
+    int64_t G;
+    sel_span(a, b, sc_unused, G);
     const uint32_t* hb = a.hist + (int64_t)b * kHistBlock;
     const uint64_t* lb = a.lists + (int64_t)b * C * SW_SLICE;
     const uint32_t* cb = a.counts + (int64_t)b * C;
@@ -498,6 +524,77 @@ __global__ void __launch_bounds__(SW_T, 1) select_finish_kernel(SelArgs a) {
     if (base != (uint32_t)k && tid == 0) raise_status(a.status, CSA_ERR_DEVICE_BOUNDS);
 }
 
+// Standalone select, first kernel: the first digit's histogram of every request's scores
+// (each CTA counts its slice in shared memory and adds the non-zero bins).
+__global__ void __launch_bounds__(SW_T) select_hist_kernel(SelArgs a) {
+    __shared__ uint32_t h[SW_BINS];
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int c = blockIdx.x, b = blockIdx.y;
+    for (int i = tid; i < SW_BINS; i += SW_T) h[i] = 0u;
+    const float* sc;
+    int64_t G;
+    sel_span(a, b, sc, G);
+    __syncthreads();
+    const int64_t pos = (int64_t)c * SW_SLICE + SW_PER * tid;
+    uint32_t key[SW_PER];
+    sel_load4(sc, pos, G, key);
+    pdl_launch_dependents();  // the scan waits for this grid before it reads the histogram
+#pragma unroll
+    for (int q = 0; q < SW_PER; ++q) {
+        const bool in = pos + q < G;
+        const uint32_t d = key[q] >> 21;
+        const unsigned m = __ballot_sync(0xffffffffu, in);
+        if (in) {
+            const unsigned peers = __match_any_sync(m, d);
+            if (lane == __ffs(peers) - 1) atomicAdd(&h[d], (uint32_t)__popc(peers));
+        }
+    }
+    __syncthreads();
+    uint32_t* hb = a.hist + (int64_t)b * kHistBlock;
+    for (int i = tid; i < SW_BINS; i += SW_T)
+        if (h[i]) atomicAdd(hb + i, h[i]);
+}
+
+// Standalone select, last kernel: request b's k selected indices (the set from the finish
+// kernel, in place in out) sorted by (score desc, index asc) -- a bitonic sort of the 63-bit
+// composites key << 32 | (2^31 - 1 - index) in shared memory, -1 padding (composite 0) last.
+constexpr int SW_SORT_T = 1024;
+__global__ void __launch_bounds__(SW_SORT_T) select_sort_kernel(SelArgs a, uint32_t* keys_out) {
+    __shared__ uint64_t v[2048];
+    const int tid = threadIdx.x, b = blockIdx.x, k = a.k;
+    const float* sc;
+    int64_t G;
+    sel_span(a, b, sc, G);
+    int32_t* out = a.out + (int64_t)b * k;
+    int n = 1;
+    while (n < k) n <<= 1;
+    pdl_wait();  // the set comes from the finish kernel
+    for (int i = tid; i < n; i += SW_SORT_T) {
+        const int32_t idx = i < k ? out[i] : -1;
+        v[i] = (idx >= 0 && idx < G) ? ((uint64_t)score_key(__ldcg(sc + idx)) << 32) | (0x7FFFFFFFu - (uint32_t)idx)
+                                     : 0ull;
+    }
+    __syncthreads();
+    for (int size = 2; size <= n; size <<= 1)
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int p = tid; p < (n >> 1); p += SW_SORT_T) {
+                const int lo = 2 * p - (p & (stride - 1)), hi = lo + stride;
+                const bool desc = (lo & size) == 0;  // every block of the last pass: descending
+                const uint64_t x = v[lo], y = v[hi];
+                if ((x < y) == desc) {
+                    v[lo] = y;
+                    v[hi] = x;
+                }
+            }
+            __syncthreads();
+        }
+    for (int i = tid; i < k; i += SW_SORT_T) {
+        const uint64_t x = v[i];
+        out[i] = x ? (int32_t)(0x7FFFFFFFu - (uint32_t)x) : -1;
+        if (keys_out) keys_out[(int64_t)b * k + i] = x ? (uint32_t)(x >> 32) : 0u;
+    }
+}
+
 // ------------------------------------------------------------------ host side
 static int64_t select_set_ctas(int64_t max_G) { return max_G <= 0 ? 1 : (max_G + SW_SLICE - 1) / SW_SLICE; }
 
@@ -517,6 +614,8 @@ cudaError_t launch_select_set(const SelectSetLaunch& h, cudaStream_t s, bool pdl
     a.score_stride = h.score_stride;
     a.n_tokens = h.n_tokens;
     a.ratio = h.ratio;
+    a.offsets = h.offsets;
+    a.G = h.G;
     a.C = (int)select_set_ctas(h.max_G);
     a.k = h.k;
     a.out = h.idx_out;
@@ -534,6 +633,9 @@ cudaError_t launch_select_set(const SelectSetLaunch& h, cudaStream_t s, bool pdl
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(select_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)SW_SCAN_SPREAD_SMEM);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(select_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)SW_SCAN_SPREAD_SMEM);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -547,10 +649,22 @@ cudaError_t launch_select_set(const SelectSetLaunch& h, cudaStream_t s, bool pdl
     cfg.blockDim = dim3(SW_T, 1, 1);
     cfg.dynamicSmemBytes = SW_SCAN_SPREAD_SMEM;
     cfg.stream = s;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, select_scan_kernel, a);
+    cudaError_t e = cudaSuccess;
+    if (h.standalone) {  // first digit counted here; the scan follows programmatically
+        cfg.numAttrs = 0;
+        e = cudaLaunchKernelEx(&cfg, select_hist_kernel, a);
+        if (e != cudaSuccess) return e;
+        cfg.numAttrs = 1;
+    }
+    e = cudaLaunchKernelEx(&cfg, select_scan_kernel, a);
     if (e != cudaSuccess) return e;
     cfg.dynamicSmemBytes = smem;
-    return cudaLaunchKernelEx(&cfg, select_finish_kernel, a);
+    e = cudaLaunchKernelEx(&cfg, select_finish_kernel, a);
+    if (e != cudaSuccess || !h.standalone) return e;
+    cfg.gridDim = dim3((unsigned)h.B, 1, 1);
+    cfg.blockDim = dim3(SW_SORT_T, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&cfg, select_sort_kernel, a, h.keys_out);
 }
 
 }  // namespace csa
