@@ -53,6 +53,8 @@ struct SelArgs {
     int ratio;
     const int64_t* offsets;
     int64_t G;
+    int sorted;              // 1: output ordered by (score desc, index asc) (standalone calls)
+    uint32_t* keys_out;      // [B][k] or nullptr (sorted output only)
     int C;                   // CTAs per request
     int k;
     int32_t* out;            // [B][k]
@@ -74,8 +76,15 @@ struct SwFinSmem {           // finish kernel
     uint32_t cpre[SW_CMAX + 1];  // ... and of their candidates
     uint32_t spre[SW_CMAX + 1];  // per region: candidates taken in the second digit, then their prefix
     uint32_t hist[SW_BINS];
-    uint2 cand[SW_CAP];      // candidates (slow path, CTA 0): {key, index}
+    uint2 cand[SW_CAP];      // candidates (slow path, CTA 0): {key, index}; sorted output: the
+                             // selected composites (first 2048 slots) and this CTA's own (next 2048)
+    uint32_t ntk, nown;
 };
+
+// 63-bit composite of a list entry key << 32 | index: larger = earlier in the output.
+__device__ __forceinline__ uint64_t sel_comp(uint64_t v) {
+    return (v & 0xFFFFFFFF00000000ull) | (0x7FFFFFFFu - (uint32_t)v);
+}
 
 __device__ __forceinline__ void sel_span(const SelArgs& a, int b, const float*& sc, int64_t& G) {
     if (a.n_tokens) {
@@ -324,11 +333,62 @@ __global__ void __launch_bounds__(SW_T, 1) select_finish_kernel(SelArgs a) {
     }
     // ---- this CTA's first-digit winners
     const uint32_t my_w = fs.wpre[c + 1] - fs.wpre[c], my_c = fs.cpre[c + 1] - fs.cpre[c];
-    if ((uint32_t)tid < my_w) out[fs.wpre[c] + tid] = (int32_t)(uint32_t)mine;
-    for (uint32_t i = SW_T + tid; i < my_w; i += SW_T) out[fs.wpre[c] + i] = (int32_t)(uint32_t)__ldcg(lc + i);
+    const bool sorted = a.sorted != 0;
+    uint64_t* tk = reinterpret_cast<uint64_t*>(fs.cand);  // sorted output: every selected composite
+    uint64_t* own = tk + 2048;                            // ... and this CTA's
+    if (!sorted) {
+        if ((uint32_t)tid < my_w) out[fs.wpre[c] + tid] = (int32_t)(uint32_t)mine;
+        for (uint32_t i = SW_T + tid; i < my_w; i += SW_T) out[fs.wpre[c] + i] = (int32_t)(uint32_t)__ldcg(lc + i);
+    }
+    if (tid == 0) {
+        fs.ntk = 0;
+        fs.nown = 0;
+    }
+    __syncthreads();
+    // Sorted output: with every selected composite in tk[0, ntk) and this CTA's own in
+    // own[0, nown), a warp per own entry counts the larger ones -- its output position.
+    auto rank_own = [&]() {
+        __syncthreads();
+        const uint32_t ntk = fs.ntk, nown = fs.nown;
+        for (uint32_t e = warp; e < nown; e += NW) {
+            const uint64_t x = own[e];
+            uint32_t r = 0;
+            for (uint32_t j = lane; j < ntk; j += 32) r += tk[j] > x ? 1u : 0u;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+            if (lane == 0 && r < (uint32_t)k) {
+                out[r] = (int32_t)(0x7FFFFFFFu - (uint32_t)x);
+                if (a.keys_out) a.keys_out[(int64_t)b * k + r] = (uint32_t)(x >> 32);
+            }
+        }
+    };
     if (all_in) {
+        if (sorted) {  // every score is selected: gather every region's (winners-only) list
+            for (int cb0 = warp; cb0 < C; cb0 += 8 * NW) {
+                uint32_t n8[8], nmax = 0;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int cj = cb0 + u * NW;
+                    n8[u] = cj < C ? fs.wpre[cj + 1] - fs.wpre[cj] : 0u;
+                    nmax = max(nmax, n8[u]);
+                }
+                for (uint32_t i0 = 0; i0 < nmax; i0 += 32) {
+                    const uint32_t i = i0 + lane;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        if (i < n8[u])
+                            tk[atomicAdd(&fs.ntk, 1u)] = sel_comp(__ldcg(lb + (int64_t)(cb0 + u * NW) * SW_SLICE + i));
+                }
+            }
+            for (uint32_t i = tid; i < my_w; i += SW_T)
+                own[atomicAdd(&fs.nown, 1u)] = sel_comp(i < (uint32_t)SW_T ? mine : __ldcg(lc + i));
+            rank_own();
+        }
         if (c == 0)
-            for (int i = (int)W0 + tid; i < k; i += SW_T) out[i] = -1;
+            for (int i = (int)W0 + tid; i < k; i += SW_T) {
+                out[i] = -1;
+                if (sorted && a.keys_out) a.keys_out[(int64_t)b * k + i] = 0u;
+            }
         return;
     }
     uint32_t need = (uint32_t)k - W0, base = W0;
@@ -345,13 +405,16 @@ __global__ void __launch_bounds__(SW_T, 1) select_finish_kernel(SelArgs a) {
     if (cnt1 == need - above1) {
         // ---- fast path: the candidates whose second digit is >= bd1 complete the set.  Count
         //      them per region (warp w: regions w, w + 16, ..., eight in flight per lane) ...
+        //      (sorted output: whole regions, winners included, and every selected composite
+        //      goes to tk)
         for (int cb0 = warp; cb0 < C; cb0 += 8 * NW) {
-            uint32_t off8[8], n8[8], t8[8], nmax = 0;
+            uint32_t nw8[8], off8[8], n8[8], t8[8], nmax = 0;
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int cj = cb0 + u * NW;
-                off8[u] = cj < C ? fs.wpre[cj + 1] - fs.wpre[cj] : 0u;
-                n8[u] = cj < C ? fs.cpre[cj + 1] - fs.cpre[cj] : 0u;
+                nw8[u] = cj < C ? fs.wpre[cj + 1] - fs.wpre[cj] : 0u;
+                off8[u] = sorted ? 0u : nw8[u];
+                n8[u] = (cj < C ? fs.cpre[cj + 1] - fs.cpre[cj] : 0u) + (sorted ? nw8[u] : 0u);
                 t8[u] = 0u;
                 nmax = max(nmax, n8[u]);
             }
@@ -363,8 +426,10 @@ __global__ void __launch_bounds__(SW_T, 1) select_finish_kernel(SelArgs a) {
                     if (i < n8[u]) v[u] = __ldcg(lb + (int64_t)(cb0 + u * NW) * SW_SLICE + off8[u] + i);
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    const bool t = i < n8[u] && ((uint32_t)(v[u] >> 42) & 2047u) >= bd1;
+                    const bool is_cand = off8[u] + i >= nw8[u];
+                    const bool t = i < n8[u] && is_cand && ((uint32_t)(v[u] >> 42) & 2047u) >= bd1;
                     t8[u] += (uint32_t)__popc(__ballot_sync(0xffffffffu, t));
+                    if (sorted && i < n8[u] && (t || !is_cand)) tk[atomicAdd(&fs.ntk, 1u)] = sel_comp(v[u]);
                 }
             }
             if (lane == 0)
@@ -393,6 +458,15 @@ __global__ void __launch_bounds__(SW_T, 1) select_finish_kernel(SelArgs a) {
         }
         __syncthreads();
         if (c == 0 && tid == 0 && taken != need) raise_status(a.status, CSA_ERR_DEVICE_BOUNDS);
+        if (sorted) {  // this CTA's selected entries, ranked among all of them
+            for (uint32_t i = tid; i < my_w + my_c; i += SW_T) {
+                const uint64_t v = i < (uint32_t)SW_T ? mine : __ldcg(lc + i);
+                if (i < my_w || ((uint32_t)(v >> 42) & 2047u) >= bd1) own[atomicAdd(&fs.nown, 1u)] = sel_comp(v);
+            }
+            if (c == 0 && tid == 0 && fs.ntk != (uint32_t)k) raise_status(a.status, CSA_ERR_DEVICE_BOUNDS);
+            rank_own();
+            return;
+        }
         // ... and this CTA's own, in index order after every earlier region's
         const uint32_t o0 = base + fs.spre[c];
         if (my_w + my_c <= (uint32_t)SW_T) {  // they sit in `mine` of threads my_w .. my_w + my_c - 1
@@ -418,6 +492,13 @@ __global__ void __launch_bounds__(SW_T, 1) select_finish_kernel(SelArgs a) {
 
     // ---- general path (ties at the threshold, wide bins): CTA 0 refines every candidate
     if (c != 0) return;
+    if (sorted) {  // the first-digit winners were not written: every region's, in fixed order
+        for (int r = warp; r < C; r += NW) {
+            const uint32_t n = fs.wpre[r + 1] - fs.wpre[r];
+            for (uint32_t i = lane; i < n; i += 32)
+                out[fs.wpre[r] + i] = (int32_t)(uint32_t)__ldcg(lb + (int64_t)r * SW_SLICE + i);
+        }
+    }
     const bool held = Cn <= (uint32_t)SW_CAP;
     auto cand_src = [&](uint32_t j) {
         const int cj = sw_owner(fs.cpre, C, j);
@@ -522,6 +603,39 @@ __global__ void __launch_bounds__(SW_T, 1) select_finish_kernel(SelArgs a) {
         need -= above;
     }
     if (base != (uint32_t)k && tid == 0) raise_status(a.status, CSA_ERR_DEVICE_BOUNDS);
+    if (!sorted) return;
+    // sorted output: order the k entries just written (the candidates are no longer needed, so
+    // their space holds the sort), a bitonic sort of the composites, descending
+    __syncthreads();
+    const float* sc;
+    int64_t Gs;
+    sel_span(a, b, sc, Gs);
+    int n = 1;
+    while (n < k) n <<= 1;
+    for (int i = tid; i < n; i += SW_T) {
+        const int32_t idx = i < k ? out[i] : -1;
+        tk[i] = (idx >= 0 && idx < Gs) ? ((uint64_t)score_key(__ldcg(sc + idx)) << 32) | (0x7FFFFFFFu - (uint32_t)idx)
+                                       : 0ull;
+    }
+    __syncthreads();
+    for (int size = 2; size <= n; size <<= 1)
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int p = tid; p < (n >> 1); p += SW_T) {
+                const int lo = 2 * p - (p & (stride - 1)), hi = lo + stride;
+                const bool desc = (lo & size) == 0;
+                const uint64_t x = tk[lo], y = tk[hi];
+                if ((x < y) == desc) {
+                    tk[lo] = y;
+                    tk[hi] = x;
+                }
+            }
+            __syncthreads();
+        }
+    for (int i = tid; i < k; i += SW_T) {
+        const uint64_t x = tk[i];
+        out[i] = x ? (int32_t)(0x7FFFFFFFu - (uint32_t)x) : -1;
+        if (a.keys_out) a.keys_out[(int64_t)b * k + i] = x ? (uint32_t)(x >> 32) : 0u;
+    }
 }
 
 // Standalone select, first kernel: the first digit's histogram of every request's scores
@@ -555,46 +669,6 @@ __global__ void __launch_bounds__(SW_T) select_hist_kernel(SelArgs a) {
         if (h[i]) atomicAdd(hb + i, h[i]);
 }
 
-// Standalone select, last kernel: request b's k selected indices (the set from the finish
-// kernel, in place in out) sorted by (score desc, index asc) -- a bitonic sort of the 63-bit
-// composites key << 32 | (2^31 - 1 - index) in shared memory, -1 padding (composite 0) last.
-constexpr int SW_SORT_T = 1024;
-__global__ void __launch_bounds__(SW_SORT_T) select_sort_kernel(SelArgs a, uint32_t* keys_out) {
-    __shared__ uint64_t v[2048];
-    const int tid = threadIdx.x, b = blockIdx.x, k = a.k;
-    const float* sc;
-    int64_t G;
-    sel_span(a, b, sc, G);
-    int32_t* out = a.out + (int64_t)b * k;
-    int n = 1;
-    while (n < k) n <<= 1;
-    pdl_wait();  // the set comes from the finish kernel
-    for (int i = tid; i < n; i += SW_SORT_T) {
-        const int32_t idx = i < k ? out[i] : -1;
-        v[i] = (idx >= 0 && idx < G) ? ((uint64_t)score_key(__ldcg(sc + idx)) << 32) | (0x7FFFFFFFu - (uint32_t)idx)
-                                     : 0ull;
-    }
-    __syncthreads();
-    for (int size = 2; size <= n; size <<= 1)
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int p = tid; p < (n >> 1); p += SW_SORT_T) {
-                const int lo = 2 * p - (p & (stride - 1)), hi = lo + stride;
-                const bool desc = (lo & size) == 0;  // every block of the last pass: descending
-                const uint64_t x = v[lo], y = v[hi];
-                if ((x < y) == desc) {
-                    v[lo] = y;
-                    v[hi] = x;
-                }
-            }
-            __syncthreads();
-        }
-    for (int i = tid; i < k; i += SW_SORT_T) {
-        const uint64_t x = v[i];
-        out[i] = x ? (int32_t)(0x7FFFFFFFu - (uint32_t)x) : -1;
-        if (keys_out) keys_out[(int64_t)b * k + i] = x ? (uint32_t)(x >> 32) : 0u;
-    }
-}
-
 // ------------------------------------------------------------------ host side
 static int64_t select_set_ctas(int64_t max_G) { return max_G <= 0 ? 1 : (max_G + SW_SLICE - 1) / SW_SLICE; }
 
@@ -616,6 +690,8 @@ cudaError_t launch_select_set(const SelectSetLaunch& h, cudaStream_t s, bool pdl
     a.ratio = h.ratio;
     a.offsets = h.offsets;
     a.G = h.G;
+    a.sorted = h.standalone ? 1 : 0;
+    a.keys_out = h.keys_out;
     a.C = (int)select_set_ctas(h.max_G);
     a.k = h.k;
     a.out = h.idx_out;
@@ -659,12 +735,7 @@ cudaError_t launch_select_set(const SelectSetLaunch& h, cudaStream_t s, bool pdl
     e = cudaLaunchKernelEx(&cfg, select_scan_kernel, a);
     if (e != cudaSuccess) return e;
     cfg.dynamicSmemBytes = smem;
-    e = cudaLaunchKernelEx(&cfg, select_finish_kernel, a);
-    if (e != cudaSuccess || !h.standalone) return e;
-    cfg.gridDim = dim3((unsigned)h.B, 1, 1);
-    cfg.blockDim = dim3(SW_SORT_T, 1, 1);
-    cfg.dynamicSmemBytes = 0;
-    return cudaLaunchKernelEx(&cfg, select_sort_kernel, a, h.keys_out);
+    return cudaLaunchKernelEx(&cfg, select_finish_kernel, a);
 }
 
 }  // namespace csa
