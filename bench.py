@@ -201,8 +201,8 @@ def other_workloads(torch, csa, entry, synth, stream, flush_l2, peak):
     res["topk_262144_to_512"] = {"us_per_call_back_to_back": round(e0.elapsed_time(e1) * 1e3 / 200, 2),
                                  "us_alone_scores_in_l2": round(warm, 2), "us_p90_alone_scores_in_l2": round(warm90, 2),
                                  "us_alone_l2_flushed": round(cold, 2), "us_p90_alone_l2_flushed": round(cold90, 2),
-                                 "output": "sorted by (score desc, index asc); each call zeroes its histograms "
-                                           "(one memset) and runs three kernels"}
+                                 "output": "sorted by (score desc, index asc); four kernels per call (clear the "
+                                           "histograms, first digit, scan, finish)"}
     # ---- C4 prefill compressor over the 1M workload's raw pool
     rp = csa.paged(b2.raw_pool, case2.rows_per_page, 1024, page_table=b2.page_table[0], n_pages=case2.n_pages)
     cout = torch.empty((G2, 512), dtype=torch.int16, device="cuda")

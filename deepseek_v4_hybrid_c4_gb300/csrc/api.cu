@@ -186,9 +186,8 @@ static csa_status topk_common(const float* scores, const int64_t* offsets, int32
     t.hist = static_cast<uint32_t*>(workspace);
     t.status = st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaMemsetAsync(workspace, 0, (size_t)B * kHistBlock * sizeof(uint32_t), s);
-    if (e != cudaSuccess) return from_cuda(e);
-    if (select_set_supported(G, k)) {  // wide select (first digit, scan, finish), then the sort
+    cudaError_t e = cudaSuccess;
+    if (select_set_supported(G, k)) {  // (its first kernel clears the histograms)  // wide select (first digit, scan, finish), then the sort
         SelectSetLaunch w;
         w.scores = scores;
         w.score_stride = 0;
@@ -207,7 +206,8 @@ static csa_status topk_common(const float* scores, const int64_t* offsets, int32
         w.keys_out = keys_out;
         e = launch_select_set(w, s, true);
     } else {
-        e = launch_topk(t, s, false);
+        e = cudaMemsetAsync(workspace, 0, (size_t)B * kHistBlock * sizeof(uint32_t), s);
+        if (e == cudaSuccess) e = launch_topk(t, s, false);
     }
     return from_cuda(e);
 }

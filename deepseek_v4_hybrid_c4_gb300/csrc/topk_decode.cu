@@ -638,7 +638,16 @@ __global__ void __launch_bounds__(SW_T, 1) select_finish_kernel(SelArgs a) {
     }
 }
 
-// Standalone select, first kernel: the first digit's histogram of every request's scores
+// Standalone select, first kernel: clears request blockIdx.x's histogram block (the first
+// digit's counts and the candidates' second digit); the histogram kernel loads its scores
+// meanwhile and waits for this grid before its first count.
+__global__ void __launch_bounds__(256) select_zero_kernel(uint32_t* hist) {
+    pdl_launch_dependents();
+    uint4* z = reinterpret_cast<uint4*>(hist + (int64_t)blockIdx.x * kHistBlock);
+    for (int i = threadIdx.x; i < 2 * kHistBins / 4; i += 256) z[i] = make_uint4(0, 0, 0, 0);
+}
+
+// Standalone select: the first digit's histogram of every request's scores
 // (each CTA counts its slice in shared memory and adds the non-zero bins).
 __global__ void __launch_bounds__(SW_T) select_hist_kernel(SelArgs a) {
     __shared__ uint32_t h[SW_BINS];
@@ -664,6 +673,7 @@ __global__ void __launch_bounds__(SW_T) select_hist_kernel(SelArgs a) {
         }
     }
     __syncthreads();
+    pdl_wait();  // the histogram block is cleared by the preceding kernel
     uint32_t* hb = a.hist + (int64_t)b * kHistBlock;
     for (int i = tid; i < SW_BINS; i += SW_T)
         if (h[i]) atomicAdd(hb + i, h[i]);
@@ -726,11 +736,15 @@ cudaError_t launch_select_set(const SelectSetLaunch& h, cudaStream_t s, bool pdl
     cfg.dynamicSmemBytes = SW_SCAN_SPREAD_SMEM;
     cfg.stream = s;
     cudaError_t e = cudaSuccess;
-    if (h.standalone) {  // first digit counted here; the scan follows programmatically
-        cfg.numAttrs = 0;
+    if (h.standalone) {  // histograms cleared, first digit counted; the scan follows programmatically
+        cudaLaunchConfig_t z = {};
+        z.gridDim = dim3((unsigned)h.B, 1, 1);
+        z.blockDim = dim3(256, 1, 1);
+        z.stream = s;
+        e = cudaLaunchKernelEx(&z, select_zero_kernel, h.hist);
+        if (e != cudaSuccess) return e;
         e = cudaLaunchKernelEx(&cfg, select_hist_kernel, a);
         if (e != cudaSuccess) return e;
-        cfg.numAttrs = 1;
     }
     e = cudaLaunchKernelEx(&cfg, select_scan_kernel, a);
     if (e != cudaSuccess) return e;
