@@ -188,11 +188,34 @@ __global__ void __launch_bounds__(SC_THREADS, HI >= 16 ? 1 : 2)
     }
     __syncwarp();
 
-    // This CTA's CTA-steps: m = blockIdx.x + k * gridDim.x for k = 0, 1, ...; in each, warp j
-    // takes step j.  Page lookups run a window of 16 CTA-steps at a time: lane l holds unit
+    // This CTA's CTA-steps: one request -- m = blockIdx.x + k gridDim.x, k = 0, 1, ...; a batch
+    // -- a contiguous share [m0, m0 + nk) of its CTA-steps, so that a CTA meets one or two
+    // requests rather than a new one (query restage, histogram flush) every CTA-step.  In each
+    // CTA-step warp j takes step j.  Page lookups run a window of 16 CTA-steps at a time: lane l
+    // holds unit
     // (l & 1) of this warp's step in CTA-step k0 + (l >> 1), all 32 loads in flight together.
     // Two register sets alternate (even / odd windows) and the next window is looked up as the
     // current one starts, so the page-table latency stays off the copy path.
+    const bool blocked = a.B > 1;
+    int64_t m0 = blockIdx.x, nk = INT64_MAX;  // (one request: the stride form, ended by the cursor)
+    if (blocked) {
+        __shared__ int64_t s_tot[SC_WARPS];
+        int64_t t = 0;  // the batch's CTA-steps (ragged requests: from the device lengths)
+        for (int b = threadIdx.x; b < a.B; b += SC_THREADS) {
+            const int64_t G = a.n_tokens ? __ldg(a.n_tokens + b) / a.ratio : a.G;
+            t += ((G + SC_SUPER - 1) / SC_SUPER + SC_WARPS - 1) / SC_WARPS;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if (lane == 0) s_tot[warp] = t;
+        __syncthreads();
+        int64_t total = 0;
+#pragma unroll
+        for (int w = 0; w < SC_WARPS; ++w) total += s_tot[w];
+        m0 = (int64_t)blockIdx.x * total / gridDim.x;
+        nk = ((int64_t)blockIdx.x + 1) * total / gridDim.x - m0;
+    }
+    auto cta_step = [&](int64_t k) { return blocked ? m0 + k : (int64_t)blockIdx.x + k * gridDim.x; };
     CtaStepCursor lc;  // this lane's lookup cursor
     int wk[2] = {0, 0}, ws[2] = {0, 0}, wp[2] = {0, 0};  // per set: kind (0 past the end, 1 copy,
                                                           // 2 nothing to copy), row in page, page
@@ -201,8 +224,8 @@ __global__ void __launch_bounds__(SC_THREADS, HI >= 16 ? 1 : 2)
         kind = 0;
         slot = 0;
         page = 0;
-        const int64_t m = blockIdx.x + k * gridDim.x;
-        if (lc.seek(a, m)) {
+        const int64_t m = cta_step(k);
+        if (k < nk && lc.seek(a, m)) {
             const int64_t gr = ((m - lc.base) * SC_WARPS + warp) * SC_SUPER + (lane & 1) * SC_UNIT;
             kind = 2;
             if (gr < lc.G) {
@@ -282,7 +305,7 @@ __global__ void __launch_bounds__(SC_THREADS, HI >= 16 ? 1 : 2)
     };
     {
         CtaStepCursor c0;
-        if (c0.seek(a, blockIdx.x)) q_fetch(c0.b);
+        if (nk > 0 && c0.seek(a, cta_step(0))) q_fetch(c0.b);
     }
     lookup_window(0, wk[0], ws[0], wp[0]);
     lookup_window(16, wk[1], ws[1], wp[1]);
@@ -309,8 +332,8 @@ __global__ void __launch_bounds__(SC_THREADS, HI >= 16 ? 1 : 2)
     const int hu = lane >> 4;       // chunk half (c)
     CtaStepCursor cur;
     for (int64_t k = 0;; ++k) {
-        const int64_t m = blockIdx.x + k * gridDim.x;
-        if (!cur.seek(a, m)) break;  // the same for every warp of the CTA
+        const int64_t m = cta_step(k);
+        if (k >= nk || !cur.seek(a, m)) break;  // the same for every warp of the CTA
         const int sl = (int)(k & 1);
         if ((k & 15) == 0 && k > 0) {  // window k/16 starts: look up window k/16 + 1 into the freed set
             if ((k >> 4) & 1) lookup_window(k + 16, wk[0], ws[0], wp[0]);
@@ -326,7 +349,7 @@ __global__ void __launch_bounds__(SC_THREADS, HI >= 16 ? 1 : 2)
         }
         {  // the CTA's next CTA-step starts another request: fetch its query now
             CtaStepCursor nx = cur;
-            if (nx.seek(a, m + gridDim.x) && nx.b != qb && nx.b != qf_b) q_fetch(nx.b);
+            if (k + 1 < nk && nx.seek(a, cta_step(k + 1)) && nx.b != qb && nx.b != qf_b) q_fetch(nx.b);
         }
         const int64_t st = (m - cur.base) * SC_WARPS + warp;  // this warp's step within the request
         const int kind_me = __shfl_sync(0xffffffffu, ((k >> 4) & 1) ? wk[1] : wk[0], 2 * (int)(k & 15) + hu);
