@@ -187,7 +187,7 @@ static csa_status topk_common(const float* scores, const int64_t* offsets, int32
     t.status = st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
-    if (select_set_supported(G, k)) {  // (its first kernel clears the histograms)  // wide select (first digit, scan, finish), then the sort
+    if (select_set_supported(G, k)) {  // wide select: clear, first digit, scan, sorted finish (no memset)
         SelectSetLaunch w;
         w.scores = scores;
         w.score_stride = 0;

@@ -139,11 +139,12 @@ __global__ void __launch_bounds__(256) compress_r4_kernel(CompressArgs a) {
     }
 }
 
-// C128: one CTA (8 warps) per group.  Each warp streams 16 of the 128 rows with an
-// online softmax (running max, sum, weighted accumulator); the 8 partial states
-// are merged through shared memory.
-constexpr int R128_WARPS = 8;
-__global__ void __launch_bounds__(256) compress_r128_kernel(CompressArgs a) {
+// C128: one CTA (16 warps) per group.  Warp w takes rows w, w + 16, ..., w + 112 of the
+// group: their page lookups go out together, then all 8 row loads, then an online softmax
+// over the 8 rows (running max, sum, weighted accumulator); the 16 partial states are merged
+// through shared memory.
+constexpr int R128_WARPS = 16;
+__global__ void __launch_bounds__(R128_WARPS * 32) compress_r128_kernel(CompressArgs a) {
     __shared__ float sm_m[R128_WARPS], sm_l[R128_WARPS];
     __shared__ __align__(16) float sm_acc[R128_WARPS][D];
     pdl_launch_dependents();
@@ -158,37 +159,34 @@ __global__ void __launch_bounds__(256) compress_r128_kernel(CompressArgs a) {
         const float4 t = __ldg(reinterpret_cast<const float4*>(a.w_gate + lane * 16 + i));
         wg[i] = t.x; wg[i + 1] = t.y; wg[i + 2] = t.z; wg[i + 3] = t.w;
     }
-    constexpr int ROWS = 128 / R128_WARPS;  // 16 rows per warp
-    constexpr int U = 4;                    // rows in flight per warp
+    constexpr int ROWS = 128 / R128_WARPS;  // 8 rows per warp, all in flight
     for (int64_t gi = blockIdx.x; gi < count; gi += gridDim.x) {
         const int64_t g = first + gi;
+        const uint8_t* rows[ROWS];
+#pragma unroll
+        for (int u = 0; u < ROWS; ++u) rows[u] = row_addr(a.raw, b, 128 * g + warp + R128_WARPS * u, ROW_BYTES, a.status);
+        uint4 v[ROWS][2];
+#pragma unroll
+        for (int u = 0; u < ROWS; ++u) load_row16(rows[u], lane, v[u]);
         float m = -INFINITY, l = 0.f, acc[16];
 #pragma unroll
         for (int d = 0; d < 16; ++d) acc[d] = 0.f;
-        for (int r0 = 0; r0 < ROWS; r0 += U) {
-            uint4 v[U][2];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int i = warp + R128_WARPS * (r0 + u);  // row within the group
-                load_row16(row_addr(a.raw, b, 128 * g + i, ROW_BYTES, a.status), lane, v[u]);
-            }
+        for (int u = 0; u < ROWS; ++u) {
+            const int i = warp + R128_WARPS * u;  // row within the group
+            float x[16];
+            unpack16(v[u], x);
+            float p = 0.f;
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int i = warp + R128_WARPS * (r0 + u);
-                float x[16];
-                unpack16(v[u], x);
-                float p = 0.f;
+            for (int e = 0; e < 16; ++e) p = fmaf(x[e], wg[e], p);
+            const float s = warp_sum(p) + __ldg(a.b_pos + i);
+            const float mn = fmaxf(m, s);
+            const float sc = expf(m - mn);
+            const float pe = expf(s - mn);
+            l = l * sc + pe;
 #pragma unroll
-                for (int e = 0; e < 16; ++e) p = fmaf(x[e], wg[e], p);
-                const float s = warp_sum(p) + __ldg(a.b_pos + i);
-                const float mn = fmaxf(m, s);
-                const float sc = expf(m - mn);
-                const float pe = expf(s - mn);
-                l = l * sc + pe;
-#pragma unroll
-                for (int d = 0; d < 16; ++d) acc[d] = fmaf(pe, x[d], acc[d] * sc);
-                m = mn;
-            }
+            for (int d = 0; d < 16; ++d) acc[d] = fmaf(pe, x[d], acc[d] * sc);
+            m = mn;
         }
         if (lane == 0) {
             sm_m[warp] = m;
@@ -198,21 +196,23 @@ __global__ void __launch_bounds__(256) compress_r128_kernel(CompressArgs a) {
         for (int d = 0; d < 16; d += 4)
             *reinterpret_cast<float4*>(&sm_acc[warp][lane * 16 + d]) = make_float4(acc[d], acc[d + 1], acc[d + 2], acc[d + 3]);
         __syncthreads();
-        float M = sm_m[0];
+        if (threadIdx.x < D / 2) {  // two columns per thread
+            float M = sm_m[0];
 #pragma unroll
-        for (int w = 1; w < R128_WARPS; ++w) M = fmaxf(M, sm_m[w]);
-        float L = 0.f, o0 = 0.f, o1 = 0.f;
-        const int d0 = 2 * threadIdx.x;
+            for (int w = 1; w < R128_WARPS; ++w) M = fmaxf(M, sm_m[w]);
+            float L = 0.f, o0 = 0.f, o1 = 0.f;
+            const int d0 = 2 * threadIdx.x;
 #pragma unroll
-        for (int w = 0; w < R128_WARPS; ++w) {
-            const float f = expf(sm_m[w] - M);
-            L = fmaf(f, sm_l[w], L);
-            o0 = fmaf(f, sm_acc[w][d0], o0);
-            o1 = fmaf(f, sm_acc[w][d0 + 1], o1);
+            for (int w = 0; w < R128_WARPS; ++w) {
+                const float f = expf(sm_m[w] - M);
+                L = fmaf(f, sm_l[w], L);
+                o0 = fmaf(f, sm_acc[w][d0], o0);
+                o1 = fmaf(f, sm_acc[w][d0 + 1], o1);
+            }
+            const float inv = 1.f / L;
+            uint8_t* dst = const_cast<uint8_t*>(row_addr(a.out, b, g, ROW_BYTES, a.status));
+            if (dst) *reinterpret_cast<uint32_t*>(dst + d0 * 2) = pack_bf16x2(o0 * inv, o1 * inv);
         }
-        const float inv = 1.f / L;
-        uint8_t* dst = const_cast<uint8_t*>(row_addr(a.out, b, g, ROW_BYTES, a.status));
-        if (dst) *reinterpret_cast<uint32_t*>(dst + d0 * 2) = pack_bf16x2(o0 * inv, o1 * inv);
         __syncthreads();
     }
 }
@@ -248,7 +248,7 @@ cudaError_t launch_compress(const CompressLaunch& h, cudaStream_t s, bool pdl) {
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     cfg.stream = s;
-    cfg.blockDim = dim3(256, 1, 1);
+    cfg.blockDim = dim3(h.ratio == 4 ? 256 : R128_WARPS * 32, 1, 1);
     int64_t gx;
     if (h.n_tokens) {
         gx = 1;  // decode: one block per request loops over its pending groups
