@@ -43,7 +43,7 @@ constexpr uint32_t SM_KOK = SM_KPTR + 64 * 8;      // 64-bit valid mask
 constexpr uint32_t AT_SMEM = SM_KOK + 64 + 1024;   // + alignment slack
 constexpr uint32_t R_PITCH = AT_DH * 2 + 16;       // staged fp16 row of one half (padded)
 constexpr uint32_t SM_STG = 0;                     // this split's [128] staged rows (the Q tile's space)
-constexpr int AT_MAX_SPLITS = 16;                  // splits per request (the merge holds them in registers)
+constexpr int AT_MAX_SPLITS = 32;                  // splits per request (the merge holds them in registers)
 constexpr uint32_t Q_SLAB = AT_M * 128;
 constexpr uint32_t K_SLAB = AT_KT * 128;
 constexpr float LOG2E = 1.4426950408889634f;
@@ -141,20 +141,22 @@ __global__ void __launch_bounds__(AT_T, 1) attn_kernel(AttnArgs a) {
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
         bool ok = true;
 
+        // address of key j's row (selected compressed entry, then the window), or nullptr
+        auto key_row = [&](int64_t j) -> const uint8_t* {
+            if (j < n_c) {
+                const int64_t g = a.sel ? (int64_t)__ldg(a.sel + (int64_t)b * a.sel_stride + j) : j;
+                return g >= 0 ? row_addr(a.kc, b, g, ROW_BYTES, a.status) : nullptr;
+            }
+            if (j < n_keys) return row_addr(a.kr, b, N - W + (j - n_c), ROW_BYTES, a.status);
+            return nullptr;
+        };
+        const uint8_t* p_next = tid < AT_KT ? key_row(t0 * AT_KT + tid) : nullptr;
         int it = 0;
         for (int64_t tile = t0; tile < t1; ++tile, ++it) {
-            // ---- key rows of this tile
+            // ---- key rows of this tile (looked up while the previous tile was gathered)
             if (tid < AT_KT) {
-                const int64_t j = tile * AT_KT + tid;
-                const uint8_t* p = nullptr;
-                if (j < n_c) {
-                    const int64_t g = a.sel ? (int64_t)__ldg(a.sel + (int64_t)b * a.sel_stride + j) : j;
-                    if (g >= 0) p = row_addr(a.kc, b, g, ROW_BYTES, a.status);
-                } else if (j < n_keys) {
-                    p = row_addr(a.kr, b, N - W + (j - n_c), ROW_BYTES, a.status);
-                }
-                kptr[tid] = p;
-                const unsigned m = __ballot_sync(0xffffffffu, p != nullptr);
+                kptr[tid] = p_next;
+                const unsigned m = __ballot_sync(0xffffffffu, p_next != nullptr);
                 if (lane == 0) reinterpret_cast<uint32_t*>(kok)[warp] = m;
             }
             // the previous tile's P.V must be done before K/V and P are overwritten
@@ -170,6 +172,13 @@ __global__ void __launch_bounds__(AT_T, 1) attn_kernel(AttnArgs a) {
                     st_shared_zero16(dst);
             }
             cp_async_commit();
+            // the next tile's rows: look them up and start pulling them into L2 while this
+            // tile's copies are in flight (the lookups are dependent loads, the pulls are
+            // fire-and-forget)
+            if (tid < AT_KT && tile + 1 < t1) {
+                p_next = key_row((tile + 1) * AT_KT + tid);
+                if (p_next) prefetch_l2_bulk(p_next, ROW_BYTES);
+            }
             cp_async_wait_all();
             fence_proxy_async_smem();
             __syncthreads();
@@ -328,18 +337,325 @@ __global__ void __launch_bounds__(AT_T, 1) attn_kernel(AttnArgs a) {
     }
 }
 
+// ---------------------------------------------------------------- H <= 64
+// With at most 64 heads, half of the M = 128 rows of every MMA would be padding.  One CTA
+// then covers both V halves of a split, and the spare rows carry the second half:
+//   O rows 0..63   += P V[:, 0:256]     O rows 64..127 += P V[:, 256:512]
+// as one M=128, N=256, K=128 product [P 0; 0 P] [V_lo; V_hi]: eight K=16 steps, the first
+// four with A = (P; 0) and B = the tile's first four slabs read MN-major, the last four with
+// A = (0; P) and the other four slabs.  P sits between two zero blocks, so both A operands
+// are windows of one 24 KiB region.  S = Q K^T keeps M = 128 with only Q's 64 rows staged
+// (64 KiB): rows 64..127 of each slab's operand read the next slab, their logits land in
+// TMEM lanes 64..127 and are never read.  The freed shared memory holds a second K tile:
+// the next tile's rows are gathered while the current one is multiplied.
+// TMEM: O [0, 256) (lane h: head h, columns 0..255; lane 64 + h: head h, columns 256..511),
+// S [256, 320).
+constexpr int A6_H = 64;
+constexpr uint32_t A6_Q_SLAB = A6_H * 128;                  // 8 KiB
+constexpr uint32_t A6_SM_Q = 0;                             // 8 slabs x 64 rows x 128 B
+constexpr uint32_t A6_SM_K = 8 * A6_Q_SLAB;                 // 2 stages x 8 slabs x 64 rows x 128 B
+constexpr uint32_t A6_KST = 8 * K_SLAB;                     // 64 KiB per stage
+constexpr uint32_t A6_SM_P = A6_SM_K + 2 * A6_KST;          // [zero 8 KiB][P 8 KiB][zero 8 KiB]
+constexpr uint32_t A6_SM_BAR = A6_SM_P + 3 * 8192;
+constexpr uint32_t A6_SM_TMEM = A6_SM_BAR + 16;
+constexpr uint32_t A6_SM_ALPHA = A6_SM_BAR + 64;            // [64] rescale factors, then [64] {m, l}
+constexpr uint32_t A6_SM_ML = A6_SM_ALPHA + 64 * 4;
+constexpr uint32_t A6_SM_KPTR = A6_SM_ML + 64 * 8;          // [2 stages][64] row pointers
+constexpr uint32_t A6_SM_KOK = A6_SM_KPTR + 2 * 64 * 8;     // [2 stages] 64-bit valid masks
+constexpr uint32_t A6_SMEM = A6_SM_KOK + 16 + 1024;         // + alignment slack
+static_assert(A6_SMEM <= 227 * 1024, "attn64 shared memory");
+static_assert(128 * R_PITCH <= A6_SM_P, "attn64 staging fits below P");
+
+__global__ void __launch_bounds__(AT_T, 1) attn64_kernel(AttnArgs a) {
+    extern __shared__ uint8_t at_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(at_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(sm);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int split = blockIdx.x, b = blockIdx.y;
+    const uint32_t bar_s = sbase + A6_SM_BAR, bar_o = sbase + A6_SM_BAR + 8;
+    const uint8_t** kptr = reinterpret_cast<const uint8_t**>(sm + A6_SM_KPTR);
+    uint64_t* kok = reinterpret_cast<uint64_t*>(sm + A6_SM_KOK);
+    float* sm_alpha = reinterpret_cast<float*>(sm + A6_SM_ALPHA);
+    float2* sm_ml = reinterpret_cast<float2*>(sm + A6_SM_ML);
+
+    const int64_t N = a.n_tokens ? a.n_tokens[b] : a.N;
+    const int64_t W = N < a.swa ? N : a.swa;
+    const int64_t n_c = a.sel ? a.n_sel : (a.n_tokens ? N / a.ratio : a.n_sel);
+    const int64_t n_keys = n_c + W;
+    const int64_t T = (n_keys + AT_KT - 1) / AT_KT;
+    const int64_t t0 = (int64_t)split * a.tps;
+    const int64_t t1 = t0 + a.tps < T ? t0 + a.tps : T;
+    const int H = a.H, S = a.S;
+    const bool direct = S == 1;
+    const bool soft = tid < A6_H;  // warps 0, 1: head tid's softmax
+    float m_run = -INFINITY, l_run = 0.f;
+
+    if (t0 >= t1) {
+        pdl_wait();
+        pdl_launch_dependents();
+        if (direct)  // no keys at all
+            for (int r = warp; r < 2 * H; r += AT_T / 32)
+                *reinterpret_cast<uint4*>(a.out + ((int64_t)b * H + (r >> 1)) * D + (r & 1) * AT_DH + lane * 8) =
+                    make_uint4(0, 0, 0, 0);
+        if (tid < H) {
+            if (!direct) {
+                const float2 z = make_float2(-INFINITY, 0.f);
+                a.part_ml[(((int64_t)b * 2 + 0) * S + split) * H + tid] = z;
+                a.part_ml[(((int64_t)b * 2 + 1) * S + split) * H + tid] = z;
+            } else if (a.lse) {
+                a.lse[(int64_t)b * H + tid] = -INFINITY;
+            }
+        }
+        return;
+    }
+    if (warp == 0) {
+        tmem_alloc(sbase + A6_SM_TMEM, 512);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(bar_s, 1);
+        mbar_init(bar_o, 1);
+        fence_mbar_init();
+    }
+    // Q -> swizzled K-major tile of 64 rows (rows >= H are zero); the zero blocks around P
+    const uint16_t* qb = a.q + (int64_t)b * H * D;
+    for (int c = tid; c < A6_H * 64; c += AT_T) {
+        const uint32_t row = c >> 6, ch = c & 63;
+        const uint32_t dst = sbase + A6_SM_Q + (ch >> 3) * A6_Q_SLAB + swz(row, ch & 7);
+        if ((int)row < H)
+            cp_async16(dst, qb + row * D + ch * 8);
+        else
+            st_shared_zero16(dst);
+    }
+    for (int c = tid; c < 1024; c += AT_T)
+        st_shared_zero16(sbase + A6_SM_P + (uint32_t)(c < 512 ? c : c + 512) * 16u);
+    cp_async_commit();
+
+    auto key_row = [&](int64_t j) -> const uint8_t* {
+        if (j < n_c) {
+            const int64_t g = a.sel ? (int64_t)__ldg(a.sel + (int64_t)b * a.sel_stride + j) : j;
+            return g >= 0 ? row_addr(a.kc, b, g, ROW_BYTES, a.status) : nullptr;
+        }
+        if (j < n_keys) return row_addr(a.kr, b, N - W + (j - n_c), ROW_BYTES, a.status);
+        return nullptr;
+    };
+    auto publish = [&](int st, const uint8_t* p) {  // warps 0, 1
+        kptr[st * AT_KT + tid] = p;
+        const unsigned m = __ballot_sync(0xffffffffu, p != nullptr);
+        if (lane == 0) reinterpret_cast<uint32_t*>(kok + st)[warp] = m;
+    };
+    auto gather = [&](int st) {  // every thread; kptr[st] published and visible
+        const uint32_t kb = sbase + A6_SM_K + (uint32_t)st * A6_KST;
+        for (int c = tid; c < AT_KT * 64; c += AT_T) {
+            const uint32_t row = c >> 6, ch = c & 63;
+            const uint32_t dst = kb + (ch >> 3) * K_SLAB + swz(row, ch & 7);
+            const uint8_t* src = kptr[st * AT_KT + row];
+            if (src)
+                cp_async16(dst, src + ch * 16);
+            else
+                st_shared_zero16(dst);
+        }
+        cp_async_commit();
+    };
+
+    // the selection and the freshly compressed rows come from the preceding kernels
+    pdl_wait();
+    pdl_launch_dependents();
+    if (soft) publish(0, key_row(t0 * AT_KT + tid));
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    gather(0);
+    const uint8_t* p_next = soft && t0 + 1 < t1 ? key_row((t0 + 1) * AT_KT + tid) : nullptr;
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + A6_SM_TMEM);
+    const uint32_t t_o = tmem, t_s = tmem + AT_DH;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    bool ok = true;
+    int it = 0;
+    for (int64_t tile = t0; tile < t1; ++tile, ++it) {
+        const int st = it & 1;
+        // P . V of the previous tile done: its K stage, P and O are free
+        if (it > 0 && !mbar_wait(bar_o, (uint32_t)((it - 1) & 1))) ok = false;
+        tc_fence_after();
+        const bool more = tile + 1 < t1;
+        if (soft && more) publish(st ^ 1, p_next);
+        cp_async_wait_all();  // this tile's rows (and Q) landed
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (more) gather(st ^ 1);  // the next tile's rows, behind this tile's products
+        // ---- S = Q K^T  (M=128, N=64, K=512); rows 64..127 are not used
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t id_s = idesc_bf16_f32(AT_M, AT_KT, false);
+            const uint32_t kb = sbase + A6_SM_K + (uint32_t)st * A6_KST;
+#pragma unroll
+            for (int s8 = 0; s8 < 8; ++s8)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t ad = sdesc_sw128(sbase + A6_SM_Q + s8 * A6_Q_SLAB + kk * 32, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(kb + s8 * K_SLAB + kk * 32, 16, 1024);
+                    tc_mma_f16(t_s, ad, bd, id_s, (s8 | kk) ? 1u : 0u);
+                }
+            tc_commit(bar_s);
+        }
+        if (soft && tile + 2 < t1) p_next = key_row((tile + 2) * AT_KT + tid);
+        float alpha = 1.f;
+        if (soft) {
+            if (!mbar_wait(bar_s, (uint32_t)(it & 1))) ok = false;
+            tc_fence_after();
+            uint32_t sr[2][32];
+            tc_ld32(t_s + lane_off, sr[0]);
+            tc_ld32(t_s + lane_off + 32, sr[1]);
+            tc_wait_ld();
+            const uint64_t valid = kok[st];
+            float x[64];
+            float mt = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                const bool v = (valid >> j) & 1ull;
+                x[j] = v ? __uint_as_float(sr[j >> 5][j & 31]) * a.sl2 : -INFINITY;
+                mt = fmaxf(mt, x[j]);
+            }
+            if (mt > -INFINITY) {
+                if (m_run == -INFINITY) {
+                    m_run = mt;
+                } else if (mt > m_run + RESCALE_THRESHOLD) {
+                    alpha = ex2(m_run - mt);
+                    m_run = mt;
+                }
+            }
+            float lsum = 0.f;
+            uint32_t pk[32];
+#pragma unroll
+            for (int j = 0; j < 64; j += 2) {
+                const float p0 = m_run == -INFINITY ? 0.f : ex2(x[j] - m_run);
+                const float p1 = m_run == -INFINITY ? 0.f : ex2(x[j + 1] - m_run);
+                const uint32_t w = pack_bf16x2(p0, p1);
+                pk[j >> 1] = w;
+                lsum += bf16lo(w) + bf16hi(w);
+            }
+            l_run = l_run * alpha + lsum;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                st_shared_v4(sbase + A6_SM_P + 8192u + swz((uint32_t)tid, (uint32_t)c),
+                             make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
+            sm_alpha[tid] = alpha;
+        }
+        __syncthreads();
+        // rescale O (both column halves of the head) when its running max moved
+        if (!soft) alpha = sm_alpha[tid - A6_H];
+        if (it > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+            for (int c = 0; c < AT_DH; c += 32) {
+                uint32_t o[32];
+                tc_ld32(t_o + lane_off + c, o);
+                tc_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                tc_st32(t_o + lane_off + c, o);
+            }
+            tc_wait_st();
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // ---- O += [P 0; 0 P] [V_lo; V_hi]  (M=128, N=256, K=128)
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t id_o = idesc_bf16_f32(AT_M, AT_DH, true);
+            const uint32_t kb = sbase + A6_SM_K + (uint32_t)st * A6_KST;
+#pragma unroll
+            for (int hv = 0; hv < 2; ++hv)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t ad = sdesc_sw128(sbase + A6_SM_P + (hv ? 0u : 8192u) + kk * 32, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(kb + (uint32_t)(hv * 4) * K_SLAB + kk * 16 * 128, K_SLAB, 1024);
+                    tc_mma_f16(t_o, ad, bd, id_o, (it > 0 || hv > 0 || kk > 0) ? 1u : 0u);
+                }
+            tc_commit(bar_o);
+        }
+    }
+    if (!mbar_wait(bar_o, (uint32_t)((it - 1) & 1))) ok = false;
+    tc_fence_after();
+    cp_async_wait_all();
+    if (!ok && tid == 0) raise_status(a.status, CSA_ERR_TIMEOUT);
+    if (soft) sm_ml[tid] = make_float2(m_run, l_run);
+    __syncthreads();
+    // ---- rows normalised (fp16 partial, or the bf16 output when S == 1), staged as
+    //      row 2 * head + column half, then coalesced to global memory
+    {
+        const int hd = tid & (A6_H - 1), hv = tid >> 6;
+        const float l = sm_ml[hd].y;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const uint32_t srow = sbase + (uint32_t)(2 * hd + hv) * R_PITCH;
+        for (int c0 = 0; c0 < AT_DH; c0 += 128) {
+            uint32_t o[4][32];
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) tc_ld32(t_o + lane_off + (uint32_t)(c0 + 32 * qq), o[qq]);
+            tc_wait_ld();
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq)
+#pragma unroll
+                for (int e = 0; e < 32; e += 8) {
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float f0 = __uint_as_float(o[qq][e + 2 * q]) * inv;
+                        const float f1 = __uint_as_float(o[qq][e + 2 * q + 1]) * inv;
+                        if (direct) {
+                            w4[q] = pack_bf16x2(f0, f1);
+                        } else {
+                            const __half2 hh = __floats2half2_rn(f0, f1);
+                            w4[q] = *reinterpret_cast<const uint32_t*>(&hh);
+                        }
+                    }
+                    st_shared_v4(srow + (uint32_t)(c0 + 32 * qq + e) * 2u, make_uint4(w4[0], w4[1], w4[2], w4[3]));
+                }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+    uint16_t* dst = direct ? a.out + (int64_t)b * H * D
+                           : reinterpret_cast<uint16_t*>(a.part_o + ((int64_t)b * S + split) * H * D);
+    constexpr int NWA = AT_T / 32;
+    for (int r0 = warp; r0 < 2 * H; r0 += 8 * NWA) {  // eight 512-byte rows per warp in flight
+        uint4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int r = r0 + j * NWA;
+            if (r < 2 * H) v[j] = ld_shared_v4(sbase + (uint32_t)r * R_PITCH + (uint32_t)lane * 16u);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int r = r0 + j * NWA;
+            if (r < 2 * H) *reinterpret_cast<uint4*>(dst + (int64_t)(r >> 1) * D + (r & 1) * AT_DH + lane * 8) = v[j];
+        }
+    }
+    if (tid < H) {
+        if (!direct) {
+            const float2 ml = make_float2(m_run, l_run);
+            a.part_ml[(((int64_t)b * 2 + 0) * S + split) * H + tid] = ml;
+            a.part_ml[(((int64_t)b * 2 + 1) * S + split) * H + tid] = ml;
+        } else if (a.lse) {
+            a.lse[(int64_t)b * H + tid] = l_run > 0.f ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
+        }
+    }
+}
+
 // Log-sum-exp merge of the splits: one CTA per (head, request); thread t owns columns
 // 4t .. 4t+3 (half t / 64).  Every split's (max, sum) and row piece are loaded at once.
+template <int MAXS>
 __global__ void __launch_bounds__(128) attn_merge_kernel(AttnArgs a) {
     pdl_wait();
     const int h = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
     const int H = a.H, S = a.S, half = t >> 6;
     const float2* mlb = a.part_ml + ((int64_t)b * 2 + half) * S * H + h;
     const __half* pb = a.part_o + ((int64_t)b * S * H + h) * D + t * 4;
-    float2 ml[AT_MAX_SPLITS];
-    uint2 x[AT_MAX_SPLITS];
+    float2 ml[MAXS];
+    uint2 x[MAXS];
 #pragma unroll
-    for (int s = 0; s < AT_MAX_SPLITS; ++s) {
+    for (int s = 0; s < MAXS; ++s) {
         if (s < S) {
             ml[s] = __ldcg(mlb + (int64_t)s * H);
             x[s] = __ldcg(reinterpret_cast<const uint2*>(pb + (int64_t)s * H * D));
@@ -347,11 +663,11 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(AttnArgs a) {
     }
     float M = -INFINITY;
 #pragma unroll
-    for (int s = 0; s < AT_MAX_SPLITS; ++s)
+    for (int s = 0; s < MAXS; ++s)
         if (s < S && ml[s].y > 0.f) M = fmaxf(M, ml[s].x);
     float L = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
 #pragma unroll
-    for (int s = 0; s < AT_MAX_SPLITS; ++s) {
+    for (int s = 0; s < MAXS; ++s) {
         if (s < S && ml[s].y > 0.f) {
             const float w = ml[s].y * ex2(ml[s].x - M);
             const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&x[s].x));
@@ -371,13 +687,15 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(AttnArgs a) {
     if (t == 0 && a.lse) a.lse[(int64_t)b * H + h] = L > 0.f ? (M + log2f(L)) * LN2 : -INFINITY;
 }
 
-// Split heuristic (device independent so workspace sizes are stable): about one
-// wave of 2*B*S CTAs on 152 SMs, at most one split per key tile.
-static void plan_splits(int B, int64_t max_keys, int* tps, int* S) {
+// Split heuristic (device independent so workspace sizes are stable): about one wave
+// of CTAs (one per SM) on 152 SMs -- 2*B*S of them above 64 heads (one per V half), B*S
+// at or below -- with at most one split per key tile.
+static void plan_splits(int B, int H, int64_t max_keys, int* tps, int* S) {
     const int64_t T = (max_keys + AT_KT - 1) / AT_KT;
-    int64_t s = 76 / (B > 0 ? B : 1);
+    const bool h64 = H <= A6_H;
+    int64_t s = (h64 ? 152 : 76) / (B > 0 ? B : 1);
     if (s < 1) s = 1;
-    if (s > AT_MAX_SPLITS) s = AT_MAX_SPLITS;
+    if (s > (h64 ? AT_MAX_SPLITS : 16)) s = h64 ? AT_MAX_SPLITS : 16;
     if (s > T) s = T;
     if (s < 1) s = 1;
     int64_t t = (T + s - 1) / s;
@@ -390,7 +708,7 @@ static void plan_splits(int B, int64_t max_keys, int* tps, int* S) {
 
 size_t attn_workspace_bytes(int B, int H, int64_t max_keys) {
     int tps, S;
-    plan_splits(B, max_keys, &tps, &S);
+    plan_splits(B, H, max_keys, &tps, &S);
     const size_t po = (size_t)B * S * H * D * sizeof(__half);
     const size_t pm = (size_t)B * 2 * S * H * sizeof(float2);
     return ((po + 255) & ~size_t(255)) + pm;
@@ -421,7 +739,7 @@ cudaError_t launch_attn(const AttnLaunch& h, cudaStream_t s, bool pdl) {
     a.ratio = h.ratio;
     a.N = h.N;
     a.swa = h.swa;
-    plan_splits(h.B, h.max_keys, &a.tps, &a.S);
+    plan_splits(h.B, h.H, h.max_keys, &a.tps, &a.S);
     const size_t po = (size_t)h.B * a.S * h.H * D * sizeof(__half);
     a.part_o = static_cast<__half*>(h.ws);
     a.part_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(h.ws) + ((po + 255) & ~size_t(255)));
@@ -431,26 +749,30 @@ cudaError_t launch_attn(const AttnLaunch& h, cudaStream_t s, bool pdl) {
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)AT_SMEM);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(attn64_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)A6_SMEM);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
+    const bool h64 = h.H <= A6_H;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    cfg.gridDim = dim3(2, (unsigned)a.S, (unsigned)h.B);
+    cfg.gridDim = h64 ? dim3((unsigned)a.S, (unsigned)h.B, 1) : dim3(2, (unsigned)a.S, (unsigned)h.B);
     cfg.blockDim = dim3(AT_T, 1, 1);
-    cfg.dynamicSmemBytes = AT_SMEM;
+    cfg.dynamicSmemBytes = h64 ? A6_SMEM : AT_SMEM;
     cfg.stream = s;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, attn_kernel, a);
+    cudaError_t e = h64 ? cudaLaunchKernelEx(&cfg, attn64_kernel, a) : cudaLaunchKernelEx(&cfg, attn_kernel, a);
     if (e != cudaSuccess || a.S == 1) return e;
     cfg.numAttrs = 1;  // the merge waits for the attention grid (griddepcontrol.wait)
     cfg.gridDim = dim3((unsigned)h.H, (unsigned)h.B, 1);
     cfg.blockDim = dim3(128, 1, 1);
     cfg.dynamicSmemBytes = 0;
-    return cudaLaunchKernelEx(&cfg, attn_merge_kernel, a);
+    return a.S <= 16 ? cudaLaunchKernelEx(&cfg, attn_merge_kernel<16>, a)
+                     : cudaLaunchKernelEx(&cfg, attn_merge_kernel<AT_MAX_SPLITS>, a);
 }
 
 }  // namespace csa
