@@ -172,13 +172,9 @@ __global__ void __launch_bounds__(AT_T, 1) attn_kernel(AttnArgs a) {
                     st_shared_zero16(dst);
             }
             cp_async_commit();
-            // the next tile's rows: look them up and start pulling them into L2 while this
-            // tile's copies are in flight (the lookups are dependent loads, the pulls are
-            // fire-and-forget)
-            if (tid < AT_KT && tile + 1 < t1) {
-                p_next = key_row((tile + 1) * AT_KT + tid);
-                if (p_next) prefetch_l2_bulk(p_next, ROW_BYTES);
-            }
+            // the next tile's rows: look them up (dependent loads) while this tile's copies
+            // are in flight
+            if (tid < AT_KT && tile + 1 < t1) p_next = key_row((tile + 1) * AT_KT + tid);
             cp_async_wait_all();
             fence_proxy_async_smem();
             __syncthreads();

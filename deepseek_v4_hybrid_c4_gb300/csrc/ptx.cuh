@@ -78,10 +78,6 @@ CSA_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;"
 CSA_DEV void cp_async16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
-// fire-and-forget L2 prefetch of [p, p + bytes): 16-byte aligned, bytes a multiple of 16
-CSA_DEV void prefetch_l2_bulk(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
 CSA_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 CSA_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy (tensor cores, TMA).

@@ -252,6 +252,31 @@ def test_dense_attn_c128_and_paged_raw(csa):
     _status_clean(csa)
 
 
+@pytest.mark.parametrize("H", [16, 64])
+def test_attn_padded_page_stride(csa, H):
+    """Raw pages padded by half a row: the page stride is not a whole number of rows, so a
+    row's address is page * stride + slot * 1 KiB, never page * rows_per_page + slot."""
+    scale = float(np.float32(1 / math.sqrt(512)))
+    cpool, raw, q, sel = _attn_case(91 + H, H, 4096, 700, 3000, 11)
+    rpp, stride = 64, 64 * 1024 + 512
+    n_pages = (3000 + rpp - 1) // rpp
+    pt = synth.permutation(n_pages + 2, 91, 9)[:n_pages].copy()
+    pool = np.zeros(((n_pages + 2) * stride) // 2, np.uint16)
+    synth.scatter_pages(raw, rpp, pt, pool, stride)
+    kc = csa.paged(dev(cpool, torch), 1, 1024, n_pages=4096)
+    kr = csa.paged(dev(pool, torch), rpp, 1024, page_table=dev(pt, torch), page_stride_bytes=stride,
+                   n_pages=n_pages + 2)
+    ws_n = csa.csa_sparse_attn_workspace_size(H, 700, 128)
+    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device="cuda")
+    out = torch.zeros((H, 512), dtype=torch.int16, device="cuda")
+    lse = torch.zeros(H, dtype=torch.float32, device="cuda")
+    csa.csa_sparse_attn(dev(q, torch), H, scale, kc, dev(sel, torch), 700, kr, 3000, 128, out, lse, ws, ws_n)
+    _, f64, rlse = oracle.sparse_attn(q, scale, cpool, sel, raw, 128)
+    assert_close(bf16_bits_to_f64(out.cpu().numpy().view(np.uint16)), f64, f"attn padded pages H={H}")
+    assert np.abs(lse.cpu().numpy() - rlse).max() <= 1e-3 * max(1.0, np.abs(rlse).max())
+    _status_clean(csa)
+
+
 def test_attn_single_key_returns_its_row(csa):
     cpool, raw, q, _ = _attn_case(5, 16, 16, 0, 4)
     out, lse = _attn_gpu(csa, cpool, raw, q, np.array([7], np.int32), 0, 0.044)
