@@ -573,6 +573,41 @@ __global__ void __launch_bounds__(SW_T, 1) select_finish_kernel(SelArgs a) {
         }
         bins[d] = bd;
         const bool last_round = cnt == need - above;  // the whole bin is taken
+        if (d == 2 && !last_round) {
+            // every key bit is fixed: the bin holds need - above or more candidates of one key,
+            // and the tie goes to the lower index -- the first ones in storage order (regions in
+            // order, each in index order).  Take them in one pass instead of three index digits.
+            const uint32_t need_t = need - above;
+            uint32_t na = 0, nt = 0;
+            for (uint32_t j = j0; j < j1; ++j) {
+                uint32_t kk;
+                int32_t ii;
+                cand_at(j, kk, ii);
+                if (sw_digit(1, kk, ii) != bins[1]) continue;
+                const uint32_t dv = sw_digit(2, kk, ii);
+                na += dv > bd ? 1u : 0u;
+                nt += dv == bd ? 1u : 0u;
+            }
+            uint32_t tot_t, tot;
+            const uint32_t t_before = sw_scan(sm, nt, &tot_t);
+            const uint32_t my_t = t_before >= need_t ? 0u : min(nt, need_t - t_before);
+            uint32_t o = base + sw_scan(sm, na + my_t, &tot);
+            uint32_t taken_t = 0;
+            for (uint32_t j = j0; j < j1; ++j) {
+                uint32_t kk;
+                int32_t ii;
+                cand_at(j, kk, ii);
+                if (sw_digit(1, kk, ii) != bins[1]) continue;
+                const uint32_t dv = sw_digit(2, kk, ii);
+                const bool t = dv > bd || (dv == bd && taken_t++ < my_t);
+                if (t) {
+                    if (o < (uint32_t)k) out[o] = ii;
+                    ++o;
+                }
+            }
+            base += tot;
+            break;
+        }
         // this round's winners in index order: digit above bd (or the whole bin, last round)
         auto takes = [&](uint32_t kk, int32_t ii) {
             for (int e = 1; e < d; ++e)
@@ -731,9 +766,17 @@ cudaError_t launch_select_set(const SelectSetLaunch& h, cudaStream_t s, bool pdl
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
+    static int sms = 0;
+    if (!sms) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    }
     cfg.gridDim = dim3((unsigned)a.C, (unsigned)h.B, 1);
     cfg.blockDim = dim3(SW_T, 1, 1);
-    cfg.dynamicSmemBytes = SW_SCAN_SPREAD_SMEM;
+    // one scan CTA per SM when the grid fits on the SMs; a larger grid is packed instead, so
+    // that it stays one wave
+    cfg.dynamicSmemBytes = (int64_t)a.C * h.B <= sms ? SW_SCAN_SPREAD_SMEM : 0;
     cfg.stream = s;
     cudaError_t e = cudaSuccess;
     if (h.standalone) {  // histograms cleared, first digit counted; the scan follows programmatically
