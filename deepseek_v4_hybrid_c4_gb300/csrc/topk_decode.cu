@@ -211,7 +211,7 @@ __device__ __forceinline__ int sw_owner(const uint32_t* pre, int C, uint32_t x) 
 __global__ void __launch_bounds__(SW_T) select_scan_kernel(SelArgs a) {
     __shared__ SwCore sm;
     const int tid = threadIdx.x;
-    const int c = blockIdx.x, b = blockIdx.y, C = a.C, k = a.k;
+    const int b = blockIdx.x, c = blockIdx.y, C = a.C, k = a.k;
     const float* sc;
     int64_t G;
     sel_span(a, b, sc, G);
@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(SW_T, 1) select_finish_kernel(SelArgs a) {
     SwCore& sm = fs.core;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int NW = SW_T / 32;
-    const int c = blockIdx.x, b = blockIdx.y, C = a.C, k = a.k;
+    const int b = blockIdx.x, c = blockIdx.y, C = a.C, k = a.k;
     const float* sc_unused;
     int64_t G;
     sel_span(a, b, sc_unused, G);
@@ -687,7 +687,7 @@ __global__ void __launch_bounds__(256) select_zero_kernel(uint32_t* hist) {
 __global__ void __launch_bounds__(SW_T) select_hist_kernel(SelArgs a) {
     __shared__ uint32_t h[SW_BINS];
     const int tid = threadIdx.x, lane = tid & 31;
-    const int c = blockIdx.x, b = blockIdx.y;
+    const int b = blockIdx.x, c = blockIdx.y;
     for (int i = tid; i < SW_BINS; i += SW_T) h[i] = 0u;
     const float* sc;
     int64_t G;
@@ -772,7 +772,9 @@ cudaError_t launch_select_set(const SelectSetLaunch& h, cudaStream_t s, bool pdl
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     }
-    cfg.gridDim = dim3((unsigned)a.C, (unsigned)h.B, 1);
+    // grid (request, region): the blocks are dispatched region-major, so a batch's region 0s
+    // (which carry the finish's general path) are all in the first wave
+    cfg.gridDim = dim3((unsigned)h.B, (unsigned)a.C, 1);
     cfg.blockDim = dim3(SW_T, 1, 1);
     // one scan CTA per SM when the grid fits on the SMs; a larger grid is packed instead, so
     // that it stays one wave
