@@ -78,6 +78,10 @@ CSA_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;"
 CSA_DEV void cp_async16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
+// barrier among `count` threads (a multiple of 32) of the CTA, id 1..15
+CSA_DEV void named_bar_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 CSA_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 CSA_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy (tensor cores, TMA).

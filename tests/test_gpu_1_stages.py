@@ -151,7 +151,11 @@ def test_topk_batched_ragged(csa):
 
 # ------------------------------------------------------------------ stage 1: compressor
 @pytest.mark.parametrize("ratio,n_tokens,paged", [(4, 4096, False), (4, 8192 + 64, True), (128, 4096, True),
-                                                  (128, 128 * 37, False)])
+                                                  (128, 128 * 37, False),
+                                                  # chunks that fill every SM take the streaming kernel:
+                                                  # ragged last stage, stages across page boundaries
+                                                  (4, 4 * 1300, False), (4, 4 * 1300, True),
+                                                  (128, 128 * 160, True), (128, 128 * 170, False)])
 def test_compress_matches_oracle(csa, ratio, n_tokens, paged):
     seed = ratio + n_tokens
     x = synth.normal_bf16((n_tokens, 512), seed, 1)
