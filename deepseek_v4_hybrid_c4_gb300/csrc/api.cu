@@ -290,6 +290,10 @@ static csa_status decode_check(const csa_decode_params* p) {
     if (!p->c_page_table && p->raw_rows_per_page % p->ratio) return CSA_ERR_UNSUPPORTED;
     if (c_rpp < 1 || (int64_t)c_rpp * 1024 > p->c_page_stride) return CSA_ERR_INVALID_ARG;
     if (p->c_page_table && p->c_n_pages < 1) return CSA_ERR_INVALID_ARG;
+    if (p->ring_pool) {
+        if (!al16(p->ring_pool) || !p->ring_page || p->ring_n_pages < 1) return CSA_ERR_INVALID_ARG;
+        if (p->ring_size < p->ratio || p->ring_size % p->ratio) return CSA_ERR_INVALID_ARG;
+    }
     if (p->ratio == 4) {
         if (p->Hi < 1 || p->Hi > 16 || p->k < 1 || p->k > 2048) return CSA_ERR_UNSUPPORTED;
         if (p->k_dtype != CSA_BF16 && p->k_dtype != CSA_FP8_E4M3) return CSA_ERR_UNSUPPORTED;
@@ -379,6 +383,10 @@ csa_status csa_decode_timed(const csa_decode_params* p, void* workspace, size_t 
     c.count = 0;
     c.hist_zero = hist;
     c.status = st;
+    c.ring_pool = p->ring_pool;
+    c.ring_page = p->ring_page;
+    c.ring_size = p->ring_size;
+    c.ring_n_pages = p->ring_n_pages;
     cudaError_t e = launch_compress(c, s, false);
     if (e != cudaSuccess) return CSA_ERR_CUDA;
     mark(1);

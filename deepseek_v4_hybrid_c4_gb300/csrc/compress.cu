@@ -23,6 +23,10 @@ struct CompressArgs {
     int ratio;
     uint32_t* hist_zero;
     int32_t* status;
+    const uint8_t* ring_pool;  // batched mode, optional: request b's token t in row
+    const int32_t* ring_page;  // ring_page[b] * ring_size + t % ring_size of ring_pool
+    int32_t ring_size;
+    int64_t ring_n_pages;
 };
 
 __device__ __forceinline__ void group_range(const CompressArgs& a, int b, int64_t& first, int64_t& count) {
@@ -35,6 +39,18 @@ __device__ __forceinline__ void group_range(const CompressArgs& a, int b, int64_
         first = a.first;
         count = a.count;
     }
+}
+
+// Raw row of token t of request b: from the compression-state ring when there is one (which
+// must still hold the token: t >= n_tokens[b] - ring_size), else from the paged raw pool.
+__device__ __forceinline__ const uint8_t* token_row(const CompressArgs& a, int b, int64_t t) {
+    if (!a.ring_pool) return row_addr(a.raw, b, t, ROW_BYTES, a.status);
+    const int64_t rp = __ldg(a.ring_page + b);
+    if (rp < 0 || rp >= a.ring_n_pages || t < a.n_tokens[b] - a.ring_size) {
+        raise_status(a.status, CSA_ERR_DEVICE_BOUNDS);
+        return nullptr;
+    }
+    return a.ring_pool + (rp * a.ring_size + t % a.ring_size) * (int64_t)ROW_BYTES;
 }
 
 __device__ __forceinline__ void zero_hist(const CompressArgs& a, int b) {
@@ -108,7 +124,7 @@ __global__ void __launch_bounds__(256) compress_r4_kernel(CompressArgs a) {
         const int64_t g = first + gi;
         uint4 v[4][2];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) load_row16(row_addr(a.raw, b, 4 * g + i, ROW_BYTES, a.status), lane, v[i]);
+        for (int i = 0; i < 4; ++i) load_row16(token_row(a, b, 4 * g + i), lane, v[i]);
         float x[4][16], s[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -172,7 +188,7 @@ __global__ void __launch_bounds__(WARPS * 32) compress_r128_kernel(CompressArgs 
             const uint8_t* rows[U];
 #pragma unroll
             for (int u = 0; u < U; ++u)
-                rows[u] = row_addr(a.raw, b, 128 * g + warp + WARPS * (r0 + u), ROW_BYTES, a.status);
+                rows[u] = token_row(a, b, 128 * g + warp + WARPS * (r0 + u));
             uint4 v[U][2];
 #pragma unroll
             for (int u = 0; u < U; ++u) load_row16(rows[u], lane, v[u]);
@@ -439,6 +455,10 @@ cudaError_t launch_compress(const CompressLaunch& h, cudaStream_t s, bool pdl) {
     a.ratio = h.ratio;
     a.hist_zero = h.hist_zero;
     a.status = h.status;
+    a.ring_pool = h.n_tokens ? static_cast<const uint8_t*>(h.ring_pool) : nullptr;  // batched mode only
+    a.ring_page = h.ring_page;
+    a.ring_size = h.ring_size;
+    a.ring_n_pages = h.ring_n_pages;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

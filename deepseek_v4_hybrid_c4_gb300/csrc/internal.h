@@ -38,6 +38,10 @@ struct CompressLaunch {
     int64_t first, count;
     uint32_t* hist_zero;
     int32_t* status;
+    const void* ring_pool = nullptr;  // batched mode: pending tokens from per-request rings
+    const int32_t* ring_page = nullptr;
+    int32_t ring_size = 0;
+    int64_t ring_n_pages = 0;
 };
 cudaError_t launch_compress(const CompressLaunch& a, cudaStream_t s, bool pdl);
 

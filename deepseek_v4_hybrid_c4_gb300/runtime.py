@@ -58,13 +58,17 @@ class DecodeBatch:
       kidx_pool  [n_pages * c_rpp, 128] bf16 / fp8        index keys (C4 only)
     page_table [B, P] int32, n_tokens / n_groups_done [B] int64, q [B, H, 512] bf16,
     q_idx [B, Hi, 128] bf16, w_h [B, Hi] fp32, w_gate [512] fp32, b_pos [ratio] fp32.
+    Optional compression-state rings: ring_pool [n_rings * ring_size, 512] bf16 and ring_page [B]
+    int32 (request b's token t in row ring_page[b] * ring_size + t % ring_size); the pending
+    groups are then compressed from the ring.
     The per-step inputs q, q_idx and w_h are views of one device buffer (`step_in`), and the
     outputs out and lse of another (`step_out`), so each group moves in a single copy.
     """
 
     def __init__(self, *, ratio, H, Hi, k, swa, scale, kdtype, rows_per_page, raw_pool, c_pool, kidx_pool,
                  page_table, n_tokens, n_groups_done, q, q_idx, w_h, w_gate, b_pos, n_pages, max_tokens=None,
-                 c_page_table=None, c_rows_per_page=0, c_n_pages=0, device="cuda"):
+                 c_page_table=None, c_rows_per_page=0, c_n_pages=0, ring_pool=None, ring_page=None, ring_size=0,
+                 device="cuda"):
         dev = torch.device(device)
         i32, i64, f32 = torch.int32, torch.int64, torch.float32
         self.ratio, self.H, self.Hi, self.k, self.swa = ratio, H, Hi, k, swa
@@ -120,12 +124,19 @@ class DecodeBatch:
         p.out = self.out.data_ptr()
         p.lse = self.lse.data_ptr()
         p.sel = self.sel.data_ptr() if self.sel is not None else None
+        self.ring_pool = None if ring_pool is None else _bits(ring_pool, dev)
+        self.ring_page = None if ring_page is None else _dev(ring_page, i32, dev)
+        if self.ring_pool is not None:
+            p.ring_pool = self.ring_pool.data_ptr()
+            p.ring_page = self.ring_page.data_ptr()
+            p.ring_size = int(ring_size)
+            p.ring_n_pages = int(self.ring_pool.shape[0]) // int(ring_size)
         self.params = p
         self.ws_bytes = csa_decode_workspace_size(p)  # 0 also when the parameters are rejected: run() reports why
         self.ws = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
         self._shape = dict(ratio=ratio, H=H, Hi=Hi, k=k, swa=swa, scale=scale, kdtype=kdtype,
                            rows_per_page=rows_per_page, n_pages=n_pages, max_tokens=max_tokens,
-                           c_rows_per_page=c_rows_per_page, c_n_pages=c_n_pages, device=device)
+                           c_rows_per_page=c_rows_per_page, c_n_pages=c_n_pages, ring_size=ring_size, device=device)
 
     def clone(self) -> "DecodeBatch":
         """The same step over copies of every device buffer (same values, other addresses):
@@ -135,7 +146,8 @@ class DecodeBatch:
                            page_table=c(self.page_table), n_tokens=c(self.n_tokens),
                            n_groups_done=c(self.n_groups_done), q=c(self.q), q_idx=c(self.q_idx) if self.Hi else None,
                            w_h=c(self.w_h) if self.Hi else None, w_gate=c(self.w_gate), b_pos=c(self.b_pos),
-                           c_page_table=c(self.c_page_table), **self._shape)
+                           c_page_table=c(self.c_page_table), ring_pool=c(self.ring_pool),
+                           ring_page=c(self.ring_page), **self._shape)
 
     def run(self, stream=None, events=None) -> None:
         if events is None:

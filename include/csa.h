@@ -202,6 +202,17 @@ typedef struct {
                                     set (the same set as csa_topk, -1 padding at the end), in a
                                     fixed order that is not the score order: the same inputs give
                                     the same order and the same output bits */
+    /* Optional compression-state ring ([V4-deploy] "ShadowRadix": the state ring nested in the
+     * SWA page index; [Day-0] "创新 1 ShadowRadix"): the raw tokens of groups still being filled live in a small
+     * per-request ring, token t of request b in row ring_page[b] * ring_size + t % ring_size
+     * of ring_pool.  When ring_pool is set, stage 1 reads the pending groups' tokens from the
+     * ring instead of kv_raw; the SWA window of stage 4 still reads kv_raw.  The ring must
+     * still hold every pending token: n_groups_done[b] * ratio >= n_tokens[b] - ring_size,
+     * else the device status gets CSA_ERR_DEVICE_BOUNDS.  Zero-initialise to leave it off. */
+    const void* ring_pool;       /* bf16 rows of 1024 B (16-byte aligned), or NULL */
+    const int32_t* ring_page;    /* device [B]: request b's ring (0 <= ring_page[b] < ring_n_pages) */
+    int32_t ring_size;           /* tokens per ring, a multiple of ratio */
+    int64_t ring_n_pages;        /* rings in ring_pool */
 } csa_decode_params;
 
 /* workspace: device, 16-byte aligned, caller-owned, at least csa_decode_workspace_size(p)

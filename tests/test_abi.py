@@ -93,3 +93,28 @@ def test_every_workload_fits_the_noalloc_scratch(libpath):
         p.kidx_page_stride = 16 * 256
         need = csa.csa_decode_workspace_size(p)
         assert 0 < need <= 32 << 20, (i, need)
+
+
+def test_ring_parameters_are_validated(libpath):
+    """The compression-state ring is checked on the host: a ring size that is not a multiple
+    of the ratio, a misaligned pool or no ring pages reject the call (workspace size 0)."""
+    import synth
+    import deepseek_v4_hybrid_c4_gb300 as csa
+    c = synth.config(0)
+    p = csa.csa_decode_params()
+    p.B, p.ratio, p.H, p.Hi, p.k, p.swa = len(c.requests), c.ratio, c.H, c.Hi, c.k, c.swa
+    p.scale, p.k_dtype, p.max_tokens = 0.04, csa.CSA_BF16, max(r.n_tokens for r in c.requests)
+    for f in ("n_tokens", "n_groups_done", "kv_raw", "kv_c", "k_idx", "w_gate", "b_pos", "q", "q_idx", "w_h",
+              "out", "lse", "sel", "page_table"):
+        setattr(p, f, 4096)  # never dereferenced by the size query
+    p.raw_rows_per_page, p.raw_page_stride, p.n_pages = c.rows_per_page, c.rows_per_page * 1024, 1 << 20
+    p.c_page_stride, p.kidx_page_stride = (c.rows_per_page // 4) * 1024, (c.rows_per_page // 4) * 256
+    base = csa.csa_decode_workspace_size(p)
+    assert base > 0
+    p.ring_pool, p.ring_page, p.ring_size, p.ring_n_pages = 8192, 4096, 8, 4
+    assert csa.csa_decode_workspace_size(p) == base
+    for field, bad in (("ring_size", 6), ("ring_size", 2), ("ring_pool", 8200), ("ring_n_pages", 0), ("ring_page", None)):
+        good = getattr(p, field)
+        setattr(p, field, bad)
+        assert csa.csa_decode_workspace_size(p) == 0, (field, bad)
+        setattr(p, field, good)

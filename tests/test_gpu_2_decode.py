@@ -28,6 +28,10 @@ def run_and_check(entry, case):
     batch.run()
     torch.cuda.synchronize()
     assert m.csa_read_device_status() == 0
+    return _check_against_oracle(case, batch)
+
+
+def _check_against_oracle(case, batch):
     refs = oracle.decode_case(case)
     out = batch.out.float().cpu().numpy().astype(np.float64)
     lse = batch.lse.cpu().numpy()
@@ -84,6 +88,70 @@ def test_decode_select_all_scores_equal(entry, G):
         r.kidx[:] = r.kidx[0]
     batch = run_and_check(entry, case)
     assert np.array_equal(np.sort(batch.sel[0].cpu().numpy()), np.arange(512))
+
+
+def _rings(case, ring_size, spare=3):
+    """Per-request compression-state rings holding each request's last ring_size tokens (token t
+    in row ring_page[b] * ring_size + t % ring_size); ring pages are a seeded permutation."""
+    B = len(case.requests)
+    page = synth.permutation(B + spare, case.seed, 31)[:B].copy()
+    pool = np.zeros(((B + spare) * ring_size, 512), np.uint16)
+    for b, r in enumerate(case.requests):
+        for t in range(max(0, r.n_tokens - ring_size), r.n_tokens):
+            pool[page[b] * ring_size + t % ring_size] = r.raw[t]
+    return dict(ring_pool=pool, ring_page=page, ring_size=ring_size)
+
+
+@pytest.mark.parametrize("ratio,ring_size,n_pending", [(4, 8, 1), (4, 8, 2), (4, 16, 3), (128, 128, 1),
+                                                       (128, 256, 2)])
+def test_decode_ring_matches_oracle(entry, ratio, ring_size, n_pending):
+    """Pending groups compressed from the compression-state rings: the whole step matches."""
+    case = synth.make_decode_case(f"ring{ratio}", 40 + ring_size, [4096 + 4 * ratio, 8192, 1024 + ratio * n_pending],
+                                  H=64, Hi=8, ratio=ratio, n_pending=n_pending)
+    case.name = f"ring r{ratio} size {ring_size}"
+    import deepseek_v4_hybrid_c4_gb300 as m
+    batch = entry.case_to_batch(case, **_rings(case, ring_size))
+    batch.run()
+    torch.cuda.synchronize()
+    assert m.csa_read_device_status() == 0
+    _check_against_oracle(case, batch)
+
+
+def test_decode_ring_is_the_source(entry):
+    """With rings set, the raw pool's pending rows are never read by the compressor: zero them
+    and the compressed rows still match the oracle on the true tokens."""
+    import deepseek_v4_hybrid_c4_gb300 as m
+    case = synth.make_decode_case("ringsrc", 45, [4096, 2048 + 8], H=16, Hi=4, n_pending=2)
+    batch = entry.case_to_batch(case, **_rings(case, 8))
+    rpp = case.rows_per_page
+    for r in case.requests:
+        G = r.n_tokens // case.ratio
+        for t in range(r.n_groups_done * case.ratio, G * case.ratio):
+            batch.raw_pool[int(r.pages[t // rpp]) * rpp + t % rpp] = 0
+    batch.run()
+    torch.cuda.synchronize()
+    assert m.csa_read_device_status() == 0
+    c_rpp = case.c_rows_per_page()
+    for b, r in enumerate(case.requests):
+        G = r.n_tokens // case.ratio
+        pages = case.c_pages(r)
+        rows = [int(pages[g // c_rpp]) * c_rpp + g % c_rpp for g in range(r.n_groups_done, G)]
+        got = batch.c_pool[torch.tensor(rows, device="cuda")].cpu().numpy().view(np.uint16)
+        ref = oracle.compress(r.raw, case.ratio, case.w_gate, case.b_pos, r.n_groups_done, G - r.n_groups_done,
+                              want_f64=True)[1]
+        assert_close(bf16_bits_to_f64(got), ref, f"ring-sourced compressed rows, request {b}")
+
+
+def test_decode_ring_too_small_sets_status(entry):
+    """A ring that no longer holds every pending token: the device status reports a bounds
+    error (no fault, no trap)."""
+    import deepseek_v4_hybrid_c4_gb300 as m
+    case = synth.make_decode_case("ringsmall", 46, [4096], H=16, Hi=4, n_pending=2)
+    batch = entry.case_to_batch(case, **_rings(case, 4))
+    batch.run()
+    torch.cuda.synchronize()
+    assert m.csa_read_device_status() == 1 << (m.CSA_ERR_DEVICE_BOUNDS - 1)
+    assert m.csa_read_device_status() == 0  # read-and-clear
 
 
 def test_decode_graph_capture_replay(entry):
