@@ -246,6 +246,30 @@ def other_workloads(torch, csa, entry, synth, stream, flush_l2, peak):
             del outs, descs
         del g, b
         torch.cuda.empty_cache()
+    # ---- speculative verify at 1M context, bs = 1: 4 query positions (draft tokens) per step,
+    #      each with its own candidates, top k and SWA window
+    case = synth.config(2)
+    nq = 4
+    b = entry.case_to_batch(case, n_q=nq, q=synth.normal_bf16((nq, case.H, 512), case.seed, 400),
+                            q_idx=synth.normal_bf16((nq, case.Hi, 128), case.seed, 401),
+                            w_h=synth.uniform_f32((nq, case.Hi), case.seed, 402))
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            b.run(stream)
+    torch.cuda.synchronize()
+    assert csa.csa_read_device_status(stream) == 0
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        b.run(stream)
+    t, t90 = timed(g.replay, 30)
+    G = case.requests[0].n_tokens // case.ratio
+    res["spec_verify_1M_4_positions"] = {
+        "us_per_step": round(t, 2), "us_p90": round(t90, 2), "us_per_query_position": round(t / nq, 2),
+        "query_positions": nq, "index_key_bytes_per_step": nq * G * 256,
+        "note": "every position streams the index keys itself (the score is bound by its fixed-order fma "
+                "rate, not by the stream)"}
+    del g, b
+    torch.cuda.empty_cache()
     assert csa.csa_read_device_status(stream) == 0
     return res
 

@@ -45,7 +45,7 @@ class csa_decode_params(ctypes.Structure):
         ("q", ctypes.c_void_p), ("q_idx", ctypes.c_void_p), ("w_h", ctypes.c_void_p),
         ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("sel", ctypes.c_void_p),
         ("ring_pool", ctypes.c_void_p), ("ring_page", ctypes.c_void_p), ("ring_size", ctypes.c_int32),
-        ("ring_n_pages", ctypes.c_int64),
+        ("ring_n_pages", ctypes.c_int64), ("n_q", ctypes.c_int32),
     ]
 
 

@@ -272,8 +272,11 @@ struct DecodeLayout {
     int64_t score_stride;
 };
 
+static int decode_nq(const csa_decode_params* p) { return p->n_q > 1 ? p->n_q : 1; }
+
 static csa_status decode_check(const csa_decode_params* p) {
     if (!p) return CSA_ERR_INVALID_ARG;
+    if (p->n_q < 0 || p->n_q > 16 || (int64_t)p->B * decode_nq(p) > 65535) return CSA_ERR_UNSUPPORTED;
     if (p->ratio != 4 && p->ratio != 128) return CSA_ERR_UNSUPPORTED;
     if (p->B < 1 || p->B > 65535 || p->H < 1 || p->H > 128 || p->swa < 0 || p->swa > 128)
         return CSA_ERR_UNSUPPORTED;
@@ -308,22 +311,23 @@ static csa_status decode_check(const csa_decode_params* p) {
 static DecodeLayout decode_layout(const csa_decode_params* p) {
     DecodeLayout L;
     const int64_t max_G = p->max_tokens / p->ratio;
+    const int Bq = p->B * decode_nq(p);  // batch entries: (request, query position)
     L.score_stride = (max_G + 3) & ~int64_t(3);
     size_t off = 0;
     L.scores = off;
-    if (p->ratio == 4) off += align256((size_t)p->B * L.score_stride * sizeof(float));
+    if (p->ratio == 4) off += align256((size_t)Bq * L.score_stride * sizeof(float));
     L.hist = off;
-    if (p->ratio == 4) off += align256((size_t)p->B * kHistBlock * sizeof(uint32_t));
+    if (p->ratio == 4) off += align256((size_t)Bq * kHistBlock * sizeof(uint32_t));
     L.lists = off;
     if (p->ratio == 4)
-        off += align256(select_set_supported(max_G, p->k) ? select_set_lists_bytes(p->B, max_G)
-                                                          : topk_lists_bytes(p->B, max_G, p->k));
+        off += align256(select_set_supported(max_G, p->k) ? select_set_lists_bytes(Bq, max_G)
+                                                          : topk_lists_bytes(Bq, max_G, p->k));
     L.sel = off;
-    if (p->ratio == 4 && !p->sel) off += align256((size_t)p->B * p->k * sizeof(int32_t));
+    if (p->ratio == 4 && !p->sel) off += align256((size_t)Bq * p->k * sizeof(int32_t));
     L.attn = off;
     const int64_t W = p->max_tokens < p->swa ? p->max_tokens : p->swa;
     const int64_t max_keys = (p->ratio == 4 ? p->k : max_G) + W;
-    off += align256(attn_workspace_bytes(p->B, p->H, max_keys));
+    off += align256(attn_workspace_bytes(Bq, p->H, max_keys));
     L.total = off > 256 ? off : 256;  // never 0: a size of 0 means the parameters were rejected
     return L;
 }
@@ -348,6 +352,8 @@ csa_status csa_decode_timed(const csa_decode_params* p, void* workspace, size_t 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     const int64_t max_G = p->max_tokens / p->ratio;
+    const int nq = decode_nq(p);
+    const int Bq = p->B * nq;  // stages 2-4 run per (request, query position)
     auto mark = [&](int i) {
         if (ev && ev[i]) cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), s);
     };
@@ -387,6 +393,7 @@ csa_status csa_decode_timed(const csa_decode_params* p, void* workspace, size_t 
     c.ring_page = p->ring_page;
     c.ring_size = p->ring_size;
     c.ring_n_pages = p->ring_n_pages;
+    c.nq = nq;
     cudaError_t e = launch_compress(c, s, false);
     if (e != cudaSuccess) return CSA_ERR_CUDA;
     mark(1);
@@ -404,7 +411,9 @@ csa_status csa_decode_timed(const csa_decode_params* p, void* workspace, size_t 
         l.fp8 = p->k_dtype == CSA_FP8_E4M3;
         l.scores = reinterpret_cast<float*>(ws + L.scores);
         l.score_stride = L.score_stride;
-        l.B = p->B;
+        l.B = Bq;
+        l.nq = nq;
+        l.kidx.qpr = nq;
         l.n_tokens = p->n_tokens;
         l.ratio = p->ratio;
         l.G = 0;
@@ -420,7 +429,8 @@ csa_status csa_decode_timed(const csa_decode_params* p, void* workspace, size_t 
             SelectSetLaunch t;
             t.scores = l.scores;
             t.score_stride = L.score_stride;
-            t.B = p->B;
+            t.B = Bq;
+            t.nq = nq;
             t.max_G = max_G;
             t.n_tokens = p->n_tokens;
             t.ratio = p->ratio;
@@ -433,7 +443,8 @@ csa_status csa_decode_timed(const csa_decode_params* p, void* workspace, size_t 
         } else {
             TopkLaunch t;
             t.scores = l.scores;
-            t.B = p->B;
+            t.B = Bq;
+            t.nq = nq;
             t.G = 0;
             t.max_G = max_G;
             t.offsets = nullptr;
@@ -463,10 +474,13 @@ csa_status csa_decode_timed(const csa_decode_params* p, void* workspace, size_t 
     a.scale = p->scale;
     a.kv_c = cp;
     a.kv_raw = raw;
+    a.kv_c.qpr = nq;
+    a.kv_raw.qpr = nq;
+    a.nq = nq;
     a.sel = sel;
     a.sel_stride = p->k;
     a.n_sel = p->ratio == 4 ? p->k : 0;
-    a.B = p->B;
+    a.B = Bq;
     a.n_tokens = p->n_tokens;
     a.ratio = p->ratio;
     a.N = 0;

@@ -60,6 +60,7 @@ struct AttnArgs {
     int n_sel;
     const int64_t* n_tokens;
     int ratio;
+    int nq;                    // decode: query positions per request
     int64_t N;
     int swa;
     int tps, S;
@@ -92,7 +93,7 @@ __global__ void __launch_bounds__(AT_T, 1) attn_kernel(AttnArgs a) {
     const uint8_t** kptr = reinterpret_cast<const uint8_t**>(sm + SM_KPTR);
     uint64_t* kok = reinterpret_cast<uint64_t*>(sm + SM_KOK);
 
-    const int64_t N = a.n_tokens ? a.n_tokens[b] : a.N;
+    const int64_t N = a.n_tokens ? query_tokens(a.n_tokens, b, a.nq) : a.N;
     const int64_t W = N < a.swa ? N : a.swa;
     const int64_t n_c = a.sel ? a.n_sel : (a.n_tokens ? N / a.ratio : a.n_sel);
     const int64_t n_keys = n_c + W;
@@ -374,7 +375,7 @@ __global__ void __launch_bounds__(AT_T, 1) attn64_kernel(AttnArgs a) {
     float* sm_alpha = reinterpret_cast<float*>(sm + A6_SM_ALPHA);
     float2* sm_ml = reinterpret_cast<float2*>(sm + A6_SM_ML);
 
-    const int64_t N = a.n_tokens ? a.n_tokens[b] : a.N;
+    const int64_t N = a.n_tokens ? query_tokens(a.n_tokens, b, a.nq) : a.N;
     const int64_t W = N < a.swa ? N : a.swa;
     const int64_t n_c = a.sel ? a.n_sel : (a.n_tokens ? N / a.ratio : a.n_sel);
     const int64_t n_keys = n_c + W;
@@ -718,6 +719,7 @@ static DPaged to_dev(const HPaged& h) {
     d.page_stride = h.page_stride;
     d.n_pages = h.n_pages;
     d.rpp = h.rpp;
+    d.qpr = h.qpr > 1 ? h.qpr : 1;
     return d;
 }
 
@@ -733,6 +735,7 @@ cudaError_t launch_attn(const AttnLaunch& h, cudaStream_t s, bool pdl) {
     a.n_sel = h.n_sel;
     a.n_tokens = h.n_tokens;
     a.ratio = h.ratio;
+    a.nq = h.nq > 1 ? h.nq : 1;
     a.N = h.N;
     a.swa = h.swa;
     plan_splits(h.B, h.H, h.max_keys, &a.tps, &a.S);

@@ -15,7 +15,8 @@ constexpr int DI = 128;       // index-key dim
 constexpr int ROW_BYTES = D * 2;
 
 // A paged row buffer as the kernels see it (see csa_paged in csa.h).  For a
-// batch, request b uses page_table + b * pt_stride.
+// batch, request b uses page_table + (b / qpr) * pt_stride: with speculative verify a
+// batch entry is one query position and qpr positions share their request's table.
 struct DPaged {
     const uint8_t* base;
     const int32_t* pt;   // nullptr -> contiguous (physical page = logical page)
@@ -23,7 +24,17 @@ struct DPaged {
     int64_t page_stride; // bytes
     int64_t n_pages;
     int32_t rpp;         // rows per page
+    int32_t qpr;         // batch entries per page table (>= 1)
 };
+
+// Tokens visible to batch entry q of a decode step whose requests carry nq query positions
+// each (speculative verify: the draft tokens are the last nq of request q / nq, and query j
+// sits at position n_tokens - nq + j, so it sees n_tokens - nq + j + 1 tokens).
+CSA_DEV int64_t query_tokens(const int64_t* n_tokens, int q, int nq) {
+    if (nq <= 1) return __ldg(n_tokens + q);
+    const int b = q / nq;
+    return __ldg(n_tokens + b) - nq + (q - b * nq) + 1;
+}
 
 // Record an error code in the sticky device status word (bit code-1).
 CSA_DEV void raise_status(int32_t* status, int code) {
@@ -36,7 +47,7 @@ CSA_DEV const uint8_t* row_addr(const DPaged& p, int b, int64_t r, int row_bytes
     const int64_t lp = r / p.rpp;
     const int64_t slot = r - lp * p.rpp;
     int64_t pp = lp;
-    if (p.pt) pp = __ldg(p.pt + (int64_t)b * p.pt_stride + lp);
+    if (p.pt) pp = __ldg(p.pt + (int64_t)(p.qpr > 1 ? b / p.qpr : b) * p.pt_stride + lp);
     if (pp < 0 || pp >= p.n_pages) {
         raise_status(status, CSA_ERR_DEVICE_BOUNDS);
         return nullptr;

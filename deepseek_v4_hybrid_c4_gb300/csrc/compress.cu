@@ -21,6 +21,7 @@ struct CompressArgs {
     const int64_t* n_done;
     int64_t first, count;
     int ratio;
+    int nq;                    // query positions per request: histogram blocks to clear
     uint32_t* hist_zero;
     int32_t* status;
     const uint8_t* ring_pool;  // batched mode, optional: request b's token t in row
@@ -54,9 +55,9 @@ __device__ __forceinline__ const uint8_t* token_row(const CompressArgs& a, int b
 }
 
 __device__ __forceinline__ void zero_hist(const CompressArgs& a, int b) {
-    if (a.hist_zero && blockIdx.x == 0) {  // 16-byte stores: the block is 16-byte aligned
-        uint4* z = reinterpret_cast<uint4*>(a.hist_zero + (int64_t)b * kHistBlock);
-        for (int i = threadIdx.x; i < kHistBlock / 4; i += blockDim.x) z[i] = make_uint4(0, 0, 0, 0);
+    if (a.hist_zero && blockIdx.x == 0) {  // 16-byte stores: the blocks are 16-byte aligned
+        uint4* z = reinterpret_cast<uint4*>(a.hist_zero + (int64_t)b * a.nq * kHistBlock);
+        for (int i = threadIdx.x; i < a.nq * kHistBlock / 4; i += blockDim.x) z[i] = make_uint4(0, 0, 0, 0);
     }
 }
 
@@ -439,6 +440,7 @@ static DPaged to_dev(const HPaged& h) {
     d.page_stride = h.page_stride;
     d.n_pages = h.n_pages;
     d.rpp = h.rpp;
+    d.qpr = h.qpr > 1 ? h.qpr : 1;
     return d;
 }
 
@@ -454,6 +456,7 @@ cudaError_t launch_compress(const CompressLaunch& h, cudaStream_t s, bool pdl) {
     a.count = h.count;
     a.ratio = h.ratio;
     a.hist_zero = h.hist_zero;
+    a.nq = h.nq > 1 ? h.nq : 1;
     a.status = h.status;
     a.ring_pool = h.n_tokens ? static_cast<const uint8_t*>(h.ring_pool) : nullptr;  // batched mode only
     a.ring_page = h.ring_page;

@@ -22,12 +22,14 @@ struct HPaged {            // host copy of a paged buffer description (see csa_p
     int64_t page_stride;   // bytes
     int64_t n_pages;
     int32_t rpp;
+    int32_t qpr = 1;       // batch entries per page table (speculative verify: query positions)
 };
 
 // Stage 1.  Single mode (n_tokens == nullptr): groups [first, first + count) of one
 // sequence.  Batched mode: request b = blockIdx.y compresses [n_done[b], n_tokens[b]/ratio).
 // hist_zero (nullable): [B][kHistBlock] words cleared by block (0, b) for stages 2 and 3.
 struct CompressLaunch {
+    int nq = 1;                // decode: query positions per request (speculative verify)
     HPaged raw, out;
     const float* w_gate;
     const float* b_pos;
@@ -48,6 +50,7 @@ cudaError_t launch_compress(const CompressLaunch& a, cudaStream_t s, bool pdl);
 // Stage 2.  Single mode (n_tokens == nullptr): one sequence of G candidates.
 // Batched: request b has n_tokens[b] / ratio candidates; scores at b * score_stride.
 struct ScoreLaunch {
+    int nq = 1;                // decode: query positions per request (speculative verify)
     const void* q_idx;     // bf16 [B, Hi, 128]
     const float* w_h;      // fp32 [B, Hi]
     int Hi;
@@ -70,6 +73,7 @@ cudaError_t launch_score(const ScoreLaunch& a, cudaStream_t s, bool pdl);
 // before the launch; with hist_fused its first kHistBins words hold digit 0's histogram
 // from stage 2, otherwise the select counts digit 0 itself.
 struct TopkLaunch {
+    int nq = 1;                // decode: query positions per request (speculative verify)
     const float* scores;
     int B;
     int64_t G;                 // single mode
@@ -94,6 +98,7 @@ cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t s, bool pdl);
 // [kHistBlock], zeroed before stage 2).  lists: select_set_lists_bytes(B, max_G) bytes of
 // workspace.  Only where select_set_supported(max_G, k).
 struct SelectSetLaunch {
+    int nq = 1;                // decode: query positions per request (speculative verify)
     const float* scores;
     int64_t score_stride;      // a multiple of 4
     int B;
@@ -120,6 +125,7 @@ cudaError_t launch_select_set(const SelectSetLaunch& a, cudaStream_t s, bool pdl
 // them, -1 = padding; sel == nullptr: rows 0..n_c-1 with n_c = n_tokens/ratio in
 // decode mode or n_sel in single mode) followed by the last min(swa, N) raw rows.
 struct AttnLaunch {
+    int nq = 1;                // decode: query positions per request (speculative verify)
     const void* q;             // bf16 [B, H, 512]
     int H;
     float scale;

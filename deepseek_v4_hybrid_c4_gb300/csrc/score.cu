@@ -59,6 +59,7 @@ struct ScoreArgs {
     int B;
     const int64_t* n_tokens;
     int ratio;
+    int nq;                  // query positions per request (batch entry b: request b / nq)
     int64_t G;
     uint32_t* hist;          // [B][kHistBlock] (the first kHistBins words) or nullptr
     int32_t* status;
@@ -72,7 +73,7 @@ struct CtaStepCursor {
     int b = -1;
     int64_t base = 0, csteps = 0, steps = 0, G = 0;
     __device__ void load(const ScoreArgs& a) {
-        G = a.n_tokens ? __ldg(a.n_tokens + b) / a.ratio : a.G;
+        G = a.n_tokens ? query_tokens(a.n_tokens, b, a.nq) / a.ratio : a.G;
         steps = (G + SC_SUPER - 1) / SC_SUPER;
         csteps = (steps + SC_WARPS - 1) / SC_WARPS;
     }
@@ -202,7 +203,7 @@ __global__ void __launch_bounds__(SC_THREADS, HI >= 16 ? 1 : 2)
         __shared__ int64_t s_tot[SC_WARPS];
         int64_t t = 0;  // the batch's CTA-steps (ragged requests: from the device lengths)
         for (int b = threadIdx.x; b < a.B; b += SC_THREADS) {
-            const int64_t G = a.n_tokens ? __ldg(a.n_tokens + b) / a.ratio : a.G;
+            const int64_t G = a.n_tokens ? query_tokens(a.n_tokens, b, a.nq) / a.ratio : a.G;
             t += ((G + SC_SUPER - 1) / SC_SUPER + SC_WARPS - 1) / SC_WARPS;
         }
 #pragma unroll
@@ -232,7 +233,7 @@ __global__ void __launch_bounds__(SC_THREADS, HI >= 16 ? 1 : 2)
                 const int64_t lp = gr / a.rpp;
                 slot = (int)(gr - lp * a.rpp);
                 int64_t pp = lp;
-                if (a.pt) pp = __ldg(a.pt + (int64_t)lc.b * a.pt_stride + lp);
+                if (a.pt) pp = __ldg(a.pt + (int64_t)(a.nq > 1 ? lc.b / a.nq : lc.b) * a.pt_stride + lp);
                 if (pp >= 0 && pp < a.n_pages) {
                     kind = 1;
                     page = (int)pp;
@@ -512,6 +513,7 @@ cudaError_t launch_score(const ScoreLaunch& h, cudaStream_t s, bool pdl) {
     a.B = h.B;
     a.n_tokens = h.n_tokens;
     a.ratio = h.ratio;
+    a.nq = h.nq > 1 ? h.nq : 1;
     a.G = h.G;
     a.hist = h.hist;
     a.status = h.status;

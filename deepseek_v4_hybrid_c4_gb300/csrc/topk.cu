@@ -40,6 +40,7 @@ constexpr int TK_SLICE = 16384;      // scores per CTA the cluster size is chose
 struct TopkArgs {
     const float* scores;
     int B;
+    int nq;  // decode mode: query positions per request
     int64_t G;
     const int64_t* offsets;
     const int64_t* n_tokens;
@@ -75,7 +76,7 @@ __device__ __forceinline__ void request_span(const TopkArgs& a, int b, const flo
         G = o1 - o0;
     } else if (a.n_tokens) {
         sc = a.scores + (int64_t)b * a.score_stride;
-        G = a.n_tokens[b] / a.ratio;
+        G = query_tokens(a.n_tokens, b, a.nq) / a.ratio;
     } else {
         sc = a.scores;
         G = a.G;
@@ -590,6 +591,7 @@ cudaError_t launch_topk(const TopkLaunch& h, cudaStream_t s, bool pdl) {
     a.G = h.G;
     a.offsets = h.offsets;
     a.n_tokens = h.n_tokens;
+    a.nq = h.nq > 1 ? h.nq : 1;
     a.ratio = h.ratio;
     a.score_stride = h.score_stride;
     a.k = h.k;

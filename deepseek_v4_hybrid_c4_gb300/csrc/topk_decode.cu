@@ -45,6 +45,7 @@ constexpr int SW_BINS = kHistBins;        // 2048: widest digit
 constexpr size_t SW_SCAN_SPREAD_SMEM = 116 * 1024;
 
 struct SelArgs {
+    int nq;  // decode mode: query positions per request (batch entry b: request b / nq)
     // request b's scores: decode mode (n_tokens): scores + b * score_stride, n_tokens[b] / ratio
     // of them; offsets mode: [offsets[b], offsets[b+1]); single: [0, G)
     const float* scores;
@@ -89,7 +90,7 @@ __device__ __forceinline__ uint64_t sel_comp(uint64_t v) {
 __device__ __forceinline__ void sel_span(const SelArgs& a, int b, const float*& sc, int64_t& G) {
     if (a.n_tokens) {
         sc = a.scores + (int64_t)b * a.score_stride;
-        G = __ldg(a.n_tokens + b) / a.ratio;
+        G = query_tokens(a.n_tokens, b, a.nq) / a.ratio;
     } else if (a.offsets) {
         const int64_t o0 = __ldg(a.offsets + b), o1 = __ldg(a.offsets + b + 1);
         sc = a.scores + o0;
@@ -732,6 +733,7 @@ cudaError_t launch_select_set(const SelectSetLaunch& h, cudaStream_t s, bool pdl
     a.scores = h.scores;
     a.score_stride = h.score_stride;
     a.n_tokens = h.n_tokens;
+    a.nq = h.nq > 1 ? h.nq : 1;
     a.ratio = h.ratio;
     a.offsets = h.offsets;
     a.G = h.G;

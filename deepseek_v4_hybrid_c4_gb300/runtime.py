@@ -58,6 +58,8 @@ class DecodeBatch:
       kidx_pool  [n_pages * c_rpp, 128] bf16 / fp8        index keys (C4 only)
     page_table [B, P] int32, n_tokens / n_groups_done [B] int64, q [B, H, 512] bf16,
     q_idx [B, Hi, 128] bf16, w_h [B, Hi] fp32, w_gate [512] fp32, b_pos [ratio] fp32.
+    Speculative verify: n_q query positions per request; q, q_idx, w_h and the outputs then have
+    B * n_q leading entries in (request, query) order.
     Optional compression-state rings: ring_pool [n_rings * ring_size, 512] bf16 and ring_page [B]
     int32 (request b's token t in row ring_page[b] * ring_size + t % ring_size); the pending
     groups are then compressed from the ring.
@@ -68,7 +70,7 @@ class DecodeBatch:
     def __init__(self, *, ratio, H, Hi, k, swa, scale, kdtype, rows_per_page, raw_pool, c_pool, kidx_pool,
                  page_table, n_tokens, n_groups_done, q, q_idx, w_h, w_gate, b_pos, n_pages, max_tokens=None,
                  c_page_table=None, c_rows_per_page=0, c_n_pages=0, ring_pool=None, ring_page=None, ring_size=0,
-                 device="cuda"):
+                 n_q=1, device="cuda"):
         dev = torch.device(device)
         i32, i64, f32 = torch.int32, torch.int64, torch.float32
         self.ratio, self.H, self.Hi, self.k, self.swa = ratio, H, Hi, k, swa
@@ -80,6 +82,11 @@ class DecodeBatch:
         self.n_tokens = _dev(n_tokens, i64, dev)
         self.n_groups_done = _dev(n_groups_done, i64, dev)
         self.B = int(self.n_tokens.shape[0])
+        self.n_q = max(1, int(n_q))
+        Bq = self.B * self.n_q  # (request, query position) entries of q, q_idx, w_h and the outputs
+        for name, x in (("q", q), ("q_idx", q_idx), ("w_h", w_h)):
+            if x is not None and int(x.shape[0]) != Bq:
+                raise ValueError(f"{name} has {int(x.shape[0])} entries; B * n_q = {Bq}")
         self.step_in, (self.q, self.q_idx, self.w_h) = _pack(dev, [
             _bits(q, dev),
             _bits(q_idx, dev) if Hi else torch.zeros(8, dtype=torch.int16, device=dev),
@@ -87,9 +94,9 @@ class DecodeBatch:
         self.w_gate = _dev(w_gate, f32, dev)
         self.b_pos = _dev(b_pos, f32, dev)
         self.step_out, (self.out, self.lse) = _pack(dev, [
-            torch.zeros((self.B, H, 512), dtype=torch.bfloat16, device=dev),
-            torch.zeros((self.B, H), dtype=f32, device=dev)])
-        self.sel = torch.zeros((self.B, max(k, 1)), dtype=i32, device=dev) if ratio == 4 else None
+            torch.zeros((Bq, H, 512), dtype=torch.bfloat16, device=dev),
+            torch.zeros((Bq, H), dtype=f32, device=dev)])
+        self.sel = torch.zeros((Bq, max(k, 1)), dtype=i32, device=dev) if ratio == 4 else None
         if max_tokens is None:
             max_tokens = int(torch.as_tensor(n_tokens).max())
         c_rpp = c_rows_per_page if c_page_table is not None else rows_per_page // ratio
@@ -124,6 +131,7 @@ class DecodeBatch:
         p.out = self.out.data_ptr()
         p.lse = self.lse.data_ptr()
         p.sel = self.sel.data_ptr() if self.sel is not None else None
+        p.n_q = self.n_q
         self.ring_pool = None if ring_pool is None else _bits(ring_pool, dev)
         self.ring_page = None if ring_page is None else _dev(ring_page, i32, dev)
         if self.ring_pool is not None:
@@ -136,7 +144,8 @@ class DecodeBatch:
         self.ws = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
         self._shape = dict(ratio=ratio, H=H, Hi=Hi, k=k, swa=swa, scale=scale, kdtype=kdtype,
                            rows_per_page=rows_per_page, n_pages=n_pages, max_tokens=max_tokens,
-                           c_rows_per_page=c_rows_per_page, c_n_pages=c_n_pages, ring_size=ring_size, device=device)
+                           c_rows_per_page=c_rows_per_page, c_n_pages=c_n_pages, ring_size=ring_size, n_q=n_q,
+                           device=device)
 
     def clone(self) -> "DecodeBatch":
         """The same step over copies of every device buffer (same values, other addresses):

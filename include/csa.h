@@ -213,6 +213,16 @@ typedef struct {
     const int32_t* ring_page;    /* device [B]: request b's ring (0 <= ring_page[b] < ring_n_pages) */
     int32_t ring_size;           /* tokens per ring, a multiple of ratio */
     int64_t ring_n_pages;        /* rings in ring_pool */
+    /* Speculative verify ([V4-deploy] "V4 到底改了啥": a one-layer MTP head drafts tokens;
+     * "MTP 投機解碼 + 圖內元數據"; 4 draft tokens at bs = 1 in the low-latency setting):
+     * n_q query positions per request, 0 or 1 meaning one.  The last n_q
+     * of request b's n_tokens[b] tokens are the draft positions; query j sits at token
+     * n_tokens[b] - n_q + j and sees the first n_tokens[b] - n_q + j + 1 tokens: the groups
+     * completed within them (floor) as candidates, its own top k and its own SWA window.  Stage 1
+     * compresses once per request, up to n_tokens[b] / ratio.  q, q_idx, w_h, out, lse and sel
+     * then hold B * n_q entries in (request, query) order: q [B, n_q, H, 512] and so on.
+     * 1 <= n_q <= 16 and B * n_q <= 65535. */
+    int32_t n_q;
 } csa_decode_params;
 
 /* workspace: device, 16-byte aligned, caller-owned, at least csa_decode_workspace_size(p)

@@ -213,6 +213,24 @@ def decode_request(req, *, ratio: int, w_gate, b_pos, k: int, swa: int, scale: f
     return res
 
 
+def decode_queries(req, queries, *, ratio: int, w_gate, b_pos, k: int, swa: int, scale: float,
+                   kdtype: str = "bf16"):
+    """Speculative verify of one request: `queries` = [(q, q_idx, w_h)] for its last n_q token
+    positions.  Query j sits at token N - n_q + j, so it is the decode step of the same request
+    cut to its first N - n_q + j + 1 tokens (the groups completed within them, its own top k and
+    SWA window).  Returns one decode_request result per query."""
+    from types import SimpleNamespace
+    N, nq = int(req.n_tokens), len(queries)
+    res = []
+    for j, (q, q_idx, w_h) in enumerate(queries):
+        Nj = N - nq + j + 1
+        sub = SimpleNamespace(raw=req.raw[:Nj], cpool=req.cpool, q=q, q_idx=q_idx, w_h=w_h, kidx=req.kidx,
+                              n_groups_done=min(int(req.n_groups_done), Nj // ratio))
+        res.append(decode_request(sub, ratio=ratio, w_gate=w_gate, b_pos=b_pos, k=k, swa=swa, scale=scale,
+                                  kdtype=kdtype))
+    return res
+
+
 def decode_case(case):
     """The decode step for every request of a synth.DecodeCase (requests are independent)."""
     return [decode_request(r, ratio=case.ratio, w_gate=case.w_gate, b_pos=case.b_pos, k=case.k, swa=case.swa,

@@ -304,7 +304,9 @@ int orc_decode_request(const uint16_t* raw, int64_t n_tokens, uint16_t* cpool, i
                        int dense, const float* w_gate, const float* b_pos, const uint16_t* q_idx, const float* w_h,
                        int Hi, const void* k_idx, int k_fp8, int k, const uint16_t* q, int H, float scale, int swa,
                        uint16_t* out_bf16, double* out_f64, double* lse, int32_t* sel, float* scores) {
-    if (ratio <= 0 || n_tokens % ratio != 0) return 1;
+    /* the candidates are the groups completed within the n_tokens tokens (floor); the tokens of
+       a trailing partial group take part only through the SWA window */
+    if (ratio <= 0 || n_tokens < 0) return 1;
     const int64_t G = n_tokens / ratio;
     if (n_groups_done < 0 || n_groups_done > G) return 1;
     int rc = orc_compress(raw, n_tokens, ratio, w_gate, b_pos, n_groups_done, G - n_groups_done,

@@ -154,6 +154,57 @@ def test_decode_ring_too_small_sets_status(entry):
     assert m.csa_read_device_status() == 0  # read-and-clear
 
 
+def _spec_queries(case, n_q, seed_stream=300):
+    """n_q query positions per request: q, q_idx, w_h drawn like the case's own (own streams)."""
+    qs = []
+    for b, r in enumerate(case.requests):
+        q = synth.normal_bf16((n_q, case.H, 512), case.seed, seed_stream + 3 * b)
+        qi = synth.normal_bf16((n_q, max(case.Hi, 1), 128), case.seed, seed_stream + 3 * b + 1)
+        wh = synth.uniform_f32((n_q, max(case.Hi, 1)), case.seed, seed_stream + 3 * b + 2)
+        qs.append([(q[j], qi[j], wh[j]) for j in range(n_q)])
+    return qs
+
+
+@pytest.mark.parametrize("ratio,n_q,n_pending", [(4, 2, 1), (4, 4, 2), (4, 3, 1), (128, 4, 1), (128, 2, 2)])
+def test_decode_speculative_verify(entry, ratio, n_q, n_pending):
+    """n_q query positions per request, each with its own candidates (groups completed before
+    it), top k and SWA window, against the oracle run once per position."""
+    import deepseek_v4_hybrid_c4_gb300 as m
+    case = synth.make_decode_case(f"spec{ratio}", 50 + n_q, [8192, 4096 + 4 * ratio, 20000 // ratio * ratio],
+                                  H=64 if ratio == 128 else 16, Hi=8, ratio=ratio, n_pending=n_pending)
+    qs = _spec_queries(case, n_q)
+    flat = [x for per in qs for x in per]  # (request, query) order
+    batch = entry.case_to_batch(case, n_q=n_q, q=np.stack([x[0] for x in flat]),
+                                q_idx=np.stack([x[1] for x in flat]), w_h=np.stack([x[2] for x in flat]))
+    batch.run()
+    torch.cuda.synchronize()
+    assert m.csa_read_device_status() == 0
+    out = batch.out.float().cpu().numpy().astype(np.float64)
+    lse = batch.lse.cpu().numpy()
+    for b, r in enumerate(case.requests):
+        refs = oracle.decode_queries(r, qs[b], ratio=ratio, w_gate=case.w_gate, b_pos=case.b_pos, k=case.k,
+                                     swa=case.swa, scale=case.scale, kdtype=case.kdtype)
+        for j, ref in enumerate(refs):
+            e = b * n_q + j
+            if ratio == 4:
+                got = batch.sel[e].cpu().numpy()
+                n = int((ref["sel"] >= 0).sum())
+                assert (got[n:] == -1).all() and np.array_equal(np.sort(got[:n]), np.sort(ref["sel"][:n])), (b, j)
+            assert_close(out[e], ref["out_f64"], f"spec verify request {b} query {j}")
+            assert np.abs(lse[e] - ref["lse"]).max() <= 1e-3 * max(1.0, np.abs(ref["lse"]).max())
+
+
+def test_decode_one_query_position_is_the_plain_step(entry):
+    """n_q = 1 is the ordinary decode step, bit for bit."""
+    case = synth.config(0)
+    a = entry.case_to_batch(case)
+    b = entry.case_to_batch(case, n_q=1)
+    a.run()
+    b.run()
+    torch.cuda.synchronize()
+    assert torch.equal(a.sel, b.sel) and torch.equal(a.out, b.out) and torch.equal(a.lse, b.lse)
+
+
 def test_decode_graph_capture_replay(entry):
     """The step enqueues only device work: it can be captured once and replayed."""
     case = synth.config(0)

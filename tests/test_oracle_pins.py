@@ -384,6 +384,34 @@ def test_decode_dense_c128():
         assert np.array_equal(o["out"], ref[0])
 
 
+def test_decode_queries_positions_and_candidates():
+    """Speculative verify in the oracle: query j of n_q sees the first N - n_q + j + 1 tokens.
+    The last query is the plain decode step; a query whose prefix holds no completed group
+    attends only its SWA window (textbook attention over those raw rows); and a query's
+    candidates are exactly the groups completed within its prefix (floor), scored as before."""
+    case = synth.make_decode_case("t", 7, [1024 + 8], H=16, Hi=4, k=64, n_pending=2)
+    r = case.requests[0]
+    kw = dict(ratio=4, w_gate=case.w_gate, b_pos=case.b_pos, k=64, swa=128, scale=case.scale)
+    qs = [(synth.normal_bf16((16, 512), 7, 90 + j), r.q_idx, r.w_h) for j in range(3)] + [(r.q, r.q_idx, r.w_h)]
+    res = oracle.decode_queries(r, qs, **kw)
+    plain = oracle.decode_request(r, **kw)
+    assert np.array_equal(res[3]["out"], plain["out"]) and np.array_equal(res[3]["sel"], plain["sel"])
+    N = r.n_tokens
+    for j in range(3):
+        Nj = N - 4 + j + 1
+        s = oracle.index_score(r.q_idx, r.w_h, r.kidx[: Nj // 4], False)
+        assert np.array_equal(res[j]["scores"], s)              # floor(Nj / 4) candidates
+        assert res[j]["sel"].tolist() == _brute_topk(s, 64)
+    # a prefix of 3 tokens: no completed group, only the window
+    tiny = synth.make_decode_case("t", 8, [8], H=4, Hi=4, k=4, n_pending=2)
+    t = tiny.requests[0]
+    q0 = synth.normal_bf16((4, 512), 8, 95)
+    one = oracle.decode_queries(t, [(q0, t.q_idx, t.w_h)] + [(t.q, t.q_idx, t.w_h)] * 5,
+                                ratio=4, w_gate=tiny.w_gate, b_pos=tiny.b_pos, k=4, swa=128, scale=tiny.scale)
+    _, f64, lse = oracle.attention(q0, tiny.scale, t.raw[:3])
+    assert np.allclose(one[0]["out_f64"], f64, atol=0, rtol=0) and (one[0]["sel"] == -1).all()
+
+
 def test_fp8_tie_codebook_creates_straddling_ties():
     """Workload 3's recipe: codebook index keys make exact score ties around rank k."""
     case = synth.make_decode_case("t", 3, [8192], H=4, Hi=8, kdtype="fp8", tie_codebook=True, k=512)
