@@ -270,6 +270,37 @@ def other_workloads(torch, csa, entry, synth, stream, flush_l2, peak):
                 "rate, not by the stream)"}
     del g, b
     torch.cuda.empty_cache()
+    # ---- HiSparse at 1M context: the C4 pool (256 MiB) as a pinned host mirror with a GPU working
+    #      set of a quarter of its pages.  Cold: every selected row comes from the mirror; warm:
+    #      after the coordinator brought the step's pages in.
+    case = synth.config(2)
+    c_rpp = case.rows_per_page // case.ratio
+    slots = case.n_pages // 4
+    b = entry.case_to_batch(case, c_page_table=case.page_table(), c_rows_per_page=c_rpp, c_n_pages=case.n_pages,
+                            hs_slots=slots)
+    b.hs_step = 1
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            b.run(stream)
+    torch.cuda.synchronize()
+    assert csa.csa_read_device_status(stream) == 0
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        b.run(stream)
+    t_cold, _ = timed(g.replay, 30)
+    t0 = time.perf_counter()
+    n_in, n_ev = b.hs_update(stream)
+    torch.cuda.synchronize()
+    t_upd = (time.perf_counter() - t0) * 1e6
+    t_warm, _ = timed(g.replay, 30)  # the graph reads the residency table, so it now hits
+    assert csa.csa_read_device_status(stream) == 0
+    res["hisparse_1M_quarter_working_set"] = {
+        "us_per_step_cold": round(t_cold, 2), "us_per_step_warm": round(t_warm, 2),
+        "us_update_host_wall": round(t_upd, 1), "pages_brought_in": int(n_in), "pages_evicted": int(n_ev),
+        "working_set_pages": int(slots), "mirror_pages": int(case.n_pages), "page_bytes": c_rpp * 1024,
+        "note": "cold: the 512 selected rows are read from pinned host memory over NVLink-C2C"}
+    del g, b
+    torch.cuda.empty_cache()
     assert csa.csa_read_device_status(stream) == 0
     return res
 

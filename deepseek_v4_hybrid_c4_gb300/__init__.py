@@ -46,6 +46,8 @@ class csa_decode_params(ctypes.Structure):
         ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("sel", ctypes.c_void_p),
         ("ring_pool", ctypes.c_void_p), ("ring_page", ctypes.c_void_p), ("ring_size", ctypes.c_int32),
         ("ring_n_pages", ctypes.c_int64), ("n_q", ctypes.c_int32),
+        ("hs_ws_pool", ctypes.c_void_p), ("hs_ws_table", ctypes.c_void_p), ("hs_n_slots", ctypes.c_int64),
+        ("hs_touch", ctypes.c_void_p), ("hs_step", ctypes.c_uint32),
     ]
 
 
@@ -76,8 +78,17 @@ def lib() -> ctypes.CDLL:
         L.csa_status_string.argtypes = [i32]
         L.csa_status_string.restype = ctypes.c_char_p
         L.csa_version.restype = i32
+        L.csa_hisparse_create.argtypes = [i32, i64, i64, ctypes.POINTER(vp)]
+        L.csa_hisparse_destroy.argtypes = [vp]
+        L.csa_hisparse_destroy.restype = None
+        L.csa_hisparse_plan.argtypes = [vp, vp, ctypes.c_uint32, vp, i64, ctypes.POINTER(i64), ctypes.POINTER(i64)]
+        L.csa_hisparse_table.argtypes = [vp]
+        L.csa_hisparse_table.restype = ctypes.POINTER(ctypes.c_int32)
+        L.csa_hisparse_update.argtypes = [vp, ctypes.POINTER(csa_decode_params), vp, ctypes.POINTER(i64),
+                                          ctypes.POINTER(i64)]
         for name in ("csa_compress", "csa_index_score", "csa_topk", "csa_topk_batched", "csa_sparse_attn",
-                     "csa_decode", "csa_decode_timed", "csa_decode_noalloc", "csa_read_device_status"):
+                     "csa_decode", "csa_decode_timed", "csa_decode_noalloc", "csa_read_device_status",
+                     "csa_hisparse_create", "csa_hisparse_plan", "csa_hisparse_update"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -178,6 +189,44 @@ def csa_sparse_attn(q, H: int, scale: float, kv_c: csa_paged, sel, n_sel: int, k
 
 def csa_decode_workspace_size(p: csa_decode_params) -> int:
     return int(lib().csa_decode_workspace_size(ctypes.byref(p)))
+
+
+def csa_hisparse_create(B: int, table_stride: int, n_slots: int) -> int:
+    """A HiSparse coordinator (an opaque handle); release it with csa_hisparse_destroy."""
+    h = ctypes.c_void_p()
+    _check(lib().csa_hisparse_create(B, table_stride, n_slots, ctypes.byref(h)), "csa_hisparse_create")
+    return h.value
+
+
+def csa_hisparse_destroy(h: int) -> None:
+    lib().csa_hisparse_destroy(h)
+
+
+def csa_hisparse_plan(h: int, touch, step: int, max_plan: int):
+    """The host-side LRU decision for `touch` (numpy uint32 [B, table_stride]) -> (plan [n, 3]
+    int32 rows (request, logical page, slot), number evicted)."""
+    import numpy as np
+    t = np.ascontiguousarray(touch, dtype=np.uint32)
+    plan = np.zeros((max(int(max_plan), 1), 3), dtype=np.int32)
+    n_in, n_ev = ctypes.c_int64(0), ctypes.c_int64(0)
+    _check(lib().csa_hisparse_plan(h, t.ctypes.data, step, plan.ctypes.data, int(max_plan), ctypes.byref(n_in),
+                                   ctypes.byref(n_ev)), "csa_hisparse_plan")
+    return plan[: n_in.value].copy(), n_ev.value
+
+
+def csa_hisparse_table(h: int, B: int, table_stride: int):
+    """A copy of the coordinator's residency table (numpy int32 [B, table_stride])."""
+    import numpy as np
+    ptr = lib().csa_hisparse_table(h)
+    return np.ctypeslib.as_array(ptr, shape=(B * table_stride,)).reshape(B, table_stride).copy()
+
+
+def csa_hisparse_update(h: int, p: csa_decode_params, stream=None):
+    """After a decode step: bring the pages it missed into the working set -> (n_in, n_evicted)."""
+    n_in, n_ev = ctypes.c_int64(0), ctypes.c_int64(0)
+    _check(lib().csa_hisparse_update(h, ctypes.byref(p), _stream(stream), ctypes.byref(n_in), ctypes.byref(n_ev)),
+           "csa_hisparse_update")
+    return n_in.value, n_ev.value
 
 
 def csa_decode(p: csa_decode_params, workspace, ws_bytes: int, stream=None) -> None:

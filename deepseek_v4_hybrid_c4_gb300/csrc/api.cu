@@ -29,6 +29,8 @@ static int32_t* status_ptr() {
     return g_status_ptr[dev];
 }
 
+int32_t* device_status_ptr() { return status_ptr(); }
+
 static bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 static bool al4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
@@ -293,6 +295,12 @@ static csa_status decode_check(const csa_decode_params* p) {
     if (!p->c_page_table && p->raw_rows_per_page % p->ratio) return CSA_ERR_UNSUPPORTED;
     if (c_rpp < 1 || (int64_t)c_rpp * 1024 > p->c_page_stride) return CSA_ERR_INVALID_ARG;
     if (p->c_page_table && p->c_n_pages < 1) return CSA_ERR_INVALID_ARG;
+    if (p->hs_ws_pool) {  // HiSparse: C4 only, explicit compressed paging
+        if (p->ratio != 4) return CSA_ERR_UNSUPPORTED;
+        if (!p->c_page_table || !p->hs_ws_table || p->hs_n_slots < 1 || p->hs_n_slots > 0x7FFFFFFF ||
+            !al16(p->hs_ws_pool))
+            return CSA_ERR_INVALID_ARG;
+    }
     if (p->ring_pool) {
         if (!al16(p->ring_pool) || !p->ring_page || p->ring_n_pages < 1) return CSA_ERR_INVALID_ARG;
         if (p->ring_size < p->ratio || p->ring_size % p->ratio) return CSA_ERR_INVALID_ARG;
@@ -394,6 +402,11 @@ csa_status csa_decode_timed(const csa_decode_params* p, void* workspace, size_t 
     c.ring_size = p->ring_size;
     c.ring_n_pages = p->ring_n_pages;
     c.nq = nq;
+    if (p->hs_ws_pool) {  // new rows go to the mirror and, when resident, to the working set
+        c.hs.table = p->hs_ws_table;
+        c.hs.base = p->hs_ws_pool;
+        c.hs.n_slots = p->hs_n_slots;
+    }
     cudaError_t e = launch_compress(c, s, false);
     if (e != cudaSuccess) return CSA_ERR_CUDA;
     mark(1);
@@ -477,6 +490,13 @@ csa_status csa_decode_timed(const csa_decode_params* p, void* workspace, size_t 
     a.kv_c.qpr = nq;
     a.kv_raw.qpr = nq;
     a.nq = nq;
+    if (p->hs_ws_pool) {  // resident pages from the working set, the others from the mirror
+        a.hs.table = p->hs_ws_table;
+        a.hs.base = p->hs_ws_pool;
+        a.hs.n_slots = p->hs_n_slots;
+        a.hs.touch = p->hs_touch;
+        a.hs.step = p->hs_step;
+    }
     a.sel = sel;
     a.sel_stride = p->k;
     a.n_sel = p->ratio == 4 ? p->k : 0;

@@ -69,6 +69,7 @@ struct AttnArgs {
     uint16_t* out;
     float* lse;
     int32_t* status;
+    DWorkSet kws;              // HiSparse working set of the compressed pool (table == nullptr: none)
 };
 
 // 2^x with the hardware's approximate exponential (ex2.approx.ftz: relative error below
@@ -146,7 +147,7 @@ __global__ void __launch_bounds__(AT_T, 1) attn_kernel(AttnArgs a) {
         auto key_row = [&](int64_t j) -> const uint8_t* {
             if (j < n_c) {
                 const int64_t g = a.sel ? (int64_t)__ldg(a.sel + (int64_t)b * a.sel_stride + j) : j;
-                return g >= 0 ? row_addr(a.kc, b, g, ROW_BYTES, a.status) : nullptr;
+                return g >= 0 ? ws_row(a.kws, a.kc, b, g, true, a.status) : nullptr;
             }
             if (j < n_keys) return row_addr(a.kr, b, N - W + (j - n_c), ROW_BYTES, a.status);
             return nullptr;
@@ -431,7 +432,7 @@ __global__ void __launch_bounds__(AT_T, 1) attn64_kernel(AttnArgs a) {
     auto key_row = [&](int64_t j) -> const uint8_t* {
         if (j < n_c) {
             const int64_t g = a.sel ? (int64_t)__ldg(a.sel + (int64_t)b * a.sel_stride + j) : j;
-            return g >= 0 ? row_addr(a.kc, b, g, ROW_BYTES, a.status) : nullptr;
+            return g >= 0 ? ws_row(a.kws, a.kc, b, g, true, a.status) : nullptr;
         }
         if (j < n_keys) return row_addr(a.kr, b, N - W + (j - n_c), ROW_BYTES, a.status);
         return nullptr;
@@ -745,6 +746,11 @@ cudaError_t launch_attn(const AttnLaunch& h, cudaStream_t s, bool pdl) {
     a.out = static_cast<uint16_t*>(h.out);
     a.lse = h.lse;
     a.status = h.status;
+    a.kws.table = h.hs.table;
+    a.kws.base = static_cast<uint8_t*>(h.hs.base);
+    a.kws.n_slots = h.hs.n_slots;
+    a.kws.touch = h.hs.touch;
+    a.kws.step = h.hs.step;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)AT_SMEM);

@@ -27,6 +27,18 @@ struct DPaged {
     int32_t qpr;         // batch entries per page table (>= 1)
 };
 
+// HiSparse working set over a paged pool whose rows live in a host mirror: table[(b / qpr) *
+// pt_stride + logical page] is the GPU slot holding that page (slots of the pool's page stride at
+// base), or -1 -- the row is then read from the pool itself, host memory mapped into the device's
+// address space.  touch, when set, gets `step` for every page read (the LRU stamps).
+struct DWorkSet {
+    const int32_t* table;  // nullptr: no working set
+    uint8_t* base;
+    int64_t n_slots;
+    uint32_t* touch;
+    uint32_t step;
+};
+
 // Tokens visible to batch entry q of a decode step whose requests carry nq query positions
 // each (speculative verify: the draft tokens are the last nq of request q / nq, and query j
 // sits at position n_tokens - nq + j, so it sees n_tokens - nq + j + 1 tokens).
@@ -53,6 +65,27 @@ CSA_DEV const uint8_t* row_addr(const DPaged& p, int b, int64_t r, int row_bytes
         return nullptr;
     }
     return p.base + pp * p.page_stride + slot * (int64_t)row_bytes;
+}
+
+// Row r of request b in its working-set slot, or nullptr when the page is not resident.
+CSA_DEV uint8_t* ws_slot_row(const DWorkSet& w, const DPaged& p, int b, int64_t r) {
+    if (!w.table) return nullptr;
+    const int64_t lp = r / p.rpp;
+    const int32_t sl = w.table[(int64_t)(p.qpr > 1 ? b / p.qpr : b) * p.pt_stride + lp];
+    return sl >= 0 && sl < w.n_slots ? w.base + sl * p.page_stride + (r - lp * p.rpp) * (int64_t)ROW_BYTES : nullptr;
+}
+
+// Row r of request b of a pool with a working set: its GPU slot when resident, else the pool's
+// own row; stamps the page when `stamp` and the set keeps stamps.
+CSA_DEV const uint8_t* ws_row(const DWorkSet& w, const DPaged& p, int b, int64_t r, bool stamp, int32_t* status) {
+    if (w.table) {
+        const int64_t lp = r / p.rpp;
+        const int64_t e = (int64_t)(p.qpr > 1 ? b / p.qpr : b) * p.pt_stride + lp;
+        if (stamp && w.touch) w.touch[e] = w.step;
+        const int32_t sl = w.table[e];
+        if (sl >= 0 && sl < w.n_slots) return w.base + sl * p.page_stride + (r - lp * p.rpp) * (int64_t)ROW_BYTES;
+    }
+    return row_addr(p, b, r, ROW_BYTES, status);
 }
 
 // Order-preserving 32-bit image of an fp32 score: larger score <-> larger key,

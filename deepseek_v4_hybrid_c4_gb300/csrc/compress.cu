@@ -24,6 +24,7 @@ struct CompressArgs {
     int nq;                    // query positions per request: histogram blocks to clear
     uint32_t* hist_zero;
     int32_t* status;
+    DWorkSet ows;              // HiSparse working set of the output pool (table == nullptr: none)
     const uint8_t* ring_pool;  // batched mode, optional: request b's token t in row
     const int32_t* ring_page;  // ring_page[b] * ring_size + t % ring_size of ring_pool
     int32_t ring_size;
@@ -87,10 +88,11 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-__device__ __forceinline__ void store_row16(const DPaged& out, int b, int64_t g, int lane, const float (&c)[16],
-                                            int32_t* status) {
+__device__ __forceinline__ void store_row16(const DPaged& out, const DWorkSet& ws, int b, int64_t g, int lane,
+                                            const float (&c)[16], int32_t* status) {
     uint8_t* dst = const_cast<uint8_t*>(row_addr(out, b, g, ROW_BYTES, status));
     if (!dst) return;
+    uint8_t* dst2 = ws_slot_row(ws, out, b, g);  // the page's working-set copy, if resident
     uint4 o0, o1;
     o0.x = pack_bf16x2(c[0], c[1]);
     o0.y = pack_bf16x2(c[2], c[3]);
@@ -102,6 +104,10 @@ __device__ __forceinline__ void store_row16(const DPaged& out, int b, int64_t g,
     o1.w = pack_bf16x2(c[14], c[15]);
     *reinterpret_cast<uint4*>(dst + lane * 32) = o0;
     *reinterpret_cast<uint4*>(dst + lane * 32 + 16) = o1;
+    if (dst2) {
+        *reinterpret_cast<uint4*>(dst2 + lane * 32) = o0;
+        *reinterpret_cast<uint4*>(dst2 + lane * 32 + 16) = o1;
+    }
 }
 
 // C4: one warp per group of 4 tokens; gate dots reduced with warp shuffles.
@@ -152,7 +158,7 @@ __global__ void __launch_bounds__(256) compress_r4_kernel(CompressArgs a) {
             for (int i = 0; i < 4; ++i) acc = fmaf(e[i] * inv, x[i][d], acc);
             c[d] = acc;
         }
-        store_row16(a.out, b, g, lane, c, a.status);
+        store_row16(a.out, a.ows, b, g, lane, c, a.status);
     }
 }
 
@@ -234,7 +240,10 @@ __global__ void __launch_bounds__(WARPS * 32) compress_r128_kernel(CompressArgs 
             }
             const float inv = 1.f / L;
             uint8_t* dst = const_cast<uint8_t*>(row_addr(a.out, b, g, ROW_BYTES, a.status));
-            if (dst) *reinterpret_cast<uint32_t*>(dst + d0 * 2) = pack_bf16x2(o0 * inv, o1 * inv);
+            const uint32_t w = pack_bf16x2(o0 * inv, o1 * inv);
+            if (dst) *reinterpret_cast<uint32_t*>(dst + d0 * 2) = w;
+            uint8_t* dst2 = ws_slot_row(a.ows, a.out, b, g);  // the page's working-set copy, if resident
+            if (dst && dst2) *reinterpret_cast<uint32_t*>(dst2 + d0 * 2) = w;
         }
         __syncthreads();
     }
@@ -459,6 +468,11 @@ cudaError_t launch_compress(const CompressLaunch& h, cudaStream_t s, bool pdl) {
     a.nq = h.nq > 1 ? h.nq : 1;
     a.status = h.status;
     a.ring_pool = h.n_tokens ? static_cast<const uint8_t*>(h.ring_pool) : nullptr;  // batched mode only
+    a.ows.table = h.n_tokens ? h.hs.table : nullptr;
+    a.ows.base = static_cast<uint8_t*>(h.hs.base);
+    a.ows.n_slots = h.hs.n_slots;
+    a.ows.touch = nullptr;
+    a.ows.step = 0;
     a.ring_page = h.ring_page;
     a.ring_size = h.ring_size;
     a.ring_n_pages = h.ring_n_pages;

@@ -15,6 +15,14 @@ constexpr int kHistBlock = 6 * kHistBins;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+struct HWorkSet {          // HiSparse working set of a pool (see DWorkSet); table == nullptr: none
+    const int32_t* table = nullptr;
+    void* base = nullptr;
+    int64_t n_slots = 0;
+    uint32_t* touch = nullptr;
+    uint32_t step = 0;
+};
+
 struct HPaged {            // host copy of a paged buffer description (see csa_paged)
     const void* base;
     const int32_t* pt;     // device page table(s) or nullptr
@@ -29,6 +37,7 @@ struct HPaged {            // host copy of a paged buffer description (see csa_p
 // sequence.  Batched mode: request b = blockIdx.y compresses [n_done[b], n_tokens[b]/ratio).
 // hist_zero (nullable): [B][kHistBlock] words cleared by block (0, b) for stages 2 and 3.
 struct CompressLaunch {
+    HWorkSet hs;               // HiSparse: the compressed pool's GPU working set (optional)
     int nq = 1;                // decode: query positions per request (speculative verify)
     HPaged raw, out;
     const float* w_gate;
@@ -125,6 +134,7 @@ cudaError_t launch_select_set(const SelectSetLaunch& a, cudaStream_t s, bool pdl
 // them, -1 = padding; sel == nullptr: rows 0..n_c-1 with n_c = n_tokens/ratio in
 // decode mode or n_sel in single mode) followed by the last min(swa, N) raw rows.
 struct AttnLaunch {
+    HWorkSet hs;               // HiSparse: the compressed pool's GPU working set (optional)
     int nq = 1;                // decode: query positions per request (speculative verify)
     const void* q;             // bf16 [B, H, 512]
     int H;
@@ -146,6 +156,8 @@ struct AttnLaunch {
     int32_t* status;
 };
 size_t attn_workspace_bytes(int B, int H, int64_t max_keys);
+// this device's sticky status word (the kernels' status argument)
+int32_t* device_status_ptr();
 cudaError_t launch_attn(const AttnLaunch& a, cudaStream_t s, bool pdl);
 
 }  // namespace csa

@@ -32,6 +32,13 @@ def _bits(x, dev):
     return torch.from_numpy(a).to(dev)
 
 
+def _np_bits(x):
+    """numpy bit patterns as a C-contiguous int16 array (bf16 rows)."""
+    import numpy as np
+    a = np.ascontiguousarray(x)
+    return a.view(np.int16) if a.dtype == np.uint16 else a
+
+
 def _pack(dev, parts):
     """One device buffer holding every tensor of `parts`, each at a 256-byte boundary, and a
     view of the buffer for each (the data copied in), so that the group moves in one copy."""
@@ -60,6 +67,9 @@ class DecodeBatch:
     q_idx [B, Hi, 128] bf16, w_h [B, Hi] fp32, w_gate [512] fp32, b_pos [ratio] fp32.
     Speculative verify: n_q query positions per request; q, q_idx, w_h and the outputs then have
     B * n_q leading entries in (request, query) order.
+    HiSparse (hs_slots > 0, C4 with an explicit c_page_table): the compressed pool becomes a
+    mirror in pinned host memory, with a GPU working set of hs_slots pages; `hs_update()` after a
+    step brings the pages it missed in, and `hs_step` stamps the next step.
     Optional compression-state rings: ring_pool [n_rings * ring_size, 512] bf16 and ring_page [B]
     int32 (request b's token t in row ring_page[b] * ring_size + t % ring_size); the pending
     groups are then compressed from the ring.
@@ -70,12 +80,18 @@ class DecodeBatch:
     def __init__(self, *, ratio, H, Hi, k, swa, scale, kdtype, rows_per_page, raw_pool, c_pool, kidx_pool,
                  page_table, n_tokens, n_groups_done, q, q_idx, w_h, w_gate, b_pos, n_pages, max_tokens=None,
                  c_page_table=None, c_rows_per_page=0, c_n_pages=0, ring_pool=None, ring_page=None, ring_size=0,
-                 n_q=1, device="cuda"):
+                 n_q=1, hs_slots=0, device="cuda"):
         dev = torch.device(device)
         i32, i64, f32 = torch.int32, torch.int64, torch.float32
         self.ratio, self.H, self.Hi, self.k, self.swa = ratio, H, Hi, k, swa
         self.raw_pool = _bits(raw_pool, dev)
-        self.c_pool = _bits(c_pool, dev)
+        self.hs_slots = int(hs_slots)
+        if self.hs_slots:  # the full compressed pool as a pinned host mirror the kernels read directly
+            src = c_pool.cpu() if isinstance(c_pool, torch.Tensor) else torch.from_numpy(_np_bits(c_pool))
+            self.c_pool = torch.empty(src.shape, dtype=torch.int16, pin_memory=True)
+            self.c_pool.copy_(src.view(torch.int16))
+        else:
+            self.c_pool = _bits(c_pool, dev)
         self.kidx_pool = None if kidx_pool is None else _bits(kidx_pool, dev)
         self.page_table = _dev(page_table, i32, dev)
         self.c_page_table = None if c_page_table is None else _dev(c_page_table, i32, dev)
@@ -139,13 +155,26 @@ class DecodeBatch:
             p.ring_page = self.ring_page.data_ptr()
             p.ring_size = int(ring_size)
             p.ring_n_pages = int(self.ring_pool.shape[0]) // int(ring_size)
+        self.hs = None
+        if self.hs_slots:
+            stride = int(self.c_page_table.shape[1])
+            self.hs_pool = torch.zeros((self.hs_slots * c_rpp, 512), dtype=torch.int16, device=dev)
+            self.hs_table = torch.full((self.B, stride), -1, dtype=i32, device=dev)
+            self.hs_touch = torch.zeros((self.B, stride), dtype=i32, device=dev)
+            p.hs_ws_pool = self.hs_pool.data_ptr()
+            p.hs_ws_table = self.hs_table.data_ptr()
+            p.hs_n_slots = self.hs_slots
+            p.hs_touch = self.hs_touch.data_ptr()
+            p.hs_step = 1
+            from . import csa_hisparse_create
+            self.hs = csa_hisparse_create(self.B, stride, self.hs_slots)
         self.params = p
         self.ws_bytes = csa_decode_workspace_size(p)  # 0 also when the parameters are rejected: run() reports why
         self.ws = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
         self._shape = dict(ratio=ratio, H=H, Hi=Hi, k=k, swa=swa, scale=scale, kdtype=kdtype,
                            rows_per_page=rows_per_page, n_pages=n_pages, max_tokens=max_tokens,
                            c_rows_per_page=c_rows_per_page, c_n_pages=c_n_pages, ring_size=ring_size, n_q=n_q,
-                           device=device)
+                           hs_slots=hs_slots, device=device)
 
     def clone(self) -> "DecodeBatch":
         """The same step over copies of every device buffer (same values, other addresses):
@@ -157,6 +186,26 @@ class DecodeBatch:
                            w_h=c(self.w_h) if self.Hi else None, w_gate=c(self.w_gate), b_pos=c(self.b_pos),
                            c_page_table=c(self.c_page_table), ring_pool=c(self.ring_pool),
                            ring_page=c(self.ring_page), **self._shape)
+
+    @property
+    def hs_step(self) -> int:
+        return int(self.params.hs_step)
+
+    @hs_step.setter
+    def hs_step(self, v: int) -> None:
+        self.params.hs_step = int(v)
+
+    def hs_update(self, stream=None):
+        """After a step: bring the pages it read from the mirror into the working set ->
+        (pages brought in, pages evicted)."""
+        from . import csa_hisparse_update
+        return csa_hisparse_update(self.hs, self.params, stream)
+
+    def __del__(self):
+        if getattr(self, "hs", None):
+            from . import csa_hisparse_destroy
+            csa_hisparse_destroy(self.hs)
+            self.hs = None
 
     def run(self, stream=None, events=None) -> None:
         if events is None:

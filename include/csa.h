@@ -223,6 +223,21 @@ typedef struct {
      * then hold B * n_q entries in (request, query) order: q [B, n_q, H, 512] and so on.
      * 1 <= n_q <= 16 and B * n_q <= 65535. */
     int32_t n_q;
+    /* HiSparse ([V4-deploy] "HiSparse：把不活躍 KV 甩到 CPU"; [Day-0] "创新 3：HiSparse"): kv_c may be
+     * a full mirror of the C4 compressed pool in pinned host memory (kernels read it through its
+     * host pointer), with only a working set on the GPU: hs_ws_pool holds hs_n_slots pages of
+     * c_page_stride bytes, and hs_ws_table [B, c_page_table_stride] gives the slot of each
+     * logical compressed page of each request, or -1.  Stage 4 reads a resident page from its
+     * slot and any other straight from the mirror; stage 1 writes new rows to the mirror and, when
+     * the page is resident, to its slot.  hs_touch [B, c_page_table_stride], when set, receives
+     * hs_step for every compressed page a query read -- the input of the coordinator
+     * (csa_hisparse_update), which brings missed pages in between steps.  The index keys stay on
+     * the GPU.  Needs ratio 4 and an explicit c_page_table.  Zero-initialise to leave it off. */
+    void* hs_ws_pool;            /* device, 16-byte aligned, or NULL */
+    int32_t* hs_ws_table;        /* device [B, c_page_table_stride] */
+    int64_t hs_n_slots;
+    uint32_t* hs_touch;          /* device [B, c_page_table_stride], or NULL */
+    uint32_t hs_step;            /* the stamp of this step (>= 1; 0 marks a page never read) */
 } csa_decode_params;
 
 /* workspace: device, 16-byte aligned, caller-owned, at least csa_decode_workspace_size(p)
@@ -264,6 +279,33 @@ const char* csa_status_string(csa_status s);
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 int32_t csa_version(void);
+
+/*
+ * HiSparse coordinator ([V4-deploy] "HiSparse": a coordinator swaps pages every step and evicts
+ * by LRU; [Day-0] "创新 3": a GPU miss is swapped in from the CPU mirror).  A host object holding
+ * the working set's bookkeeping: which (request, logical page) each slot holds and the last step
+ * that read it.  Its first csa_hisparse_update allocates a device buffer of 12 * n_slots bytes
+ * for the swap plans, freed by csa_hisparse_destroy; nothing else is allocated.
+ */
+typedef struct csa_hisparse csa_hisparse;
+csa_status csa_hisparse_create(int32_t B, int64_t table_stride, int64_t n_slots, csa_hisparse** out);
+void csa_hisparse_destroy(csa_hisparse* h);
+/* The LRU decision alone, on the host.  touch [B, table_stride] holds the stamps after a step.
+ * Every page stamped `step` that is not resident gets a slot, in (request, logical page)
+ * order: a free slot (lowest first), else the resident page with the oldest stamp other than
+ * `step` (ties: the lowest slot), which is evicted.  When every slot holds a page of this step
+ * the rest stay in the mirror.  Writes up to max_plan (request, logical page, slot) triples to
+ * plan and the counts; the coordinator's residency table follows the plan. */
+csa_status csa_hisparse_plan(csa_hisparse* h, const uint32_t* touch, uint32_t step, int32_t* plan, int64_t max_plan,
+                             int64_t* n_in, int64_t* n_evicted);
+/* The residency table the coordinator holds: host memory, [B, table_stride] slots or -1. */
+const int32_t* csa_hisparse_table(const csa_hisparse* h);
+/* After a decode step with p on `stream`: reads p->hs_touch back (waiting for the stream), plans
+ * for p->hs_step as csa_hisparse_plan, then enqueues on the stream one gather kernel that copies
+ * every planned page from the mirror (kv_c) into its slot, and the new residency table into
+ * p->hs_ws_table.  The next step on the stream sees the new working set. */
+csa_status csa_hisparse_update(csa_hisparse* h, const csa_decode_params* p, void* stream, int64_t* n_in,
+                               int64_t* n_evicted);
 
 #ifdef __cplusplus
 }

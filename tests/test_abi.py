@@ -118,3 +118,61 @@ def test_ring_parameters_are_validated(libpath):
         setattr(p, field, bad)
         assert csa.csa_decode_workspace_size(p) == 0, (field, bad)
         setattr(p, field, good)
+
+
+def _ref_lru(state, touch, step):
+    """The documented coordinator policy, restated: refresh this step's resident pages; then each
+    missed page of this step, in (request, page) order, takes a free slot (lowest first) or
+    evicts the resident page with the oldest stamp other than this step's (lowest slot on ties)."""
+    import numpy as np
+    table, owner, stamp = state
+    flat = table.reshape(-1)
+    t = touch.reshape(-1)
+    for e in np.nonzero(t == step)[0]:
+        if flat[e] >= 0:
+            stamp[flat[e]] = step
+    cand = [s for s in range(len(owner)) if owner[s] < 0]
+    cand += sorted([s for s in range(len(owner)) if owner[s] >= 0 and stamp[s] != step], key=lambda s: (stamp[s], s))
+    plan, ev = [], 0
+    for e in np.nonzero(t == step)[0]:
+        if flat[e] >= 0:
+            continue
+        if not cand:
+            break
+        s = cand.pop(0)
+        if owner[s] >= 0:
+            flat[owner[s]] = -1
+            ev += 1
+        owner[s], stamp[s], flat[e] = e, step, s
+        plan.append((e // table.shape[1], e % table.shape[1], s))
+    return plan, ev
+
+
+def test_hisparse_plan_is_lru(libpath):
+    """The coordinator's host-side decisions over random access traces equal the restated
+    policy, keep slots and table consistent, and never evict a page read in the same step."""
+    import numpy as np
+    import deepseek_v4_hybrid_c4_gb300 as csa
+    rng = np.random.default_rng(5)
+    B, stride, slots = 3, 40, 24
+    h = csa.csa_hisparse_create(B, stride, slots)
+    try:
+        state = (np.full((B, stride), -1, np.int64), np.full(slots, -1, np.int64), np.zeros(slots, np.int64))
+        for step in range(1, 30):
+            touch = np.zeros((B, stride), np.uint32)
+            hot = rng.integers(0, 8)  # a drifting hot set plus random pages
+            for b in range(B):
+                touch[b, (hot + np.arange(5)) % stride] = step
+                touch[b, rng.integers(0, stride, size=rng.integers(0, 9))] = step
+            touch[touch == 0] = rng.integers(0, step, size=int((touch == 0).sum()))  # older stamps
+            plan, ev = csa.csa_hisparse_plan(h, touch, step, slots)
+            rplan, rev = _ref_lru(state, touch, step)
+            assert [tuple(x) for x in plan.tolist()] == rplan and ev == rev, step
+            table = csa.csa_hisparse_table(h, B, stride)
+            assert np.array_equal(table, state[0])
+            held = table[table >= 0]
+            assert len(np.unique(held)) == len(held)  # no slot twice
+            n_touched = int((touch == step).sum())
+            assert int(((table >= 0) & (touch == step)).sum()) == min(n_touched, slots)
+    finally:
+        csa.csa_hisparse_destroy(h)

@@ -50,7 +50,7 @@ def _check_against_oracle(case, batch):
         if r.n_groups_done < G:
             pages = case.c_pages(r)
             rows = [int(pages[g // c_rpp]) * c_rpp + g % c_rpp for g in range(r.n_groups_done, G)]
-            got_rows = batch.c_pool[torch.tensor(rows, device="cuda")].cpu().numpy().view(np.uint16)
+            got_rows = batch.c_pool[torch.tensor(rows, device=batch.c_pool.device)].cpu().numpy().view(np.uint16)
             ref_rows = oracle.compress(r.raw, case.ratio, case.w_gate, case.b_pos, r.n_groups_done,
                                        G - r.n_groups_done, want_f64=True)[1]
             assert_close(bf16_bits_to_f64(got_rows), ref_rows, f"{case.name} request {b} compressed rows")
@@ -203,6 +203,90 @@ def test_decode_one_query_position_is_the_plain_step(entry):
     b.run()
     torch.cuda.synchronize()
     assert torch.equal(a.sel, b.sel) and torch.equal(a.out, b.out) and torch.equal(a.lse, b.lse)
+
+
+def _hisparse_batch(entry, case, slots):
+    """The case with its C4 pool as a pinned host mirror (the shadow paging made explicit) and a
+    GPU working set of `slots` pages, empty at first."""
+    c_rpp = case.rows_per_page // case.ratio
+    return entry.case_to_batch(case, c_page_table=case.page_table(), c_rows_per_page=c_rpp, c_n_pages=case.n_pages,
+                               hs_slots=slots), c_rpp
+
+
+def test_hisparse_mirror_and_working_set(entry):
+    """Step 1 reads every selected row from the host mirror and stamps their pages; the
+    coordinator then brings those pages in; step 2 reads them from the working set.  Both steps
+    match the oracle, the stamps are exactly the selected pages, and the slots hold the mirror's
+    bytes."""
+    import deepseek_v4_hybrid_c4_gb300 as m
+    case = synth.make_decode_case("hs", 60, [65536, 20000], H=16, Hi=8, n_pending=1)
+    batch, c_rpp = _hisparse_batch(entry, case, slots=2048)
+    batch.hs_step = 1
+    batch.run()
+    torch.cuda.synchronize()
+    assert m.csa_read_device_status() == 0
+    _check_against_oracle(case, batch)
+    touch = batch.hs_touch.cpu().numpy()
+    want = np.zeros_like(touch)
+    for b in range(len(case.requests)):
+        s = batch.sel[b].cpu().numpy()
+        want[b, np.unique(s[s >= 0] // c_rpp)] = 1
+    assert np.array_equal(touch, want)
+    n_in, n_ev = batch.hs_update()
+    assert n_in == int(want.sum()) and n_ev == 0
+    table = batch.hs_table.cpu().numpy()
+    assert ((table >= 0) == (want == 1)).all()
+    pt = case.page_table()
+    pool = batch.c_pool.numpy()
+    slots = batch.hs_pool.cpu().numpy()
+    for b, lp in zip(*np.nonzero(table >= 0)):
+        sl = table[b, lp]
+        assert np.array_equal(slots[sl * c_rpp:(sl + 1) * c_rpp], pool[pt[b, lp] * c_rpp:(pt[b, lp] + 1) * c_rpp])
+    batch.out.zero_()
+    batch.hs_step = 2
+    batch.run()
+    torch.cuda.synchronize()
+    assert m.csa_read_device_status() == 0
+    _check_against_oracle(case, batch)
+    assert np.array_equal(batch.hs_touch.cpu().numpy(), want * 2)
+
+
+def test_hisparse_small_working_set_evicts(entry):
+    """A working set smaller than one step's pages: the coordinator fills it, the rest stay in
+    the mirror, and the step still matches the oracle with pages on both sides."""
+    import deepseek_v4_hybrid_c4_gb300 as m
+    case = synth.make_decode_case("hs2", 61, [40000], H=16, Hi=4, n_pending=1)
+    batch, c_rpp = _hisparse_batch(entry, case, slots=64)
+    for step in (1, 2, 3):
+        batch.hs_step = step
+        batch.run()
+        torch.cuda.synchronize()
+        assert m.csa_read_device_status() == 0
+        _check_against_oracle(case, batch)
+        n_in, n_ev = batch.hs_update()
+        resident = int((batch.hs_table.cpu().numpy() >= 0).sum())
+        assert resident == 64 and n_in == (64 if step == 1 else 0)
+
+
+def test_hisparse_new_rows_reach_mirror_and_slot(entry):
+    """The pending group's compressed row goes to the mirror and, its page being resident, to
+    the slot as well."""
+    import deepseek_v4_hybrid_c4_gb300 as m
+    case = synth.make_decode_case("hs3", 62, [8192 + 64], H=16, Hi=4, n_pending=1)
+    batch, c_rpp = _hisparse_batch(entry, case, slots=8)
+    r = case.requests[0]
+    G = r.n_tokens // 4
+    lp = (G - 1) // c_rpp
+    batch.hs_table[0, lp] = 5
+    batch.run()
+    torch.cuda.synchronize()
+    assert m.csa_read_device_status() == 0
+    ref = oracle.compress(r.raw, 4, case.w_gate, case.b_pos, G - 1, 1, want_f64=True)[1]
+    page = int(case.page_table()[0, lp])
+    in_mirror = batch.c_pool.numpy().view(np.uint16)[page * c_rpp + (G - 1) % c_rpp]
+    in_slot = batch.hs_pool.cpu().numpy().view(np.uint16)[5 * c_rpp + (G - 1) % c_rpp]
+    assert_close(bf16_bits_to_f64(in_mirror[None]), ref, "new row in the mirror")
+    assert np.array_equal(in_slot, in_mirror)
 
 
 def test_decode_graph_capture_replay(entry):
