@@ -164,36 +164,46 @@ __global__ void __launch_bounds__(AT_T, 1) attn_kernel(AttnArgs a) {
             // the previous tile's P.V must be done before K/V and P are overwritten
             if (it > 0 && !mbar_wait(bar_o, (uint32_t)((it - 1) & 1))) ok = false;
             __syncthreads();
-            for (int c = tid; c < AT_KT * 64; c += AT_T) {
-                const uint32_t row = c >> 6, ch = c & 63;
-                const uint32_t dst = sbase + SM_K + (ch >> 3) * K_SLAB + swz(row, ch & 7);
-                const uint8_t* src = kptr[row];
-                if (src)
-                    cp_async16(dst, src + ch * 16);
-                else
-                    st_shared_zero16(dst);
+            // the rows slab-major, in four commit groups of two 128-byte slabs (the first group
+            // also carries the staged Q), so that S runs on each pair of slabs as it lands
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                for (int c = tid; c < AT_KT * 16; c += AT_T) {
+                    const uint32_t row = c >> 4, ch = 16 * g + (c & 15);
+                    const uint32_t dst = sbase + SM_K + (ch >> 3) * K_SLAB + swz(row, ch & 7);
+                    const uint8_t* src = kptr[row];
+                    if (src)
+                        cp_async16(dst, src + ch * 16);
+                    else
+                        st_shared_zero16(dst);
+                }
+                cp_async_commit();
             }
-            cp_async_commit();
-            // the next tile's rows: look them up (dependent loads) while this tile's copies
-            // are in flight
+            // ---- S = Q K^T  (M=128, N=64, K=512: 8 slabs x 4 steps of 16), two slabs per group
+            constexpr uint32_t id_s = idesc_bf16_f32(AT_M, AT_KT, false);
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                if (g == 0) cp_async_wait_group<3>();
+                else if (g == 1) cp_async_wait_group<2>();
+                else if (g == 2) cp_async_wait_group<1>();
+                else cp_async_wait_group<0>();
+                fence_proxy_async_smem();
+                __syncthreads();
+                if (tid == 0) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int s = 2 * g; s < 2 * g + 2; ++s)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t ad = sdesc_sw128(sbase + SM_Q + s * Q_SLAB + kk * 32, 16, 1024);
+                            const uint64_t bd = sdesc_sw128(sbase + SM_K + s * K_SLAB + kk * 32, 16, 1024);
+                            tc_mma_f16(t_s, ad, bd, id_s, (s | kk) ? 1u : 0u);
+                        }
+                    if (g == 3) tc_commit(bar_s);
+                }
+            }
+            // the next tile's rows: look them up (dependent loads) while S runs
             if (tid < AT_KT && tile + 1 < t1) p_next = key_row((tile + 1) * AT_KT + tid);
-            cp_async_wait_all();
-            fence_proxy_async_smem();
-            __syncthreads();
-            // ---- S = Q K^T  (M=128, N=64, K=512: 8 slabs x 4 steps of 16)
-            if (tid == 0) {
-                tc_fence_after();
-                constexpr uint32_t id_s = idesc_bf16_f32(AT_M, AT_KT, false);
-#pragma unroll
-                for (int s = 0; s < 8; ++s)
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = sdesc_sw128(sbase + SM_Q + s * Q_SLAB + kk * 32, 16, 1024);
-                        const uint64_t bd = sdesc_sw128(sbase + SM_K + s * K_SLAB + kk * 32, 16, 1024);
-                        tc_mma_f16(t_s, ad, bd, id_s, (s | kk) ? 1u : 0u);
-                    }
-                tc_commit(bar_s);
-            }
             if (!mbar_wait(bar_s, (uint32_t)(it & 1))) ok = false;
             tc_fence_after();
             // ---- online softmax for row h

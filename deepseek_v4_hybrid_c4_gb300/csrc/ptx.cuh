@@ -84,6 +84,11 @@ CSA_DEV void named_bar_sync(uint32_t id, uint32_t count) {
 }
 CSA_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 CSA_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// wait until at most N of this thread's most recent cp.async groups are still pending
+template <int N>
+CSA_DEV void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy (tensor cores, TMA).
 CSA_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
