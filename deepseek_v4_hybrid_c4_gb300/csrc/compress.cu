@@ -131,7 +131,13 @@ __global__ void __launch_bounds__(256) compress_r4_kernel(CompressArgs a) {
         const int64_t g = first + gi;
         uint4 v[4][2];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) load_row16(token_row(a, b, 4 * g + i), lane, v[i]);
+        if (!a.ring_pool) {  // (uniform) the paged raw pool
+#pragma unroll
+            for (int i = 0; i < 4; ++i) load_row16(row_addr(a.raw, b, 4 * g + i, ROW_BYTES, a.status), lane, v[i]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) load_row16(token_row(a, b, 4 * g + i), lane, v[i]);
+        }
         float x[4][16], s[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -193,9 +199,14 @@ __global__ void __launch_bounds__(WARPS * 32) compress_r128_kernel(CompressArgs 
         for (int d = 0; d < 16; ++d) acc[d] = 0.f;
         for (int r0 = 0; r0 < ROWS; r0 += U) {
             const uint8_t* rows[U];
+            if (!a.ring_pool) {  // (uniform) the paged raw pool: all page lookups go out together
 #pragma unroll
-            for (int u = 0; u < U; ++u)
-                rows[u] = token_row(a, b, 128 * g + warp + WARPS * (r0 + u));
+                for (int u = 0; u < U; ++u)
+                    rows[u] = row_addr(a.raw, b, 128 * g + warp + WARPS * (r0 + u), ROW_BYTES, a.status);
+            } else {
+#pragma unroll
+                for (int u = 0; u < U; ++u) rows[u] = token_row(a, b, 128 * g + warp + WARPS * (r0 + u));
+            }
             uint4 v[U][2];
 #pragma unroll
             for (int u = 0; u < U; ++u) load_row16(rows[u], lane, v[u]);
@@ -242,8 +253,10 @@ __global__ void __launch_bounds__(WARPS * 32) compress_r128_kernel(CompressArgs 
             uint8_t* dst = const_cast<uint8_t*>(row_addr(a.out, b, g, ROW_BYTES, a.status));
             const uint32_t w = pack_bf16x2(o0 * inv, o1 * inv);
             if (dst) *reinterpret_cast<uint32_t*>(dst + d0 * 2) = w;
-            uint8_t* dst2 = ws_slot_row(a.ows, a.out, b, g);  // the page's working-set copy, if resident
-            if (dst && dst2) *reinterpret_cast<uint32_t*>(dst2 + d0 * 2) = w;
+            if (a.ows.table) {  // (uniform) the page's working-set copy, if resident
+                uint8_t* dst2 = ws_slot_row(a.ows, a.out, b, g);
+                if (dst && dst2) *reinterpret_cast<uint32_t*>(dst2 + d0 * 2) = w;
+            }
         }
         __syncthreads();
     }
