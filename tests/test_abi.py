@@ -176,3 +176,34 @@ def test_hisparse_plan_is_lru(libpath):
             assert int(((table >= 0) & (touch == step)).sum()) == min(n_touched, slots)
     finally:
         csa.csa_hisparse_destroy(h)
+
+
+def test_ctypes_structs_match_the_header(tmp_path):
+    """Every field offset and the size of csa_paged and csa_decode_params, as a C compiler lays
+    them out from include/csa.h, equal the ctypes binding's."""
+    import ctypes
+    import shutil
+    import subprocess
+    import deepseek_v4_hybrid_c4_gb300 as csa
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    lines = ['#include <stddef.h>', '#include <stdio.h>', '#include "csa.h"', "int main(void) {"]
+    for st in (csa.csa_paged, csa.csa_decode_params):
+        cname = st.__name__
+        lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
+        for f, _ in st._fields_:
+            lines.append(f'printf("{cname} {f} %zu\\n", offsetof({cname}, {f}));')
+    lines += ["return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.check_call([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
+    got = {}
+    for line in subprocess.check_output([str(exe)], text=True).splitlines():
+        name, field, value = line.split()
+        got[(name, field)] = int(value)
+    for st in (csa.csa_paged, csa.csa_decode_params):
+        assert got[(st.__name__, "size")] == ctypes.sizeof(st), st.__name__
+        for f, _ in st._fields_:
+            assert got[(st.__name__, f)] == getattr(st, f).offset, (st.__name__, f)
