@@ -316,6 +316,30 @@ def _score_source_sha():
     return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
 
 
+def rank_barrier(dist, sync=None):
+    """Every rank's queued device work done (sync), then every rank here."""
+    if sync:
+        sync()
+    if dist:
+        dist.barrier()
+
+
+def rank_max(dist, x: float, device="cuda") -> float:
+    """The largest x over the ranks (a time: the job takes as long as its slowest rank)."""
+    if not dist:
+        return x
+    import torch
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_us_per_step(ms_per_step_max: float, world: int) -> float:
+    """Replicas: `world` ranks each run the timed steps, so the job does world x K layer-steps in
+    the slowest rank's time; the line reports µs per layer-step of the whole job."""
+    return ms_per_step_max * 1e3 / world
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -362,16 +386,10 @@ def main():
         torch.sum(flush_rd, dim=0, dtype=torch.int64, out=flush_sum)
 
     def barrier():
-        torch.cuda.synchronize()
-        if dist:
-            dist.barrier()
+        rank_barrier(dist, torch.cuda.synchronize)
 
     def max_over_ranks(x):
-        if not dist:
-            return x
-        t = torch.tensor([x], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return rank_max(dist, x, "cuda")
 
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
@@ -517,7 +535,7 @@ def main():
         except Exception:
             traffic = None
     line = {
-        "metric": METRIC, "value": round(ms * 1e3 / world, 3), "unit": "µs/layer-step", "n_gpus": world,
+        "metric": METRIC, "value": round(job_us_per_step(ms, world), 3), "unit": "µs/layer-step", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (fp32 accumulate; fp32 fixed-order index score)",
         "data": "synthetic (seeded Philox4x32-10 generators; shapes of the 1M-context workload)",
