@@ -31,6 +31,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -426,8 +427,7 @@ def main():
     barrier()
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    clk_path = os.path.join(ROOT, "gpurun_out", "bench_clocks.csv") if os.path.isdir(
-        os.path.join(ROOT, "gpurun_out")) else "/tmp/bench_clocks.csv"
+    clk_path = os.path.join(tempfile.gettempdir(), f"bench_clocks_{os.getpid()}.csv")
     clocks = ClockSampler(clk_path)
     barrier()
     with clocks:
