@@ -78,6 +78,7 @@ def lib() -> ctypes.CDLL:
         L.csa_status_string.argtypes = [i32]
         L.csa_status_string.restype = ctypes.c_char_p
         L.csa_version.restype = i32
+        L.csa_selftest_bounded_wait.argtypes = [vp]
         L.csa_hisparse_create.argtypes = [i32, i64, i64, ctypes.POINTER(vp)]
         L.csa_hisparse_destroy.argtypes = [vp]
         L.csa_hisparse_destroy.restype = None
@@ -88,7 +89,7 @@ def lib() -> ctypes.CDLL:
                                           ctypes.POINTER(i64)]
         for name in ("csa_compress", "csa_index_score", "csa_topk", "csa_topk_batched", "csa_sparse_attn",
                      "csa_decode", "csa_decode_timed", "csa_decode_noalloc", "csa_read_device_status",
-                     "csa_hisparse_create", "csa_hisparse_plan", "csa_hisparse_update"):
+                     "csa_hisparse_create", "csa_hisparse_plan", "csa_hisparse_update", "csa_selftest_bounded_wait"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -189,6 +190,12 @@ def csa_sparse_attn(q, H: int, scale: float, kv_c: csa_paged, sel, n_sel: int, k
 
 def csa_decode_workspace_size(p: csa_decode_params) -> int:
     return int(lib().csa_decode_workspace_size(ctypes.byref(p)))
+
+
+def csa_selftest_bounded_wait(stream=None) -> None:
+    """Enqueue the bounded-wait self-test: its wait runs out and sets CSA_ERR_TIMEOUT in the
+    device status word (read it with csa_read_device_status)."""
+    _check(lib().csa_selftest_bounded_wait(_stream(stream)), "csa_selftest_bounded_wait")
 
 
 def csa_hisparse_create(B: int, table_stride: int, n_slots: int) -> int:

@@ -31,6 +31,7 @@ static int32_t* status_ptr() {
 
 int32_t* device_status_ptr() { return status_ptr(); }
 
+
 static bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 static bool al4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 

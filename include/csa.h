@@ -281,6 +281,15 @@ const char* csa_status_string(csa_status s);
 int32_t csa_version(void);
 
 /*
+ * Failure-detection self-test: enqueues one kernel that waits on an mbarrier nothing will ever
+ * arrive on.  Its wait is bounded the way every wait in the library is (a poll limit with
+ * back-off; about a second here, about 8 s for the library's own waits); when it runs out the
+ * kernel sets CSA_ERR_TIMEOUT in the device status word (csa_read_device_status) and returns.  Nothing traps or faults, and the
+ * context stays usable.  Returns CSA_ERR_CUDA if the launch fails.
+ */
+csa_status csa_selftest_bounded_wait(void* stream);
+
+/*
  * HiSparse coordinator ([V4-deploy] "HiSparse": a coordinator swaps pages every step and evicts
  * by LRU; [Day-0] "创新 3": a GPU miss is swapped in from the CPU mirror).  A host object holding
  * the working set's bookkeeping: which (request, logical page) each slot holds and the last step

@@ -330,3 +330,25 @@ def test_bad_page_id_sets_device_status_without_fault(csa):
     st = csa.csa_read_device_status()
     assert st & (1 << (csa.CSA_ERR_DEVICE_BOUNDS - 1))
     assert csa.csa_read_device_status() == 0  # read clears it
+
+
+def test_bounded_wait_runs_out_without_fault(csa):
+    """A wait that nothing satisfies (an mbarrier no one arrives on) runs out after its bounded
+    spin, sets CSA_ERR_TIMEOUT in the device status word and returns; the context stays usable
+    (a score call afterwards is correct and leaves the status clean)."""
+    csa.csa_read_device_status()
+    csa.csa_selftest_bounded_wait()
+    torch.cuda.synchronize()
+    st = csa.csa_read_device_status()
+    assert st & (1 << (csa.CSA_ERR_TIMEOUT - 1))
+    assert csa.csa_read_device_status() == 0
+    k = synth.normal_bf16((64, 128), 3, 1)
+    q = synth.normal_bf16((4, 128), 3, 2)
+    w = np.ones(4, np.float32)
+    out = torch.zeros(64, device="cuda")
+    csa.csa_index_score(dev(q, torch), dev(w, torch), 4, csa.paged(dev(k, torch), 64, 256, n_pages=1), csa.CSA_BF16,
+                        64, out)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy().view(np.uint32),
+                          oracle.index_score(q, w, k, False).view(np.uint32))
+    _status_clean(csa)
