@@ -207,3 +207,71 @@ def test_ctypes_structs_match_the_header(tmp_path):
         assert got[(st.__name__, "size")] == ctypes.sizeof(st), st.__name__
         for f, _ in st._fields_:
             assert got[(st.__name__, f)] == getattr(st, f).offset, (st.__name__, f)
+
+
+def _valid_params(csa, synth):
+    """Decode parameters of workload 0 that the host accepts (pointers never dereferenced)."""
+    c = synth.config(0)
+    p = csa.csa_decode_params()
+    p.B, p.ratio, p.H, p.Hi, p.k, p.swa = len(c.requests), c.ratio, c.H, c.Hi, c.k, c.swa
+    p.scale, p.k_dtype, p.max_tokens = 0.04, csa.CSA_BF16, max(r.n_tokens for r in c.requests)
+    for f in ("n_tokens", "n_groups_done", "kv_raw", "kv_c", "k_idx", "w_gate", "b_pos", "q", "q_idx", "w_h",
+              "out", "lse", "sel", "page_table"):
+        setattr(p, f, 4096)
+    p.raw_rows_per_page, p.raw_page_stride, p.n_pages = c.rows_per_page, c.rows_per_page * 1024, 1 << 20
+    p.c_page_stride, p.kidx_page_stride = (c.rows_per_page // 4) * 1024, (c.rows_per_page // 4) * 256
+    return p
+
+
+def test_query_positions_are_validated(libpath):
+    """n_q: 0 and 1 are one position; up to 16 positions; B * n_q within the grid limit.  The
+    workspace grows with the positions (scores, histograms, lists, partials per position)."""
+    import synth
+    import deepseek_v4_hybrid_c4_gb300 as csa
+    p = _valid_params(csa, synth)
+    one = csa.csa_decode_workspace_size(p)
+    p.n_q = 1
+    assert csa.csa_decode_workspace_size(p) == one
+    p.n_q = 4
+    four = csa.csa_decode_workspace_size(p)
+    assert four > one
+    for bad in (17, -1):
+        p.n_q = bad
+        assert csa.csa_decode_workspace_size(p) == 0, bad
+    p.n_q, p.B = 16, 5000  # 80,000 batch entries > 65,535
+    assert csa.csa_decode_workspace_size(p) == 0
+
+
+def test_hisparse_parameters_are_validated(libpath):
+    """HiSparse needs ratio 4, an explicit compressed page table, a residency table, at least one
+    slot and a 16-byte aligned working set; otherwise the call is refused on the host."""
+    import synth
+    import deepseek_v4_hybrid_c4_gb300 as csa
+    p = _valid_params(csa, synth)
+    p.c_page_table, p.c_page_table_stride, p.c_rows_per_page, p.c_n_pages = 4096, 64, 16, 1 << 20
+    base = csa.csa_decode_workspace_size(p)
+    assert base > 0
+    p.hs_ws_pool, p.hs_ws_table, p.hs_n_slots, p.hs_touch, p.hs_step = 8192, 4096, 32, 4096, 1
+    assert csa.csa_decode_workspace_size(p) == base  # the working set needs no workspace
+    for field, bad in (("hs_ws_table", None), ("hs_n_slots", 0), ("hs_ws_pool", 8200), ("c_page_table", None)):
+        good = getattr(p, field)
+        setattr(p, field, bad)
+        assert csa.csa_decode_workspace_size(p) == 0, (field, bad)
+        setattr(p, field, good)
+    p.ratio = 128  # C128 is dense: every step reads every entry, so no mirror
+    assert csa.csa_decode_workspace_size(p) == 0
+
+
+def test_hisparse_coordinator_rejects_bad_arguments(libpath):
+    import deepseek_v4_hybrid_c4_gb300 as csa
+    for args in ((0, 10, 4), (2, 0, 4), (2, 10, 0)):
+        with pytest.raises(csa.CsaError):
+            csa.csa_hisparse_create(*args)
+    h = csa.csa_hisparse_create(1, 8, 2)
+    try:
+        import numpy as np
+        plan, ev = csa.csa_hisparse_plan(h, np.zeros((1, 8), np.uint32), 1, 2)
+        assert len(plan) == 0 and ev == 0  # nothing read in step 1: nothing to bring in
+        assert (csa.csa_hisparse_table(h, 1, 8) == -1).all()
+    finally:
+        csa.csa_hisparse_destroy(h)
