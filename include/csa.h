@@ -191,11 +191,11 @@ typedef struct {
     /* layer weights */
     const float* w_gate;         /* fp32 [512] */
     const float* b_pos;          /* fp32 [ratio] */
-    /* per-request queries */
+    /* per-request queries (B * n_q entries with speculative verify, see n_q) */
     const void* q;               /* bf16 [B, H, 512] */
     const void* q_idx;           /* bf16 [B, Hi, 128] (ratio 4) */
     const float* w_h;            /* fp32 [B, Hi] (ratio 4) */
-    /* outputs */
+    /* outputs (B * n_q entries with speculative verify) */
     void* out;                   /* bf16 [B, H, 512] */
     float* lse;                  /* fp32 [B, H], nullable */
     int32_t* sel;                /* int32 [B, k], nullable (ratio 4): the selected candidates as a
@@ -203,9 +203,9 @@ typedef struct {
                                     fixed order that is not the score order: the same inputs give
                                     the same order and the same output bits */
     /* Optional compression-state ring ([V4-deploy] "ShadowRadix": the state ring nested in the
-     * SWA page index; [Day-0] "创新 1 ShadowRadix"): the raw tokens of groups still being filled live in a small
-     * per-request ring, token t of request b in row ring_page[b] * ring_size + t % ring_size
-     * of ring_pool.  When ring_pool is set, stage 1 reads the pending groups' tokens from the
+     * SWA page index; [Day-0] "创新 1 ShadowRadix"): the raw tokens of groups still being
+     * filled live in a small per-request ring, token t of request b in row
+     * ring_page[b] * ring_size + t % ring_size of ring_pool.  When ring_pool is set, stage 1 reads the pending groups' tokens from the
      * ring instead of kv_raw; the SWA window of stage 4 still reads kv_raw.  The ring must
      * still hold every pending token: n_groups_done[b] * ratio >= n_tokens[b] - ring_size,
      * else the device status gets CSA_ERR_DEVICE_BOUNDS.  Zero-initialise to leave it off. */
