@@ -59,23 +59,6 @@ CSA_DEV void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t ba
         "l"(src), "r"(bytes), "r"(bar)
         : "memory");
 }
-// Bulk copy from this CTA's shared memory into another CTA's shared memory of the cluster
-// (dst and bar: shared::cluster addresses from mapa), completing on the destination's
-// mbarrier by transaction bytes.  Both addresses 16-byte aligned, bytes % 16 == 0.
-CSA_DEV void bulk_s2cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-        "r"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
-// Bulk (non-tensor) copy of this CTA's shared memory to global, tracked by bulk groups.
-CSA_DEV void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
-                 : "memory");
-}
-CSA_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Wait until every committed bulk group of this thread has finished reading its source.
-CSA_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 CSA_DEV void cp_async16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
@@ -217,49 +200,6 @@ CSA_DEV uint32_t ld_dsmem_u32(uint32_t cluster_addr) {
     uint32_t v;
     asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
     return v;
-}
-CSA_DEV float4 ld_dsmem_f4(uint32_t cluster_addr) {
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(cluster_addr)
-                 : "memory");
-    return v;
-}
-CSA_DEV float2 ld_dsmem_f2(uint32_t cluster_addr) {
-    float2 v;
-    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(cluster_addr) : "memory");
-    return v;
-}
-CSA_DEV void st_dsmem_v4(uint32_t cluster_addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(a), "r"(b), "r"(c),
-                 "r"(d)
-                 : "memory");
-}
-CSA_DEV void st_dsmem_f2(uint32_t cluster_addr, float a, float b) {
-    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(cluster_addr), "f"(a), "f"(b) : "memory");
-}
-// Arrive on an mbarrier of another CTA of the cluster, releasing this thread's prior
-// writes (including its distributed-shared-memory stores) at cluster scope.
-CSA_DEV void mbar_arrive_remote(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-// Bounded wait on this CTA's mbarrier, acquiring at cluster scope (pairs with
-// mbar_arrive_remote); false when it ran out.
-CSA_DEV bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
-    for (uint32_t i = 0; i < CSA_SPIN_LIMIT; ++i) {
-        uint32_t ok;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(ok)
-            : "r"(bar), "r"(parity)
-            : "memory");
-        if (ok) return true;
-        if (i >= 32) __nanosleep(64);
-    }
-    return false;
 }
 CSA_DEV void st_dsmem_u32(uint32_t cluster_addr, uint32_t v) {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
