@@ -204,6 +204,25 @@ def other_workloads(torch, csa, entry, synth, stream, flush_l2, peak):
                                  "us_alone_l2_flushed": round(cold, 2), "us_p90_alone_l2_flushed": round(cold90, 2),
                                  "output": "sorted by (score desc, index asc); four kernels per call (clear the "
                                            "histograms, first digit, scan, finish)"}
+    # the same select in its single-cluster form (csa_topk_cluster: every digit's histogram summed
+    # across the cluster through distributed shared memory), same scores, same box
+    idx_c = torch.empty(case2.k, dtype=torch.int32, device="cuda")
+    topk_c = lambda: csa.csa_topk_cluster(scores, None, 1, G2, case2.k, idx_c, None, stream.cuda_stream)
+    warm_c, warm90_c = timed(topk_c, 50, flush=False)
+    cold_c, cold90_c = timed(topk_c, 50, flush=True)
+    with torch.cuda.stream(stream):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(200):
+            topk_c()
+        e1.record(stream)
+    e1.synchronize()
+    assert torch.equal(idx_c, idx)
+    res["topk_262144_to_512_cluster_form"] = {
+        "us_per_call_back_to_back": round(e0.elapsed_time(e1) * 1e3 / 200, 2),
+        "us_alone_scores_in_l2": round(warm_c, 2), "us_p90_alone_scores_in_l2": round(warm90_c, 2),
+        "us_alone_l2_flushed": round(cold_c, 2), "us_p90_alone_l2_flushed": round(cold90_c, 2),
+        "output": "identical indices; one cluster of 16 CTAs, one kernel per call"}
     # ---- C4 prefill compressor over the 1M workload's raw pool
     rp = csa.paged(b2.raw_pool, case2.rows_per_page, 1024, page_table=b2.page_table[0], n_pages=case2.n_pages)
     cout = torch.empty((G2, 512), dtype=torch.int16, device="cuda")

@@ -64,6 +64,7 @@ def lib() -> ctypes.CDLL:
         L.csa_index_score.argtypes = [vp, vp, i32, csa_paged, i32, i64, vp, vp]
         L.csa_topk.argtypes = [vp, i64, i32, vp, vp, vp, sz, vp]
         L.csa_topk_batched.argtypes = [vp, vp, i32, i64, i32, vp, vp, vp, sz, vp]
+        L.csa_topk_cluster.argtypes = [vp, vp, i32, i64, i32, vp, vp, vp]
         L.csa_topk_workspace_size.argtypes = [i32, i64, i32]
         L.csa_topk_workspace_size.restype = sz
         L.csa_sparse_attn.argtypes = [vp, i32, f32, csa_paged, vp, i32, csa_paged, i64, i32, vp, vp, vp, sz, vp]
@@ -87,7 +88,8 @@ def lib() -> ctypes.CDLL:
         L.csa_hisparse_table.restype = ctypes.POINTER(ctypes.c_int32)
         L.csa_hisparse_update.argtypes = [vp, ctypes.POINTER(csa_decode_params), vp, ctypes.POINTER(i64),
                                           ctypes.POINTER(i64)]
-        for name in ("csa_compress", "csa_index_score", "csa_topk", "csa_topk_batched", "csa_sparse_attn",
+        for name in ("csa_compress", "csa_index_score", "csa_topk", "csa_topk_batched", "csa_topk_cluster",
+                     "csa_sparse_attn",
                      "csa_decode", "csa_decode_timed", "csa_decode_noalloc", "csa_read_device_status",
                      "csa_hisparse_create", "csa_hisparse_plan", "csa_hisparse_update", "csa_selftest_bounded_wait"):
             getattr(L, name).restype = i32
@@ -176,6 +178,11 @@ def csa_topk_batched(scores, offsets, B: int, max_G: int, k: int, idx_out, keys_
         workspace = _scratch(ws_bytes, scores)
     _check(lib().csa_topk_batched(_ptr(scores), _ptr(offsets), B, max_G, k, _ptr(idx_out), _ptr(keys_out),
                                   _ptr(workspace), ws_bytes, _stream(stream)), "csa_topk_batched")
+
+
+def csa_topk_cluster(scores, offsets, B: int, max_G: int, k: int, idx_out, keys_out=None, stream=None) -> None:
+    _check(lib().csa_topk_cluster(_ptr(scores), _ptr(offsets), B, max_G, k, _ptr(idx_out), _ptr(keys_out),
+                                  _stream(stream)), "csa_topk_cluster")
 
 
 def csa_sparse_attn_workspace_size(H: int, n_sel: int, swa: int) -> int:

@@ -4,6 +4,7 @@
 
 #include <cstdint>
 #include <mutex>
+#include <vector>
 
 #include "csa.h"
 #include "internal.h"
@@ -30,6 +31,38 @@ static int32_t* status_ptr() {
 }
 
 int32_t* device_status_ptr() { return status_ptr(); }
+
+struct AttrDone {
+    const void* func;
+    cudaFuncAttribute attr;
+    int value;
+};
+static std::vector<AttrDone> g_attr_done[kMaxDevices];
+static int g_sm_count[kMaxDevices];
+static std::mutex g_launch_mu;
+
+int device_sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    std::lock_guard<std::mutex> lk(g_launch_mu);
+    if (!g_sm_count[dev] &&
+        cudaDeviceGetAttribute(&g_sm_count[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        g_sm_count[dev] = 0;
+    return g_sm_count[dev];
+}
+
+cudaError_t set_func_attr_once(const void* func, cudaFuncAttribute attr, int value) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_launch_mu);
+    for (const AttrDone& d : g_attr_done[dev])
+        if (d.func == func && d.attr == attr && d.value == value) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, attr, value);
+    if (e == cudaSuccess) g_attr_done[dev].push_back({func, attr, value});
+    return e;
+}
 
 
 static bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -208,9 +241,8 @@ static csa_status topk_common(const float* scores, const int64_t* offsets, int32
         w.standalone = true;
         w.keys_out = keys_out;
         e = launch_select_set(w, s, true);
-    } else {
-        e = cudaMemsetAsync(workspace, 0, (size_t)B * kHistBlock * sizeof(uint32_t), s);
-        if (e == cudaSuccess) e = launch_topk(t, s, false);
+    } else {  // one cluster per request; its histograms live in the cluster's shared memory
+        e = launch_topk(t, s, false);
     }
     return from_cuda(e);
 }
@@ -225,6 +257,34 @@ csa_status csa_topk_batched(const float* scores, const int64_t* offsets, int32_t
                             void* stream) {
     if (!offsets) return CSA_ERR_INVALID_ARG;
     return topk_common(scores, offsets, B, max_G, k, idx_out, keys_out, workspace, ws_bytes, stream);
+}
+
+csa_status csa_topk_cluster(const float* scores, const int64_t* offsets, int32_t B, int64_t max_G, int32_t k,
+                            int32_t* idx_out, uint32_t* keys_out, void* stream) {
+    if (k < 1 || k > 2048) return CSA_ERR_UNSUPPORTED;
+    if (!scores || !al4(scores) || !idx_out || !al4(idx_out)) return CSA_ERR_INVALID_ARG;
+    if (keys_out && !al4(keys_out)) return CSA_ERR_INVALID_ARG;
+    if (B < 1 || B > 65535 || max_G < 0 || max_G > 0x7FFFFFFFLL) return CSA_ERR_INVALID_ARG;
+    if (!offsets && B != 1) return CSA_ERR_INVALID_ARG;
+    int32_t* st = status_ptr();
+    if (!st) return CSA_ERR_CUDA;
+    TopkLaunch t;
+    t.scores = scores;
+    t.B = B;
+    t.G = max_G;
+    t.max_G = max_G;
+    t.offsets = offsets;
+    t.n_tokens = nullptr;
+    t.ratio = 1;
+    t.score_stride = 0;
+    t.k = k;
+    t.idx_out = idx_out;
+    t.keys_out = keys_out;
+    t.sorted = true;
+    t.hist_fused = false;
+    t.hist = nullptr;
+    t.status = st;
+    return from_cuda(launch_topk(t, static_cast<cudaStream_t>(stream), false));
 }
 
 size_t csa_sparse_attn_workspace_size(int32_t H, int32_t n_sel, int32_t swa) {

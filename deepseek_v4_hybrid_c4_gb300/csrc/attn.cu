@@ -761,13 +761,13 @@ cudaError_t launch_attn(const AttnLaunch& h, cudaStream_t s, bool pdl) {
     a.kws.n_slots = h.hs.n_slots;
     a.kws.touch = h.hs.touch;
     a.kws.step = h.hs.step;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)AT_SMEM);
+    {
+        cudaError_t e = set_func_attr_once((const void*)attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)AT_SMEM);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(attn64_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)A6_SMEM);
+            e = set_func_attr_once((const void*)attn64_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)A6_SMEM);
         if (e != cudaSuccess) return e;
-        attr_set = true;
     }
     const bool h64 = h.H <= A6_H;
     cudaLaunchConfig_t cfg = {};

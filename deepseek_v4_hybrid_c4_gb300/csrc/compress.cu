@@ -496,21 +496,13 @@ cudaError_t launch_compress(const CompressLaunch& h, cudaStream_t s, bool pdl) {
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     cfg.stream = s;
-    static int sms = 0;
-    if (!sms) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    }
+    const int sms = device_sm_count();
+    if (!sms) return cudaErrorInvalidDevice;
     if (!h.n_tokens && h.B == 1 && (h.ratio == 4 ? (h.count + 7) / 8 : h.count) >= sms) {
         // a prefill chunk that fills every SM: stream it through shared memory
-        static bool attr_set = false;
-        if (!attr_set) {
-            cudaError_t e =
-                cudaFuncSetAttribute(compress_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)CS_SMEM);
-            if (e != cudaSuccess) return e;
-            attr_set = true;
-        }
+        cudaError_t e = set_func_attr_once((const void*)compress_stream_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)CS_SMEM);
+        if (e != cudaSuccess) return e;
         cfg.blockDim = dim3((CS_WARPS + 1) * 32, 1, 1);
         cfg.gridDim = dim3((unsigned)sms, 1, 1);
         cfg.dynamicSmemBytes = CS_SMEM;

@@ -15,6 +15,12 @@ constexpr int kHistBlock = 6 * kHistBins;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Per-device launch facts, safe to call from several host threads and on several devices:
+// the current device's SM count (0 on failure), and a kernel attribute set once per device
+// (cudaFuncSetAttribute applies to the current device only).
+int device_sm_count();
+cudaError_t set_func_attr_once(const void* func, cudaFuncAttribute attr, int value);
+
 struct HWorkSet {          // HiSparse working set of a pool (see DWorkSet); table == nullptr: none
     const int32_t* table = nullptr;
     void* base = nullptr;

@@ -473,19 +473,13 @@ static cudaError_t launch_score_t(const CUtensorMap& map, const ScoreArgs& a, in
     constexpr size_t base = 1024 + (size_t)SC_WARPS * 2 * SC_SLOT_BYTES + (size_t)QF4 * 16 + 64 + SC_WARPS * 16;
     constexpr size_t with_hist = base + (size_t)kHistBins * 4;
     const size_t smem = a.hist ? with_hist : base;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e =
-            cudaFuncSetAttribute(score_kernel<HI, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)with_hist);
+    {
+        cudaError_t e = set_func_attr_once((const void*)score_kernel<HI, FP8>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)with_hist);
         if (e != cudaSuccess) return e;
-        attr_set = true;
     }
-    static int sms = 0;
-    if (!sms) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    }
+    const int sms = device_sm_count();
+    if (!sms) return cudaErrorInvalidDevice;
     int64_t grid = (HI >= 16 ? 1LL : 2LL) * sms;  // one wave of resident CTAs
     if (total_steps_bound < grid) grid = total_steps_bound < 1 ? 1 : total_steps_bound;
     cudaLaunchConfig_t cfg = {};

@@ -12,19 +12,21 @@
 // One thread-block cluster of CL <= 16 CTAs per request; CTA r owns the contiguous slice
 // r of the scores and keeps everything about it in its own shared memory:
 //  1. The first digit's histogram of the whole request -- fused into the score kernel in
-//     the decode step, otherwise counted per CTA and summed the same way as the rounds --
-//     gives the bin b0 holding the k-th key.
+//     the decode step (read from global memory), otherwise counted per CTA and summed the
+//     same way as the rounds -- gives the bin b0 holding the k-th key.
 //  2. One scan of the slice: keys above b0 are winners, keys in b0 survivors, each list
 //     compacted in index order (block-wide prefix sums, no atomics).
-//  3. Rounds over the next digits: each CTA counts its survivors' digit in shared memory
-//     and adds its non-zero bins to the round's histogram in global memory (L2); after
-//     one cluster barrier every CTA reads that histogram and finds the same bin;
+//  3. Rounds over the next digits: each CTA counts its survivors' digit in its own shared
+//     memory; after one cluster barrier every CTA sums every CTA's counts of its bins through
+//     distributed shared memory (the reduction inside the cluster) and finds the same bin;
 //     survivors above it join the winners, the others leave.  The rounds stop when winners plus survivors are exactly
 //     k (set output) or fit one ranking (sorted output).  A CTA whose survivors overflow
 //     its shared memory rescans its slice (in L2) each round instead.
 //  4. Output: the set -- each CTA writes its lists at offsets given by a prefix over the
 //     CTAs' published counts (winners of all CTAs first, then survivors; a fixed order);
 //     or sorted -- every CTA copies its lists into CTA 0, which ranks them.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -297,18 +299,31 @@ __device__ __forceinline__ void ordered_reserve(TkSmem& sm, uint32_t ns, uint32_
     __syncthreads();
 }
 
-// Add this CTA's non-zero counts of local histogram `hb` to the global histogram gh;
-// then a cluster barrier (release/acquire: every CTA's additions are visible) and the
-// bin of `need` in gh, read from L2.
-__device__ __forceinline__ void cluster_find_bin(TkSmem& sm, int hb, uint32_t* gh, int nbins, uint32_t need) {
-    __syncthreads();  // the local histogram is complete
-    for (int i = threadIdx.x; i < nbins; i += TK_T) {
-        const uint32_t c = sm.hist[hb][i];
-        if (c) atomicAdd(gh + i, c);
-    }
+// The round's histogram of the whole request, summed over the cluster's CTAs through
+// distributed shared memory: after one cluster barrier (release/acquire: every CTA's counts
+// in its own hist[hb] are complete and visible), thread t reads its two bins from every CTA's
+// shared memory, and every CTA finds the same bin of `need`.  hist[hb] is not written again
+// before the next round's barrier (the rounds alternate between two histograms), so no CTA
+// overwrites counts another may still be reading.
+__device__ __forceinline__ void cluster_find_bin(TkSmem& sm, int hb, int nbins, uint32_t need) {
     cluster_sync();
+    const int cl = (int)gridDim.x;
     const int bh = nbins - 1 - 2 * (int)threadIdx.x, bl = bh - 1;
-    const uint32_t th = bl >= 0 ? __ldcg(gh + bh) : 0u, tl = bl >= 0 ? __ldcg(gh + bl) : 0u;
+    uint32_t th = 0, tl = 0;
+    if (bl >= 0) {
+        const uint32_t ah = smem_u32(&sm.hist[hb][bh]), al = smem_u32(&sm.hist[hb][bl]);
+        uint32_t vh[TK_MAXCL], vl[TK_MAXCL];
+#pragma unroll
+        for (int r = 0; r < TK_MAXCL; ++r) {  // all loads in flight, then the sums
+            vh[r] = r < cl ? ld_dsmem_u32(mapa(ah, (uint32_t)r)) : 0u;
+            vl[r] = r < cl ? ld_dsmem_u32(mapa(al, (uint32_t)r)) : 0u;
+        }
+#pragma unroll
+        for (int r = 0; r < TK_MAXCL; ++r) {
+            th += vh[r];
+            tl += vl[r];
+        }
+    }
     find_bin_vals(sm, th, tl, nbins, need);
 }
 
@@ -353,7 +368,7 @@ __global__ void __launch_bounds__(TK_T, 1) topk_cluster_kernel(TopkArgs a) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) hist_add(sm.hist[0], key[q] >> 21, pos + q < hi);
             }
-            cluster_find_bin(sm, 0, a.hist + (int64_t)b * kHistBlock, TK_BINS, need);
+            cluster_find_bin(sm, 0, TK_BINS, need);
         }
         bins[0] = sm.bin;
         need -= sm.above;
@@ -428,7 +443,7 @@ __global__ void __launch_bounds__(TK_T, 1) topk_cluster_kernel(TopkArgs a) {
                 }
             }
         }
-        cluster_find_bin(sm, hb, a.hist + (int64_t)b * kHistBlock + (int64_t)d * TK_BINS, nb, need);
+        cluster_find_bin(sm, hb, nb, need);
         const uint32_t dbin = sm.bin;
         need -= sm.above;
         tot_w += sm.above;
@@ -565,15 +580,15 @@ __global__ void __launch_bounds__(TK_T, 1) topk_cluster_kernel(TopkArgs a) {
 }
 
 // ------------------------------------------------------------------ host side
-static int g_max_cluster = 0;
+constexpr int kTopkMaxDevices = 64;
+static int g_max_cluster[kTopkMaxDevices];  // largest schedulable cluster of the kernel, per device
+static std::mutex g_topk_mu;
 
-// CTAs per request: about TK_SLICE scores each, a power of two, at most the largest
-// cluster of this kernel the device can schedule.
-static int topk_cluster_size(int64_t max_G) {
+// CTAs per request: about TK_SLICE scores each, a power of two, at most `max_cl`.
+static int topk_cluster_size(int64_t max_G, int max_cl) {
     int c = 1;
     while ((int64_t)c * TK_SLICE < max_G && c < TK_MAXCL) c <<= 1;
-    if (g_max_cluster > 0)
-        while (c > g_max_cluster) c >>= 1;
+    while (c > max_cl && c > 1) c >>= 1;
     return c;
 }
 
@@ -602,25 +617,33 @@ cudaError_t launch_topk(const TopkLaunch& h, cudaStream_t s, bool pdl) {
     a.hist = h.hist;
     a.status = h.status;
     const size_t smem = sizeof(TkSmem);
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-        cudaLaunchConfig_t q = {};
-        q.gridDim = dim3(TK_MAXCL, 1, 1);
-        q.blockDim = dim3(TK_T, 1, 1);
-        q.dynamicSmemBytes = smem;
-        int mc = 0;
-        if (cudaOccupancyMaxPotentialClusterSize(&mc, topk_cluster_kernel, &q) == cudaSuccess && mc > 0)
-            g_max_cluster = mc;
-        else
-            g_max_cluster = 8;
-        cudaGetLastError();
-        attr_set = true;
+    cudaError_t e = set_func_attr_once((const void*)topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+    if (e == cudaSuccess)
+        e = set_func_attr_once((const void*)topk_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kTopkMaxDevices) return cudaErrorInvalidDevice;
+    int max_cl;
+    {
+        std::lock_guard<std::mutex> lk(g_topk_mu);
+        if (!g_max_cluster[dev]) {
+            cudaLaunchConfig_t q = {};
+            q.gridDim = dim3(TK_MAXCL, 1, 1);
+            q.blockDim = dim3(TK_T, 1, 1);
+            q.dynamicSmemBytes = smem;
+            int mc = 0;
+            if (cudaOccupancyMaxPotentialClusterSize(&mc, topk_cluster_kernel, &q) != cudaSuccess || mc < 1) {
+                cudaGetLastError();
+                mc = 8;  // portable cluster size
+            }
+            g_max_cluster[dev] = mc < TK_MAXCL ? mc : TK_MAXCL;
+        }
+        max_cl = g_max_cluster[dev];
     }
-    const int cl = topk_cluster_size(h.max_G);
+    const int cl = topk_cluster_size(h.max_G, max_cl);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -749,18 +749,16 @@ cudaError_t launch_select_set(const SelectSetLaunch& h, cudaStream_t s, bool pdl
     a.status = h.status;
     const size_t smem = sizeof(SwFinSmem);
     static_assert(sizeof(SwFinSmem) + SW_SCAN_SPREAD_SMEM + 2 * 1024 <= 228 * 1024, "a scan and a finish CTA share an SM");
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e =
-            cudaFuncSetAttribute(select_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    {
+        cudaError_t e = set_func_attr_once((const void*)select_finish_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(select_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)SW_SCAN_SPREAD_SMEM);
+            e = set_func_attr_once((const void*)select_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)SW_SCAN_SPREAD_SMEM);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(select_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)SW_SCAN_SPREAD_SMEM);
+            e = set_func_attr_once((const void*)select_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)SW_SCAN_SPREAD_SMEM);
         if (e != cudaSuccess) return e;
-        attr_set = true;
     }
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -768,12 +766,8 @@ cudaError_t launch_select_set(const SelectSetLaunch& h, cudaStream_t s, bool pdl
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    static int sms = 0;
-    if (!sms) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    }
+    const int sms = device_sm_count();
+    if (!sms) return cudaErrorInvalidDevice;
     // grid (request, region): the blocks are dispatched region-major, so a batch's region 0s
     // (which carry the finish's general path) are all in the first wave
     cfg.gridDim = dim3((unsigned)h.B, (unsigned)a.C, 1);

@@ -110,9 +110,12 @@ csa_status csa_index_score(const void* q_idx, const float* w_h, int32_t Hi, csa_
  * scores ordered by (score desc, index asc), then -1 padding.  Scores compare
  * through the order-preserving key (-0 == +0; key = bits ^ (sign ? ~0 : 1<<31)).
  * keys_out (nullable) uint32 [k] receives those keys (0 for padding).
- * Radix select over the key's digits: the first digit's histogram is built by CTAs
- * whose shared-memory histograms are summed inside a cluster of 8 (distributed shared
- * memory); the select then runs wide over the scores and finishes in one CTA.
+ * Radix select over the key's digits.  Up to 4,194,304 scores per request: CTAs of 2,048
+ * scores each count the first digit and add their counts into a histogram in global
+ * memory (L2 atomics); a wide grid then compacts every slice's winners and threshold
+ * candidates, and a finish kernel in which every CTA ranks its own slice's entries writes
+ * the output (no CTA gathers them all).  Above that size the call takes the single-cluster
+ * form of csa_topk_cluster.
  * workspace: device, 16-byte aligned, at least csa_topk_workspace_size(1, G, k) bytes,
  * owned by the caller, its contents overwritten (no state is kept between calls).
  * 1 <= k <= 2048, G <= 2^31 - 1.  CSA_ERR_WORKSPACE when it is missing or small.
@@ -130,6 +133,22 @@ csa_status csa_topk(const float* scores, int64_t G, int32_t k, int32_t* idx_out,
 csa_status csa_topk_batched(const float* scores, const int64_t* offsets, int32_t B, int64_t max_G, int32_t k,
                             int32_t* idx_out, uint32_t* keys_out, void* workspace, size_t ws_bytes,
                             void* stream);
+
+/*
+ * Stage 3, single-cluster form: the output of csa_topk_batched (indices sorted by (score
+ * desc, index asc), keys_out optional, -1 padding), computed by one thread-block cluster
+ * per request as the pages describe Lightning TopK ([Day-0] "创新 2": per-CTA histograms
+ * reduced inside the cluster to the threshold, then the entries above it scattered).  Each
+ * CTA of the cluster (up to 16, a power of two, about 16,384 scores each) owns a contiguous
+ * slice and keeps its winners and threshold candidates in its own shared memory; every
+ * radix digit is counted in each CTA's shared memory and the cluster's counts are summed
+ * through distributed shared memory; CTA 0 ranks the union.  csa_topk and
+ * csa_topk_batched take this form by themselves above 4,194,304 scores per request; this
+ * entry point takes it at any size.  offsets: device int64 [B+1], or NULL with B = 1 for
+ * one request of max_G scores.  No workspace; nothing is allocated.
+ */
+csa_status csa_topk_cluster(const float* scores, const int64_t* offsets, int32_t B, int64_t max_G, int32_t k,
+                            int32_t* idx_out, uint32_t* keys_out, void* stream);
 
 /*
  * Stage 4: one attention over the selected compressed entries plus the last

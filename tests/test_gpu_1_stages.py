@@ -149,6 +149,67 @@ def test_topk_batched_ragged(csa):
     _status_clean(csa)
 
 
+def _straddling(G, k, seed):
+    """Ragged random scores whose k-th largest value is shared by a group of about 3k entries
+    spread over the whole range, so the tie group straddles rank k."""
+    s = _scores_with_ties(G, seed)
+    t = np.float32(np.partition(s, G - k)[G - k])
+    rng = np.random.default_rng(seed + 1)
+    s[rng.integers(0, G, min(G, 3 * k))] = t
+    return s
+
+
+@pytest.mark.parametrize("G", [1, 511, 513, 20000, 262144, 300001])
+@pytest.mark.parametrize("k", [1, 512, 2048])
+def test_topk_cluster_bitexact(csa, G, k):
+    """The single-cluster form (distributed-shared-memory histograms) at any size."""
+    s = _straddling(G, k, G + 3 * k) if G > k else _scores_with_ties(G, G + 3 * k)
+    sd = torch.from_numpy(s).cuda()
+    idx = torch.full((k,), -7, dtype=torch.int32, device="cuda")
+    keys = torch.zeros((k,), dtype=torch.int32, device="cuda")
+    csa.csa_topk_cluster(sd, None, 1, G, k, idx, keys)
+    ref, rkeys = oracle.topk(s, k, want_keys=True)
+    assert np.array_equal(idx.cpu().numpy(), ref)
+    assert np.array_equal(keys.cpu().numpy().view(np.uint32), rkeys)
+    _status_clean(csa)
+
+
+def test_topk_cluster_batched_ragged(csa):
+    lens = [1, 300, 512, 513, 70000, 0, 33000, 262144]
+    segs = [_scores_with_ties(n, 90 + i) for i, n in enumerate(lens)]
+    flat = np.concatenate(segs).astype(np.float32)
+    offs = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    k = 512
+    idx = torch.full((len(lens), k), -7, dtype=torch.int32, device="cuda")
+    csa.csa_topk_cluster(torch.from_numpy(flat).cuda(), torch.from_numpy(offs).cuda(), len(lens), max(lens), k, idx)
+    got = idx.cpu().numpy()
+    for b, sgm in enumerate(segs):
+        assert np.array_equal(got[b], oracle.topk(sgm, k)), b
+    _status_clean(csa)
+
+
+@pytest.mark.parametrize("G", [4194305, 6000000])
+@pytest.mark.parametrize("k", [512, 2048])
+def test_topk_above_the_wide_select(csa, G, k):
+    """csa_topk and csa_topk_batched above 4,194,304 scores per request (the cluster form, its
+    candidates overflowing shared memory and re-read from L2 each round), a tie group
+    straddling rank k."""
+    s = _straddling(G, k, G + k)
+    idx, keys = _topk_gpu(csa, s, k)
+    ref, rkeys = oracle.topk(s, k, want_keys=True)
+    assert np.array_equal(idx, ref)
+    assert np.array_equal(keys, rkeys)
+    small = _scores_with_ties(1000, 5)
+    flat = np.concatenate([small, s]).astype(np.float32)
+    offs = np.array([0, 1000, 1000 + G], np.int64)
+    got = torch.full((2, k), -7, dtype=torch.int32, device="cuda")
+    csa.csa_topk_batched(torch.from_numpy(flat).cuda(), torch.from_numpy(offs).cuda(), 2, G, k, got)
+    got = got.cpu().numpy()
+    assert np.array_equal(got[0], oracle.topk(small, k))
+    assert np.array_equal(got[1], ref)
+    _status_clean(csa)
+
+
 # ------------------------------------------------------------------ stage 1: compressor
 @pytest.mark.parametrize("ratio,n_tokens,paged", [(4, 4096, False), (4, 8192 + 64, True), (128, 4096, True),
                                                   (128, 128 * 37, False),

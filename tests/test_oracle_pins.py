@@ -118,7 +118,11 @@ def test_compress_zero_gate_is_arithmetic_mean():
     out, f64 = oracle.compress(x, 4, np.zeros(512, np.float32), np.zeros(4, np.float32), want_f64=True)
     mean = bf2f(x).astype(np.float64).reshape(3, 4, 512).mean(axis=1)
     assert np.allclose(f64, mean, atol=1e-15, rtol=0)
-    assert np.array_equal(out, f2bf(mean.astype(np.float32))) or np.abs(bf2f(out) - mean).max() <= 2 ** -8 * np.abs(mean).max()
+    # the bf16 output is the fp64 mean rounded once, to nearest with ties to even: 8 significant
+    # bits from frexp's mantissa in [0.5, 1), rounded by rint (half to even); all values normal
+    m, e = np.frexp(mean)
+    expect = np.ldexp(np.rint(m * 256.0), e - 8)
+    assert np.array_equal(out, f2bf(expect.astype(np.float32)))  # expect is on the bf16 grid: exact
 
 
 def test_compress_one_hot_bias_selects_token():

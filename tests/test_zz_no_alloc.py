@@ -2,17 +2,15 @@
 (allocator callbacks, hosts that only pass their own input/output buffers).  It must give
 the same result as csa_decode with a caller-provided workspace, on consecutive calls that
 share the library's fixed scratch array.  This file is collected last on purpose."""
-import numpy as np
 import pytest
 
 import synth
-from helpers import assert_close
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 
-@pytest.mark.parametrize("cfg,scale_down", [(2, 16), (3, 16)])
+@pytest.mark.parametrize("cfg,scale_down", [(2, 16), (3, 16), (4, 16)])
 def test_noalloc_matches_workspace_entry_point_twice(cfg, scale_down):
     import __graft_entry__
     __graft_entry__.build()
@@ -23,16 +21,19 @@ def test_noalloc_matches_workspace_entry_point_twice(cfg, scale_down):
     batch.run()
     torch.cuda.synchronize()
     ref_out = batch.out.clone()
-    ref_sel = batch.sel.clone()
+    ref_sel = batch.sel.clone() if batch.sel is not None else None  # ratio 128: no selection
     ref_lse = batch.lse.clone()
     for _ in range(2):  # two calls in a row share (and reuse) the library's scratch array
         batch.out.zero_()
-        batch.sel.fill_(-7)
+        if batch.sel is not None:
+            batch.sel.fill_(-7)
         batch.lse.zero_()
         csa.csa_decode_noalloc(batch.params)
         torch.cuda.synchronize()
         assert csa.csa_read_device_status() == 0
-        assert torch.equal(batch.sel, ref_sel)
-        for b in range(batch.B):
-            assert_close(batch.out[b].float().cpu().numpy(), ref_out[b].float().cpu().numpy(), f"noalloc request {b}")
-        assert np.abs(batch.lse.cpu().numpy() - ref_lse.cpu().numpy()).max() <= 1e-4
+        # the same deterministic kernels on the same inputs: the same bytes, whatever the
+        # scratch array held before
+        if batch.sel is not None:
+            assert torch.equal(batch.sel, ref_sel)
+        assert torch.equal(batch.out, ref_out)
+        assert torch.equal(batch.lse, ref_lse)
