@@ -70,6 +70,12 @@ def lib() -> ctypes.CDLL:
         L.csa_sparse_attn.argtypes = [vp, i32, f32, csa_paged, vp, i32, csa_paged, i64, i32, vp, vp, vp, sz, vp]
         L.csa_sparse_attn_workspace_size.argtypes = [i32, i32, i32]
         L.csa_sparse_attn_workspace_size.restype = sz
+        L.csa_topk_merge_workspace_size.argtypes = [i32, i32]
+        L.csa_topk_merge_workspace_size.restype = sz
+        L.csa_topk_merge.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, sz, vp]
+        L.csa_sparse_attn_partial.argtypes = [vp, i32, f32, csa_paged, vp, i32, csa_paged, i64, i32, vp, vp, vp, sz,
+                                              vp]
+        L.csa_attn_merge.argtypes = [vp, vp, i32, i32, vp, vp, vp]
         L.csa_decode.argtypes = [ctypes.POINTER(csa_decode_params), vp, sz, vp]
         L.csa_decode_timed.argtypes = [ctypes.POINTER(csa_decode_params), vp, sz, vp, ctypes.POINTER(vp)]
         L.csa_decode_noalloc.argtypes = [ctypes.POINTER(csa_decode_params), vp]
@@ -89,7 +95,7 @@ def lib() -> ctypes.CDLL:
         L.csa_hisparse_update.argtypes = [vp, ctypes.POINTER(csa_decode_params), vp, ctypes.POINTER(i64),
                                           ctypes.POINTER(i64)]
         for name in ("csa_compress", "csa_index_score", "csa_topk", "csa_topk_batched", "csa_topk_cluster",
-                     "csa_sparse_attn",
+                     "csa_topk_merge", "csa_sparse_attn_partial", "csa_attn_merge", "csa_sparse_attn",
                      "csa_decode", "csa_decode_timed", "csa_decode_noalloc", "csa_read_device_status",
                      "csa_hisparse_create", "csa_hisparse_plan", "csa_hisparse_update", "csa_selftest_bounded_wait"):
             getattr(L, name).restype = i32
@@ -193,6 +199,35 @@ def csa_sparse_attn(q, H: int, scale: float, kv_c: csa_paged, sel, n_sel: int, k
                     swa: int, out, lse=None, workspace=None, ws_bytes: int = 0, stream=None) -> None:
     _check(lib().csa_sparse_attn(_ptr(q), H, scale, kv_c, _ptr(sel), n_sel, kv_raw, n_tokens, swa, _ptr(out),
                                  _ptr(lse), _ptr(workspace), ws_bytes, _stream(stream)), "csa_sparse_attn")
+
+
+def csa_topk_merge_workspace_size(R: int, k: int) -> int:
+    return int(lib().csa_topk_merge_workspace_size(R, k))
+
+
+def csa_topk_merge(keys, idx, rank_lo, R: int, k: int, rank: int = -1, sel_local=None, idx_out=None, keys_out=None,
+                   workspace=None, ws_bytes: int = 0, stream=None) -> None:
+    if workspace is None:
+        ws_bytes = csa_topk_merge_workspace_size(R, k)
+        workspace = _scratch(ws_bytes, keys)
+    _check(lib().csa_topk_merge(_ptr(keys), _ptr(idx), _ptr(rank_lo), R, k, rank, _ptr(sel_local), _ptr(idx_out),
+                                _ptr(keys_out), _ptr(workspace), ws_bytes, _stream(stream)), "csa_topk_merge")
+
+
+def csa_sparse_attn_partial(q, H: int, scale: float, kv_c: csa_paged, sel, n_sel: int, kv_raw: csa_paged,
+                            n_tokens: int, swa: int, o_part, lse_part, workspace=None, ws_bytes: int = 0,
+                            stream=None) -> None:
+    if workspace is None:
+        ws_bytes = csa_sparse_attn_workspace_size(H, n_sel, swa)
+        workspace = _scratch(ws_bytes, q)
+    _check(lib().csa_sparse_attn_partial(_ptr(q), H, scale, kv_c, _ptr(sel), n_sel, kv_raw, n_tokens, swa,
+                                         _ptr(o_part), _ptr(lse_part), _ptr(workspace), ws_bytes, _stream(stream)),
+           "csa_sparse_attn_partial")
+
+
+def csa_attn_merge(o_parts, lse_parts, R: int, H: int, out, lse=None, stream=None) -> None:
+    _check(lib().csa_attn_merge(_ptr(o_parts), _ptr(lse_parts), R, H, _ptr(out), _ptr(lse), _stream(stream)),
+           "csa_attn_merge")
 
 
 def csa_decode_workspace_size(p: csa_decode_params) -> int:

@@ -329,6 +329,85 @@ csa_status csa_sparse_attn(const void* q, int32_t H, float scale, csa_paged kv_c
     return from_cuda(launch_attn(a, static_cast<cudaStream_t>(stream), false));
 }
 
+// ------------------------------------------------------------------ context-parallel pieces
+csa_status csa_sparse_attn_partial(const void* q, int32_t H, float scale, csa_paged kv_c, const int32_t* sel,
+                                   int32_t n_sel, csa_paged kv_raw, int64_t n_tokens, int32_t swa, float* o_part,
+                                   float* lse_part, void* workspace, size_t ws_bytes, void* stream) {
+    if (H < 1 || H > 128 || swa < 0 || swa > 128) return CSA_ERR_UNSUPPORTED;
+    if (!q || !al16(q) || !o_part || !al16(o_part) || !lse_part || !al4(lse_part) || (sel && !al4(sel)))
+        return CSA_ERR_INVALID_ARG;
+    if (n_sel < 0 || n_tokens < 0 || (n_sel > 0 && !sel)) return CSA_ERR_INVALID_ARG;
+    const int64_t W = n_tokens < swa ? n_tokens : swa;
+    if (n_sel > 0 && check_paged(kv_c, kLatentRowBytes)) return CSA_ERR_INVALID_ARG;
+    if (W > 0 && check_paged(kv_raw, kLatentRowBytes)) return CSA_ERR_INVALID_ARG;
+    const size_t need = attn_workspace_bytes(1, H, n_sel + W);
+    if (!workspace || ws_bytes < need || !al16(workspace)) return CSA_ERR_WORKSPACE;
+    int32_t* st = status_ptr();
+    if (!st) return CSA_ERR_CUDA;
+    AttnLaunch a;
+    a.q = q;
+    a.H = H;
+    a.scale = scale;
+    a.kv_c = host_paged(kv_c);
+    a.kv_raw = host_paged(kv_raw);
+    a.sel = sel;
+    a.sel_stride = 0;
+    a.n_sel = n_sel;
+    a.B = 1;
+    a.n_tokens = nullptr;
+    a.ratio = 4;
+    a.N = n_tokens;
+    a.max_keys = n_sel + W;
+    a.swa = swa;
+    a.out = nullptr;
+    a.out_f32 = o_part;
+    a.lse = lse_part;
+    a.ws = workspace;
+    a.ws_bytes = ws_bytes;
+    a.status = st;
+    return from_cuda(launch_attn(a, static_cast<cudaStream_t>(stream), false));
+}
+
+csa_status csa_attn_merge(const float* o_parts, const float* lse_parts, int32_t R, int32_t H, void* out, float* lse,
+                          void* stream) {
+    if (H < 1 || H > 128 || R < 1) return CSA_ERR_UNSUPPORTED;
+    if (!o_parts || !al16(o_parts) || !lse_parts || !al4(lse_parts) || !out || !al16(out) || (lse && !al4(lse)))
+        return CSA_ERR_INVALID_ARG;
+    return from_cuda(launch_lse_merge(o_parts, lse_parts, R, H, out, lse, static_cast<cudaStream_t>(stream)));
+}
+
+size_t csa_topk_merge_workspace_size(int32_t R, int32_t k) {
+    if (R < 1 || k < 1 || k > 2048 || (int64_t)R * k > 4194304) return 0;
+    return topk_merge_workspace_bytes(R, k);
+}
+
+csa_status csa_topk_merge(const uint32_t* keys, const int32_t* idx, const int64_t* rank_lo, int32_t R, int32_t k,
+                          int32_t rank, int32_t* sel_local, int32_t* idx_out, uint32_t* keys_out, void* workspace,
+                          size_t ws_bytes, void* stream) {
+    if (k < 1 || k > 2048 || R < 1 || (int64_t)R * k > 4194304) return CSA_ERR_UNSUPPORTED;
+    if (!keys || !al4(keys) || !idx || !al4(idx) || !rank_lo || (reinterpret_cast<uintptr_t>(rank_lo) & 7u))
+        return CSA_ERR_INVALID_ARG;
+    if ((sel_local && !al4(sel_local)) || (idx_out && !al4(idx_out)) || (keys_out && !al4(keys_out)))
+        return CSA_ERR_INVALID_ARG;
+    if (sel_local && (rank < 0 || rank >= R)) return CSA_ERR_INVALID_ARG;
+    if (!workspace || ws_bytes < topk_merge_workspace_bytes(R, k) || !al16(workspace)) return CSA_ERR_WORKSPACE;
+    int32_t* st = status_ptr();
+    if (!st) return CSA_ERR_CUDA;
+    TopkMergeLaunch m;
+    m.keys = keys;
+    m.idx = idx;
+    m.rank_lo = rank_lo;
+    m.R = R;
+    m.k = k;
+    m.rank = sel_local ? rank : -1;
+    m.sel_local = sel_local;
+    m.idx_out = idx_out;
+    m.keys_out = keys_out;
+    m.ws = workspace;
+    m.status = st;
+    return from_cuda(launch_topk_merge(m, static_cast<cudaStream_t>(stream)));
+}
+
 // ------------------------------------------------------------------ fused decode
 struct DecodeLayout {
     size_t scores, hist, lists, sel, attn, total;

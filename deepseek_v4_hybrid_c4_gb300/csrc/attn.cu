@@ -68,6 +68,7 @@ struct AttnArgs {
     float2* part_ml;           // [B][2 halves][S][H] {max (log2 units), sum}
     uint16_t* out;
     float* lse;
+    float* out_f32;            // mergeable partial: fp32 [B][H][512] normalised rows instead of out
     int32_t* status;
     DWorkSet kws;              // HiSparse working set of the compressed pool (table == nullptr: none)
 };
@@ -282,7 +283,7 @@ __global__ void __launch_bounds__(AT_T, 1) attn_kernel(AttnArgs a) {
     // ---- this split's rows, normalised (fp16 partial, or the bf16 output when S == 1), into
     //      shared memory (every MMA has completed, so the Q/K tiles' space is free), then
     //      coalesced to global memory
-    const bool direct = S == 1;
+    const bool direct = S == 1 && !a.out_f32;
     if (t0 < t1) {
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
         const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + SM_TMEM);
@@ -394,7 +395,7 @@ __global__ void __launch_bounds__(AT_T, 1) attn64_kernel(AttnArgs a) {
     const int64_t t0 = (int64_t)split * a.tps;
     const int64_t t1 = t0 + a.tps < T ? t0 + a.tps : T;
     const int H = a.H, S = a.S;
-    const bool direct = S == 1;
+    const bool direct = S == 1 && !a.out_f32;
     const bool soft = tid < A6_H;  // warps 0, 1: head tid's softmax
     float m_run = -INFINITY, l_run = 0.f;
 
@@ -688,11 +689,53 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(AttnArgs a) {
         }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    uint2 r;
-    r.x = pack_bf16x2(o0 * inv, o1 * inv);
-    r.y = pack_bf16x2(o2 * inv, o3 * inv);
-    *reinterpret_cast<uint2*>(a.out + ((int64_t)b * H + h) * D + t * 4) = r;
+    if (a.out_f32) {  // a mergeable partial: fp32 rows (zero when no key was attended)
+        *reinterpret_cast<float4*>(a.out_f32 + ((int64_t)b * H + h) * D + t * 4) =
+            make_float4(o0 * inv, o1 * inv, o2 * inv, o3 * inv);
+    } else {
+        uint2 r;
+        r.x = pack_bf16x2(o0 * inv, o1 * inv);
+        r.y = pack_bf16x2(o2 * inv, o3 * inv);
+        *reinterpret_cast<uint2*>(a.out + ((int64_t)b * H + h) * D + t * 4) = r;
+    }
     if (t == 0 && a.lse) a.lse[(int64_t)b * H + h] = L > 0.f ? (M + log2f(L)) * LN2 : -INFINITY;
+}
+
+// Log-sum-exp merge of R partial attentions of the same heads over disjoint key sets (each a
+// normalised fp32 row O_r and its natural-log lse_r; lse_r = -inf for an empty set):
+//   L = sum_r e^(lse_r - M), O = sum_r e^(lse_r - M) O_r / L, lse = M + ln L,  M = max_r lse_r.
+// One CTA per head, thread t owns columns 4t .. 4t+3; the partials are read in rank order.
+__global__ void __launch_bounds__(128) attn_lse_merge_kernel(const float* o_parts, const float* lse_parts, int R, int H,
+                                                             uint16_t* out, float* lse) {
+    const int h = blockIdx.x, t = threadIdx.x;
+    float M = -INFINITY;
+    for (int r = 0; r < R; ++r) M = fmaxf(M, __ldg(lse_parts + (int64_t)r * H + h));
+    float L = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+    if (M > -INFINITY) {
+        for (int r = 0; r < R; ++r) {
+            const float lr = __ldg(lse_parts + (int64_t)r * H + h);
+            if (!(lr > -INFINITY)) continue;
+            const float w = expf(lr - M);
+            const float4 v = __ldg(reinterpret_cast<const float4*>(o_parts + ((int64_t)r * H + h) * D) + t);
+            L += w;
+            o0 = fmaf(w, v.x, o0);
+            o1 = fmaf(w, v.y, o1);
+            o2 = fmaf(w, v.z, o2);
+            o3 = fmaf(w, v.w, o3);
+        }
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    uint2 rr;
+    rr.x = pack_bf16x2(o0 * inv, o1 * inv);
+    rr.y = pack_bf16x2(o2 * inv, o3 * inv);
+    *reinterpret_cast<uint2*>(out + (int64_t)h * D + t * 4) = rr;
+    if (t == 0 && lse) lse[h] = L > 0.f ? M + logf(L) : -INFINITY;
+}
+
+cudaError_t launch_lse_merge(const float* o_parts, const float* lse_parts, int R, int H, void* out, float* lse,
+                             cudaStream_t s) {
+    attn_lse_merge_kernel<<<H, 128, 0, s>>>(o_parts, lse_parts, R, H, static_cast<uint16_t*>(out), lse);
+    return cudaGetLastError();
 }
 
 // Split heuristic (device independent so workspace sizes are stable): about one wave
@@ -754,6 +797,7 @@ cudaError_t launch_attn(const AttnLaunch& h, cudaStream_t s, bool pdl) {
     a.part_o = static_cast<__half*>(h.ws);
     a.part_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(h.ws) + ((po + 255) & ~size_t(255)));
     a.out = static_cast<uint16_t*>(h.out);
+    a.out_f32 = h.out_f32;
     a.lse = h.lse;
     a.status = h.status;
     a.kws.table = h.hs.table;
@@ -781,7 +825,7 @@ cudaError_t launch_attn(const AttnLaunch& h, cudaStream_t s, bool pdl) {
     cfg.dynamicSmemBytes = h64 ? A6_SMEM : AT_SMEM;
     cfg.stream = s;
     cudaError_t e = h64 ? cudaLaunchKernelEx(&cfg, attn64_kernel, a) : cudaLaunchKernelEx(&cfg, attn_kernel, a);
-    if (e != cudaSuccess || a.S == 1) return e;
+    if (e != cudaSuccess || (a.S == 1 && !a.out_f32)) return e;
     cfg.numAttrs = 1;  // the merge waits for the attention grid (griddepcontrol.wait)
     cfg.gridDim = dim3((unsigned)h.H, (unsigned)h.B, 1);
     cfg.blockDim = dim3(128, 1, 1);

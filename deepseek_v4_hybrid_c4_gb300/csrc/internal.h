@@ -157,6 +157,7 @@ struct AttnLaunch {
     int swa;
     void* out;                 // bf16 [B, H, 512]
     float* lse;                // [B, H] or nullptr
+    float* out_f32 = nullptr;  // instead of out: fp32 [B, H, 512] rows of a mergeable partial
     void* ws;
     size_t ws_bytes;
     int32_t* status;
@@ -165,5 +166,25 @@ size_t attn_workspace_bytes(int B, int H, int64_t max_keys);
 // this device's sticky status word (the kernels' status argument)
 int32_t* device_status_ptr();
 cudaError_t launch_attn(const AttnLaunch& a, cudaStream_t s, bool pdl);
+// Log-sum-exp merge of R partials (fp32 rows [R][H][512], natural-log lse [R][H]) into bf16
+// out [H][512] and lse [H] (nullable).
+cudaError_t launch_lse_merge(const float* o_parts, const float* lse_parts, int R, int H, void* out, float* lse,
+                             cudaStream_t s);
+// Context-parallel global top-k: the k best of R ranks' sorted local top-k lists (keys, indices
+// local to each rank's range), as global indices and as rows of one rank's range.
+struct TopkMergeLaunch {
+    const uint32_t* keys;      // [R * k]
+    const int32_t* idx;        // [R * k] indices local to rank p / k's range, < 0: padding
+    const int64_t* rank_lo;    // device [R + 1]: rank r holds global candidates [rank_lo[r], rank_lo[r+1])
+    int R, k;
+    int rank;                  // the rank whose rows sel_local lists (-1: none)
+    int32_t* sel_local;        // [k] or nullptr
+    int32_t* idx_out;          // [k] or nullptr
+    uint32_t* keys_out;        // [k] or nullptr
+    void* ws;
+    int32_t* status;
+};
+size_t topk_merge_workspace_bytes(int R, int k);
+cudaError_t launch_topk_merge(const TopkMergeLaunch& a, cudaStream_t s);
 
 }  // namespace csa

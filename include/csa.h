@@ -168,6 +168,59 @@ csa_status csa_sparse_attn(const void* q, int32_t H, float scale, csa_paged kv_c
 size_t csa_sparse_attn_workspace_size(int32_t H, int32_t n_sel, int32_t swa);
 
 /*
+ * Context-parallel split of one request ([Day-0] "3.1 长上下文预填充：Context Parallelism
+ * (CP)": the tokens are shared out over ranks and the indexer's results meet in one
+ * exchange).  Rank r holds the contiguous candidate range [lo_r, hi_r) of the request (its
+ * index keys and compressed rows), the last rank also the raw rows of the SWA window.  A
+ * decode step:
+ *   1. each rank: csa_index_score over its range, csa_topk of those scores with keys_out
+ *      (sorted; indices local to the range);
+ *   2. exchange: all-gather the R lists of k (key, index) pairs, in rank order;
+ *   3. each rank: csa_topk_merge -> the exact global top k (every rank gets the same set),
+ *      and the rows of it that the rank holds;
+ *   4. each rank: csa_sparse_attn_partial over those rows (the last rank adding the window);
+ *   5. exchange: gather the R partials; csa_attn_merge -> the step's output.
+ * The result equals the single-device step: the same selected set (bit-exact), the same
+ * attention within rounding.
+ */
+
+/*
+ * The exact top k of the union of R sorted local top-k lists.  keys uint32 [R * k] (from
+ * csa_topk's keys_out: order-preserving keys), idx int32 [R * k] (csa_topk's indices, local to
+ * each rank's range; < 0: padding), both rank-major.  rank_lo: device int64 [R + 1], rank r
+ * holding the global candidates [rank_lo[r], rank_lo[r+1]) (increasing ranges).  Output,
+ * each nullable: idx_out int32 [k] global indices by (score desc, index asc), -1 padding;
+ * keys_out uint32 [k]; sel_local int32 [k]: g - rank_lo[rank] for the selected g that rank
+ * `rank` holds, -1 for the others (the selection argument of csa_sparse_attn_partial on that
+ * rank).  workspace: csa_topk_merge_workspace_size(R, k) bytes.  R * k <= 4,194,304,
+ * k <= 2048.  An index outside its rank's range sets CSA_ERR_DEVICE_BOUNDS and is dropped.
+ */
+size_t csa_topk_merge_workspace_size(int32_t R, int32_t k);
+csa_status csa_topk_merge(const uint32_t* keys, const int32_t* idx, const int64_t* rank_lo, int32_t R, int32_t k,
+                          int32_t rank, int32_t* sel_local, int32_t* idx_out, uint32_t* keys_out, void* workspace,
+                          size_t ws_bytes, void* stream);
+
+/*
+ * Stage 4 over one rank's share of the keys, as a mergeable partial: the arguments of
+ * csa_sparse_attn, but the output is o_part fp32 [H, 512] (the normalised rows,
+ * softmax(l) . V over this share) and lse_part fp32 [H] (natural log of the share's sum of
+ * exp(l)).  An empty share (n_sel = 0 or only -1 entries, and no window) gives zero rows
+ * and lse = -inf.  Workspace: csa_sparse_attn_workspace_size(H, n_sel, swa).
+ */
+csa_status csa_sparse_attn_partial(const void* q, int32_t H, float scale, csa_paged kv_c, const int32_t* sel,
+                                   int32_t n_sel, csa_paged kv_raw, int64_t n_tokens, int32_t swa, float* o_part,
+                                   float* lse_part, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Log-sum-exp merge of R partials over disjoint key sets of the same heads: o_parts fp32
+ * [R, H, 512], lse_parts fp32 [R, H] -> out bf16 [H, 512] = sum_r e^(lse_r - M) O_r / L and
+ * lse fp32 [H] (nullable) = M + ln L, with M = max_r lse_r, L = sum_r e^(lse_r - M).
+ * Partials with lse = -inf contribute nothing; if all are empty, out = 0 and lse = -inf.
+ */
+csa_status csa_attn_merge(const float* o_parts, const float* lse_parts, int32_t R, int32_t H, void* out, float* lse,
+                          void* stream);
+
+/*
  * The fused decode step over a ragged batch of B requests ([V4-deploy] "V4 到底改了啥",
  * "Kernel 層一堆狠活"; [Day-0] "创新 2").  Per request b, with N = n_tokens[b],
  * G = N / ratio, done = n_groups_done[b]:
