@@ -133,6 +133,37 @@ def oracle_step_times(case, n_min, budget_s):
     return times
 
 
+def oracle_stage_times(case, reps=3):
+    """The oracle's stages on the workload's request, each timed alone (median of `reps`):
+    compress the pending groups, score every candidate, select by full sort and by selection
+    (partition to rank k, then sort the k), attend the selected rows plus the window."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    r = case.requests[0]
+    G = r.n_tokens // case.ratio
+    fp8 = case.kdtype == "fp8"
+
+    def med(fn):
+        ts = []
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            v = fn()
+            ts.append(time.perf_counter() - t0)
+        return statistics.median(ts) * 1e6, v
+
+    t_comp, _ = med(lambda: oracle.compress(r.raw, case.ratio, case.w_gate, case.b_pos, r.n_groups_done,
+                                            G - r.n_groups_done))
+    t_score, scores = med(lambda: oracle.index_score(r.q_idx, r.w_h, r.kidx, fp8))
+    t_sort, sel = med(lambda: oracle.topk(scores, case.k))
+    t_nth, sel2 = med(lambda: oracle.topk_select(scores, case.k))
+    assert np.array_equal(sel, sel2)
+    rows = np.concatenate([r.cpool[sel[sel >= 0]], r.raw[r.n_tokens - min(case.swa, r.n_tokens):]])
+    t_attn, _ = med(lambda: oracle.attention(r.q, case.scale, rows))
+    return {"compress": round(t_comp, 1), "score": round(t_score, 1), "select_full_sort": round(t_sort, 1),
+            "select_partition_then_sort": round(t_nth, 1), "attention": round(t_attn, 1)}
+
+
 def run_reference(args, rank):
     """--impl reference: the CPU oracle on the host cores, rank 0 only."""
     if rank != 0:
@@ -159,6 +190,7 @@ def other_workloads(torch, csa, entry, synth, stream, flush_l2, peak):
     the ragged fp8 batch and the C128 dense batch as decode steps; the prefill compressors
     (C128 over 8 x 524,288 tokens, C4 over 1,048,576) as bandwidth.  Each step or call is timed
     alone between CUDA events after an L2 flush (write then read); medians over the runs."""
+    import numpy as np
     res = {}
 
     def timed(fn, n, flush=True):
@@ -235,7 +267,8 @@ def other_workloads(torch, csa, entry, synth, stream, flush_l2, peak):
     del b2, cout, scores
     torch.cuda.empty_cache()
     # ---- decode steps of the ragged fp8 batch and of the C128 dense batch
-    for cfg, name in [(3, "ragged32_fp8_decode"), (4, "c128_dense_bs8_decode")]:
+    for cfg, name in [(0, "tiny_4K_decode"), (1, "c4_128K_decode"), (3, "ragged32_fp8_decode"),
+                      (4, "c128_dense_bs8_decode")]:
         case = synth.config(cfg)
         b = entry.case_to_batch(case)
         with torch.cuda.stream(stream):
@@ -289,6 +322,67 @@ def other_workloads(torch, csa, entry, synth, stream, flush_l2, peak):
         "note": "every position streams the index keys itself (the score is bound by its fixed-order fma "
                 "rate, not by the stream)"}
     del g, b
+    torch.cuda.empty_cache()
+    # ---- context-parallel split of the 1M request into 4 contiguous shards, on this one GPU: the
+    #      stages of the rank holding the last shard (which also attends the window), with the
+    #      exchanged lists and partials already in place, and the full 4-shard step run in turn
+    from deepseek_v4_hybrid_c4_gb300 import cp as cpm
+    case = synth.config(2)
+    r = case.requests[0]
+    G = r.n_tokens // case.ratio
+    R = 4
+    ranges = cpm.contiguous_ranges(G, R)
+    rank_lo = torch.tensor(ranges, dtype=torch.int64, device="cuda")
+    kidx_d = torch.from_numpy(np.ascontiguousarray(r.kidx).view(np.int16)).cuda()
+    cpool_d = torch.from_numpy(np.ascontiguousarray(r.cpool).view(np.int16)).cuda()
+    raw_d = torch.from_numpy(np.ascontiguousarray(r.raw).view(np.int16)).cuda()
+    shards = []
+    for q_ in range(R):
+        lo, hi = ranges[q_], ranges[q_ + 1]
+        shards.append(cpm.CPShard(
+            rank=q_, world=R, rank_lo=rank_lo, lo=lo, hi=hi,
+            kidx=csa.paged(kidx_d[lo:hi], 16, 256, n_pages=(hi - lo + 15) // 16),
+            kv_c=csa.paged(cpool_d[lo:hi], 16, 1024, n_pages=(hi - lo + 15) // 16),
+            kv_raw=csa.paged(raw_d, 64, 1024, n_pages=r.n_tokens // 64) if q_ == R - 1 else None,
+            n_tokens=r.n_tokens, H=case.H, Hi=case.Hi, k=case.k, swa=case.swa, scale=case.scale))
+    qd = torch.from_numpy(np.ascontiguousarray(r.q).view(np.int16)).cuda()
+    qid = torch.from_numpy(np.ascontiguousarray(r.q_idx).view(np.int16)).cuda()
+    whd = torch.from_numpy(r.w_h.astype(np.float32)).cuda()
+    be = cpm.LibcsaBackend()
+    out_d = torch.empty((case.H, 512), dtype=torch.int16, device="cuda")
+    lse_d = torch.empty(case.H, dtype=torch.float32, device="cuda")
+    with torch.cuda.stream(stream):
+        cpm.run_local(shards, qd, qid, whd, be, out_d, lse_d, stream.cuda_stream)
+        lists = [be.local_topk(sh, qid, whd, stream.cuda_stream) for sh in shards]
+        keys_all = torch.cat([k_ for k_, _ in lists])
+        idx_all = torch.cat([i_ for _, i_ in lists])
+        parts = [be.attn_partial(sh, qd, stream.cuda_stream) for sh in shards]
+        o_all = torch.cat([o_ for o_, _ in parts])
+        l_all = torch.cat([l_ for _, l_ in parts])
+    torch.cuda.synchronize()
+    last = shards[-1]
+
+    def one_rank():  # the last rank's stages, the exchanged tensors in place
+        be.local_topk(last, qid, whd, stream.cuda_stream)
+        be.global_select(last, keys_all, idx_all, stream.cuda_stream)
+        be.attn_partial(last, qd, stream.cuda_stream)
+        be.merge(o_all, l_all, R, case.H, out_d, lse_d, stream.cuda_stream)
+
+    g_rank, g_all = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()  # no host launch cost in the timing
+    with torch.cuda.graph(g_rank, stream=stream):
+        one_rank()
+    with torch.cuda.graph(g_all, stream=stream):
+        cpm.run_local(shards, qd, qid, whd, be, out_d, lse_d, stream.cuda_stream)
+    t_rank, t_rank90 = timed(g_rank.replay, 30)
+    t_all, _ = timed(g_all.replay, 10)
+    assert csa.csa_read_device_status(stream) == 0
+    res["cp_split_1M_4_shards_one_gpu"] = {
+        "us_one_rank_stages": round(t_rank, 2), "us_p90_one_rank_stages": round(t_rank90, 2),
+        "us_all_4_shards_in_turn": round(t_all, 2), "shards": R, "candidates_per_shard": ranges[1] - ranges[0],
+        "note": "one GPU, CUDA graphs: a rank's own work (score and top-k of its shard, global merge, partial "
+                "attention with the window, final merge) with the exchanged lists and partials in place, and the "
+                "4 shards' stages in turn; the all-gathers between GPUs are not measured (one GPU per box)"}
+    del g_rank, g_all, shards, kidx_d, cpool_d, raw_d, o_all, l_all, keys_all, idx_all, parts, lists
     torch.cuda.empty_cache()
     # ---- HiSparse at 1M context: the C4 pool (256 MiB) as a pinned host mirror with a GPU working
     #      set of a quarter of its pages.  Cold: every selected row comes from the mirror; warm:
@@ -592,7 +686,8 @@ def main():
         line["cpu_baseline"] = {"value": round(statistics.median(times) * 1e6, 1), "unit": "µs/layer-step",
                                 "cores": 1, "kind": "oracle",
                                 "sample": f"{len(times)} full decode steps of the same 1M workload (median); "
-                                          f"host nproc={os.cpu_count()}"}
+                                          f"host nproc={os.cpu_count()}",
+                                "stages_us": oracle_stage_times(case)}
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()

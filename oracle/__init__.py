@@ -55,6 +55,8 @@ def _L():
         lib.orc_index_score.restype = None
         lib.orc_topk.argtypes = [vp, i64, i32, vp, vp]
         lib.orc_topk.restype = i32
+        lib.orc_topk_select.argtypes = [vp, i64, i32, vp, vp]
+        lib.orc_topk_select.restype = i32
         lib.orc_attention.argtypes = [vp, i32, f32, vp, i64, vp, vp, vp]
         lib.orc_attention.restype = None
         lib.orc_sparse_attn.argtypes = [vp, i32, f32, vp, i64, vp, i32, vp, i64, i32, vp, vp, vp]
@@ -139,6 +141,17 @@ def topk(scores, k: int, want_keys: bool = False):
     rc = _L().orc_topk(_p(s), s.shape[0], k, _p(idx), _p(keys))
     if rc:
         raise ValueError(f"orc_topk rc={rc}")
+    return (idx, keys) if want_keys else idx
+
+
+def topk_select(scores, k: int, want_keys: bool = False):
+    """topk by selection (partition to rank k, then sort only the k): the same result."""
+    s = _c(scores, np.float32)
+    idx = np.zeros(k, dtype=np.int32)
+    keys = np.zeros(k, dtype=np.uint32) if want_keys else None
+    rc = _L().orc_topk_select(_p(s), s.shape[0], k, _p(idx), _p(keys))
+    if rc:
+        raise ValueError(f"orc_topk_select rc={rc}")
     return (idx, keys) if want_keys else idx
 
 

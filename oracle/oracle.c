@@ -203,6 +203,66 @@ static int orc_kv_cmp(const void* a, const void* b) {
     return (x->idx > y->idx) - (x->idx < y->idx);
 }
 
+static void orc_kv_swap(orc_kv* x, orc_kv* y) {
+    const orc_kv t = *x;
+    *x = *y;
+    *y = t;
+}
+
+/* Rearrange a[0..n) so that a[m] holds the element a full sort would put there, everything
+ * before it precedes it in the order and everything after follows it (selection by
+ * repeated partitioning, pivot = median of the first, middle and last element).  The keys
+ * are distinct under the total order, so the partition is well defined. */
+static void orc_select_nth(orc_kv* a, int64_t n, int64_t m) {
+    int64_t lo = 0, hi = n - 1;
+    while (lo < hi) {
+        const int64_t mid = lo + (hi - lo) / 2;
+        if (orc_kv_cmp(&a[mid], &a[lo]) < 0) orc_kv_swap(&a[mid], &a[lo]);
+        if (orc_kv_cmp(&a[hi], &a[lo]) < 0) orc_kv_swap(&a[hi], &a[lo]);
+        if (orc_kv_cmp(&a[hi], &a[mid]) < 0) orc_kv_swap(&a[hi], &a[mid]);
+        const orc_kv p = a[mid];
+        int64_t i = lo, j = hi;
+        while (i <= j) {
+            while (orc_kv_cmp(&a[i], &p) < 0) ++i;
+            while (orc_kv_cmp(&p, &a[j]) < 0) --j;
+            if (i <= j) {
+                orc_kv_swap(&a[i], &a[j]);
+                ++i;
+                --j;
+            }
+        }
+        if (m <= j)
+            hi = j;
+        else if (m >= i)
+            lo = i;
+        else
+            break; /* a[m] equals the pivot: in place */
+    }
+}
+
+/* Top-k as in orc_topk, by selection: the k first elements by the same total order are
+ * moved to the front (orc_select_nth on rank k - 1), and only those k are sorted.  The
+ * result is the same (the order is total, so the k best and their order are unique); it is
+ * the second CPU method the timing reports. */
+int orc_topk_select(const float* scores, int64_t G, int k, int32_t* idx_out, uint32_t* keys_out) {
+    if (G < 0 || k < 0) return 1;
+    orc_kv* a = (orc_kv*)malloc(sizeof(orc_kv) * (size_t)(G > 0 ? G : 1));
+    if (!a) return 2;
+    for (int64_t g = 0; g < G; ++g) {
+        a[g].key = orc_score_key(scores[g]);
+        a[g].idx = (int32_t)g;
+    }
+    const int64_t m = k < G ? k : G;
+    if (m > 0 && m < G) orc_select_nth(a, G, m - 1);
+    qsort(a, (size_t)m, sizeof(orc_kv), orc_kv_cmp);
+    for (int i = 0; i < k; ++i) {
+        idx_out[i] = i < G ? a[i].idx : -1;
+        if (keys_out) keys_out[i] = i < G ? a[i].key : 0u;
+    }
+    free(a);
+    return 0;
+}
+
 int orc_topk(const float* scores, int64_t G, int k, int32_t* idx_out, uint32_t* keys_out) {
     if (G < 0 || k < 0) return 1;
     orc_kv* a = (orc_kv*)malloc(sizeof(orc_kv) * (size_t)(G > 0 ? G : 1));

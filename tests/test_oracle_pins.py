@@ -278,6 +278,18 @@ def test_topk_equals_brute_force_with_ties(G, k):
     assert oracle.topk(s, k).tolist() == _brute_topk(s, k)
 
 
+@pytest.mark.parametrize("G,k", [(1, 4), (7, 16), (64, 8), (64, 64), (200, 17), (1000, 512), (20000, 512)])
+def test_topk_by_selection_equals_brute_force(G, k):
+    """The selection form (partition to rank k, sort the k) against the brute-force order."""
+    rng = np.random.default_rng(G * 7 + k)
+    vals = np.array([0.0, -0.0, 1.5, -2.0, np.inf, -np.inf, 3.25], np.float32)
+    s = np.where(rng.random(G) < 0.5, vals[rng.integers(0, len(vals), G)], rng.standard_normal(G).astype(np.float32))
+    idx, keys = oracle.topk_select(s, k, want_keys=True)
+    assert idx.tolist() == _brute_topk(s, k)
+    assert np.array_equal(keys[: min(k, G)], np.array([oracle.score_key(s[g]) for g in idx[: min(k, G)]], np.uint32))
+    assert (keys[min(k, G):] == 0).all()
+
+
 def test_topk_all_equal_and_k_ge_G():
     s = np.full(50, 2.0, np.float32)
     assert oracle.topk(s, 10).tolist() == list(range(10))
