@@ -408,11 +408,52 @@ def other_workloads(torch, csa, entry, synth, stream, flush_l2, peak):
     t_upd = (time.perf_counter() - t0) * 1e6
     t_warm, _ = timed(g.replay, 30)  # the graph reads the residency table, so it now hits
     assert csa.csa_read_device_status(stream) == 0
+    # the asynchronous coordinator in a decode loop: after each step its stamps are collected and
+    # the swap of the previous step's misses is applied (evictions on the decode stream, copies on a
+    # side stream).  Two query sets alternate, so every step selects pages the previous one did not.
+    # Each loop is host-driven (eager steps); the coordinator's cost is the loop's time per step
+    # against the same loop without it.
+    side = torch.cuda.Stream()
+    n_tok = np.array([rq.n_tokens for rq in case.requests], np.int64)
+    q_alt = [b.q.clone(), torch.from_numpy(synth.normal_bf16((1, case.H, 512), case.seed, 410).view(np.int16)).cuda()]
+    qi_alt = [b.q_idx.clone(),
+              torch.from_numpy(synth.normal_bf16((1, case.Hi, 128), case.seed, 411).view(np.int16)).cuda()]
+    step_no = [10]
+
+    def loop(T, coord):
+        moved = 0
+        with torch.cuda.stream(stream):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for t in range(T):
+                b.q.copy_(q_alt[t % 2])
+                b.q_idx.copy_(qi_alt[t % 2])
+                step_no[0] += 1
+                b.hs_step = step_no[0]
+                b.run(stream)
+                if coord:
+                    if t > 0:
+                        moved += b.hs_apply(n_tok, stream, side)[0]
+                    b.hs_collect(stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / T, moved
+
+    loop(6, True)
+    t_plain, _ = loop(60, False)
+    t_coord, moved = loop(60, True)
+    assert csa.csa_read_device_status(stream) == 0
     res["hisparse_1M_quarter_working_set"] = {
         "us_per_step_cold": round(t_cold, 2), "us_per_step_warm": round(t_warm, 2),
         "us_update_host_wall": round(t_upd, 1), "pages_brought_in": int(n_in), "pages_evicted": int(n_ev),
         "working_set_pages": int(slots), "mirror_pages": int(case.n_pages), "page_bytes": c_rpp * 1024,
-        "note": "cold: the 512 selected rows are read from pinned host memory over NVLink-C2C"}
+        "async_loop_us_per_step_with_coordinator": round(t_coord, 2),
+        "async_loop_us_per_step_without": round(t_plain, 2),
+        "async_coordinator_us_per_step": round(t_coord - t_plain, 2),
+        "async_pages_moved_per_step": round(moved / 59, 1),
+        "note": "cold: the 512 selected rows are read from pinned host memory over NVLink-C2C; async loop: "
+                "eager (host-driven) steps alternating two query sets, collect after each step, apply after "
+                "the next is enqueued"}
     del g, b
     torch.cuda.empty_cache()
     assert csa.csa_read_device_status(stream) == 0

@@ -92,12 +92,16 @@ def lib() -> ctypes.CDLL:
         L.csa_hisparse_plan.argtypes = [vp, vp, ctypes.c_uint32, vp, i64, ctypes.POINTER(i64), ctypes.POINTER(i64)]
         L.csa_hisparse_table.argtypes = [vp]
         L.csa_hisparse_table.restype = ctypes.POINTER(ctypes.c_int32)
+        L.csa_hisparse_collect.argtypes = [vp, ctypes.POINTER(csa_decode_params), vp]
+        L.csa_hisparse_apply.argtypes = [vp, ctypes.POINTER(csa_decode_params), vp, vp, vp, ctypes.POINTER(i64),
+                                         ctypes.POINTER(i64)]
         L.csa_hisparse_update.argtypes = [vp, ctypes.POINTER(csa_decode_params), vp, ctypes.POINTER(i64),
                                           ctypes.POINTER(i64)]
         for name in ("csa_compress", "csa_index_score", "csa_topk", "csa_topk_batched", "csa_topk_cluster",
                      "csa_topk_merge", "csa_sparse_attn_partial", "csa_attn_merge", "csa_sparse_attn",
                      "csa_decode", "csa_decode_timed", "csa_decode_noalloc", "csa_read_device_status",
-                     "csa_hisparse_create", "csa_hisparse_plan", "csa_hisparse_update", "csa_selftest_bounded_wait"):
+                     "csa_hisparse_create", "csa_hisparse_plan", "csa_hisparse_update", "csa_hisparse_collect",
+                     "csa_hisparse_apply", "csa_selftest_bounded_wait"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -275,6 +279,22 @@ def csa_hisparse_update(h: int, p: csa_decode_params, stream=None):
     n_in, n_ev = ctypes.c_int64(0), ctypes.c_int64(0)
     _check(lib().csa_hisparse_update(h, ctypes.byref(p), _stream(stream), ctypes.byref(n_in), ctypes.byref(n_ev)),
            "csa_hisparse_update")
+    return n_in.value, n_ev.value
+
+
+def csa_hisparse_collect(h: int, p: csa_decode_params, stream=None) -> None:
+    """After a decode step: enqueue the readback of its page stamps (no wait)."""
+    _check(lib().csa_hisparse_collect(h, ctypes.byref(p), _stream(stream)), "csa_hisparse_collect")
+
+
+def csa_hisparse_apply(h: int, p: csa_decode_params, n_tokens_host, stream=None, side_stream=None):
+    """Plan from the collected stamps; evictions on `stream`, the swap on `side_stream`
+    (n_tokens_host: numpy int64 [B], the token counts of the last enqueued step) -> (n_in, n_evicted)."""
+    import numpy as np
+    nt = np.ascontiguousarray(n_tokens_host, dtype=np.int64)
+    n_in, n_ev = ctypes.c_int64(0), ctypes.c_int64(0)
+    _check(lib().csa_hisparse_apply(h, ctypes.byref(p), nt.ctypes.data, _stream(stream), _stream(side_stream),
+                                    ctypes.byref(n_in), ctypes.byref(n_ev)), "csa_hisparse_apply")
     return n_in.value, n_ev.value
 
 

@@ -9,6 +9,9 @@
 // the step stamps every page it read.  Between steps the coordinator reads the stamps back,
 // decides on the host which pages to bring in (LRU over the slots), and one gather kernel copies
 // those pages from the mirror into their slots; the new residency table follows on the stream.
+// The asynchronous form (collect, then apply one or more steps later) keeps the host and the
+// swap off the decode stream: the evictions are published on it, the copies and the installs
+// run on a side stream beside the next steps.
 #include <algorithm>
 #include <cstring>
 #include <new>
@@ -27,6 +30,17 @@ struct csa_hisparse {
     std::vector<uint32_t> touch;    // host copy of the step's stamps
     std::vector<int32_t> plan;      // host copy of the last plan (request, logical page, slot)
     int32_t* d_plan = nullptr;      // device copy, n_slots triples
+    // asynchronous form (csa_hisparse_collect / csa_hisparse_apply): pinned host buffers and events
+    uint32_t* h_touch = nullptr;    // [B * stride] stamps read back by collect
+    uint32_t collected_step = 0;    // the step those stamps belong to
+    bool collected = false;
+    int32_t* h_table_evict = nullptr;    // [B * stride] the table with this plan's evictions only
+    int32_t* h_table_install = nullptr;  // [B * stride] the table with the plan's pages installed
+    int32_t* h_plan = nullptr;           // [3 * n_slots] the plan, for its upload
+    cudaEvent_t ev_touch = nullptr;      // the stamps have landed in h_touch
+    cudaEvent_t ev_evict = nullptr;      // the evictions are in the device table (decode stream)
+    cudaEvent_t ev_swap = nullptr;       // the last apply's swap and installs are done (side stream)
+    bool swap_pending = false;
 };
 
 namespace csa {
@@ -72,19 +86,39 @@ csa_status csa_hisparse_create(int32_t B, int64_t table_stride, int64_t n_slots,
 
 void csa_hisparse_destroy(csa_hisparse* h) {
     if (!h) return;
+    if (h->swap_pending) cudaEventSynchronize(h->ev_swap);
     cudaFree(h->d_plan);
+    cudaFreeHost(h->h_touch);
+    cudaFreeHost(h->h_table_evict);
+    cudaFreeHost(h->h_table_install);
+    cudaFreeHost(h->h_plan);
+    if (h->ev_touch) cudaEventDestroy(h->ev_touch);
+    if (h->ev_evict) cudaEventDestroy(h->ev_evict);
+    if (h->ev_swap) cudaEventDestroy(h->ev_swap);
     delete h;
 }
 
 const int32_t* csa_hisparse_table(const csa_hisparse* h) { return h ? h->table.data() : nullptr; }
 
-csa_status csa_hisparse_plan(csa_hisparse* h, const uint32_t* touch, uint32_t step, int32_t* plan, int64_t max_plan,
-                             int64_t* n_in, int64_t* n_evicted) {
-    if (!h || !touch || (max_plan > 0 && !plan) || max_plan < 0) return CSA_ERR_INVALID_ARG;
+// The LRU plan (see csa_hisparse_plan).  With grow_from (nullable), page lp of request b is
+// never brought in when lp >= grow_from[b]: a page that can still receive compressed rows.
+static csa_status plan_impl(csa_hisparse* h, const uint32_t* touch, uint32_t step, int32_t* plan, int64_t max_plan,
+                            int64_t* n_in, int64_t* n_evicted, const int64_t* grow_from) {
     const int64_t n = (int64_t)h->B * h->stride;
     // the step's resident pages are refreshed first, so that none of them is evicted below
-    for (int64_t e = 0; e < n; ++e)
-        if (touch[e] == step && h->table[e] >= 0) h->stamp[h->table[e]] = step;
+    bool missed = false;
+    for (int64_t e = 0; e < n; ++e) {
+        if (touch[e] != step) continue;
+        if (h->table[e] >= 0)
+            h->stamp[h->table[e]] = step;
+        else if (!grow_from || e % h->stride < grow_from[e / h->stride])
+            missed = true;
+    }
+    if (!missed || max_plan == 0) {  // every page the step read is resident (or may not come in)
+        if (n_in) *n_in = 0;
+        if (n_evicted) *n_evicted = 0;
+        return CSA_OK;
+    }
     // candidates: free slots in order, then resident slots by (stamp, slot), never this step's
     std::vector<int64_t> cand;
     cand.reserve((size_t)h->n_slots);
@@ -100,6 +134,7 @@ csa_status csa_hisparse_plan(csa_hisparse* h, const uint32_t* touch, uint32_t st
     size_t next = 0;
     for (int64_t e = 0; e < n && taken < max_plan; ++e) {
         if (touch[e] != step || h->table[e] >= 0) continue;
+        if (grow_from && e % h->stride >= grow_from[e / h->stride]) continue;
         if (next >= cand.size()) break;  // every slot holds a page of this step
         const int64_t s = cand[next++];
         if (h->owner[s] >= 0) {
@@ -119,6 +154,12 @@ csa_status csa_hisparse_plan(csa_hisparse* h, const uint32_t* touch, uint32_t st
     return CSA_OK;
 }
 
+csa_status csa_hisparse_plan(csa_hisparse* h, const uint32_t* touch, uint32_t step, int32_t* plan, int64_t max_plan,
+                             int64_t* n_in, int64_t* n_evicted) {
+    if (!h || !touch || (max_plan > 0 && !plan) || max_plan < 0) return CSA_ERR_INVALID_ARG;
+    return plan_impl(h, touch, step, plan, max_plan, n_in, n_evicted, nullptr);
+}
+
 csa_status csa_hisparse_update(csa_hisparse* h, const csa_decode_params* p, void* stream, int64_t* n_in,
                                int64_t* n_evicted) {
     if (!h || !p || !p->hs_ws_pool || !p->hs_ws_table || !p->hs_touch || !p->c_page_table || !p->kv_c)
@@ -126,6 +167,10 @@ csa_status csa_hisparse_update(csa_hisparse* h, const csa_decode_params* p, void
     if (p->B != h->B || p->c_page_table_stride != h->stride || p->hs_n_slots != h->n_slots) return CSA_ERR_INVALID_ARG;
     int32_t* st = device_status_ptr();
     if (!st) return CSA_ERR_CUDA;
+    if (h->swap_pending) {  // an asynchronous apply's uploads read the coordinator's buffers
+        if (cudaEventSynchronize(h->ev_swap) != cudaSuccess) return CSA_ERR_CUDA;
+        h->swap_pending = false;
+    }
     if (!h->d_plan && cudaMalloc(&h->d_plan, (size_t)h->n_slots * 3 * sizeof(int32_t)) != cudaSuccess)
         return CSA_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -151,6 +196,103 @@ csa_status csa_hisparse_update(csa_hisparse* h, const csa_decode_params* p, void
     }
     if (n_in) *n_in = taken;
     if (n_evicted) *n_evicted = ev;
+    return CSA_OK;
+}
+
+// The pinned buffers and events of the asynchronous form, made on first use.
+static csa_status async_setup(csa_hisparse* h) {
+    if (h->h_touch) return CSA_OK;
+    const size_t n = (size_t)h->B * h->stride;
+    if (!h->d_plan && cudaMalloc(&h->d_plan, (size_t)h->n_slots * 3 * sizeof(int32_t)) != cudaSuccess)
+        return CSA_ERR_CUDA;
+    if (cudaHostAlloc(&h->h_touch, n * sizeof(uint32_t), cudaHostAllocDefault) != cudaSuccess ||
+        cudaHostAlloc(&h->h_table_evict, n * sizeof(int32_t), cudaHostAllocDefault) != cudaSuccess ||
+        cudaHostAlloc(&h->h_table_install, n * sizeof(int32_t), cudaHostAllocDefault) != cudaSuccess ||
+        cudaHostAlloc(&h->h_plan, (size_t)h->n_slots * 3 * sizeof(int32_t), cudaHostAllocDefault) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->ev_touch, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->ev_evict, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->ev_swap, cudaEventDisableTiming) != cudaSuccess)
+        return CSA_ERR_CUDA;
+    return CSA_OK;
+}
+
+static csa_status check_update_args(const csa_hisparse* h, const csa_decode_params* p) {
+    if (!h || !p || !p->hs_ws_pool || !p->hs_ws_table || !p->hs_touch || !p->c_page_table || !p->kv_c)
+        return CSA_ERR_INVALID_ARG;
+    if (p->B != h->B || p->c_page_table_stride != h->stride || p->hs_n_slots != h->n_slots) return CSA_ERR_INVALID_ARG;
+    return CSA_OK;
+}
+
+csa_status csa_hisparse_collect(csa_hisparse* h, const csa_decode_params* p, void* stream) {
+    csa_status rc = check_update_args(h, p);
+    if (rc) return rc;
+    if ((rc = async_setup(h))) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t n = (size_t)h->B * h->stride;
+    // a collect after an unapplied one replaces it: its event is recorded again below
+    if (cudaMemcpyAsync(h->h_touch, p->hs_touch, n * sizeof(uint32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaEventRecord(h->ev_touch, s) != cudaSuccess)
+        return CSA_ERR_CUDA;
+    h->collected_step = p->hs_step;
+    h->collected = true;
+    return CSA_OK;
+}
+
+csa_status csa_hisparse_apply(csa_hisparse* h, const csa_decode_params* p, const int64_t* n_tokens_host,
+                              void* stream, void* side_stream, int64_t* n_in, int64_t* n_evicted) {
+    csa_status rc = check_update_args(h, p);
+    if (rc) return rc;
+    if (!h->collected || !n_tokens_host || p->ratio < 1 || p->c_rows_per_page < 1) return CSA_ERR_INVALID_ARG;
+    int32_t* st = device_status_ptr();
+    if (!st) return CSA_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream), side = static_cast<cudaStream_t>(side_stream);
+    const size_t n = (size_t)h->B * h->stride;
+    // the stamps (usually landed long ago) and the previous apply's uploads, which read the
+    // pinned buffers rewritten below
+    if (cudaEventSynchronize(h->ev_touch) != cudaSuccess) return CSA_ERR_CUDA;
+    if (h->swap_pending && cudaEventSynchronize(h->ev_swap) != cudaSuccess) return CSA_ERR_CUDA;
+    h->swap_pending = false;
+    h->collected = false;
+    h->plan.resize((size_t)h->n_slots * 3);
+    // the page holding each request's newest compressed row (and any later one) can still be
+    // written by the steps this swap overlaps: it stays in the mirror
+    std::vector<int64_t> grow((size_t)h->B);
+    for (int32_t b = 0; b < h->B; ++b) {
+        const int64_t G = n_tokens_host[b] / p->ratio;
+        grow[(size_t)b] = G > 0 ? (G - 1) / p->c_rows_per_page : 0;
+    }
+    int64_t taken = 0, ev = 0;
+    rc = plan_impl(h, h->h_touch, h->collected_step, h->plan.data(), h->n_slots, &taken, &ev, grow.data());
+    if (rc) return rc;
+    if (n_in) *n_in = taken;
+    if (n_evicted) *n_evicted = ev;
+    if (taken == 0) return CSA_OK;
+    // 1. evictions first, on the decode stream: steps enqueued after this read those pages from
+    //    the mirror, so no step reads a slot while it is refilled
+    std::memcpy(h->h_table_install, h->table.data(), n * sizeof(int32_t));
+    std::memcpy(h->h_table_evict, h->table.data(), n * sizeof(int32_t));
+    for (int64_t i = 0; i < taken; ++i)  // the incoming pages stay in the mirror until installed
+        h->h_table_evict[(int64_t)h->plan[3 * i] * h->stride + h->plan[3 * i + 1]] = -1;
+    std::memcpy(h->h_plan, h->plan.data(), (size_t)taken * 3 * sizeof(int32_t));
+    if (cudaMemcpyAsync(p->hs_ws_table, h->h_table_evict, n * sizeof(int32_t), cudaMemcpyHostToDevice, s) !=
+            cudaSuccess ||
+        cudaEventRecord(h->ev_evict, s) != cudaSuccess)
+        return CSA_ERR_CUDA;
+    // 2. on the side stream, overlapping the next steps: the pages into their slots, then the
+    //    installed table (an entry only ever goes from -1 to a slot whose bytes are in place)
+    if (cudaStreamWaitEvent(side, h->ev_evict, 0) != cudaSuccess ||
+        cudaMemcpyAsync(h->d_plan, h->h_plan, (size_t)taken * 3 * sizeof(int32_t), cudaMemcpyHostToDevice, side) !=
+            cudaSuccess)
+        return CSA_ERR_CUDA;
+    hisparse_swap_kernel<<<(unsigned)taken, 256, 0, side>>>(h->d_plan, static_cast<const uint8_t*>(p->kv_c),
+                                                            p->c_page_table, p->c_page_table_stride, p->c_n_pages,
+                                                            p->c_page_stride, static_cast<uint8_t*>(p->hs_ws_pool), st);
+    if (cudaGetLastError() != cudaSuccess) return CSA_ERR_CUDA;
+    if (cudaMemcpyAsync(p->hs_ws_table, h->h_table_install, n * sizeof(int32_t), cudaMemcpyHostToDevice, side) !=
+            cudaSuccess ||
+        cudaEventRecord(h->ev_swap, side) != cudaSuccess)
+        return CSA_ERR_CUDA;
+    h->swap_pending = true;
     return CSA_OK;
 }
 

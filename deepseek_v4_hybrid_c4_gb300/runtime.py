@@ -201,6 +201,16 @@ class DecodeBatch:
         from . import csa_hisparse_update
         return csa_hisparse_update(self.hs, self.params, stream)
 
+    def hs_collect(self, stream=None):
+        """After a step: enqueue the readback of its stamps (no wait)."""
+        from . import csa_hisparse_collect
+        csa_hisparse_collect(self.hs, self.params, stream)
+
+    def hs_apply(self, n_tokens_host, stream=None, side_stream=None):
+        """Bring in the pages the collected step missed, beside the next steps -> (n_in, n_evicted)."""
+        from . import csa_hisparse_apply
+        return csa_hisparse_apply(self.hs, self.params, n_tokens_host, stream, side_stream)
+
     def __del__(self):
         if getattr(self, "hs", None):
             from . import csa_hisparse_destroy

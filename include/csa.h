@@ -365,8 +365,8 @@ csa_status csa_selftest_bounded_wait(void* stream);
  * HiSparse coordinator ([V4-deploy] "HiSparse": a coordinator swaps pages every step and evicts
  * by LRU; [Day-0] "创新 3": a GPU miss is swapped in from the CPU mirror).  A host object holding
  * the working set's bookkeeping: which (request, logical page) each slot holds and the last step
- * that read it.  Its first csa_hisparse_update allocates a device buffer of 12 * n_slots bytes
- * for the swap plans, freed by csa_hisparse_destroy; nothing else is allocated.
+ * that read it.  Its first csa_hisparse_update (or csa_hisparse_collect) allocates a device
+ * buffer of 12 * n_slots bytes for the swap plans, freed by csa_hisparse_destroy.
  */
 typedef struct csa_hisparse csa_hisparse;
 csa_status csa_hisparse_create(int32_t B, int64_t table_stride, int64_t n_slots, csa_hisparse** out);
@@ -387,6 +387,25 @@ const int32_t* csa_hisparse_table(const csa_hisparse* h);
  * p->hs_ws_table.  The next step on the stream sees the new working set. */
 csa_status csa_hisparse_update(csa_hisparse* h, const csa_decode_params* p, void* stream, int64_t* n_in,
                                int64_t* n_evicted);
+/* The same update without stalling the decode stream, in two calls.
+ * csa_hisparse_collect, after a decode step with p on `stream`: enqueues the readback of
+ *   p->hs_touch into the coordinator's pinned host buffer (no wait); remembers p->hs_step.
+ * csa_hisparse_apply, any time later (typically after the next step is enqueued): waits on the
+ *   host for that readback only, plans as csa_hisparse_plan for the collected step, then
+ *   (1) enqueues on `stream` the residency table with this plan's evictions (the incoming pages
+ *   still absent), so that every step enqueued after it reads those pages from the mirror, and
+ *   (2) on `side_stream`, once (1) is done: one gather kernel copying the planned pages from the
+ *   mirror into their slots, then the table with them installed.  Steps on `stream` overlap (2);
+ *   an entry only ever goes from -1 to a slot whose bytes are in place, and no slot is rewritten
+ *   before the steps that could read its old page are done.  n_tokens_host [B]: each request's
+ *   token count as of the last enqueued step; the page holding a request's newest compressed
+ *   row (which the overlapped steps may still write) is not brought in.  An apply waits for the
+ *   previous apply's side-stream work before it plans.  The first collect allocates the pinned
+ *   buffers (about 12 * B * table_stride + 12 * n_slots bytes) and three events, freed by
+ *   csa_hisparse_destroy.  CSA_ERR_INVALID_ARG for an apply without a collect before it. */
+csa_status csa_hisparse_collect(csa_hisparse* h, const csa_decode_params* p, void* stream);
+csa_status csa_hisparse_apply(csa_hisparse* h, const csa_decode_params* p, const int64_t* n_tokens_host,
+                              void* stream, void* side_stream, int64_t* n_in, int64_t* n_evicted);
 
 #ifdef __cplusplus
 }

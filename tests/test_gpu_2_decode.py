@@ -289,6 +289,55 @@ def test_hisparse_new_rows_reach_mirror_and_slot(entry):
     assert np.array_equal(in_slot, in_mirror)
 
 
+def test_hisparse_async_swaps_beside_the_steps(entry):
+    """The asynchronous coordinator: each step's stamps are collected, and the swap they call for
+    is applied after the next step is enqueued -- evictions on the decode stream, the copies and
+    installs on a side stream beside the following steps.  The queries change every step, so
+    pages come and go; every step still matches the oracle, and the final slots hold the
+    mirror's bytes."""
+    import deepseek_v4_hybrid_c4_gb300 as m
+    case = synth.make_decode_case("hs4", 63, [65536, 30000], H=16, Hi=8, n_pending=1)
+    batch, c_rpp = _hisparse_batch(entry, case, slots=96)
+    s, side = torch.cuda.Stream(), torch.cuda.Stream()
+    n_tok = np.array([r.n_tokens for r in case.requests], np.int64)
+    steps, outs, moved = 6, [], []
+    qs = []
+    for t in range(1, steps + 1):
+        q = [synth.normal_bf16((case.H, 512), 63, 900 + 10 * t + b) for b in range(len(case.requests))]
+        qi = [synth.normal_bf16((case.Hi, 128), 63, 950 + 10 * t + b) for b in range(len(case.requests))]
+        qs.append((q, qi))
+        with torch.cuda.stream(s):
+            batch.q.copy_(torch.from_numpy(np.stack(q).view(np.int16)))
+            batch.q_idx.copy_(torch.from_numpy(np.stack(qi).view(np.int16)))
+            batch.hs_step = t
+            batch.run(s)
+            outs.append((batch.out.clone(), batch.lse.clone(), batch.sel.clone()))
+            if t > 1:
+                moved.append(batch.hs_apply(n_tok, s, side))  # the previous step's stamps
+            batch.hs_collect(s)
+    torch.cuda.synchronize()
+    assert m.csa_read_device_status() == 0
+    assert sum(n for n, _ in moved) > 0 and sum(e for _, e in moved) > 0  # pages came in and went out
+    for t, ((q, qi), (out, lse, sel)) in enumerate(zip(qs, outs)):
+        for b, r in enumerate(case.requests):
+            r.q, r.q_idx = q[b], qi[b]
+        batch.out.copy_(out)
+        batch.lse.copy_(lse)
+        batch.sel.copy_(sel)
+        _check_against_oracle(case, batch)
+    table = batch.hs_table.cpu().numpy()
+    assert np.array_equal(table, m.csa_hisparse_table(batch.hs, batch.B, table.shape[1]))
+    pt = case.page_table()
+    pool = batch.c_pool.numpy()
+    slots = batch.hs_pool.cpu().numpy()
+    assert (table >= 0).sum() > 0
+    for b, lp in zip(*np.nonzero(table >= 0)):
+        sl = table[b, lp]
+        assert np.array_equal(slots[sl * c_rpp:(sl + 1) * c_rpp], pool[pt[b, lp] * c_rpp:(pt[b, lp] + 1) * c_rpp])
+        G = case.requests[b].n_tokens // 4
+        assert lp < (G - 1) // c_rpp  # the page still receiving rows was never brought in
+
+
 def test_decode_graph_capture_replay(entry):
     """The step enqueues only device work: it can be captured once and replayed."""
     case = synth.config(0)
