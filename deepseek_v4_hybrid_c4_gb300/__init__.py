@@ -62,6 +62,7 @@ def lib() -> ctypes.CDLL:
         vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
         L.csa_compress.argtypes = [csa_paged, i64, i32, vp, vp, i64, i64, csa_paged, vp]
         L.csa_index_score.argtypes = [vp, vp, i32, csa_paged, i32, i64, vp, vp]
+        L.csa_index_score_bounds.argtypes = [vp, vp, i32, csa_paged, i32, i64, vp, vp, vp]
         L.csa_topk.argtypes = [vp, i64, i32, vp, vp, vp, sz, vp]
         L.csa_topk_batched.argtypes = [vp, vp, i32, i64, i32, vp, vp, vp, sz, vp]
         L.csa_topk_cluster.argtypes = [vp, vp, i32, i64, i32, vp, vp, vp]
@@ -97,8 +98,8 @@ def lib() -> ctypes.CDLL:
                                          ctypes.POINTER(i64)]
         L.csa_hisparse_update.argtypes = [vp, ctypes.POINTER(csa_decode_params), vp, ctypes.POINTER(i64),
                                           ctypes.POINTER(i64)]
-        for name in ("csa_compress", "csa_index_score", "csa_topk", "csa_topk_batched", "csa_topk_cluster",
-                     "csa_topk_merge", "csa_sparse_attn_partial", "csa_attn_merge", "csa_sparse_attn",
+        for name in ("csa_compress", "csa_index_score", "csa_index_score_bounds", "csa_topk", "csa_topk_batched",
+                     "csa_topk_cluster", "csa_topk_merge", "csa_sparse_attn_partial", "csa_attn_merge", "csa_sparse_attn",
                      "csa_decode", "csa_decode_timed", "csa_decode_noalloc", "csa_read_device_status",
                      "csa_hisparse_create", "csa_hisparse_plan", "csa_hisparse_update", "csa_hisparse_collect",
                      "csa_hisparse_apply", "csa_selftest_bounded_wait"):
@@ -160,6 +161,13 @@ def csa_compress(kv_raw: csa_paged, n_tokens: int, ratio: int, w_gate, b_pos, fi
 def csa_index_score(q_idx, w_h, Hi: int, k_idx: csa_paged, k_dtype: int, G: int, scores, stream=None) -> None:
     _check(lib().csa_index_score(_ptr(q_idx), _ptr(w_h), Hi, k_idx, k_dtype, G, _ptr(scores), _stream(stream)),
            "csa_index_score")
+
+
+def csa_index_score_bounds(q_idx, w_h, Hi: int, k_idx: csa_paged, k_dtype: int, G: int, lower, upper,
+                           stream=None) -> None:
+    _check(lib().csa_index_score_bounds(_ptr(q_idx), _ptr(w_h), Hi, k_idx, k_dtype, G,
+                                        _ptr(lower) if lower is not None else None, _ptr(upper), _stream(stream)),
+           "csa_index_score_bounds")
 
 
 def csa_topk_workspace_size(B: int, max_G: int, k: int) -> int:

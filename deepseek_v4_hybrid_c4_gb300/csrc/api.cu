@@ -57,13 +57,20 @@ cudaError_t set_func_attr_once(const void* func, cudaFuncAttribute attr, int val
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lk(g_launch_mu);
-    for (const AttrDone& d : g_attr_done[dev])
-        if (d.func == func && d.attr == attr && d.value == value) return cudaSuccess;
+    AttrDone* cur = nullptr;  // the value this attribute holds now, if set here before
+    for (AttrDone& d : g_attr_done[dev])
+        if (d.func == func && d.attr == attr) cur = &d;
+    if (cur && cur->value == value) return cudaSuccess;
     e = cudaFuncSetAttribute(func, attr, value);
-    if (e == cudaSuccess) g_attr_done[dev].push_back({func, attr, value});
-    return e;
+    if (e != cudaSuccess) return e;
+    if (cur) cur->value = value;
+    else g_attr_done[dev].push_back({func, attr, value});
+    return cudaSuccess;
 }
 
+
+// Query positions per request from which the decode step scores through the tensor-core bounds.
+constexpr int kBoundMinQueries = 3;
 
 static bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 static bool al4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -186,6 +193,41 @@ csa_status csa_index_score(const void* q_idx, const float* w_h, int32_t Hi, csa_
     l.hist = nullptr;
     l.status = st;
     return from_cuda(launch_score(l, static_cast<cudaStream_t>(stream), false));
+}
+
+csa_status csa_index_score_bounds(const void* q_idx, const float* w_h, int32_t Hi, csa_paged k_idx, csa_dtype k_dtype,
+                                  int64_t G, float* lower, float* upper, void* stream) {
+    if (Hi < 1 || Hi > 16) return CSA_ERR_UNSUPPORTED;
+    if (k_dtype != CSA_BF16) return CSA_ERR_UNSUPPORTED;
+    if (!q_idx || !al16(q_idx) || !w_h || !al4(w_h) || !upper || !al4(upper) || (lower && !al4(lower)))
+        return CSA_ERR_INVALID_ARG;
+    if (check_paged(k_idx, 256)) return CSA_ERR_INVALID_ARG;
+    if (G < 0 || G > 0x7FFFFFFFLL) return CSA_ERR_INVALID_ARG;
+    if (k_idx.page_table && k_idx.rows_per_page % 16) return CSA_ERR_UNSUPPORTED;
+    if (G == 0) return CSA_OK;
+    int32_t* st = status_ptr();
+    if (!st) return CSA_ERR_CUDA;
+    ScoreLaunch l;
+    l.q_idx = q_idx;
+    l.w_h = w_h;
+    l.Hi = Hi;
+    l.kidx = host_paged(k_idx);
+    if (!k_idx.page_table) {  // contiguous rows: one logical page holds everything
+        l.kidx.rpp = 1 << 30;
+        l.kidx.page_stride = 0;
+        l.kidx.n_pages = 1;
+    }
+    l.fp8 = false;
+    l.scores = upper;
+    l.score_stride = 0;
+    l.B = 1;
+    l.n_tokens = nullptr;
+    l.ratio = 4;
+    l.G = G;
+    l.max_G = G;
+    l.hist = nullptr;
+    l.status = st;
+    return from_cuda(launch_score_bound(l, lower, static_cast<cudaStream_t>(stream), false));
 }
 
 size_t csa_topk_workspace_size(int32_t B, int64_t max_G, int32_t k) {
@@ -573,12 +615,38 @@ csa_status csa_decode_timed(const csa_decode_params* p, void* workspace, size_t 
         l.max_G = max_G;
         l.hist = hist;
         l.status = st;
-        e = launch_score(l, s, ev == nullptr);
+        // Speculative verify with bf16 keys: one pass over the keys for every query position,
+        // brackets on the tensor cores, exact rescoring of the candidates they leave open.  (With
+        // fewer positions the fixed-order kernel is as fast as the pass, which is bound by
+        // reading the scattered key pages, and the shorter select wins.)
+        const bool bound = nq >= kBoundMinQueries && p->k_dtype == CSA_BF16 &&
+                           score_bound_supported(p->Hi, nq, false) && select_set_supported(max_G, p->k);
+        e = bound ? launch_score_bound(l, nullptr, s, ev == nullptr) : launch_score(l, s, ev == nullptr);
         if (e != cudaSuccess) return CSA_ERR_CUDA;
         mark(2);
         // 3. top-k per request
         int32_t* sel_out = p->sel ? p->sel : reinterpret_cast<int32_t*>(ws + L.sel);
-        if (select_set_supported(max_G, p->k)) {
+        if (bound) {
+            SelectSetLaunch t;
+            t.scores = l.scores;
+            t.score_stride = L.score_stride;
+            t.B = Bq;
+            t.nq = nq;
+            t.max_G = max_G;
+            t.n_tokens = p->n_tokens;
+            t.ratio = p->ratio;
+            t.k = p->k;
+            t.idx_out = sel_out;
+            t.hist = hist;
+            t.lists = ws + L.lists;
+            t.status = st;
+            BoundRescore r;
+            r.q_idx = p->q_idx;
+            r.w_h = p->w_h;
+            r.Hi = p->Hi;
+            r.kidx = l.kidx;
+            e = launch_select_bound(t, r, s, ev == nullptr);
+        } else if (select_set_supported(max_G, p->k)) {
             SelectSetLaunch t;
             t.scores = l.scores;
             t.score_stride = L.score_stride;

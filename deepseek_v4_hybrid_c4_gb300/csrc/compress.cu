@@ -523,7 +523,15 @@ cudaError_t launch_compress(const CompressLaunch& h, cudaStream_t s, bool pdl) {
     if (gx < 1) gx = 1;
     if (gx > 0x7FFFFFFFLL) gx = 0x7FFFFFFFLL;
     cfg.gridDim = dim3((unsigned)gx, (unsigned)h.B, 1);
-    if (h.ratio == 4) return cudaLaunchKernelEx(&cfg, compress_r4_kernel, a);
+    if (h.ratio == 4) {
+        // prefer the largest shared-memory carveout: the SM that runs this warp keeps room for
+        // the index-score kernel's CTA (about 200 KB), which starts right behind it
+        cudaError_t e = set_func_attr_once((const void*)compress_r4_kernel,
+                                           cudaFuncAttributePreferredSharedMemoryCarveout,
+                                           (int)cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        return cudaLaunchKernelEx(&cfg, compress_r4_kernel, a);
+    }
     return r128_wide ? cudaLaunchKernelEx(&cfg, compress_r128_kernel<16, 8>, a)
                      : cudaLaunchKernelEx(&cfg, compress_r128_kernel<8, 4>, a);
 }

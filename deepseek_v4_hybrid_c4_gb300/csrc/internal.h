@@ -9,15 +9,20 @@ namespace csa {
 
 constexpr int kLatentRowBytes = 1024;  // one bf16 latent row (512 dims)
 constexpr int kHistBins = 2048;        // first top-k digit: key >> 21
-// Per-request top-k block in the workspace: one histogram per radix digit (six of
-// kHistBins counters; digit 0 first); cleared before every step.
-constexpr int kHistBlock = 6 * kHistBins;
+// Per-request top-k block in the workspace, cleared before every step: one histogram per radix
+// digit (six of kHistBins counters; digit 0 first), or, after the tensor-core bounds, one
+// histogram of up to 2^14 bins.
+constexpr int kHistBlock = 8 * kHistBins;
+// Bits of the lower bounds' first digit after the tensor-core bounds, by query positions per
+// request (the score kernel keeps n_q such histograms in shared memory).
+inline int bound_hist_bits(int nq) { return nq <= 1 ? 14 : (nq == 2 ? 13 : 12); }
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Per-device launch facts, safe to call from several host threads and on several devices:
-// the current device's SM count (0 on failure), and a kernel attribute set once per device
-// (cudaFuncSetAttribute applies to the current device only).
+// the current device's SM count (0 on failure), and a kernel attribute set per device
+// (cudaFuncSetAttribute applies to the current device only) -- again whenever the value asked for
+// differs from the one it holds, a call with the value it holds costing nothing.
 int device_sm_count();
 cudaError_t set_func_attr_once(const void* func, cudaFuncAttribute attr, int value);
 
@@ -82,6 +87,14 @@ struct ScoreLaunch {
     int32_t* status;
 };
 cudaError_t launch_score(const ScoreLaunch& a, cudaStream_t s, bool pdl);
+// The TMA tensor map (a CUtensorMap at `map`) of an index-key pool seen as [pages][rows per
+// page][128 dims], box 16 rows x 128 B, 128-byte swizzle; false when it cannot be encoded.
+bool make_kidx_map(void* map, const HPaged& p, bool fp8, int64_t rows_per_page, int64_t n_pages);
+// Stage 2 on the tensor cores, bf16 keys: for every candidate a bracket [lower, upper] that holds
+// the fixed-order score (upper to `scores`, lower to `lower` when set), and, with hist, the first
+// digit of the lower bounds' keys.  Needs Hi <= 16, nq <= 4.
+bool score_bound_supported(int Hi, int nq, bool fp8);
+cudaError_t launch_score_bound(const ScoreLaunch& a, float* lower, cudaStream_t s, bool pdl);
 
 // Stage 3.  Request b's scores: single: [0, G); offsets mode: [offsets[b], offsets[b+1]);
 // decode mode: b * score_stride + [0, n_tokens[b] / ratio).  hist: [B][kHistBlock], zeroed
@@ -133,6 +146,17 @@ struct SelectSetLaunch {
     uint32_t* keys_out = nullptr;
 };
 bool select_set_supported(int64_t max_G, int k);
+// Stage 3 after launch_score_bound: scores hold the upper bounds and hist the lower bounds'
+// first digit; the candidates the bounds cannot rule out are rescored in the fixed order from
+// the query and the bf16 key rows, then an exact top-k picks the set (ascending index order).
+// Decode mode only.
+struct BoundRescore {
+    const void* q_idx;         // bf16 [B, Hi, 128]
+    const float* w_h;          // fp32 [B, Hi]
+    int Hi;
+    HPaged kidx;               // bf16 rows of 256 B
+};
+cudaError_t launch_select_bound(const SelectSetLaunch& a, const BoundRescore& r, cudaStream_t s, bool pdl);
 size_t select_set_lists_bytes(int B, int64_t max_G);
 cudaError_t launch_select_set(const SelectSetLaunch& a, cudaStream_t s, bool pdl);
 

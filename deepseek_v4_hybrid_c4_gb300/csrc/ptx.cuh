@@ -59,6 +59,16 @@ CSA_DEV void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t ba
         "l"(src), "r"(bytes), "r"(bar)
         : "memory");
 }
+// Tiled 3-D tensor copy (TMA) of the box at coordinates {c0, c1, c2} of the tensor map at `map`
+// (a CUtensorMap in parameter, constant or global memory) into this CTA's shared memory,
+// completing on an mbarrier.  c0 * element size must be a multiple of 16 bytes.
+CSA_DEV void tma_load_3d(uint32_t dst, const void* map, int c0, int c1, int c2, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
 CSA_DEV void cp_async16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
@@ -144,6 +154,14 @@ CSA_DEV void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
         "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
         : CSA_R8(0), CSA_R8(8), CSA_R8(16), CSA_R8(24)
+        : "r"(taddr));
+}
+// The same over 16 consecutive columns.
+CSA_DEV void tc_ld16(uint32_t taddr, uint32_t* r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : CSA_R8(0), CSA_R8(8)
         : "r"(taddr));
 }
 CSA_DEV void tc_st32(uint32_t taddr, const uint32_t (&r)[32]) {

@@ -115,15 +115,6 @@ __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
     return d;
 }
 
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
-        "[%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
-        : "memory");
-}
-
 __device__ __forceinline__ void fp8x8(uint2 raw, float (&k)[8]) {
     const uint32_t w[2] = {raw.x, raw.y};
 #pragma unroll
@@ -450,7 +441,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 
 // 3-D view of the index-key pool: [pages][rows per page][128 dims], box = 16 rows x
 // (64 bf16 | 128 fp8) = 16 x 128 B, 128-byte swizzle.
-static bool make_kmap(CUtensorMap* m, const HPaged& p, bool fp8, int64_t rows_per_page, int64_t n_pages) {
+bool make_kidx_map(void* map, const HPaged& p, bool fp8, int64_t rows_per_page, int64_t n_pages) {
+    CUtensorMap* m = static_cast<CUtensorMap*>(map);
     auto enc = encoder();
     if (!enc) return false;
     const int rb = fp8 ? 128 : 256;
@@ -522,7 +514,7 @@ cudaError_t launch_score(const ScoreLaunch& h, cudaStream_t s, bool pdl) {
     a.rpp = (int32_t)rpp;
     a.n_pages = n_pages;
     CUtensorMap map;
-    if (!make_kmap(&map, h.kidx, h.fp8, rpp, n_pages)) return cudaErrorInvalidValue;
+    if (!make_kidx_map(&map, h.kidx, h.fp8, rpp, n_pages)) return cudaErrorInvalidValue;
     const int64_t steps = (int64_t)h.B * (((h.max_G + SC_SUPER - 1) / SC_SUPER + SC_WARPS - 1) / SC_WARPS);
     const int hi = h.Hi <= 4 ? 4 : (h.Hi <= 8 ? 8 : 16);
     if (h.fp8) {

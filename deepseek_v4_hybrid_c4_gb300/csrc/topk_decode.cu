@@ -28,6 +28,8 @@
 //          holds exactly the number still needed.
 // Output: the k indices as a set in a fixed order (first-digit winners, then each round's
 // winners, each in index order); -1 pads when the request has fewer than k candidates.
+#include <cstddef>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -715,6 +717,339 @@ __global__ void __launch_bounds__(SW_T) select_hist_kernel(SelArgs a) {
         if (h[i]) atomicAdd(hb + i, h[i]);
 }
 
+// ------------------------------------------------------------------ the select after the bounds
+// With the tensor-core brackets of score_bound.cu, scores holds each candidate's upper bound U
+// and hist the histogram of the top HB bits of the lower bounds' keys (HB = 12..14).  The bin
+// b0 holding the k-th largest lower bound puts at least k exact scores at or above the bin's
+// lowest value, so every candidate whose key(U) >> (32 - HB) is below b0 is out of the top k.
+//  scan:  each CTA compacts its slice's candidates with key(U) >> (32 - HB) >= b0 (all of them
+//         when the request has at most k) in index order and rescores them exactly in the
+//         fixed chain order -- every (candidate, chain) pair a thread's work, four chains per
+//         thread in flight, the chains combined per candidate in head order -- and writes
+//         (exact key << 32 | index) to its region of the lists, with the count.
+//  exact: SX_CTAS CTAs per batch entry; each loads every region's entries (a few hundred at
+//         the 1M workload) into shared memory and ranks its share of them against all: an
+//         entry with rank r < k (the number of composites above its own) goes to out[r].
+//         Above SX_CAP entries (degenerate inputs, e.g. every score tied) the first CTA runs a
+//         radix select over the lists instead and writes the set in index order.
+// Output: the k indices ordered by (score desc, index asc) (or, above SX_CAP entries, as a
+// set in index order), then -1 padding.
+constexpr int SX_CAP = 4096;   // list entries the exact select ranks in shared memory
+constexpr int SX_CTAS = 16;    // CTAs per batch entry of the exact select
+constexpr int SX_QMAX = 16;    // index heads
+constexpr int SX_SLOTS = SW_T * 4;  // chain slots of one rescoring round (four per thread)
+
+struct BoundSelArgs {
+    SelArgs s;                 // scores = upper bounds; hist: top HB bits of the lower bounds' keys
+    const uint16_t* q_idx;     // [B][Hi][128]
+    const float* w_h;          // [B][Hi]
+    int Hi;
+    DPaged kidx;               // bf16 rows of 256 B
+};
+
+struct SxSmem {
+    uint64_t ent[SX_CAP];                // composites, region by region
+    alignas(16) uint32_t hist[SW_BINS];  // radix path: one digit's counts (16-byte loads)
+    SwCore core;
+    uint32_t pre[SW_CMAX + 1];           // exclusive prefix of the regions' entries
+    uint32_t spre[SW_CMAX + 1];          // radix path: per region its selected entries, then their prefix
+};
+static_assert(offsetof(SxSmem, hist) % 16 == 0, "16-byte loads of the histogram");
+
+struct SbSmem {                          // bound scan
+    SwCore core;
+    uint32_t cidx[SW_SLICE];             // the slice's candidates (index order)
+    const uint8_t* rowp[SW_SLICE];       // their key rows (nullptr: page out of range)
+    float qf[4 * SX_QMAX * 33];          // chain n = 4h + j: q_h[32j + d] at n * 33 + d
+    float wf[SX_QMAX];
+    float qv[SX_SLOTS + SW_T];           // a round's chain results, candidate c at c * (4 Hi + 1)
+};
+
+// The bin holding the need-th largest element of a 2^HB-bin histogram hb (global memory),
+// counting from the top: thread t owns bins [top - PER + 1, top], top = 2^HB - 1 - PER t.
+// Sets sm.bin (~0 when the counts hold fewer than need), sm.above and sm.cnt.
+template <int HB>
+__device__ __forceinline__ void sw_find_bin_wide(SwCore& sm, const uint32_t* hb, uint32_t need) {
+    constexpr int PER = (1 << HB) / SW_T;
+    const int top = (1 << HB) - 1 - PER * (int)threadIdx.x;
+    uint32_t c[PER];
+    uint32_t sum = 0;
+#pragma unroll
+    for (int i = 0; i < PER; i += 4) {
+        const uint4 v = __ldcg(reinterpret_cast<const uint4*>(hb + top - PER + 1 + i));
+        c[i] = v.x; c[i + 1] = v.y; c[i + 2] = v.z; c[i + 3] = v.w;
+        sum += v.x + v.y + v.z + v.w;
+    }
+    if (threadIdx.x == 0) {
+        sm.bin = ~0u;
+        sm.above = 0;
+        sm.cnt = 0;
+    }
+    uint32_t tot;
+    uint32_t acc = sw_scan(sm, sum, &tot);  // its barriers order the reset
+    if (sum > 0 && acc < need && need <= acc + sum) {
+#pragma unroll
+        for (int i = PER - 1; i >= 0; --i) {  // c[PER - 1] is bin `top`
+            if (acc < need && need <= acc + c[i]) {
+                sm.bin = (uint32_t)(top - (PER - 1 - i));
+                sm.above = acc;
+                sm.cnt = c[i];
+            }
+            acc += c[i];
+        }
+    }
+    __syncthreads();
+}
+
+template <int HB>
+__global__ void __launch_bounds__(SW_T) select_bound_scan_kernel(BoundSelArgs a) {
+    __shared__ SbSmem sm;
+    const int tid = threadIdx.x;
+    const int b = blockIdx.x, c = blockIdx.y, C = a.s.C, k = a.s.k;
+    const float* sc;
+    int64_t G;
+    sel_span(a.s, b, sc, G);
+    const uint32_t* hb = a.s.hist + (int64_t)b * kHistBlock;
+    uint64_t* lc = a.s.lists + ((int64_t)b * C + c) * SW_SLICE;
+    const bool all_in = G <= k;
+    const int Hi = a.Hi, nch = 4 * Hi;
+    if (!all_in) {  // the entry's query as fp32 by chain, and its weights: inputs of the step
+        for (int i = tid; i < Hi * DI; i += SW_T) {
+            const uint16_t v = a.q_idx[(int64_t)b * Hi * DI + i];
+            const int h = i >> 7, dd = i & 127;
+            sm.qf[(4 * h + (dd >> 5)) * 33 + (dd & 31)] = __uint_as_float((uint32_t)v << 16);
+        }
+        if (tid < Hi) sm.wf[tid] = a.w_h[(int64_t)b * Hi + tid];
+    }
+    pdl_wait();  // the bounds and the lower bounds' histogram come from the score kernel
+    pdl_launch_dependents();
+
+    const int64_t pos = (int64_t)c * SW_SLICE + SW_PER * tid;
+    uint32_t key[SW_PER];
+    sel_load4(sc, pos, G, key);
+    uint32_t b0 = 0;
+    if (!all_in) {
+        sw_find_bin_wide<HB>(sm.core, hb, (uint32_t)k);
+        b0 = sm.core.bin == ~0u ? 0u : sm.core.bin;  // (fewer than k counted cannot happen; then keep all)
+    }
+    bool cand[SW_PER];
+    uint32_t nc = 0;
+#pragma unroll
+    for (int q = 0; q < SW_PER; ++q) {
+        cand[q] = pos + q < G && (all_in || (key[q] >> (32 - HB)) >= b0);
+        nc += cand[q] ? 1u : 0u;
+    }
+    uint32_t tot;
+    uint32_t oc = sw_scan(sm.core, nc, &tot);
+#pragma unroll
+    for (int q = 0; q < SW_PER; ++q)
+        if (cand[q]) sm.cidx[oc++] = (uint32_t)(pos + q);
+    __syncthreads();
+    if (all_in) {
+        for (uint32_t i = tid; i < tot; i += SW_T) lc[i] = sm.cidx[i];
+    } else {
+        for (uint32_t i = tid; i < tot; i += SW_T) sm.rowp[i] = row_addr(a.kidx, b, sm.cidx[i], 256, a.s.status);
+        __syncthreads();
+        const int rc = SX_SLOTS / nch;  // candidates per round
+        for (uint32_t base = 0; base < tot; base += (uint32_t)rc) {
+            // four chains per thread: slot = tid + s * SW_T -> candidate slot / nch, chain slot % nch
+            float p[4];
+            uint4 kv[4][4];
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const int slot = tid + s * SW_T;
+                const uint32_t i = base + (uint32_t)(slot / nch);
+                const uint8_t* row = (slot < rc * nch && i < tot) ? sm.rowp[i] : nullptr;
+                const int j = (slot % nch) & 3;
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    kv[s][v] = row ? __ldg(reinterpret_cast<const uint4*>(row + 64 * j) + v) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int s = 0; s < 4; ++s) p[s] = 0.f;
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int d = 8 * v + e;
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) {
+                        const int n = (tid + s * SW_T) % nch;
+                        const uint32_t wd = (e >> 1) == 0 ? kv[s][v].x : (e >> 1) == 1 ? kv[s][v].y
+                                          : (e >> 1) == 2 ? kv[s][v].z : kv[s][v].w;
+                        const float kf = (e & 1) ? bf16hi(wd) : bf16lo(wd);
+                        const float qq = sm.qf[n * 33 + d];
+                        p[s] = d == 0 ? __fmul_rn(qq, kf) : __fmaf_rn(qq, kf, p[s]);
+                    }
+                }
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const int slot = tid + s * SW_T;
+                if (slot < rc * nch) sm.qv[(slot / nch) * (nch + 1) + slot % nch] = p[s];
+            }
+            __syncthreads();
+            // combine: dot_h = (Q[0] + Q[2]) + (Q[1] + Q[3]), acc = fma(w_h, ReLU(dot_h), acc) in head order
+            if (tid < rc && base + (uint32_t)tid < tot) {
+                const uint32_t i = base + (uint32_t)tid;
+                const float* qr = sm.qv + tid * (nch + 1);
+                float acc = 0.f;
+                for (int h = 0; h < Hi; ++h) {
+                    const float dot = (qr[4 * h] + qr[4 * h + 2]) + (qr[4 * h + 1] + qr[4 * h + 3]);
+                    acc = __fmaf_rn(sm.wf[h], dot > 0.f ? dot : 0.f, acc);
+                }
+                if (!sm.rowp[i]) acc = 0.f;  // page out of range: scored 0, as by the fixed-order kernel
+                lc[i] = ((uint64_t)score_key(acc) << 32) | sm.cidx[i];
+            }
+            __syncthreads();
+        }
+    }
+    if (tid == 0) a.s.counts[(int64_t)b * C + c] = tot;
+}
+
+__global__ void __launch_bounds__(SW_T, 1) select_exact_kernel(SelArgs a) {
+    extern __shared__ __align__(16) uint8_t sx_raw[];
+    SxSmem& sm = *reinterpret_cast<SxSmem*>(sx_raw);  // the dynamic shared memory starts 16-byte aligned
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int b = blockIdx.x, part = blockIdx.y, C = a.C, k = a.k;
+    const uint64_t* lb = a.lists + (int64_t)b * C * SW_SLICE;
+    const uint32_t* cb = a.counts + (int64_t)b * C;
+    int32_t* out = a.out + (int64_t)b * k;
+    pdl_wait();  // the lists and their counts come from the scan
+    pdl_launch_dependents();
+
+    uint32_t cnt[SW_PER];
+#pragma unroll
+    for (int j = 0; j < SW_PER; ++j) {
+        const int cc = SW_PER * tid + j;
+        cnt[j] = cc < C ? __ldcg(cb + cc) : 0u;
+    }
+    uint32_t n;
+    uint32_t ex = sw_scan(sm.core, cnt[0] + cnt[1] + cnt[2] + cnt[3], &n);
+#pragma unroll
+    for (int j = 0; j < SW_PER; ++j) {
+        const int cc = SW_PER * tid + j;
+        if (cc < C) sm.pre[cc] = ex;
+        ex += cnt[j];
+    }
+    if (tid == 0) sm.pre[C] = n;
+    __syncthreads();
+
+    if (n <= (uint32_t)SX_CAP) {
+        // ---- rank every entry against all: out[rank] for rank < k.  Entry i of the concatenation
+        // lies in region sw_owner(pre, i); every thread's loads go out together.
+        constexpr int LPT = SX_CAP / SW_T;  // entries per thread, at most
+        uint64_t ld[LPT];
+#pragma unroll
+        for (int q = 0; q < LPT; ++q) {
+            const uint32_t i = tid + (uint32_t)q * SW_T;
+            if (i < n) {
+                const int cc = sw_owner(sm.pre, C, i);
+                ld[q] = __ldcg(lb + (int64_t)cc * SW_SLICE + (i - sm.pre[cc]));
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < LPT; ++q) {
+            const uint32_t i = tid + (uint32_t)q * SW_T;
+            if (i < n) sm.ent[i] = sel_comp(ld[q]);
+        }
+        __syncthreads();
+        const uint32_t per = (n + SX_CTAS - 1) / SX_CTAS;
+        const uint32_t i0 = (uint32_t)part * per, i1 = i0 + per < n ? i0 + per : n;
+        for (uint32_t i = i0 + tid; i < i1; i += SW_T) {
+            const uint64_t v = sm.ent[i];
+            uint32_t r = 0;
+#pragma unroll 8
+            for (uint32_t m = 0; m < n; ++m) r += sm.ent[m] > v ? 1u : 0u;
+            if (r < (uint32_t)k) out[r] = (int32_t)(0x7FFFFFFFu - (uint32_t)(v & 0x7FFFFFFFu));
+        }
+        if (part == 0)
+            for (uint32_t i = n + tid; i < (uint32_t)k; i += SW_T) out[i] = -1;
+        return;
+    }
+    if (part != 0) return;  // (uniform per CTA)
+
+    // ---- more entries than fit: radix select over the lists in L2, the set in index order.
+    // Digits key 31..21 | 20..10 | 9..0, inverted index 30..20 | 19..10 | 9..0 (composite bits
+    // 63..53 | 52..42 | 41..32 | 30..20 | 19..10 | 9..0).
+    auto entry = [&](int cc, uint32_t i) -> uint64_t { return sel_comp(__ldcg(lb + (int64_t)cc * SW_SLICE + i)); };
+    uint64_t prefix = 0, pmask = 0;
+    {
+        const int shift[6] = {53, 42, 32, 20, 10, 0};
+        const uint32_t dmask[6] = {2047u, 2047u, 1023u, 2047u, 1023u, 1023u};
+        uint32_t need = (uint32_t)k;
+        for (int dgt = 0; dgt < 6; ++dgt) {
+            for (int i = tid; i < SW_BINS; i += SW_T) sm.hist[i] = 0;
+            __syncthreads();
+            for (int cc = warp; cc < C; cc += SW_T / 32) {
+                const uint32_t m = sm.pre[cc + 1] - sm.pre[cc];
+                for (uint32_t i = lane; i < m; i += 32) {
+                    const uint64_t v = entry(cc, i);
+                    if ((v & pmask) == prefix) atomicAdd(&sm.hist[(v >> shift[dgt]) & dmask[dgt]], 1u);
+                }
+            }
+            __syncthreads();
+            const uint4 hv = *reinterpret_cast<const uint4*>(&sm.hist[SW_BINS - 4 - 4 * tid]);
+            const uint32_t h[4] = {hv.w, hv.z, hv.y, hv.x};
+            sw_find_bin(sm.core, h, need);
+            const uint32_t bd = sm.core.bin, above = sm.core.above, cn = sm.core.cnt;
+            if (bd == ~0u) {  // inconsistent counts: cannot happen
+                raise_status(a.status, CSA_ERR_DEVICE_BOUNDS);
+                break;
+            }
+            prefix |= (uint64_t)bd << shift[dgt];
+            pmask |= (uint64_t)dmask[dgt] << shift[dgt];
+            need -= above;
+            if (cn == need) break;  // every composite of the bin is in
+        }
+    }
+    // selected: (v & pmask) >= prefix; per region count, prefix, then write in index order
+    for (int cc = warp; cc < C; cc += SW_T / 32) {
+        const uint32_t m = sm.pre[cc + 1] - sm.pre[cc];
+        uint32_t s = 0;
+        for (uint32_t i0 = 0; i0 < m; i0 += 32) {
+            const uint32_t i = i0 + lane;
+            const bool f = i < m && (entry(cc, i) & pmask) >= prefix;
+            s += __popc(__ballot_sync(0xffffffffu, f));
+        }
+        if (lane == 0) sm.spre[cc] = s;
+    }
+    __syncthreads();
+    uint32_t v[SW_PER];
+#pragma unroll
+    for (int j = 0; j < SW_PER; ++j) {
+        const int cc = SW_PER * tid + j;
+        v[j] = cc < C ? sm.spre[cc] : 0u;
+    }
+    uint32_t total;
+    ex = sw_scan(sm.core, v[0] + v[1] + v[2] + v[3], &total);
+#pragma unroll
+    for (int j = 0; j < SW_PER; ++j) {
+        const int cc = SW_PER * tid + j;
+        if (cc < C) sm.spre[cc] = ex;
+        ex += v[j];
+    }
+    __syncthreads();
+    for (int cc = warp; cc < C; cc += SW_T / 32) {
+        const uint32_t m = sm.pre[cc + 1] - sm.pre[cc];
+        uint32_t base = sm.spre[cc];
+        for (uint32_t i0 = 0; i0 < m; i0 += 32) {
+            const uint32_t i = i0 + lane;
+            uint64_t e = 0;
+            bool f = false;
+            if (i < m) {
+                e = entry(cc, i);
+                f = (e & pmask) >= prefix;
+            }
+            const unsigned bal = __ballot_sync(0xffffffffu, f);
+            const uint32_t o = base + __popc(bal & ((1u << lane) - 1u));
+            if (f && o < (uint32_t)k) out[o] = (int32_t)(0x7FFFFFFFu - (uint32_t)(e & 0x7FFFFFFFu));
+            base += __popc(bal);
+        }
+    }
+    if (total != (n < (uint32_t)k ? n : (uint32_t)k)) raise_status(a.status, CSA_ERR_DEVICE_BOUNDS);
+    for (uint32_t i = total + tid; i < (uint32_t)k; i += SW_T) out[i] = -1;
+}
+
 // ------------------------------------------------------------------ host side
 static int64_t select_set_ctas(int64_t max_G) { return max_G <= 0 ? 1 : (max_G + SW_SLICE - 1) / SW_SLICE; }
 
@@ -791,6 +1126,69 @@ cudaError_t launch_select_set(const SelectSetLaunch& h, cudaStream_t s, bool pdl
     if (e != cudaSuccess) return e;
     cfg.dynamicSmemBytes = smem;
     return cudaLaunchKernelEx(&cfg, select_finish_kernel, a);
+}
+
+cudaError_t launch_select_bound(const SelectSetLaunch& h, const BoundRescore& r, cudaStream_t s, bool pdl) {
+    if (!h.n_tokens || h.standalone || r.Hi < 1 || r.Hi > SX_QMAX) return cudaErrorInvalidValue;
+    BoundSelArgs a;
+    a.s.scores = h.scores;
+    a.s.score_stride = h.score_stride;
+    a.s.n_tokens = h.n_tokens;
+    a.s.nq = h.nq > 1 ? h.nq : 1;
+    a.s.ratio = h.ratio;
+    a.s.offsets = nullptr;
+    a.s.G = 0;
+    a.s.sorted = 0;
+    a.s.keys_out = nullptr;
+    a.s.C = (int)select_set_ctas(h.max_G);
+    a.s.k = h.k;
+    a.s.out = h.idx_out;
+    a.s.hist = h.hist;
+    a.s.lists = reinterpret_cast<uint64_t*>(h.lists);
+    a.s.counts = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(h.lists) +
+                                             align_up((size_t)h.B * a.s.C * SW_SLICE * sizeof(uint64_t), 256));
+    a.s.status = h.status;
+    a.q_idx = static_cast<const uint16_t*>(r.q_idx);
+    a.w_h = r.w_h;
+    a.Hi = r.Hi;
+    a.kidx.base = static_cast<const uint8_t*>(r.kidx.base);
+    a.kidx.pt = r.kidx.pt;
+    a.kidx.pt_stride = r.kidx.pt_stride;
+    a.kidx.page_stride = r.kidx.page_stride;
+    a.kidx.n_pages = r.kidx.n_pages;
+    a.kidx.rpp = r.kidx.rpp;
+    a.kidx.qpr = h.nq > 1 ? h.nq : 1;
+    const size_t smem = sizeof(SxSmem);
+    const int hbits = bound_hist_bits(a.s.nq);
+    const void* scan = hbits == 14 ? (const void*)select_bound_scan_kernel<14>
+                     : hbits == 13 ? (const void*)select_bound_scan_kernel<13>
+                                   : (const void*)select_bound_scan_kernel<12>;
+    {
+        cudaError_t e = set_func_attr_once((const void*)select_exact_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess)
+            e = set_func_attr_once(scan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SW_SCAN_SPREAD_SMEM);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    const int sms = device_sm_count();
+    if (!sms) return cudaErrorInvalidDevice;
+    cfg.gridDim = dim3((unsigned)h.B, (unsigned)a.s.C, 1);
+    cfg.blockDim = dim3(SW_T, 1, 1);
+    cfg.dynamicSmemBytes = (int64_t)a.s.C * h.B <= sms ? SW_SCAN_SPREAD_SMEM : 0;  // one scan CTA per SM
+    cfg.stream = s;
+    void* args[] = {&a};
+    cudaError_t e = cudaLaunchKernelExC(&cfg, scan, args);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3((unsigned)h.B, (unsigned)SX_CTAS, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.numAttrs = 1;  // waits for the scan (griddepcontrol.wait)
+    return cudaLaunchKernelEx(&cfg, select_exact_kernel, a.s);
 }
 
 }  // namespace csa

@@ -104,6 +104,25 @@ csa_status csa_index_score(const void* q_idx, const float* w_h, int32_t Hi, csa_
                            int64_t G, float* scores, void* stream);
 
 /*
+ * Stage 2 as brackets, on the tensor cores ([V4-deploy] "Kernel 層一堆狠活": the indexer's
+ * q.k products are a dense contraction): for every candidate g, lower[g] <= s[g] <= upper[g],
+ * s the fixed-order score of csa_index_score.  The dots q_h . k_g come from tcgen05 MMAs (bf16
+ * operands, fp32 accumulation); the half-width is
+ *   e_g = 2^-13 * max_j |k_gj| * sum_h |w_h| * ||q_h||_1 + 1e-30   (rounded up),
+ * which covers the fixed-order chains' rounding (at most 33 * 2^-24 of sum_j |q_hj k_gj|) and
+ * an MMA accumulation error of up to 2^-14 of the same sum.  A non-finite input or a bound past
+ * 1e30 gives (-inf, +inf); a row whose page id is out of range gives [0, 0] and the device
+ * status CSA_ERR_DEVICE_BOUNDS.  Arguments as csa_index_score; k_dtype must be CSA_BF16
+ * (otherwise CSA_ERR_UNSUPPORTED); lower is nullable, both fp32 [G], 4-byte aligned.
+ * csa_decode takes this form in speculative verify with bf16 index keys (3 <= n_q <= 4, Hi <= 16):
+ * one pass over the keys serves every query position, and the select rescores in the fixed
+ * order only the candidates whose upper bound reaches the histogram bin (top 12 bits of the key)
+ * of the k-th largest lower bound, so its top k is the fixed-order score's top k.
+ */
+csa_status csa_index_score_bounds(const void* q_idx, const float* w_h, int32_t Hi, csa_paged k_idx,
+                                  csa_dtype k_dtype, int64_t G, float* lower, float* upper, void* stream);
+
+/*
  * Stage 3: top-k ([Day-0] "创新 2", Lightning TopK: per-CTA histograms reduced to
  * a threshold, then a scatter of the entries above it).
  * scores fp32 [G] -> idx_out int32 [k]: the indices of the min(k, G) largest
