@@ -315,30 +315,33 @@ def other_workloads(torch, csa, entry, synth, stream, flush_l2, peak):
             del outs, descs
         del g, b
         torch.cuda.empty_cache()
-    # ---- speculative verify at 1M context, bs = 1: 4 query positions (draft tokens) per step,
-    #      each with its own candidates, top k and SWA window
+    # ---- speculative verify at 1M context, bs = 1: n_q query positions (draft tokens) per step,
+    #      each with its own candidates, top k and SWA window.  Two positions take the fixed-order
+    #      score per position; three and four take one pass over the keys on the tensor cores
+    #      (brackets, then the candidates they leave open rescored in the fixed order).
     case = synth.config(2)
-    nq = 4
-    b = entry.case_to_batch(case, n_q=nq, q=synth.normal_bf16((nq, case.H, 512), case.seed, 400),
-                            q_idx=synth.normal_bf16((nq, case.Hi, 128), case.seed, 401),
-                            w_h=synth.uniform_f32((nq, case.Hi), case.seed, 402))
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            b.run(stream)
-    torch.cuda.synchronize()
-    assert csa.csa_read_device_status(stream) == 0
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        b.run(stream)
-    t, t90 = timed(g.replay, 30)
     G = case.requests[0].n_tokens // case.ratio
-    res["spec_verify_1M_4_positions"] = {
-        "us_per_step": round(t, 2), "us_p90": round(t90, 2), "us_per_query_position": round(t / nq, 2),
-        "query_positions": nq, "index_key_bytes_per_step": nq * G * 256,
-        "note": "every position streams the index keys itself (the score is bound by its fixed-order fma "
-                "rate, not by the stream)"}
-    del g, b
-    torch.cuda.empty_cache()
+    for nq in (2, 3, 4):
+        b = entry.case_to_batch(case, n_q=nq, q=synth.normal_bf16((nq, case.H, 512), case.seed, 400),
+                                q_idx=synth.normal_bf16((nq, case.Hi, 128), case.seed, 401),
+                                w_h=synth.uniform_f32((nq, case.Hi), case.seed, 402))
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                b.run(stream)
+        torch.cuda.synchronize()
+        assert csa.csa_read_device_status(stream) == 0
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            b.run(stream)
+        t, t90 = timed(g.replay, 30)
+        one_pass = nq >= 3
+        res[f"spec_verify_1M_{nq}_positions"] = {
+            "us_per_step": round(t, 2), "us_p90": round(t90, 2), "us_per_query_position": round(t / nq, 2),
+            "query_positions": nq, "index_key_bytes_per_step": (1 if one_pass else nq) * G * 256,
+            "score": "one pass over the keys for every position: tcgen05 brackets, then exact rescoring of the "
+                     "candidates they leave open" if one_pass else "the fixed-order kernel once per position"}
+        del g, b
+        torch.cuda.empty_cache()
     # ---- context-parallel split of the 1M request into 4 contiguous shards, on this one GPU: the
     #      stages of the rank holding the last shard (which also attends the window), with the
     #      exchanged lists and partials already in place, and the full 4-shard step run in turn

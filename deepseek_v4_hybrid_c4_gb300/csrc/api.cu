@@ -564,6 +564,12 @@ csa_status csa_decode_timed(const csa_decode_params* p, void* workspace, size_t 
     cp.n_pages = p->c_page_table ? p->c_n_pages : p->n_pages;
     cp.rpp = p->c_page_table ? p->c_rows_per_page : p->raw_rows_per_page / p->ratio;
     uint32_t* hist = p->ratio == 4 ? reinterpret_cast<uint32_t*>(ws + L.hist) : nullptr;
+    // Speculative verify with bf16 keys: one pass over the keys for every query position,
+    // brackets on the tensor cores, exact rescoring of the candidates they leave open.  (With
+    // fewer positions the fixed-order kernel is as fast as the pass, which is bound by reading
+    // the scattered key pages, and the shorter select wins.)
+    const bool bound = p->ratio == 4 && nq >= kBoundMinQueries && p->k_dtype == CSA_BF16 &&
+                       score_bound_supported(p->Hi, nq, false) && select_set_supported(max_G, p->k);
 
     // 1. compress the completed groups that are not in the pool yet (and clear the histogram)
     CompressLaunch c;
@@ -578,6 +584,10 @@ csa_status csa_decode_timed(const csa_decode_params* p, void* workspace, size_t 
     c.first = 0;
     c.count = 0;
     c.hist_zero = hist;
+    c.hist_words = bound ? 1 << bound_hist_bits(nq) : kWideSelectHistWords;
+    // bf16 keys: the score kernel's CTAs fill the SM's shared memory (two of about 100 KB, or one
+    // of about 200 KB), so the compressor's SM takes the largest carveout too
+    c.carveout = p->k_dtype == CSA_BF16 ? (int)cudaSharedmemCarveoutMaxShared : (int)cudaSharedmemCarveoutDefault;
     c.status = st;
     c.ring_pool = p->ring_pool;
     c.ring_page = p->ring_page;
@@ -615,12 +625,6 @@ csa_status csa_decode_timed(const csa_decode_params* p, void* workspace, size_t 
         l.max_G = max_G;
         l.hist = hist;
         l.status = st;
-        // Speculative verify with bf16 keys: one pass over the keys for every query position,
-        // brackets on the tensor cores, exact rescoring of the candidates they leave open.  (With
-        // fewer positions the fixed-order kernel is as fast as the pass, which is bound by
-        // reading the scattered key pages, and the shorter select wins.)
-        const bool bound = nq >= kBoundMinQueries && p->k_dtype == CSA_BF16 &&
-                           score_bound_supported(p->Hi, nq, false) && select_set_supported(max_G, p->k);
         e = bound ? launch_score_bound(l, nullptr, s, ev == nullptr) : launch_score(l, s, ev == nullptr);
         if (e != cudaSuccess) return CSA_ERR_CUDA;
         mark(2);

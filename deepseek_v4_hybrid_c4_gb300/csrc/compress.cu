@@ -23,6 +23,7 @@ struct CompressArgs {
     int ratio;
     int nq;                    // query positions per request: histogram blocks to clear
     uint32_t* hist_zero;
+    int hist_words;      // words cleared at the start of each batch entry's block
     int32_t* status;
     DWorkSet ows;              // HiSparse working set of the output pool (table == nullptr: none)
     const uint8_t* ring_pool;  // batched mode, optional: request b's token t in row
@@ -57,8 +58,11 @@ __device__ __forceinline__ const uint8_t* token_row(const CompressArgs& a, int b
 
 __device__ __forceinline__ void zero_hist(const CompressArgs& a, int b) {
     if (a.hist_zero && blockIdx.x == 0) {  // 16-byte stores: the blocks are 16-byte aligned
-        uint4* z = reinterpret_cast<uint4*>(a.hist_zero + (int64_t)b * a.nq * kHistBlock);
-        for (int i = threadIdx.x; i < a.nq * kHistBlock / 4; i += blockDim.x) z[i] = make_uint4(0, 0, 0, 0);
+        const int w4 = a.hist_words / 4;
+        for (int q = 0; q < a.nq; ++q) {
+            uint4* z = reinterpret_cast<uint4*>(a.hist_zero + ((int64_t)b * a.nq + q) * kHistBlock);
+            for (int i = threadIdx.x; i < w4; i += blockDim.x) z[i] = make_uint4(0, 0, 0, 0);
+        }
     }
 }
 
@@ -478,6 +482,7 @@ cudaError_t launch_compress(const CompressLaunch& h, cudaStream_t s, bool pdl) {
     a.count = h.count;
     a.ratio = h.ratio;
     a.hist_zero = h.hist_zero;
+    a.hist_words = h.hist_words > 0 && h.hist_words <= kHistBlock ? h.hist_words : kHistBlock;
     a.nq = h.nq > 1 ? h.nq : 1;
     a.status = h.status;
     a.ring_pool = h.n_tokens ? static_cast<const uint8_t*>(h.ring_pool) : nullptr;  // batched mode only
@@ -524,11 +529,11 @@ cudaError_t launch_compress(const CompressLaunch& h, cudaStream_t s, bool pdl) {
     if (gx > 0x7FFFFFFFLL) gx = 0x7FFFFFFFLL;
     cfg.gridDim = dim3((unsigned)gx, (unsigned)h.B, 1);
     if (h.ratio == 4) {
-        // prefer the largest shared-memory carveout: the SM that runs this warp keeps room for
-        // the index-score kernel's CTA (about 200 KB), which starts right behind it
+        // the carveout the caller asks for: the SM that runs this warp then keeps room for the
+        // score kernel's CTAs, which start right behind it (a CTA can join an SM only in the
+        // shared-memory configuration the SM runs in)
         cudaError_t e = set_func_attr_once((const void*)compress_r4_kernel,
-                                           cudaFuncAttributePreferredSharedMemoryCarveout,
-                                           (int)cudaSharedmemCarveoutMaxShared);
+                                           cudaFuncAttributePreferredSharedMemoryCarveout, h.carveout);
         if (e != cudaSuccess) return e;
         return cudaLaunchKernelEx(&cfg, compress_r4_kernel, a);
     }

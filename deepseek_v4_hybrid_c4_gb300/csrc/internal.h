@@ -46,7 +46,8 @@ struct HPaged {            // host copy of a paged buffer description (see csa_p
 
 // Stage 1.  Single mode (n_tokens == nullptr): groups [first, first + count) of one
 // sequence.  Batched mode: request b = blockIdx.y compresses [n_done[b], n_tokens[b]/ratio).
-// hist_zero (nullable): [B][kHistBlock] words cleared by block (0, b) for stages 2 and 3.
+// hist_zero (nullable): [B][kHistBlock] blocks whose first hist_words words block (0, b) clears
+// for stages 2 and 3 (the histograms the chosen select uses).
 struct CompressLaunch {
     HWorkSet hs;               // HiSparse: the compressed pool's GPU working set (optional)
     int nq = 1;                // decode: query positions per request (speculative verify)
@@ -59,6 +60,8 @@ struct CompressLaunch {
     const int64_t* n_done;
     int64_t first, count;
     uint32_t* hist_zero;
+    int hist_words = kHistBlock;
+    int carveout = cudaSharedmemCarveoutDefault;  // C4 decode: the shared-memory carveout asked for
     int32_t* status;
     const void* ring_pool = nullptr;  // batched mode: pending tokens from per-request rings
     const int32_t* ring_page = nullptr;
@@ -94,6 +97,9 @@ bool make_kidx_map(void* map, const HPaged& p, bool fp8, int64_t rows_per_page, 
 // the fixed-order score (upper to `scores`, lower to `lower` when set), and, with hist, the first
 // digit of the lower bounds' keys.  Needs Hi <= 16, nq <= 4.
 bool score_bound_supported(int Hi, int nq, bool fp8);
+// Words of each batch entry's histogram block that a decode step's select uses: the six digit
+// histograms of the wide select, or the 2^bound_hist_bits(nq) bins after the bounds.
+constexpr int kWideSelectHistWords = 6 * kHistBins;
 cudaError_t launch_score_bound(const ScoreLaunch& a, float* lower, cudaStream_t s, bool pdl);
 
 // Stage 3.  Request b's scores: single: [0, G); offsets mode: [offsets[b], offsets[b+1]);

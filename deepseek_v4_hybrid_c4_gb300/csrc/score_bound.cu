@@ -44,10 +44,11 @@ constexpr int SB_ROWS = 128;                   // candidates per tile (MMA M)
 constexpr int SB_UNIT = 16;                    // rows per TMA box
 constexpr uint32_t SB_HALF = SB_ROWS * 128;    // dims 0..63 (or 64..127) of a tile: 16 KB
 constexpr uint32_t SB_TILE = 2 * SB_HALF;
-constexpr int SB_THREADS = 192;
+constexpr int SB_EPI = 8;                      // epilogue warps: two groups of four, one per accumulator buffer
+constexpr int SB_THREADS = (2 + SB_EPI) * 32;
 constexpr int SB_NQ = 4;                       // query positions per request, at most
 constexpr int SB_MAX_STAGES = 6;
-constexpr int SB_FLUSH_T = 128;                // epilogue threads
+constexpr int SB_FLUSH_T = SB_EPI * 32;         // epilogue threads
 constexpr float SB_MARGIN = 1.220703125e-4f;   // 2^-13
 constexpr int64_t SB_PAST = INT64_MIN;         // a unit with nothing to copy
 
@@ -82,7 +83,7 @@ __host__ __device__ inline BoundLayout bound_layout(int S, int N, int nq, bool h
     L.hist = o;
     o += hist ? ((uint32_t)nq << hb) * 4u : 0u;
     L.cst = o;
-    o += 4 * 512;  // per epilogue warp: weights [SB_NQ * 16], bounds [SB_NQ], lengths [SB_NQ]
+    o += SB_EPI * 512;  // per epilogue warp: weights [SB_NQ * 16], bounds [SB_NQ], lengths [SB_NQ]
     L.bar = o;
     o += 256;
     L.tmem = o;
@@ -157,14 +158,14 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(bar + 8u * s, 1);           // the producer's arrive + the copies' bytes
-            mbar_init(bar + 48u + 8u * s, 5);     // the MMAs' commit + 4 epilogue warps
+            mbar_init(bar + 48u + 8u * s, 5);     // the MMAs' commit + the tile's 4 epilogue warps
         }
         mbar_init(accfull, 1);
         mbar_init(accfull + 8, 1);
         mbar_init(accempty, 4);
         mbar_init(accempty + 8, 4);
         mbar_init(qbar, 1);
-        mbar_init(ebar, 4);
+        mbar_init(ebar, SB_EPI);
         fence_mbar_init();
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kmap)) : "memory");
     }
@@ -307,13 +308,14 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
     } else {
         // ---------------------------------------------------------------- epilogue
         const int qw = warp & 3;          // TMEM lane quarter
+        const int grp = (warp - 2) >> 2;  // tiles with accumulator buffer grp (jl & 1 == grp)
         const int row = qw * 32 + lane;   // the candidate of the tile this thread takes
-        float* wv = reinterpret_cast<float*>(sm + L.cst + qw * 512);  // [SB_NQ * HI] weights
+        float* wv = reinterpret_cast<float*>(sm + L.cst + (warp - 2) * 512);  // [SB_NQ * HI] weights
         float* cv = wv + SB_NQ * 16;                                  // [SB_NQ] bound factors
         int64_t* gv = reinterpret_cast<int64_t*>(cv + SB_NQ);          // [SB_NQ] candidates
         uint32_t eph = 0;
         bool ok = true, waited = false;
-        // all four epilogue warps meet (an mbarrier: the wait is bounded)
+        // all epilogue warps meet (an mbarrier: the wait is bounded)
         auto rendezvous = [&]() {
             __syncwarp();
             if (lane == 0) mbar_arrive(ebar);
@@ -377,8 +379,9 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
                 __syncwarp();
                 er = c.r;
             }
-            const int s = (int)(jl % S);
             const int buf = (int)(jl & 1);
+            if (buf != grp) continue;  // the other group's tile
+            const int s = (int)(jl % S);
             if (!mbar_wait(bar + 8u * s, (uint32_t)((jl / S) & 1)) ||
                 !mbar_wait(accfull + 8u * buf, (uint32_t)((jl >> 1) & 1))) {
                 ok = false;
@@ -437,14 +440,9 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
                     a.upper[o] = up;
                     if (a.lower) a.lower[o] = lo;
                 }
-                if (a.hist) {
-                    const uint32_t dg = score_key(lo) >> (32 - a.hb);
-                    const unsigned m = __ballot_sync(0xffffffffu, in);
-                    if (in) {
-                        const unsigned peers = __match_any_sync(m, dg);
-                        if (lane == __ffs(peers) - 1) atomicAdd(&hist[(p << a.hb) + dg], (uint32_t)__popc(peers));
-                    }
-                }
+                // 4K-16K bins over scattered scores: the lanes' bins rarely coincide, so plain
+                // shared-memory atomics (no warp aggregation)
+                if (a.hist && in) atomicAdd(&hist[(p << a.hb) + (score_key(lo) >> (32 - a.hb))], 1u);
             }
         }
         if (!ok) raise_status(a.status, CSA_ERR_TIMEOUT);

@@ -63,6 +63,8 @@ struct SelArgs {
     int32_t* out;            // [B][k]
     uint32_t* hist;          // [B][kHistBlock]: digit 0 from the score kernel; digit 1 and the counter here
     uint64_t* lists;         // [B][C * SW_SLICE]: per CTA, winners then candidates, key << 32 | index
+                             // (after the tensor-core bounds: [B][C * SB_SLICE], see slice)
+    int slice = 0;           // region stride of lists for the exact select (SB_SLICE)
     uint32_t* counts;        // [B][C]: winners << 16 | candidates
     int32_t* status;
 };
@@ -738,6 +740,8 @@ constexpr int SX_CAP = 4096;   // list entries the exact select ranks in shared 
 constexpr int SX_CTAS = 16;    // CTAs per batch entry of the exact select
 constexpr int SX_QMAX = 16;    // index heads
 constexpr int SX_SLOTS = SW_T * 4;  // chain slots of one rescoring round (four per thread)
+constexpr int SB_PER = 8;              // upper bounds per thread of the bound scan
+constexpr int SB_SLICE = SW_T * SB_PER;  // per bound-scan CTA: the lists region of the exact select
 
 struct BoundSelArgs {
     SelArgs s;                 // scores = upper bounds; hist: top HB bits of the lower bounds' keys
@@ -758,11 +762,11 @@ static_assert(offsetof(SxSmem, hist) % 16 == 0, "16-byte loads of the histogram"
 
 struct SbSmem {                          // bound scan
     SwCore core;
-    uint32_t cidx[SW_SLICE];             // the slice's candidates (index order)
-    const uint8_t* rowp[SW_SLICE];       // their key rows (nullptr: page out of range)
+    uint32_t cidx[SB_SLICE];             // the slice's candidates (index order)
     float qf[4 * SX_QMAX * 33];          // chain n = 4h + j: q_h[32j + d] at n * 33 + d
     float wf[SX_QMAX];
     float qv[SX_SLOTS + SW_T];           // a round's chain results, candidate c at c * (4 Hi + 1)
+    uint8_t gone[SX_SLOTS / 16];         // a round's candidates whose page id is out of range
 };
 
 // The bin holding the need-th largest element of a 2^HB-bin histogram hb (global memory),
@@ -802,7 +806,7 @@ __device__ __forceinline__ void sw_find_bin_wide(SwCore& sm, const uint32_t* hb,
 }
 
 template <int HB>
-__global__ void __launch_bounds__(SW_T) select_bound_scan_kernel(BoundSelArgs a) {
+__global__ void __launch_bounds__(SW_T, 2) select_bound_scan_kernel(BoundSelArgs a) {
     __shared__ SbSmem sm;
     const int tid = threadIdx.x;
     const int b = blockIdx.x, c = blockIdx.y, C = a.s.C, k = a.s.k;
@@ -810,7 +814,7 @@ __global__ void __launch_bounds__(SW_T) select_bound_scan_kernel(BoundSelArgs a)
     int64_t G;
     sel_span(a.s, b, sc, G);
     const uint32_t* hb = a.s.hist + (int64_t)b * kHistBlock;
-    uint64_t* lc = a.s.lists + ((int64_t)b * C + c) * SW_SLICE;
+    uint64_t* lc = a.s.lists + ((int64_t)b * C + c) * SB_SLICE;
     const bool all_in = G <= k;
     const int Hi = a.Hi, nch = 4 * Hi;
     if (!all_in) {  // the entry's query as fp32 by chain, and its weights: inputs of the step
@@ -824,72 +828,81 @@ __global__ void __launch_bounds__(SW_T) select_bound_scan_kernel(BoundSelArgs a)
     pdl_wait();  // the bounds and the lower bounds' histogram come from the score kernel
     pdl_launch_dependents();
 
-    const int64_t pos = (int64_t)c * SW_SLICE + SW_PER * tid;
-    uint32_t key[SW_PER];
-    sel_load4(sc, pos, G, key);
+    const int64_t pos = (int64_t)c * SB_SLICE + SB_PER * tid;
+    uint32_t key[SB_PER];
+    sel_load4(sc, pos, G, *reinterpret_cast<uint32_t(*)[SW_PER]>(key));
+    sel_load4(sc, pos + SW_PER, G, *reinterpret_cast<uint32_t(*)[SW_PER]>(key + SW_PER));
     uint32_t b0 = 0;
     if (!all_in) {
         sw_find_bin_wide<HB>(sm.core, hb, (uint32_t)k);
         b0 = sm.core.bin == ~0u ? 0u : sm.core.bin;  // (fewer than k counted cannot happen; then keep all)
     }
-    bool cand[SW_PER];
-    uint32_t nc = 0;
+    uint32_t cm = 0, nc = 0;  // candidate mask over the thread's 8 scores
 #pragma unroll
-    for (int q = 0; q < SW_PER; ++q) {
-        cand[q] = pos + q < G && (all_in || (key[q] >> (32 - HB)) >= b0);
-        nc += cand[q] ? 1u : 0u;
-    }
+    for (int q = 0; q < SB_PER; ++q)
+        if (pos + q < G && (all_in || (key[q] >> (32 - HB)) >= b0)) {
+            cm |= 1u << q;
+            ++nc;
+        }
     uint32_t tot;
     uint32_t oc = sw_scan(sm.core, nc, &tot);
 #pragma unroll
-    for (int q = 0; q < SW_PER; ++q)
-        if (cand[q]) sm.cidx[oc++] = (uint32_t)(pos + q);
+    for (int q = 0; q < SB_PER; ++q)
+        if (cm >> q & 1u) sm.cidx[oc++] = (uint32_t)(pos + q);
     __syncthreads();
     if (all_in) {
         for (uint32_t i = tid; i < tot; i += SW_T) lc[i] = sm.cidx[i];
     } else {
-        for (uint32_t i = tid; i < tot; i += SW_T) sm.rowp[i] = row_addr(a.kidx, b, sm.cidx[i], 256, a.s.status);
-        __syncthreads();
         const int rc = SX_SLOTS / nch;  // candidates per round
         for (uint32_t base = 0; base < tot; base += (uint32_t)rc) {
-            // four chains per thread: slot = tid + s * SW_T -> candidate slot / nch, chain slot % nch
-            float p[4];
-            uint4 kv[4][4];
+            const int nr = (int)(tot - base < (uint32_t)rc ? tot - base : (uint32_t)rc);
+            const int act = nr * nch;  // active chain slots of the round
+            // chain slot tid + s * SW_T (s < 4) -> candidate slot / nch, chain slot % nch; two
+            // slots in flight at a time
+#pragma unroll 1
+            for (int s2 = 0; s2 < 4; s2 += 2) {
+                if ((tid & ~31) + s2 * SW_T >= act) break;  // (warp-uniform) no active slot left
+                float p[2] = {0.f, 0.f};
+                uint4 kv[2][4];
+                bool ok[2];
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const int slot = tid + s * SW_T;
-                const uint32_t i = base + (uint32_t)(slot / nch);
-                const uint8_t* row = (slot < rc * nch && i < tot) ? sm.rowp[i] : nullptr;
-                const int j = (slot % nch) & 3;
+                for (int u = 0; u < 2; ++u) {
+                    const int slot = tid + (s2 + u) * SW_T;
+                    const uint8_t* row = nullptr;
+                    if (slot < act) row = row_addr(a.kidx, b, sm.cidx[base + slot / nch], 256, a.s.status);
+                    ok[u] = row != nullptr;
+                    const int j = (slot % nch) & 3;
 #pragma unroll
-                for (int v = 0; v < 4; ++v)
-                    kv[s][v] = row ? __ldg(reinterpret_cast<const uint4*>(row + 64 * j) + v) : make_uint4(0, 0, 0, 0);
-            }
+                    for (int v = 0; v < 4; ++v)
+                        kv[u][v] = ok[u] ? __ldg(reinterpret_cast<const uint4*>(row + 64 * j) + v) : make_uint4(0, 0, 0, 0);
+                }
 #pragma unroll
-            for (int s = 0; s < 4; ++s) p[s] = 0.f;
+                for (int u = 0; u < 2; ++u) {
+                    const int n = (tid + (s2 + u) * SW_T) % nch;
+                    const float* qn = sm.qf + n * 33;
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
+                    for (int v = 0; v < 4; ++v) {
+                        const uint32_t wd[4] = {kv[u][v].x, kv[u][v].y, kv[u][v].z, kv[u][v].w};
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int d = 8 * v + e;
-#pragma unroll
-                    for (int s = 0; s < 4; ++s) {
-                        const int n = (tid + s * SW_T) % nch;
-                        const uint32_t wd = (e >> 1) == 0 ? kv[s][v].x : (e >> 1) == 1 ? kv[s][v].y
-                                          : (e >> 1) == 2 ? kv[s][v].z : kv[s][v].w;
-                        const float kf = (e & 1) ? bf16hi(wd) : bf16lo(wd);
-                        const float qq = sm.qf[n * 33 + d];
-                        p[s] = d == 0 ? __fmul_rn(qq, kf) : __fmaf_rn(qq, kf, p[s]);
+                        for (int e = 0; e < 8; ++e) {
+                            const int d = 8 * v + e;
+                            const float kf = (e & 1) ? bf16hi(wd[e >> 1]) : bf16lo(wd[e >> 1]);
+                            p[u] = d == 0 ? __fmul_rn(qn[0], kf) : __fmaf_rn(qn[d], kf, p[u]);
+                        }
                     }
                 }
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const int slot = tid + s * SW_T;
-                if (slot < rc * nch) sm.qv[(slot / nch) * (nch + 1) + slot % nch] = p[s];
+                for (int u = 0; u < 2; ++u) {
+                    const int slot = tid + (s2 + u) * SW_T;
+                    if (slot < act) {
+                        sm.qv[(slot / nch) * (nch + 1) + slot % nch] = p[u];
+                        if (slot % nch == 0) sm.gone[slot / nch] = ok[u] ? 0 : 1;
+                    }
+                }
             }
             __syncthreads();
             // combine: dot_h = (Q[0] + Q[2]) + (Q[1] + Q[3]), acc = fma(w_h, ReLU(dot_h), acc) in head order
-            if (tid < rc && base + (uint32_t)tid < tot) {
+            if (tid < nr) {
                 const uint32_t i = base + (uint32_t)tid;
                 const float* qr = sm.qv + tid * (nch + 1);
                 float acc = 0.f;
@@ -897,7 +910,7 @@ __global__ void __launch_bounds__(SW_T) select_bound_scan_kernel(BoundSelArgs a)
                     const float dot = (qr[4 * h] + qr[4 * h + 2]) + (qr[4 * h + 1] + qr[4 * h + 3]);
                     acc = __fmaf_rn(sm.wf[h], dot > 0.f ? dot : 0.f, acc);
                 }
-                if (!sm.rowp[i]) acc = 0.f;  // page out of range: scored 0, as by the fixed-order kernel
+                if (sm.gone[tid]) acc = 0.f;  // page out of range: scored 0, as by the fixed-order kernel
                 lc[i] = ((uint64_t)score_key(acc) << 32) | sm.cidx[i];
             }
             __syncthreads();
@@ -911,7 +924,8 @@ __global__ void __launch_bounds__(SW_T, 1) select_exact_kernel(SelArgs a) {
     SxSmem& sm = *reinterpret_cast<SxSmem*>(sx_raw);  // the dynamic shared memory starts 16-byte aligned
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int b = blockIdx.x, part = blockIdx.y, C = a.C, k = a.k;
-    const uint64_t* lb = a.lists + (int64_t)b * C * SW_SLICE;
+    const int64_t rs = a.slice;  // region stride of the lists
+    const uint64_t* lb = a.lists + (int64_t)b * C * rs;
     const uint32_t* cb = a.counts + (int64_t)b * C;
     int32_t* out = a.out + (int64_t)b * k;
     pdl_wait();  // the lists and their counts come from the scan
@@ -944,7 +958,7 @@ __global__ void __launch_bounds__(SW_T, 1) select_exact_kernel(SelArgs a) {
             const uint32_t i = tid + (uint32_t)q * SW_T;
             if (i < n) {
                 const int cc = sw_owner(sm.pre, C, i);
-                ld[q] = __ldcg(lb + (int64_t)cc * SW_SLICE + (i - sm.pre[cc]));
+                ld[q] = __ldcg(lb + (int64_t)cc * rs + (i - sm.pre[cc]));
             }
         }
 #pragma unroll
@@ -953,14 +967,20 @@ __global__ void __launch_bounds__(SW_T, 1) select_exact_kernel(SelArgs a) {
             if (i < n) sm.ent[i] = sel_comp(ld[q]);
         }
         __syncthreads();
+        // eight lanes per entry, each over every eighth composite, summed with shuffles
         const uint32_t per = (n + SX_CTAS - 1) / SX_CTAS;
         const uint32_t i0 = (uint32_t)part * per, i1 = i0 + per < n ? i0 + per : n;
-        for (uint32_t i = i0 + tid; i < i1; i += SW_T) {
-            const uint64_t v = sm.ent[i];
+        const uint32_t sub = (uint32_t)tid & 7u;
+        for (uint32_t e0 = i0; e0 < i1; e0 += SW_T / 8) {  // (the same trip count in every lane)
+            const uint32_t i = e0 + ((uint32_t)tid >> 3);
+            const uint64_t v = i < i1 ? sm.ent[i] : ~0ull;
             uint32_t r = 0;
-#pragma unroll 8
-            for (uint32_t m = 0; m < n; ++m) r += sm.ent[m] > v ? 1u : 0u;
-            if (r < (uint32_t)k) out[r] = (int32_t)(0x7FFFFFFFu - (uint32_t)(v & 0x7FFFFFFFu));
+#pragma unroll 4
+            for (uint32_t m = sub; m < n; m += 8) r += sm.ent[m] > v ? 1u : 0u;
+            r += __shfl_xor_sync(0xffffffffu, r, 1);
+            r += __shfl_xor_sync(0xffffffffu, r, 2);
+            r += __shfl_xor_sync(0xffffffffu, r, 4);
+            if (i < i1 && sub == 0 && r < (uint32_t)k) out[r] = (int32_t)(0x7FFFFFFFu - (uint32_t)(v & 0x7FFFFFFFu));
         }
         if (part == 0)
             for (uint32_t i = n + tid; i < (uint32_t)k; i += SW_T) out[i] = -1;
@@ -971,7 +991,7 @@ __global__ void __launch_bounds__(SW_T, 1) select_exact_kernel(SelArgs a) {
     // ---- more entries than fit: radix select over the lists in L2, the set in index order.
     // Digits key 31..21 | 20..10 | 9..0, inverted index 30..20 | 19..10 | 9..0 (composite bits
     // 63..53 | 52..42 | 41..32 | 30..20 | 19..10 | 9..0).
-    auto entry = [&](int cc, uint32_t i) -> uint64_t { return sel_comp(__ldcg(lb + (int64_t)cc * SW_SLICE + i)); };
+    auto entry = [&](int cc, uint32_t i) -> uint64_t { return sel_comp(__ldcg(lb + (int64_t)cc * rs + i)); };
     uint64_t prefix = 0, pmask = 0;
     {
         const int shift[6] = {53, 42, 32, 20, 10, 0};
@@ -1057,10 +1077,16 @@ bool select_set_supported(int64_t max_G, int k) {
     return select_set_ctas(max_G) <= SW_CMAX && k >= 1 && k <= 2048;
 }
 
+static int64_t bound_scan_ctas(int64_t max_G) { return max_G <= 0 ? 1 : (max_G + SB_SLICE - 1) / SB_SLICE; }
+
 size_t select_set_lists_bytes(int B, int64_t max_G) {
     if (!select_set_supported(max_G, 1)) return 0;
-    const int64_t C = select_set_ctas(max_G);
-    return align_up((size_t)B * C * SW_SLICE * sizeof(uint64_t), 256) + align_up((size_t)B * C * sizeof(uint32_t), 256);
+    const int64_t C = select_set_ctas(max_G), Cb = bound_scan_ctas(max_G);  // (either select's layout)
+    const size_t wide = align_up((size_t)B * C * SW_SLICE * sizeof(uint64_t), 256) +
+                        align_up((size_t)B * C * sizeof(uint32_t), 256);
+    const size_t bound = align_up((size_t)B * Cb * SB_SLICE * sizeof(uint64_t), 256) +
+                         align_up((size_t)B * Cb * sizeof(uint32_t), 256);
+    return wide > bound ? wide : bound;
 }
 
 cudaError_t launch_select_set(const SelectSetLaunch& h, cudaStream_t s, bool pdl) {
@@ -1081,6 +1107,7 @@ cudaError_t launch_select_set(const SelectSetLaunch& h, cudaStream_t s, bool pdl
     a.lists = reinterpret_cast<uint64_t*>(h.lists);
     a.counts = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(h.lists) +
                                            align_up((size_t)h.B * a.C * SW_SLICE * sizeof(uint64_t), 256));
+    a.slice = SW_SLICE;
     a.status = h.status;
     const size_t smem = sizeof(SwFinSmem);
     static_assert(sizeof(SwFinSmem) + SW_SCAN_SPREAD_SMEM + 2 * 1024 <= 228 * 1024, "a scan and a finish CTA share an SM");
@@ -1140,13 +1167,14 @@ cudaError_t launch_select_bound(const SelectSetLaunch& h, const BoundRescore& r,
     a.s.G = 0;
     a.s.sorted = 0;
     a.s.keys_out = nullptr;
-    a.s.C = (int)select_set_ctas(h.max_G);
+    a.s.C = (int)bound_scan_ctas(h.max_G);
     a.s.k = h.k;
     a.s.out = h.idx_out;
     a.s.hist = h.hist;
     a.s.lists = reinterpret_cast<uint64_t*>(h.lists);
     a.s.counts = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(h.lists) +
-                                             align_up((size_t)h.B * a.s.C * SW_SLICE * sizeof(uint64_t), 256));
+                                             align_up((size_t)h.B * a.s.C * SB_SLICE * sizeof(uint64_t), 256));
+    a.s.slice = SB_SLICE;
     a.s.status = h.status;
     a.q_idx = static_cast<const uint16_t*>(r.q_idx);
     a.w_h = r.w_h;
@@ -1166,8 +1194,6 @@ cudaError_t launch_select_bound(const SelectSetLaunch& h, const BoundRescore& r,
     {
         cudaError_t e = set_func_attr_once((const void*)select_exact_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e == cudaSuccess)
-            e = set_func_attr_once(scan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SW_SCAN_SPREAD_SMEM);
         if (e != cudaSuccess) return e;
     }
     cudaLaunchConfig_t cfg = {};
@@ -1180,7 +1206,7 @@ cudaError_t launch_select_bound(const SelectSetLaunch& h, const BoundRescore& r,
     if (!sms) return cudaErrorInvalidDevice;
     cfg.gridDim = dim3((unsigned)h.B, (unsigned)a.s.C, 1);
     cfg.blockDim = dim3(SW_T, 1, 1);
-    cfg.dynamicSmemBytes = (int64_t)a.s.C * h.B <= sms ? SW_SCAN_SPREAD_SMEM : 0;  // one scan CTA per SM
+    cfg.dynamicSmemBytes = 0;  // two scan CTAs per SM: 4 x 64 slices of the 1M workload are one wave
     cfg.stream = s;
     void* args[] = {&a};
     cudaError_t e = cudaLaunchKernelExC(&cfg, scan, args);
