@@ -267,7 +267,9 @@ __global__ void __launch_bounds__(SW_T) select_scan_kernel(SelArgs a) {
     if (tid == 0) a.counts[(int64_t)b * C + c] = (tw << 16) | tc;
 }
 
-__global__ void __launch_bounds__(SW_T, 1) select_finish_kernel(SelArgs a) {
+// At most 88 registers: 512 x 88 plus a scan CTA's 512 x 40 fill the register file exactly, so a
+// finish CTA becomes resident beside its SM's scan CTA and waits there (no spills at this cap).
+__global__ void __maxnreg__(88) select_finish_kernel(SelArgs a) {
     extern __shared__ __align__(16) uint8_t sw_raw[];
     SwFinSmem& fs = *reinterpret_cast<SwFinSmem*>(sw_raw);
     SwCore& sm = fs.core;
