@@ -710,6 +710,7 @@ csa_status csa_decode_timed(const csa_decode_params* p, void* workspace, size_t 
         a.hs.step = p->hs_step;
     }
     a.sel = sel;
+    a.n_done = p->n_groups_done;
     a.sel_stride = p->k;
     a.n_sel = p->ratio == 4 ? p->k : 0;
     a.B = Bq;

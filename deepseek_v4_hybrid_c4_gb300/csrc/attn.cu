@@ -61,6 +61,8 @@ struct AttnArgs {
     const int64_t* n_tokens;
     int ratio;
     int nq;                    // decode: query positions per request
+    const int64_t* n_done;     // decode, dense (sel == nullptr): compressed rows of earlier steps per
+                               // request; rows [n_done, n_c) come from this step's compressor
     int64_t N;
     int swa;
     int tps, S;
@@ -467,14 +469,30 @@ __global__ void __launch_bounds__(AT_T, 1) attn64_kernel(AttnArgs a) {
         cp_async_commit();
     };
 
-    // the selection and the freshly compressed rows come from the preceding kernels
-    pdl_wait();
-    pdl_launch_dependents();
+    // The selection and the freshly compressed rows come from the preceding kernels.  A dense
+    // step (no selection) needs them only from the first tile holding a row its compressor wrote,
+    // so a split over earlier rows starts at once; everything else waits before its first tile.
+    int64_t t_fresh = 0;  // the first tile that must wait for the preceding kernels
+    if (!a.sel && a.n_tokens && a.n_done) {
+        const int64_t done = __ldg(a.n_done + b / a.nq);
+        t_fresh = done < n_c ? done / AT_KT : T;
+    }
+    bool waited = false;
+    auto wait_for = [&](int64_t tile) {  // every thread, at the same points
+        if (!waited && tile >= t_fresh) {
+            pdl_wait();
+            pdl_launch_dependents();
+            waited = true;
+        }
+    };
+    if (t_fresh >= t1) pdl_launch_dependents();  // this split never waits (the merge waits for the grid)
+    wait_for(t0);
     if (soft) publish(0, key_row(t0 * AT_KT + tid));
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     gather(0);
+    if (t0 + 1 < t1) wait_for(t0 + 1);
     const uint8_t* p_next = soft && t0 + 1 < t1 ? key_row((t0 + 1) * AT_KT + tid) : nullptr;
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + A6_SM_TMEM);
     const uint32_t t_o = tmem, t_s = tmem + AT_DH;
@@ -507,6 +525,7 @@ __global__ void __launch_bounds__(AT_T, 1) attn64_kernel(AttnArgs a) {
                 }
             tc_commit(bar_s);
         }
+        if (tile + 2 < t1) wait_for(tile + 2);
         if (soft && tile + 2 < t1) p_next = key_row((tile + 2) * AT_KT + tid);
         float alpha = 1.f;
         if (soft) {
@@ -654,38 +673,69 @@ __global__ void __launch_bounds__(AT_T, 1) attn64_kernel(AttnArgs a) {
 
 // Log-sum-exp merge of the splits: one CTA per (head, request); thread t owns columns
 // 4t .. 4t+3 (half t / 64).  Every split's (max, sum) and row piece are loaded at once.
+// Up to 16 splits every split's row piece is loaded at once; above, 8 at a time, so that four
+// CTAs fit on an SM (a batch of 8 requests x 64 heads is 512 CTAs: one wave).
 template <int MAXS>
-__global__ void __launch_bounds__(128) attn_merge_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(128, MAXS > 16 ? 4 : 0) attn_merge_kernel(AttnArgs a) {
     pdl_wait();
     const int h = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
     const int H = a.H, S = a.S, half = t >> 6;
     const float2* mlb = a.part_ml + ((int64_t)b * 2 + half) * S * H + h;
     const __half* pb = a.part_o + ((int64_t)b * S * H + h) * D + t * 4;
+    float M = -INFINITY, L = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
     float2 ml[MAXS];
-    uint2 x[MAXS];
+    if constexpr (MAXS <= 16) {
+        uint2 x[MAXS];
 #pragma unroll
-    for (int s = 0; s < MAXS; ++s) {
-        if (s < S) {
-            ml[s] = __ldcg(mlb + (int64_t)s * H);
-            x[s] = __ldcg(reinterpret_cast<const uint2*>(pb + (int64_t)s * H * D));
+        for (int s = 0; s < MAXS; ++s) {
+            if (s < S) {
+                ml[s] = __ldcg(mlb + (int64_t)s * H);
+                x[s] = __ldcg(reinterpret_cast<const uint2*>(pb + (int64_t)s * H * D));
+            }
         }
-    }
-    float M = -INFINITY;
 #pragma unroll
-    for (int s = 0; s < MAXS; ++s)
-        if (s < S && ml[s].y > 0.f) M = fmaxf(M, ml[s].x);
-    float L = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+        for (int s = 0; s < MAXS; ++s)
+            if (s < S && ml[s].y > 0.f) M = fmaxf(M, ml[s].x);
 #pragma unroll
-    for (int s = 0; s < MAXS; ++s) {
-        if (s < S && ml[s].y > 0.f) {
-            const float w = ml[s].y * ex2(ml[s].x - M);
-            const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&x[s].x));
-            const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&x[s].y));
-            L += w;
-            o0 = fmaf(w, f01.x, o0);
-            o1 = fmaf(w, f01.y, o1);
-            o2 = fmaf(w, f23.x, o2);
-            o3 = fmaf(w, f23.y, o3);
+        for (int s = 0; s < MAXS; ++s) {
+            if (s < S && ml[s].y > 0.f) {
+                const float w = ml[s].y * ex2(ml[s].x - M);
+                const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&x[s].x));
+                const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&x[s].y));
+                L += w;
+                o0 = fmaf(w, f01.x, o0);
+                o1 = fmaf(w, f01.y, o1);
+                o2 = fmaf(w, f23.x, o2);
+                o3 = fmaf(w, f23.y, o3);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int s = 0; s < MAXS; ++s)
+            if (s < S) ml[s] = __ldcg(mlb + (int64_t)s * H);
+#pragma unroll
+        for (int s = 0; s < MAXS; ++s)
+            if (s < S && ml[s].y > 0.f) M = fmaxf(M, ml[s].x);
+#pragma unroll
+        for (int s0 = 0; s0 < MAXS; s0 += 8) {
+            uint2 x[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (s0 + j < S) x[j] = __ldcg(reinterpret_cast<const uint2*>(pb + (int64_t)(s0 + j) * H * D));
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int s = s0 + j;
+                if (s < S && ml[s].y > 0.f) {
+                    const float w = ml[s].y * ex2(ml[s].x - M);
+                    const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&x[j].x));
+                    const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&x[j].y));
+                    L += w;
+                    o0 = fmaf(w, f01.x, o0);
+                    o1 = fmaf(w, f01.y, o1);
+                    o2 = fmaf(w, f23.x, o2);
+                    o3 = fmaf(w, f23.y, o3);
+                }
+            }
         }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
@@ -790,6 +840,7 @@ cudaError_t launch_attn(const AttnLaunch& h, cudaStream_t s, bool pdl) {
     a.n_tokens = h.n_tokens;
     a.ratio = h.ratio;
     a.nq = h.nq > 1 ? h.nq : 1;
+    a.n_done = h.n_done;
     a.N = h.N;
     a.swa = h.swa;
     plan_splits(h.B, h.H, h.max_keys, &a.tps, &a.S);

@@ -188,6 +188,7 @@ struct AttnLaunch {
     void* out;                 // bf16 [B, H, 512]
     float* lse;                // [B, H] or nullptr
     float* out_f32 = nullptr;  // instead of out: fp32 [B, H, 512] rows of a mergeable partial
+    const int64_t* n_done = nullptr;  // decode, dense: rows of earlier steps per request (see attn.cu)
     void* ws;
     size_t ws_bytes;
     int32_t* status;
