@@ -55,6 +55,31 @@ def test_library_loads_and_answers_host_queries(libpath):
     assert csa.csa_decode_workspace_size(p) == 0
 
 
+def test_index_score_bounds_validates_its_arguments(libpath):
+    """csa_index_score_bounds rejects synchronously, with nothing enqueued: fp8 keys and head
+    counts outside 1..16 (unsupported), missing or misaligned pointers, a negative or oversized G,
+    a page table whose pages are not whole 16-row boxes."""
+    import ctypes
+    import deepseek_v4_hybrid_c4_gb300 as csa
+    L = csa.lib()
+    a16 = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
+    a4 = ctypes.c_void_p(0x10004)
+    contiguous = csa.csa_paged(0x20000, None, 16, 16 * 256, 4)
+    f = L.csa_index_score_bounds
+    assert f(a16, a16, 8, contiguous, csa.CSA_FP8_E4M3, 64, None, a16, None) == csa.CSA_ERR_UNSUPPORTED
+    assert f(a16, a16, 0, contiguous, csa.CSA_BF16, 64, None, a16, None) == csa.CSA_ERR_UNSUPPORTED
+    assert f(a16, a16, 17, contiguous, csa.CSA_BF16, 64, None, a16, None) == csa.CSA_ERR_UNSUPPORTED
+    assert f(None, a16, 8, contiguous, csa.CSA_BF16, 64, None, a16, None) == csa.CSA_ERR_INVALID_ARG
+    assert f(a4, a16, 8, contiguous, csa.CSA_BF16, 64, None, a16, None) == csa.CSA_ERR_INVALID_ARG
+    assert f(a16, a16, 8, contiguous, csa.CSA_BF16, 64, None, None, None) == csa.CSA_ERR_INVALID_ARG
+    assert f(a16, a16, 8, contiguous, csa.CSA_BF16, 64, ctypes.c_void_p(0x10002), a16, None) == csa.CSA_ERR_INVALID_ARG
+    assert f(a16, a16, 8, contiguous, csa.CSA_BF16, -1, None, a16, None) == csa.CSA_ERR_INVALID_ARG
+    assert f(a16, a16, 8, contiguous, csa.CSA_BF16, 1 << 31, None, a16, None) == csa.CSA_ERR_INVALID_ARG
+    paged8 = csa.csa_paged(0x20000, 0x30000, 8, 8 * 256, 4)
+    assert f(a16, a16, 8, paged8, csa.CSA_BF16, 64, None, a16, None) == csa.CSA_ERR_UNSUPPORTED
+    assert f(a16, a16, 8, contiguous, csa.CSA_BF16, 0, None, a16, None) == csa.CSA_OK  # nothing to do
+
+
 def test_binding_has_the_c_names():
     import deepseek_v4_hybrid_c4_gb300 as csa
     for n in declared_functions():
