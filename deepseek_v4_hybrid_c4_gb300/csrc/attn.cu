@@ -29,7 +29,8 @@
 
 namespace csa {
 
-constexpr int AT_T = 128;
+constexpr int AT_T = 128;                          // threads that own a TMEM lane (head row) each
+constexpr int A1_T = 384;                          // attn_kernel: warps 4-11 only help gather and store
 constexpr int AT_M = 128;
 constexpr int AT_KT = 64;
 constexpr int AT_DH = 256;
@@ -87,7 +88,7 @@ __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk) {  // byte
     return row * 128u + ((chunk ^ (row & 7u)) << 4);
 }
 
-__global__ void __launch_bounds__(AT_T, 1) attn_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(A1_T, 1) attn_kernel(AttnArgs a) {
     extern __shared__ uint8_t at_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(at_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(sm);
@@ -125,7 +126,7 @@ __global__ void __launch_bounds__(AT_T, 1) attn_kernel(AttnArgs a) {
         }
         // Q -> swizzled K-major tile (rows >= H are zero)
         const uint16_t* qb = a.q + (int64_t)b * H * D;
-        for (int c = tid; c < AT_M * 64; c += AT_T) {
+        for (int c = tid; c < AT_M * 64; c += A1_T) {
             const uint32_t row = c >> 6, ch = c & 63;
             const uint32_t dst = sbase + SM_Q + (ch >> 3) * Q_SLAB + swz(row, ch & 7);
             if ((int)row < H)
@@ -171,7 +172,7 @@ __global__ void __launch_bounds__(AT_T, 1) attn_kernel(AttnArgs a) {
             // also carries the staged Q), so that S runs on each pair of slabs as it lands
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
-                for (int c = tid; c < AT_KT * 16; c += AT_T) {
+                for (int c = tid; c < AT_KT * 16; c += A1_T) {
                     const uint32_t row = c >> 4, ch = 16 * g + (c & 15);
                     const uint32_t dst = sbase + SM_K + (ch >> 3) * K_SLAB + swz(row, ch & 7);
                     const uint8_t* src = kptr[row];
@@ -207,60 +208,61 @@ __global__ void __launch_bounds__(AT_T, 1) attn_kernel(AttnArgs a) {
             }
             // the next tile's rows: look them up (dependent loads) while S runs
             if (tid < AT_KT && tile + 1 < t1) p_next = key_row((tile + 1) * AT_KT + tid);
-            if (!mbar_wait(bar_s, (uint32_t)(it & 1))) ok = false;
-            tc_fence_after();
-            // ---- online softmax for row h
-            uint32_t sr[2][32];
-            tc_ld32(t_s + lane_off, sr[0]);
-            tc_ld32(t_s + lane_off + 32, sr[1]);
-            tc_wait_ld();
-            const uint64_t valid = *kok;
-            float x[64];
-            float mt = -INFINITY;
+            if (tid < AT_T) {  // ---- online softmax for row h (warps 0-3)
+                if (!mbar_wait(bar_s, (uint32_t)(it & 1))) ok = false;
+                tc_fence_after();
+                uint32_t sr[2][32];
+                tc_ld32(t_s + lane_off, sr[0]);
+                tc_ld32(t_s + lane_off + 32, sr[1]);
+                tc_wait_ld();
+                const uint64_t valid = *kok;
+                float x[64];
+                float mt = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                const bool v = (valid >> j) & 1ull;
-                x[j] = v ? __uint_as_float(sr[j >> 5][j & 31]) * a.sl2 : -INFINITY;
-                mt = fmaxf(mt, x[j]);
-            }
-            float alpha = 1.f;
-            if (mt > -INFINITY) {
-                if (m_run == -INFINITY) {
-                    m_run = mt;
-                } else if (mt > m_run + RESCALE_THRESHOLD) {
-                    alpha = ex2(m_run - mt);
-                    m_run = mt;
+                for (int j = 0; j < 64; ++j) {
+                    const bool v = (valid >> j) & 1ull;
+                    x[j] = v ? __uint_as_float(sr[j >> 5][j & 31]) * a.sl2 : -INFINITY;
+                    mt = fmaxf(mt, x[j]);
                 }
-            }
-            // rescale O (columns of this CTA's half) when the running max moved
-            const bool need = it > 0 && alpha != 1.f;
-            if (__any_sync(0xffffffffu, need)) {
+                float alpha = 1.f;
+                if (mt > -INFINITY) {
+                    if (m_run == -INFINITY) {
+                        m_run = mt;
+                    } else if (mt > m_run + RESCALE_THRESHOLD) {
+                        alpha = ex2(m_run - mt);
+                        m_run = mt;
+                    }
+                }
+                // rescale O (columns of this CTA's half) when the running max moved
+                const bool need = it > 0 && alpha != 1.f;
+                if (__any_sync(0xffffffffu, need)) {
 #pragma unroll 1
-                for (int c = 0; c < AT_DH; c += 32) {
-                    uint32_t o[32];
-                    tc_ld32(t_o + lane_off + c, o);
-                    tc_wait_ld();
+                    for (int c = 0; c < AT_DH; c += 32) {
+                        uint32_t o[32];
+                        tc_ld32(t_o + lane_off + c, o);
+                        tc_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                    tc_st32(t_o + lane_off + c, o);
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tc_st32(t_o + lane_off + c, o);
+                    }
+                    tc_wait_st();
                 }
-                tc_wait_st();
-            }
-            float lsum = 0.f;
-            uint32_t pk[32];
+                float lsum = 0.f;
+                uint32_t pk[32];
 #pragma unroll
-            for (int j = 0; j < 64; j += 2) {
-                const float p0 = m_run == -INFINITY ? 0.f : ex2(x[j] - m_run);
-                const float p1 = m_run == -INFINITY ? 0.f : ex2(x[j + 1] - m_run);
-                const uint32_t w = pack_bf16x2(p0, p1);
-                pk[j >> 1] = w;
-                lsum += bf16lo(w) + bf16hi(w);
-            }
-            l_run = l_run * alpha + lsum;
+                for (int j = 0; j < 64; j += 2) {
+                    const float p0 = m_run == -INFINITY ? 0.f : ex2(x[j] - m_run);
+                    const float p1 = m_run == -INFINITY ? 0.f : ex2(x[j + 1] - m_run);
+                    const uint32_t w = pack_bf16x2(p0, p1);
+                    pk[j >> 1] = w;
+                    lsum += bf16lo(w) + bf16hi(w);
+                }
+                l_run = l_run * alpha + lsum;
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-                st_shared_v4(sbase + SM_P + swz((uint32_t)h, (uint32_t)c),
-                             make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
+                for (int c = 0; c < 8; ++c)
+                    st_shared_v4(sbase + SM_P + swz((uint32_t)h, (uint32_t)c),
+                                 make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
+            }
             fence_proxy_async_smem();
             tc_fence_before();
             __syncthreads();
@@ -290,7 +292,7 @@ __global__ void __launch_bounds__(AT_T, 1) attn_kernel(AttnArgs a) {
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
         const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + SM_TMEM);
         const uint32_t srow = sbase + SM_STG + (uint32_t)h * R_PITCH;
-        for (int c0 = 0; c0 < AT_DH; c0 += 128) {  // four TMEM loads in flight, one wait
+        for (int c0 = 0; c0 < AT_DH && tid < AT_T; c0 += 128) {  // four TMEM loads in flight, one wait
             uint32_t o[4][32];
 #pragma unroll
             for (int qq = 0; qq < 4; ++qq)
@@ -321,7 +323,7 @@ __global__ void __launch_bounds__(AT_T, 1) attn_kernel(AttnArgs a) {
         // warp w copies rows w, w + 4, ...: one 512-byte row per warp instruction
         uint16_t* dst = direct ? a.out + (int64_t)b * H * D + half * AT_DH
                                : reinterpret_cast<uint16_t*>(a.part_o + ((int64_t)b * S + split) * H * D + half * AT_DH);
-        constexpr int NWA = AT_T / 32;
+        constexpr int NWA = A1_T / 32;
         for (int r0 = warp; r0 < H; r0 += 8 * NWA) {  // eight rows per warp in flight
             uint4 v[8];
 #pragma unroll
@@ -336,7 +338,7 @@ __global__ void __launch_bounds__(AT_T, 1) attn_kernel(AttnArgs a) {
             }
         }
     } else if (direct) {  // no keys at all
-        for (int r = warp; r < H; r += AT_T / 32)
+        for (int r = warp; r < H; r += A1_T / 32)
             *reinterpret_cast<uint4*>(a.out + ((int64_t)b * H + r) * D + half * AT_DH + lane * 8) = make_uint4(0, 0, 0, 0);
     }
     if (h < H) {
@@ -362,6 +364,7 @@ __global__ void __launch_bounds__(AT_T, 1) attn_kernel(AttnArgs a) {
 // TMEM: O [0, 256) (lane h: head h, columns 0..255; lane 64 + h: head h, columns 256..511),
 // S [256, 320).
 constexpr int A6_H = 64;
+constexpr int A6_T = 384;  // warps 0-3 own the TMEM lane quarters; warps 4-11 only help gather and store
 constexpr uint32_t A6_Q_SLAB = A6_H * 128;                  // 8 KiB
 constexpr uint32_t A6_SM_Q = 0;                             // 8 slabs x 64 rows x 128 B
 constexpr uint32_t A6_SM_K = 8 * A6_Q_SLAB;                 // 2 stages x 8 slabs x 64 rows x 128 B
@@ -377,7 +380,7 @@ constexpr uint32_t A6_SMEM = A6_SM_KOK + 16 + 1024;         // + alignment slack
 static_assert(A6_SMEM <= 227 * 1024, "attn64 shared memory");
 static_assert(128 * R_PITCH <= A6_SM_P, "attn64 staging fits below P");
 
-__global__ void __launch_bounds__(AT_T, 1) attn64_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(A6_T, 1) attn64_kernel(AttnArgs a) {
     extern __shared__ uint8_t at_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(at_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(sm);
@@ -405,7 +408,7 @@ __global__ void __launch_bounds__(AT_T, 1) attn64_kernel(AttnArgs a) {
         pdl_wait();
         pdl_launch_dependents();
         if (direct)  // no keys at all
-            for (int r = warp; r < 2 * H; r += AT_T / 32)
+            for (int r = warp; r < 2 * H; r += A6_T / 32)
                 *reinterpret_cast<uint4*>(a.out + ((int64_t)b * H + (r >> 1)) * D + (r & 1) * AT_DH + lane * 8) =
                     make_uint4(0, 0, 0, 0);
         if (tid < H) {
@@ -430,7 +433,7 @@ __global__ void __launch_bounds__(AT_T, 1) attn64_kernel(AttnArgs a) {
     }
     // Q -> swizzled K-major tile of 64 rows (rows >= H are zero); the zero blocks around P
     const uint16_t* qb = a.q + (int64_t)b * H * D;
-    for (int c = tid; c < A6_H * 64; c += AT_T) {
+    for (int c = tid; c < A6_H * 64; c += A6_T) {
         const uint32_t row = c >> 6, ch = c & 63;
         const uint32_t dst = sbase + A6_SM_Q + (ch >> 3) * A6_Q_SLAB + swz(row, ch & 7);
         if ((int)row < H)
@@ -438,7 +441,7 @@ __global__ void __launch_bounds__(AT_T, 1) attn64_kernel(AttnArgs a) {
         else
             st_shared_zero16(dst);
     }
-    for (int c = tid; c < 1024; c += AT_T)
+    for (int c = tid; c < 1024; c += A6_T)
         st_shared_zero16(sbase + A6_SM_P + (uint32_t)(c < 512 ? c : c + 512) * 16u);
     cp_async_commit();
 
@@ -457,7 +460,7 @@ __global__ void __launch_bounds__(AT_T, 1) attn64_kernel(AttnArgs a) {
     };
     auto gather = [&](int st) {  // every thread; kptr[st] published and visible
         const uint32_t kb = sbase + A6_SM_K + (uint32_t)st * A6_KST;
-        for (int c = tid; c < AT_KT * 64; c += AT_T) {
+        for (int c = tid; c < AT_KT * 64; c += A6_T) {
             const uint32_t row = c >> 6, ch = c & 63;
             const uint32_t dst = kb + (ch >> 3) * K_SLAB + swz(row, ch & 7);
             const uint8_t* src = kptr[st * AT_KT + row];
@@ -571,8 +574,8 @@ __global__ void __launch_bounds__(AT_T, 1) attn64_kernel(AttnArgs a) {
         }
         __syncthreads();
         // rescale O (both column halves of the head) when its running max moved
-        if (!soft) alpha = sm_alpha[tid - A6_H];
-        if (it > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        if (!soft && tid < AT_T) alpha = sm_alpha[tid - A6_H];
+        if (tid < AT_T && it > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
             for (int c = 0; c < AT_DH; c += 32) {
                 uint32_t o[32];
@@ -610,8 +613,8 @@ __global__ void __launch_bounds__(AT_T, 1) attn64_kernel(AttnArgs a) {
     if (soft) sm_ml[tid] = make_float2(m_run, l_run);
     __syncthreads();
     // ---- rows normalised (fp16 partial, or the bf16 output when S == 1), staged as
-    //      row 2 * head + column half, then coalesced to global memory
-    {
+    //      row 2 * head + column half by warps 0-3, then coalesced to global memory by all
+    if (tid < AT_T) {
         const int hd = tid & (A6_H - 1), hv = tid >> 6;
         const float l = sm_ml[hd].y;
         const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -646,7 +649,7 @@ __global__ void __launch_bounds__(AT_T, 1) attn64_kernel(AttnArgs a) {
     if (warp == 0) tmem_dealloc(tmem, 512);
     uint16_t* dst = direct ? a.out + (int64_t)b * H * D
                            : reinterpret_cast<uint16_t*>(a.part_o + ((int64_t)b * S + split) * H * D);
-    constexpr int NWA = AT_T / 32;
+    constexpr int NWA = A6_T / 32;
     for (int r0 = warp; r0 < 2 * H; r0 += 8 * NWA) {  // eight 512-byte rows per warp in flight
         uint4 v[8];
 #pragma unroll
@@ -872,7 +875,7 @@ cudaError_t launch_attn(const AttnLaunch& h, cudaStream_t s, bool pdl) {
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     cfg.gridDim = h64 ? dim3((unsigned)a.S, (unsigned)h.B, 1) : dim3(2, (unsigned)a.S, (unsigned)h.B);
-    cfg.blockDim = dim3(AT_T, 1, 1);
+    cfg.blockDim = dim3(h64 ? A6_T : A1_T, 1, 1);
     cfg.dynamicSmemBytes = h64 ? A6_SMEM : AT_SMEM;
     cfg.stream = s;
     cudaError_t e = h64 ? cudaLaunchKernelEx(&cfg, attn64_kernel, a) : cudaLaunchKernelEx(&cfg, attn_kernel, a);
