@@ -625,6 +625,7 @@ csa_status csa_decode_timed(const csa_decode_params* p, void* workspace, size_t 
         l.max_G = max_G;
         l.hist = hist;
         l.status = st;
+        l.reserve = Bq == 1 ? 1 : 0;  // the compressor's single warp, which starts just ahead
         e = bound ? launch_score_bound(l, nullptr, s, ev == nullptr) : launch_score(l, s, ev == nullptr);
         if (e != cudaSuccess) return CSA_ERR_CUDA;
         mark(2);

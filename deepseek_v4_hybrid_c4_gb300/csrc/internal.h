@@ -88,6 +88,8 @@ struct ScoreLaunch {
     int64_t max_G;         // host bound (grid sizing)
     uint32_t* hist;        // fused first-digit histogram, [B][kHistBlock] (zeroed beforehand), or nullptr
     int32_t* status;
+    int reserve = 0;       // CTA slots left free for a kernel running beside this one (the decode
+                           // compressor's warp holds one SM's second slot while the score kernel starts)
 };
 cudaError_t launch_score(const ScoreLaunch& a, cudaStream_t s, bool pdl);
 // The TMA tensor map (a CUtensorMap at `map`) of an index-key pool seen as [pages][rows per

@@ -24,7 +24,9 @@
 //
 // Scheduling: CTAs of 6 warps, two per SM, one wave.  The work is cut into CTA-steps of 6
 // consecutive steps of one request (warp j takes step j), so all warps of a CTA work on the
-// same request at a time and share one staged query and one histogram.
+// same request at a time and share one staged query and one histogram.  With one batch entry
+// every CTA takes an equal contiguous range of steps (26 or 27 at 1M context), so whichever
+// SM a CTA lands on holds the same work within one step.
 //
 // Optional fused epilogue: a per-CTA histogram of the top 11 bits of each score's
 // order-preserving key (the first digit of the top-k radix select), flushed per
@@ -64,6 +66,8 @@ struct ScoreArgs {
     uint32_t* hist;          // [B][kHistBlock] (the first kHistBins words) or nullptr
     int32_t* status;
 };
+// With one batch entry, CTA i of n takes the steps [i S / n, (i + 1) S / n) of the S = ceil(G / 32)
+// 32-row steps: its CTA-step k covers steps s0 + 6k .. s0 + 6k + 5 (warp j the j-th), clipped at s1.
 
 // Walks the concatenated CTA-steps of the batch.  Request b has steps = ceil(G_b / 32)
 // steps of 32 rows, grouped into ceil(steps / SC_WARPS) CTA-steps of SC_WARPS consecutive
@@ -189,8 +193,15 @@ __global__ void __launch_bounds__(SC_THREADS, HI >= 16 ? 1 : 2)
     // Two register sets alternate (even / odd windows) and the next window is looked up as the
     // current one starts, so the page-table latency stays off the copy path.
     const bool blocked = a.B > 1;
-    int64_t m0 = blockIdx.x, nk = INT64_MAX;  // (one request: the stride form, ended by the cursor)
-    if (blocked) {
+    int64_t m0 = blockIdx.x, nk = INT64_MAX;
+    int64_t s0 = 0, s1 = 0;  // one batch entry: this CTA's steps [s0, s1)
+    if (!blocked) {
+        const int64_t G0 = a.B < 1 ? 0 : (a.n_tokens ? query_tokens(a.n_tokens, 0, a.nq) / a.ratio : a.G);
+        const int64_t S0 = (G0 + SC_SUPER - 1) / SC_SUPER;
+        s0 = (int64_t)blockIdx.x * S0 / gridDim.x;
+        s1 = ((int64_t)blockIdx.x + 1) * S0 / gridDim.x;
+        nk = (s1 - s0 + SC_WARPS - 1) / SC_WARPS;
+    } else {
         __shared__ int64_t s_tot[SC_WARPS];
         int64_t t = 0;  // the batch's CTA-steps (ragged requests: from the device lengths)
         for (int b = threadIdx.x; b < a.B; b += SC_THREADS) {
@@ -207,7 +218,14 @@ __global__ void __launch_bounds__(SC_THREADS, HI >= 16 ? 1 : 2)
         m0 = (int64_t)blockIdx.x * total / gridDim.x;
         nk = ((int64_t)blockIdx.x + 1) * total / gridDim.x - m0;
     }
-    auto cta_step = [&](int64_t k) { return blocked ? m0 + k : (int64_t)blockIdx.x + k * gridDim.x; };
+    // the CTA-step index of the CTA's k-th CTA-step (one batch entry: 0, the entry's; the warp's
+    // step then comes from s0), and warp `warp`'s step within its request, or -1 past the CTA's range
+    auto cta_step = [&](int64_t k) { return blocked ? m0 + k : (int64_t)0; };
+    auto warp_step = [&](int64_t k, int64_t m, int64_t base) -> int64_t {
+        if (blocked) return (m - base) * SC_WARPS + warp;
+        const int64_t st = s0 + k * SC_WARPS + warp;
+        return st < s1 ? st : -1;
+    };
     CtaStepCursor lc;  // this lane's lookup cursor
     int wk[2] = {0, 0}, ws[2] = {0, 0}, wp[2] = {0, 0};  // per set: kind (0 past the end, 1 copy,
                                                           // 2 nothing to copy), row in page, page
@@ -218,9 +236,10 @@ __global__ void __launch_bounds__(SC_THREADS, HI >= 16 ? 1 : 2)
         page = 0;
         const int64_t m = cta_step(k);
         if (k < nk && lc.seek(a, m)) {
-            const int64_t gr = ((m - lc.base) * SC_WARPS + warp) * SC_SUPER + (lane & 1) * SC_UNIT;
+            const int64_t ws_ = warp_step(k, m, lc.base);
+            const int64_t gr = ws_ * SC_SUPER + (lane & 1) * SC_UNIT;
             kind = 2;
-            if (gr < lc.G) {
+            if (ws_ >= 0 && gr < lc.G) {
                 const int64_t lp = gr / a.rpp;
                 slot = (int)(gr - lp * a.rpp);
                 int64_t pp = lp;
@@ -343,14 +362,14 @@ __global__ void __launch_bounds__(SC_THREADS, HI >= 16 ? 1 : 2)
             CtaStepCursor nx = cur;
             if (k + 1 < nk && nx.seek(a, cta_step(k + 1)) && nx.b != qb && nx.b != qf_b) q_fetch(nx.b);
         }
-        const int64_t st = (m - cur.base) * SC_WARPS + warp;  // this warp's step within the request
+        const int64_t st = warp_step(k, m, cur.base);  // this warp's step within the request (-1: none)
         const int kind_me = __shfl_sync(0xffffffffu, ((k >> 4) & 1) ? wk[1] : wk[0], 2 * (int)(k & 15) + hu);
         if (!dead && !mbar_wait(smem_u32(&full[sl]), (uint32_t)((k >> 1) & 1))) {
             raise_status(a.status, CSA_ERR_TIMEOUT);
             dead = true;
         }
         if (dead) continue;
-        if (st >= cur.steps) {  // the request's last CTA-step has fewer steps than warps
+        if (st < 0 || st >= cur.steps) {  // the request's (or this CTA's) last CTA-step has fewer steps than warps
             issue(k + 2);
             continue;
         }
@@ -460,7 +479,7 @@ bool make_kidx_map(void* map, const HPaged& p, bool fp8, int64_t rows_per_page, 
 
 template <int HI, bool FP8>
 static cudaError_t launch_score_t(const CUtensorMap& map, const ScoreArgs& a, int64_t total_steps_bound,
-                                  cudaStream_t s, bool pdl) {
+                                  int reserve, cudaStream_t s, bool pdl) {
     constexpr int QF4 = 8 * 8 * (HI / 2);
     constexpr size_t base = 1024 + (size_t)SC_WARPS * 2 * SC_SLOT_BYTES + (size_t)QF4 * 16 + 64 + SC_WARPS * 16;
     constexpr size_t with_hist = base + (size_t)kHistBins * 4;
@@ -472,7 +491,8 @@ static cudaError_t launch_score_t(const CUtensorMap& map, const ScoreArgs& a, in
     }
     const int sms = device_sm_count();
     if (!sms) return cudaErrorInvalidDevice;
-    int64_t grid = (HI >= 16 ? 1LL : 2LL) * sms;  // one wave of resident CTAs
+    int64_t grid = (HI >= 16 ? 1LL : 2LL) * sms - reserve;  // one wave of resident CTAs
+    if (grid < 1) grid = 1;
     if (total_steps_bound < grid) grid = total_steps_bound < 1 ? 1 : total_steps_bound;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -518,13 +538,13 @@ cudaError_t launch_score(const ScoreLaunch& h, cudaStream_t s, bool pdl) {
     const int64_t steps = (int64_t)h.B * (((h.max_G + SC_SUPER - 1) / SC_SUPER + SC_WARPS - 1) / SC_WARPS);
     const int hi = h.Hi <= 4 ? 4 : (h.Hi <= 8 ? 8 : 16);
     if (h.fp8) {
-        if (hi == 4) return launch_score_t<4, true>(map, a, steps, s, pdl);
-        if (hi == 8) return launch_score_t<8, true>(map, a, steps, s, pdl);
-        return launch_score_t<16, true>(map, a, steps, s, pdl);
+        if (hi == 4) return launch_score_t<4, true>(map, a, steps, h.reserve, s, pdl);
+        if (hi == 8) return launch_score_t<8, true>(map, a, steps, h.reserve, s, pdl);
+        return launch_score_t<16, true>(map, a, steps, h.reserve, s, pdl);
     }
-    if (hi == 4) return launch_score_t<4, false>(map, a, steps, s, pdl);
-    if (hi == 8) return launch_score_t<8, false>(map, a, steps, s, pdl);
-    return launch_score_t<16, false>(map, a, steps, s, pdl);
+    if (hi == 4) return launch_score_t<4, false>(map, a, steps, h.reserve, s, pdl);
+    if (hi == 8) return launch_score_t<8, false>(map, a, steps, h.reserve, s, pdl);
+    return launch_score_t<16, false>(map, a, steps, h.reserve, s, pdl);
 }
 
 }  // namespace csa
