@@ -22,11 +22,12 @@
 // steps ahead.  The swizzle puts 16-byte chunk c of row r at position c ^ (r & 7), so the
 // lanes' reads of one logical chunk of 16 rows spread over the banks.
 //
-// Scheduling: CTAs of 6 warps, two per SM, one wave.  The work is cut into CTA-steps of 6
-// consecutive steps of one request (warp j takes step j), so all warps of a CTA work on the
-// same request at a time and share one staged query and one histogram.  With one batch entry
-// every CTA takes an equal contiguous range of steps (26 or 27 at 1M context), so whichever
-// SM a CTA lands on holds the same work within one step.
+// Scheduling: one CTA per SM, one wave: 12 warps (6 for 16 index heads).  Two CTAs of 6 warps
+// per SM ran unevenly: the warp schedulers favour older warps, so the CTA dispatched first to an
+// SM finished well before its partner (by half on the fp8 path), which then ran alone.  The work
+// is cut into CTA-steps of W consecutive steps of one request (warp j takes step j), so all warps
+// of a CTA work on the same request at a time and share one staged query and one histogram.
+// With one batch entry every CTA takes an equal contiguous range of steps.
 //
 // Optional fused epilogue: a per-CTA histogram of the top 11 bits of each score's
 // order-preserving key (the first digit of the top-k radix select), flushed per
@@ -41,8 +42,11 @@
 
 namespace csa {
 
-constexpr int SC_WARPS = 6;                  // warps per CTA; each takes 32 rows (2 units) per CTA-step
-constexpr int SC_THREADS = SC_WARPS * 32;
+// Warps per CTA (one CTA per SM); each takes 32 rows (2 units) per CTA-step.  Up to 8 index heads
+// twelve warps fit the register file (at most 168 registers per thread); 16 heads need more
+// registers per thread and run six.
+template <int HI>
+__host__ __device__ constexpr int sc_warps() { return HI >= 16 ? 6 : 12; }
 constexpr int SC_UNIT = 16;                  // rows per unit (one TMA box height)
 constexpr int SC_SUPER = 32;                 // rows per warp step
 constexpr int SC_STAGE_BYTES = SC_UNIT * 256;  // one unit (bf16; fp8 uses half)
@@ -70,16 +74,17 @@ struct ScoreArgs {
 // 32-row steps: its CTA-step k covers steps s0 + 6k .. s0 + 6k + 5 (warp j the j-th), clipped at s1.
 
 // Walks the concatenated CTA-steps of the batch.  Request b has steps = ceil(G_b / 32)
-// steps of 32 rows, grouped into ceil(steps / SC_WARPS) CTA-steps of SC_WARPS consecutive
-// steps (warp j of the CTA takes step j), so a CTA-step never straddles two requests.
-// After seek(m), CTA-step m belongs to request b.  Calls must come with non-decreasing m.
+// steps of 32 rows, grouped into ceil(steps / W) CTA-steps of W consecutive steps (warp j of
+// the CTA takes step j), so a CTA-step never straddles two requests.  After seek(m), CTA-step m
+// belongs to request b.  Calls must come with non-decreasing m.
+template <int W>
 struct CtaStepCursor {
     int b = -1;
     int64_t base = 0, csteps = 0, steps = 0, G = 0;
     __device__ void load(const ScoreArgs& a) {
         G = a.n_tokens ? query_tokens(a.n_tokens, b, a.nq) / a.ratio : a.G;
         steps = (G + SC_SUPER - 1) / SC_SUPER;
-        csteps = (steps + SC_WARPS - 1) / SC_WARPS;
+        csteps = (steps + W - 1) / W;
     }
     __device__ bool seek(const ScoreArgs& a, int64_t m) {
         if (b < 0) {
@@ -157,8 +162,9 @@ __device__ __forceinline__ void load_pair(const uint8_t* stage, int r, int a, fl
 }
 
 template <int HI, bool FP8>
-__global__ void __launch_bounds__(SC_THREADS, HI >= 16 ? 1 : 2)
+__global__ void __launch_bounds__(sc_warps<HI>() * 32, 1)
     score_kernel(const __grid_constant__ CUtensorMap kmap, ScoreArgs a) {
+    constexpr int SC_WARPS = sc_warps<HI>(), SC_THREADS = SC_WARPS * 32;
     constexpr int UB = FP8 ? SC_UNIT * 128 : SC_UNIT * 256;   // bytes per 16-row unit
     constexpr int QF4 = 32 * (HI / 2) * 2;                     // float4 entries of the staged query
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -226,7 +232,7 @@ __global__ void __launch_bounds__(SC_THREADS, HI >= 16 ? 1 : 2)
         const int64_t st = s0 + k * SC_WARPS + warp;
         return st < s1 ? st : -1;
     };
-    CtaStepCursor lc;  // this lane's lookup cursor
+    CtaStepCursor<SC_WARPS> lc;  // this lane's lookup cursor
     int wk[2] = {0, 0}, ws[2] = {0, 0}, wp[2] = {0, 0};  // per set: kind (0 past the end, 1 copy,
                                                           // 2 nothing to copy), row in page, page
     auto lookup_window = [&](int64_t k0, int& kind, int& slot, int& page) {
@@ -315,7 +321,7 @@ __global__ void __launch_bounds__(SC_THREADS, HI >= 16 ? 1 : 2)
         if (threadIdx.x < HI) wsm[threadIdx.x] = wv;
     };
     {
-        CtaStepCursor c0;
+        CtaStepCursor<SC_WARPS> c0;
         if (nk > 0 && c0.seek(a, cta_step(0))) q_fetch(c0.b);
     }
     lookup_window(0, wk[0], ws[0], wp[0]);
@@ -341,7 +347,7 @@ __global__ void __launch_bounds__(SC_THREADS, HI >= 16 ? 1 : 2)
     };
     const int r = lane & 15;        // row within its unit
     const int hu = lane >> 4;       // chunk half (c)
-    CtaStepCursor cur;
+    CtaStepCursor<SC_WARPS> cur;
     for (int64_t k = 0;; ++k) {
         const int64_t m = cta_step(k);
         if (k >= nk || !cur.seek(a, m)) break;  // the same for every warp of the CTA
@@ -359,7 +365,7 @@ __global__ void __launch_bounds__(SC_THREADS, HI >= 16 ? 1 : 2)
             __syncthreads();
         }
         {  // the CTA's next CTA-step starts another request: fetch its query now
-            CtaStepCursor nx = cur;
+            CtaStepCursor<SC_WARPS> nx = cur;
             if (k + 1 < nk && nx.seek(a, cta_step(k + 1)) && nx.b != qb && nx.b != qf_b) q_fetch(nx.b);
         }
         const int64_t st = warp_step(k, m, cur.base);  // this warp's step within the request (-1: none)
@@ -478,9 +484,10 @@ bool make_kidx_map(void* map, const HPaged& p, bool fp8, int64_t rows_per_page, 
 }
 
 template <int HI, bool FP8>
-static cudaError_t launch_score_t(const CUtensorMap& map, const ScoreArgs& a, int64_t total_steps_bound,
+static cudaError_t launch_score_t(const CUtensorMap& map, const ScoreArgs& a, int64_t max_steps,
                                   int reserve, cudaStream_t s, bool pdl) {
     constexpr int QF4 = 8 * 8 * (HI / 2);
+    constexpr int SC_WARPS = sc_warps<HI>();
     constexpr size_t base = 1024 + (size_t)SC_WARPS * 2 * SC_SLOT_BYTES + (size_t)QF4 * 16 + 64 + SC_WARPS * 16;
     constexpr size_t with_hist = base + (size_t)kHistBins * 4;
     const size_t smem = a.hist ? with_hist : base;
@@ -491,7 +498,8 @@ static cudaError_t launch_score_t(const CUtensorMap& map, const ScoreArgs& a, in
     }
     const int sms = device_sm_count();
     if (!sms) return cudaErrorInvalidDevice;
-    int64_t grid = (HI >= 16 ? 1LL : 2LL) * sms - reserve;  // one wave of resident CTAs
+    int64_t grid = (int64_t)sms - reserve;  // one wave: a CTA per SM
+    const int64_t total_steps_bound = (int64_t)a.B * ((max_steps + SC_WARPS - 1) / SC_WARPS);
     if (grid < 1) grid = 1;
     if (total_steps_bound < grid) grid = total_steps_bound < 1 ? 1 : total_steps_bound;
     cudaLaunchConfig_t cfg = {};
@@ -501,7 +509,7 @@ static cudaError_t launch_score_t(const CUtensorMap& map, const ScoreArgs& a, in
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
-    cfg.blockDim = dim3(SC_THREADS, 1, 1);
+    cfg.blockDim = dim3(SC_WARPS * 32, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     return cudaLaunchKernelEx(&cfg, score_kernel<HI, FP8>, map, a);
@@ -535,7 +543,7 @@ cudaError_t launch_score(const ScoreLaunch& h, cudaStream_t s, bool pdl) {
     a.n_pages = n_pages;
     CUtensorMap map;
     if (!make_kidx_map(&map, h.kidx, h.fp8, rpp, n_pages)) return cudaErrorInvalidValue;
-    const int64_t steps = (int64_t)h.B * (((h.max_G + SC_SUPER - 1) / SC_SUPER + SC_WARPS - 1) / SC_WARPS);
+    const int64_t steps = (h.max_G + SC_SUPER - 1) / SC_SUPER;  // 32-row steps of the longest request
     const int hi = h.Hi <= 4 ? 4 : (h.Hi <= 8 ? 8 : 16);
     if (h.fp8) {
         if (hi == 4) return launch_score_t<4, true>(map, a, steps, h.reserve, s, pdl);
