@@ -36,6 +36,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "internal.h"
@@ -71,7 +72,8 @@ struct ScoreArgs {
     int32_t* status;
 };
 // With one batch entry, CTA i of n takes the steps [i S / n, (i + 1) S / n) of the S = ceil(G / 32)
-// 32-row steps: its CTA-step k covers steps s0 + 6k .. s0 + 6k + 5 (warp j the j-th), clipped at s1.
+// 32-row steps: its CTA-step k covers steps s0 + W k .. s0 + W k + W - 1 (warp j the j-th), clipped
+// at s1.
 
 // Walks the concatenated CTA-steps of the batch.  Request b has steps = ceil(G_b / 32)
 // steps of 32 rows, grouped into ceil(steps / W) CTA-steps of W consecutive steps (warp j of
@@ -85,6 +87,12 @@ struct CtaStepCursor {
         G = a.n_tokens ? query_tokens(a.n_tokens, b, a.nq) / a.ratio : a.G;
         steps = (G + SC_SUPER - 1) / SC_SUPER;
         csteps = (steps + W - 1) / W;
+    }
+    // Start at request b0, whose first CTA-step is base0 (every later seek must lie at or past it).
+    __device__ void start(const ScoreArgs& a, int b0, int64_t base0) {
+        b = b0 < a.B ? b0 : a.B;
+        base = base0;
+        if (b < a.B) load(a);
     }
     __device__ bool seek(const ScoreArgs& a, int64_t m) {
         if (b < 0) {
@@ -161,7 +169,77 @@ __device__ __forceinline__ void load_pair(const uint8_t* stage, int r, int a, fl
     }
 }
 
-template <int HI, bool FP8>
+// Several batch entries: this CTA's contiguous share [m0, m0 + nk) of the batch's CTA-steps,
+// the request holding CTA-step m0 (b_start) and that request's first CTA-step (base_start).
+template <int SC_WARPS>
+__device__ __forceinline__ void batch_share(const ScoreArgs& a, int64_t& m0, int64_t& nk, int& b_start,
+                                         int64_t& base_start) {
+    constexpr int SC_THREADS = SC_WARPS * 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __shared__ int64_t s_tot[SC_WARPS];
+    int64_t t = 0;  // the batch's CTA-steps (ragged requests: from the device lengths)
+    for (int b = threadIdx.x; b < a.B; b += SC_THREADS) {
+        const int64_t G = a.n_tokens ? query_tokens(a.n_tokens, b, a.nq) / a.ratio : a.G;
+        t += ((G + SC_SUPER - 1) / SC_SUPER + SC_WARPS - 1) / SC_WARPS;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    if (lane == 0) s_tot[warp] = t;
+    __syncthreads();
+    int64_t total = 0;
+#pragma unroll
+    for (int w = 0; w < SC_WARPS; ++w) total += s_tot[w];
+    m0 = (int64_t)blockIdx.x * total / gridDim.x;
+    nk = ((int64_t)blockIdx.x + 1) * total / gridDim.x - m0;
+    // The request holding CTA-step m0 and its first CTA-step, by a prefix over the requests in
+    // chunks of SC_THREADS: the cursors start there.  (Walking from request 0 costs one
+    // dependent length load per request: about 17 us before the first copy for a CTA that
+    // starts 25 requests into a 32-request batch.)
+    __shared__ int s_b0;
+    __shared__ int64_t s_base0, s_part[SC_WARPS];
+    if (threadIdx.x == 0) {
+        s_b0 = a.B;
+        s_base0 = total;
+    }
+    int64_t carry = 0;
+    for (int c0 = 0; c0 < a.B; c0 += SC_THREADS) {
+        const int b = c0 + (int)threadIdx.x;
+        int64_t cs = 0;
+        if (b < a.B) {
+            const int64_t G = a.n_tokens ? query_tokens(a.n_tokens, b, a.nq) / a.ratio : a.G;
+            cs = ((G + SC_SUPER - 1) / SC_SUPER + SC_WARPS - 1) / SC_WARPS;
+        }
+        int64_t x = cs;  // inclusive prefix within the warp
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        __syncthreads();  // (s_part's previous chunk read, s_b0 written)
+        if (lane == 31) s_part[warp] = x;
+        __syncthreads();
+        int64_t before = 0, chunk = 0;
+        for (int w = 0; w < SC_WARPS; ++w) {
+            before += w < warp ? s_part[w] : 0;
+            chunk += s_part[w];
+        }
+        const int64_t first = carry + before + x - cs;  // request b's first CTA-step
+        if (b < a.B && cs > 0 && m0 >= first && m0 < first + cs) {
+            s_b0 = b;
+            s_base0 = first;
+        }
+        carry += chunk;
+        __syncthreads();
+        if (s_b0 < a.B) break;  // (the same for every thread)
+    }
+    b_start = s_b0;
+    base_start = s_base0;
+}
+
+// BLK: several batch entries (contiguous shares of the batch's CTA-steps); otherwise one entry.
+// The two are separate instantiations: with the several-entry set-up compiled into the one-entry
+// kernel, the 1M step measured 0.8-1.8 us slower (same box).
+template <int HI, bool FP8, bool BLK>
 __global__ void __launch_bounds__(sc_warps<HI>() * 32) __maxnreg__(HI >= 16 ? 255 : 160)
     score_kernel(const __grid_constant__ CUtensorMap kmap, ScoreArgs a) {
     constexpr int SC_WARPS = sc_warps<HI>(), SC_THREADS = SC_WARPS * 32;
@@ -198,8 +276,10 @@ __global__ void __launch_bounds__(sc_warps<HI>() * 32) __maxnreg__(HI >= 16 ? 25
     // (l & 1) of this warp's step in CTA-step k0 + (l >> 1), all 32 loads in flight together.
     // Two register sets alternate (even / odd windows) and the next window is looked up as the
     // current one starts, so the page-table latency stays off the copy path.
-    const bool blocked = a.B > 1;
+    constexpr bool blocked = BLK;
     int64_t m0 = blockIdx.x, nk = INT64_MAX;
+    int b_start = 0;          // the cursors' starting request and its first CTA-step
+    int64_t base_start = 0;
     int64_t s0 = 0, s1 = 0;  // one batch entry: this CTA's steps [s0, s1)
     if (!blocked) {
         const int64_t G0 = a.B < 1 ? 0 : (a.n_tokens ? query_tokens(a.n_tokens, 0, a.nq) / a.ratio : a.G);
@@ -208,21 +288,7 @@ __global__ void __launch_bounds__(sc_warps<HI>() * 32) __maxnreg__(HI >= 16 ? 25
         s1 = ((int64_t)blockIdx.x + 1) * S0 / gridDim.x;
         nk = (s1 - s0 + SC_WARPS - 1) / SC_WARPS;
     } else {
-        __shared__ int64_t s_tot[SC_WARPS];
-        int64_t t = 0;  // the batch's CTA-steps (ragged requests: from the device lengths)
-        for (int b = threadIdx.x; b < a.B; b += SC_THREADS) {
-            const int64_t G = a.n_tokens ? query_tokens(a.n_tokens, b, a.nq) / a.ratio : a.G;
-            t += ((G + SC_SUPER - 1) / SC_SUPER + SC_WARPS - 1) / SC_WARPS;
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-        if (lane == 0) s_tot[warp] = t;
-        __syncthreads();
-        int64_t total = 0;
-#pragma unroll
-        for (int w = 0; w < SC_WARPS; ++w) total += s_tot[w];
-        m0 = (int64_t)blockIdx.x * total / gridDim.x;
-        nk = ((int64_t)blockIdx.x + 1) * total / gridDim.x - m0;
+        if constexpr (BLK) batch_share<SC_WARPS>(a, m0, nk, b_start, base_start);
     }
     // the CTA-step index of the CTA's k-th CTA-step (one batch entry: 0, the entry's; the warp's
     // step then comes from s0), and warp `warp`'s step within its request, or -1 past the CTA's range
@@ -233,6 +299,7 @@ __global__ void __launch_bounds__(sc_warps<HI>() * 32) __maxnreg__(HI >= 16 ? 25
         return st < s1 ? st : -1;
     };
     CtaStepCursor<SC_WARPS> lc;  // this lane's lookup cursor
+    if constexpr (BLK) lc.start(a, b_start, base_start);
     int wk[2] = {0, 0}, ws[2] = {0, 0}, wp[2] = {0, 0};  // per set: kind (0 past the end, 1 copy,
                                                           // 2 nothing to copy), row in page, page
     auto lookup_window = [&](int64_t k0, int& kind, int& slot, int& page) {
@@ -322,6 +389,7 @@ __global__ void __launch_bounds__(sc_warps<HI>() * 32) __maxnreg__(HI >= 16 ? 25
     };
     {
         CtaStepCursor<SC_WARPS> c0;
+        if constexpr (BLK) c0.start(a, b_start, base_start);
         if (nk > 0 && c0.seek(a, cta_step(0))) q_fetch(c0.b);
     }
     lookup_window(0, wk[0], ws[0], wp[0]);
@@ -348,6 +416,7 @@ __global__ void __launch_bounds__(sc_warps<HI>() * 32) __maxnreg__(HI >= 16 ? 25
     const int r = lane & 15;        // row within its unit
     const int hu = lane >> 4;       // chunk half (c)
     CtaStepCursor<SC_WARPS> cur;
+    if constexpr (BLK) cur.start(a, b_start, base_start);
     for (int64_t k = 0;; ++k) {
         const int64_t m = cta_step(k);
         if (k >= nk || !cur.seek(a, m)) break;  // the same for every warp of the CTA
@@ -483,7 +552,7 @@ bool make_kidx_map(void* map, const HPaged& p, bool fp8, int64_t rows_per_page, 
     return r == CUDA_SUCCESS;
 }
 
-template <int HI, bool FP8>
+template <int HI, bool FP8, bool BLK>
 static cudaError_t launch_score_t(const CUtensorMap& map, const ScoreArgs& a, int64_t max_steps,
                                   int reserve, cudaStream_t s, bool pdl) {
     constexpr int QF4 = 8 * 8 * (HI / 2);
@@ -492,7 +561,7 @@ static cudaError_t launch_score_t(const CUtensorMap& map, const ScoreArgs& a, in
     constexpr size_t with_hist = base + (size_t)kHistBins * 4;
     const size_t smem = a.hist ? with_hist : base;
     {
-        cudaError_t e = set_func_attr_once((const void*)score_kernel<HI, FP8>,
+        cudaError_t e = set_func_attr_once((const void*)score_kernel<HI, FP8, BLK>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)with_hist);
         if (e != cudaSuccess) return e;
     }
@@ -512,7 +581,7 @@ static cudaError_t launch_score_t(const CUtensorMap& map, const ScoreArgs& a, in
     cfg.blockDim = dim3(SC_WARPS * 32, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    return cudaLaunchKernelEx(&cfg, score_kernel<HI, FP8>, map, a);
+    return cudaLaunchKernelEx(&cfg, score_kernel<HI, FP8, BLK>, map, a);
 }
 
 cudaError_t launch_score(const ScoreLaunch& h, cudaStream_t s, bool pdl) {
@@ -545,14 +614,17 @@ cudaError_t launch_score(const ScoreLaunch& h, cudaStream_t s, bool pdl) {
     if (!make_kidx_map(&map, h.kidx, h.fp8, rpp, n_pages)) return cudaErrorInvalidValue;
     const int64_t steps = (h.max_G + SC_SUPER - 1) / SC_SUPER;  // 32-row steps of the longest request
     const int hi = h.Hi <= 4 ? 4 : (h.Hi <= 8 ? 8 : 16);
-    if (h.fp8) {
-        if (hi == 4) return launch_score_t<4, true>(map, a, steps, h.reserve, s, pdl);
-        if (hi == 8) return launch_score_t<8, true>(map, a, steps, h.reserve, s, pdl);
-        return launch_score_t<16, true>(map, a, steps, h.reserve, s, pdl);
-    }
-    if (hi == 4) return launch_score_t<4, false>(map, a, steps, h.reserve, s, pdl);
-    if (hi == 8) return launch_score_t<8, false>(map, a, steps, h.reserve, s, pdl);
-    return launch_score_t<16, false>(map, a, steps, h.reserve, s, pdl);
+    const bool blk = h.B > 1;
+    auto go = [&](auto fp8, auto blkc) -> cudaError_t {
+        constexpr bool F = decltype(fp8)::value, K = decltype(blkc)::value;
+        if (hi == 4) return launch_score_t<4, F, K>(map, a, steps, h.reserve, s, pdl);
+        if (hi == 8) return launch_score_t<8, F, K>(map, a, steps, h.reserve, s, pdl);
+        return launch_score_t<16, F, K>(map, a, steps, h.reserve, s, pdl);
+    };
+    using T = std::true_type;
+    using F = std::false_type;
+    if (h.fp8) return blk ? go(T{}, T{}) : go(T{}, F{});
+    return blk ? go(F{}, T{}) : go(F{}, F{});
 }
 
 }  // namespace csa
