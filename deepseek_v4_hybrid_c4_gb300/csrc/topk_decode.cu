@@ -225,6 +225,10 @@ __global__ void __launch_bounds__(SW_T) select_scan_kernel(SelArgs a) {
     const bool all_in = G <= k;
     pdl_wait();  // the scores and the first digit's histogram come from the score kernel
     pdl_launch_dependents();
+    if ((int64_t)c * SW_SLICE >= G && c > 0) {  // a slice past a shorter request's end: nothing in it
+        if (tid == 0) a.counts[(int64_t)b * C + c] = 0u;
+        return;
+    }
 
     // ---- this thread's four keys, and the first digit's bin
     const int64_t pos = (int64_t)c * SW_SLICE + SW_PER * tid;
@@ -286,6 +290,7 @@ __global__ void __maxnreg__(88) select_finish_kernel(SelArgs a) {
     const bool all_in = G <= k;
     pdl_wait();  // the lists, their counts and the second digit's histogram come from the scan
     pdl_launch_dependents();
+    if ((int64_t)c * SW_SLICE >= G && c > 0) return;  // an empty region (a shorter request): nothing to place
     // entry tid of this CTA's own region, read with the counts: it holds the region's winners
     // and candidates whenever they number at most SW_T (the other entries go unused)
     const uint64_t* lc = lb + (int64_t)c * SW_SLICE;
