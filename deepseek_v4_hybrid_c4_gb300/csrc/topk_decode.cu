@@ -273,7 +273,11 @@ __global__ void __launch_bounds__(SW_T) select_scan_kernel(SelArgs a) {
 
 // At most 88 registers: 512 x 88 plus a scan CTA's 512 x 40 fill the register file exactly, so a
 // finish CTA becomes resident beside its SM's scan CTA and waits there (no spills at this cap).
-__global__ void __maxnreg__(88) select_finish_kernel(SelArgs a) {
+// A grid of more CTAs than SMs but at most twice as many takes the 64-register instance instead
+// (two finish CTAs per SM, one wave; it spills a little): speculative verify with two query
+// positions, 70.8 -> 68.8 us.  Larger grids (the 32-request ragged batch) keep 88.
+template <int MAXREG>
+__global__ void __maxnreg__(MAXREG) select_finish_kernel(SelArgs a) {
     extern __shared__ __align__(16) uint8_t sw_raw[];
     SwFinSmem& fs = *reinterpret_cast<SwFinSmem*>(sw_raw);
     SwCore& sm = fs.core;
@@ -1119,8 +1123,11 @@ cudaError_t launch_select_set(const SelectSetLaunch& h, cudaStream_t s, bool pdl
     const size_t smem = sizeof(SwFinSmem);
     static_assert(sizeof(SwFinSmem) + SW_SCAN_SPREAD_SMEM + 2 * 1024 <= 228 * 1024, "a scan and a finish CTA share an SM");
     {
-        cudaError_t e = set_func_attr_once((const void*)select_finish_kernel,
+        cudaError_t e = set_func_attr_once((const void*)select_finish_kernel<88>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess)
+            e = set_func_attr_once((const void*)select_finish_kernel<64>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e == cudaSuccess)
             e = set_func_attr_once((const void*)select_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    (int)SW_SCAN_SPREAD_SMEM);
@@ -1159,7 +1166,9 @@ cudaError_t launch_select_set(const SelectSetLaunch& h, cudaStream_t s, bool pdl
     e = cudaLaunchKernelEx(&cfg, select_scan_kernel, a);
     if (e != cudaSuccess) return e;
     cfg.dynamicSmemBytes = smem;
-    return cudaLaunchKernelEx(&cfg, select_finish_kernel, a);
+    const int64_t ctas = (int64_t)h.B * a.C;
+    return ctas > sms && ctas <= 2LL * sms ? cudaLaunchKernelEx(&cfg, select_finish_kernel<64>, a)
+                                           : cudaLaunchKernelEx(&cfg, select_finish_kernel<88>, a);
 }
 
 cudaError_t launch_select_bound(const SelectSetLaunch& h, const BoundRescore& r, cudaStream_t s, bool pdl) {
