@@ -114,10 +114,10 @@ csa_status csa_index_score(const void* q_idx, const float* w_h, int32_t Hi, csa_
  * 1e30 gives (-inf, +inf); a row whose page id is out of range gives [0, 0] and the device
  * status CSA_ERR_DEVICE_BOUNDS.  Arguments as csa_index_score; k_dtype must be CSA_BF16
  * (otherwise CSA_ERR_UNSUPPORTED); lower is nullable, both fp32 [G], 4-byte aligned.
- * csa_decode takes this form in speculative verify with bf16 index keys (3 <= n_q <= 4, Hi <= 16):
+ * csa_decode takes this form in speculative verify with bf16 index keys (2 <= n_q <= 4, Hi <= 16):
  * one pass over the keys serves every query position, and the select rescores in the fixed
- * order only the candidates whose upper bound reaches the histogram bin (top 12 bits of the key)
- * of the k-th largest lower bound, so its top k is the fixed-order score's top k.
+ * order only the candidates whose upper bound reaches the histogram bin (top 12 or 13 bits of
+ * the key) of the k-th largest lower bound, so its top k is the fixed-order score's top k.
  */
 csa_status csa_index_score_bounds(const void* q_idx, const float* w_h, int32_t Hi, csa_paged k_idx,
                                   csa_dtype k_dtype, int64_t G, float* lower, float* upper, void* stream);

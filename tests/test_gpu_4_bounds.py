@@ -174,7 +174,7 @@ def entry(csa):
     return __graft_entry__
 
 
-@pytest.mark.parametrize("n_q", [1, 4])
+@pytest.mark.parametrize("n_q", [1, 2, 4])
 @pytest.mark.parametrize("G,rows_per_book", [(30000, 16), (65536, 64), (5000, 2)])
 def test_decode_bf16_ties_at_the_threshold(entry, G, rows_per_book, n_q):
     """bf16 keys drawn from a small codebook: groups of candidates with identical exact scores,
@@ -187,7 +187,7 @@ def test_decode_bf16_ties_at_the_threshold(entry, G, rows_per_book, n_q):
     _decode_check(entry, case, n_q)
 
 
-@pytest.mark.parametrize("n_q", [1, 3])
+@pytest.mark.parametrize("n_q", [1, 2, 3])
 def test_decode_near_ties_inside_the_bounds(entry, n_q):
     """Candidates whose exact scores differ by a few ulps (keys that differ in one low bit):
     inside any bracket's width, so only the exact rescoring can order them."""
@@ -204,7 +204,7 @@ def test_decode_near_ties_inside_the_bounds(entry, n_q):
     _decode_check(entry, case, n_q)
 
 
-@pytest.mark.parametrize("n_q", [1, 4])
+@pytest.mark.parametrize("n_q", [1, 2, 4])
 def test_decode_negative_weights_and_batch(entry, n_q):
     """Index weights of both signs (scores below zero) in a ragged bf16 batch."""
     case = synth.make_decode_case("negw", 91, [4096, 40000, 516, 131072 // 8], H=64, Hi=8, paged=True, n_pending=2)
