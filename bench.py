@@ -680,7 +680,8 @@ def main():
     # ---- end to end through host buffers: the new token's state goes up, the output comes back.
     #      Per layer one CUDA graph holds the step with its copies: the packed per-step inputs
     #      (q | q_idx | w_h), the completed group's raw rows and its index row up from pinned
-    #      host memory, and the packed outputs (out | lse) back down.
+    #      host memory in one csa_copy_batch launch, and the packed outputs (out | lse) back down
+    #      in another.
     h_in = batch.step_in.cpu().pin_memory()
     h_out = torch.empty(batch.step_out.shape, dtype=batch.step_out.dtype).pin_memory()
     r0 = case.requests[0]
@@ -697,12 +698,13 @@ def main():
     e2e_graphs = []
     for lb in layers:
         g = torch.cuda.CUDAGraph()
+        up = csa.copy_batch_args([(h_in, lb.step_in), (hraw, lb.raw_pool[row0: row0 + n_new]),
+                                  (hkidx, lb.kidx_pool[krow: krow + 1])])
+        down = csa.copy_batch_args([(lb.step_out, h_out)])
         with torch.cuda.graph(g, stream=stream):
-            lb.step_in.copy_(h_in, non_blocking=True)
-            lb.raw_pool[row0: row0 + n_new].copy_(hraw, non_blocking=True)
-            lb.kidx_pool[krow: krow + 1].copy_(hkidx, non_blocking=True)
+            csa.csa_copy_batch(up, stream)
             lb.run(stream)
-            h_out.copy_(lb.step_out, non_blocking=True)
+            csa.csa_copy_batch(down, stream)
         e2e_graphs.append(g)
     with torch.cuda.stream(stream):
         for i in range(max(3, args.warmup) * n_layers):

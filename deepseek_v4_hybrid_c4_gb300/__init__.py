@@ -30,6 +30,13 @@ class csa_paged(ctypes.Structure):
                 ("page_stride_bytes", ctypes.c_int64), ("n_pages", ctypes.c_int64)]
 
 
+CSA_COPY_MAX = 16
+
+
+class csa_copy(ctypes.Structure):
+    _fields_ = [("src", ctypes.c_void_p), ("dst", ctypes.c_void_p), ("bytes", ctypes.c_uint64)]
+
+
 class csa_decode_params(ctypes.Structure):
     _fields_ = [
         ("B", ctypes.c_int32), ("ratio", ctypes.c_int32), ("H", ctypes.c_int32), ("Hi", ctypes.c_int32),
@@ -87,6 +94,7 @@ def lib() -> ctypes.CDLL:
         L.csa_status_string.restype = ctypes.c_char_p
         L.csa_version.restype = i32
         L.csa_selftest_bounded_wait.argtypes = [vp]
+        L.csa_copy_batch.argtypes = [i32, ctypes.POINTER(csa_copy), vp]
         L.csa_hisparse_create.argtypes = [i32, i64, i64, ctypes.POINTER(vp)]
         L.csa_hisparse_destroy.argtypes = [vp]
         L.csa_hisparse_destroy.restype = None
@@ -102,7 +110,7 @@ def lib() -> ctypes.CDLL:
                      "csa_topk_cluster", "csa_topk_merge", "csa_sparse_attn_partial", "csa_attn_merge", "csa_sparse_attn",
                      "csa_decode", "csa_decode_timed", "csa_decode_noalloc", "csa_read_device_status",
                      "csa_hisparse_create", "csa_hisparse_plan", "csa_hisparse_update", "csa_hisparse_collect",
-                     "csa_hisparse_apply", "csa_selftest_bounded_wait"):
+                     "csa_hisparse_apply", "csa_selftest_bounded_wait", "csa_copy_batch"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -244,6 +252,29 @@ def csa_attn_merge(o_parts, lse_parts, R: int, H: int, out, lse=None, stream=Non
 
 def csa_decode_workspace_size(p: csa_decode_params) -> int:
     return int(lib().csa_decode_workspace_size(ctypes.byref(p)))
+
+
+def copy_batch_args(pairs) -> "ctypes.Array":
+    """The csa_copy array for csa_copy_batch from (src, dst[, bytes]) pairs of tensors or raw
+    pointers; bytes defaults to the source tensor's size."""
+    def addr(x):  # a device tensor, a pinned host tensor, or a raw pointer
+        if isinstance(x, int):
+            return x
+        if not x.is_cuda and not x.is_pinned():
+            raise ValueError("csa_copy_batch takes device or pinned host tensors")
+        return x.data_ptr()
+    arr = (csa_copy * len(pairs))()
+    for i, pr in enumerate(pairs):
+        src, dst = pr[0], pr[1]
+        nbytes = pr[2] if len(pr) > 2 else src.numel() * src.element_size()
+        arr[i] = csa_copy(addr(src), addr(dst), nbytes)
+    return arr
+
+
+def csa_copy_batch(copies, stream=None) -> None:
+    """Enqueue up to CSA_COPY_MAX copies as one kernel (device or pinned host memory on either
+    side; 16-byte aligned, sizes multiples of 16).  `copies`: a csa_copy array (copy_batch_args)."""
+    _check(lib().csa_copy_batch(len(copies), copies, _stream(stream)), "csa_copy_batch")
 
 
 def csa_selftest_bounded_wait(stream=None) -> None:

@@ -13,7 +13,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libcsa.so")
 SOURCES = ["api.cu", "attn.cu", "topk.cu", "topk_decode.cu", "score.cu", "score_bound.cu", "compress.cu", "noalloc.cu",
-           "hisparse.cu", "selftest.cu", "cp.cu"]
+           "hisparse.cu", "selftest.cu", "cp.cu", "copy.cu"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc" if os.path.exists("/usr/local/cuda/bin/nvcc") else "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include"),

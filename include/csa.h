@@ -362,6 +362,25 @@ csa_status csa_decode_timed(const csa_decode_params* p, void* workspace, size_t 
  */
 csa_status csa_decode_noalloc(const csa_decode_params* p, void* stream);
 
+/*
+ * Batched copy: up to CSA_COPY_MAX copies enqueued on `stream` as one kernel.  Each copy moves
+ * `bytes` bytes from src to dst; either side may be device memory or page-locked host memory
+ * allocated with the CUDA runtime (pinned), which with unified virtual addressing the kernel
+ * reads and writes through the same pointer.  A decode step's uploads of its new inputs and the
+ * download of its outputs are a few small copies; one launch carries them all, where separate
+ * copy-engine operations would each add a copy's fixed latency.  src, dst 16-byte aligned,
+ * bytes a multiple of 16 (0 allowed), copies not overlapping; otherwise, or for n outside
+ * [1, CSA_COPY_MAX], CSA_ERR_INVALID_ARG and nothing is enqueued.  The caller owns the memory.
+ * CSA_ERR_CUDA if the launch fails.  Graph capture: yes.
+ */
+#define CSA_COPY_MAX 16
+typedef struct {
+    const void* src;
+    void* dst;
+    uint64_t bytes;
+} csa_copy;
+csa_status csa_copy_batch(int32_t n, const csa_copy* copies, void* stream);
+
 /* Read and clear the calling device's sticky status word (synchronises `stream`).
  * *out receives a bit set: bit (code-1) for each csa_status code raised on the device. */
 csa_status csa_read_device_status(void* stream, int32_t* out);

@@ -204,8 +204,8 @@ def test_hisparse_plan_is_lru(libpath):
 
 
 def test_ctypes_structs_match_the_header(tmp_path):
-    """Every field offset and the size of csa_paged and csa_decode_params, as a C compiler lays
-    them out from include/csa.h, equal the ctypes binding's."""
+    """Every field offset and the size of csa_paged, csa_decode_params and csa_copy, as a C
+    compiler lays them out from include/csa.h, equal the ctypes binding's."""
     import ctypes
     import shutil
     import subprocess
@@ -214,7 +214,7 @@ def test_ctypes_structs_match_the_header(tmp_path):
     if cc is None:
         pytest.skip("no C compiler")
     lines = ['#include <stddef.h>', '#include <stdio.h>', '#include "csa.h"', "int main(void) {"]
-    for st in (csa.csa_paged, csa.csa_decode_params):
+    for st in (csa.csa_paged, csa.csa_decode_params, csa.csa_copy):
         cname = st.__name__
         lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
         for f, _ in st._fields_:
@@ -228,7 +228,7 @@ def test_ctypes_structs_match_the_header(tmp_path):
     for line in subprocess.check_output([str(exe)], text=True).splitlines():
         name, field, value = line.split()
         got[(name, field)] = int(value)
-    for st in (csa.csa_paged, csa.csa_decode_params):
+    for st in (csa.csa_paged, csa.csa_decode_params, csa.csa_copy):
         assert got[(st.__name__, "size")] == ctypes.sizeof(st), st.__name__
         for f, _ in st._fields_:
             assert got[(st.__name__, f)] == getattr(st, f).offset, (st.__name__, f)
@@ -300,3 +300,21 @@ def test_hisparse_coordinator_rejects_bad_arguments(libpath):
         assert (csa.csa_hisparse_table(h, 1, 8) == -1).all()
     finally:
         csa.csa_hisparse_destroy(h)
+
+
+def test_copy_batch_validates_its_arguments(libpath):
+    """csa_copy_batch rejects, before enqueueing anything: no copies or more than CSA_COPY_MAX, a
+    null array or pointer, a source or destination not 16-byte aligned, a size not a multiple of
+    16; an all-empty batch is accepted with nothing to do (no GPU touched: the pointers below are
+    never dereferenced)."""
+    import deepseek_v4_hybrid_c4_gb300 as csa
+    f = csa.lib().csa_copy_batch
+    one = (csa.csa_copy * 1)()
+    assert f(0, one, None) == csa.CSA_ERR_INVALID_ARG
+    assert f(csa.CSA_COPY_MAX + 1, (csa.csa_copy * (csa.CSA_COPY_MAX + 1))(), None) == csa.CSA_ERR_INVALID_ARG
+    assert f(1, None, None) == csa.CSA_ERR_INVALID_ARG
+    for src, dst, n in [(0, 32, 16), (16, 0, 16), (8, 32, 16), (16, 40, 16), (16, 32, 24)]:
+        one[0] = csa.csa_copy(src, dst, n)
+        assert f(1, one, None) == csa.CSA_ERR_INVALID_ARG, (src, dst, n)
+    one[0] = csa.csa_copy(16, 32, 0)
+    assert f(1, one, None) == csa.CSA_OK

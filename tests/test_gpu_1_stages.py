@@ -413,3 +413,36 @@ def test_bounded_wait_runs_out_without_fault(csa):
     assert np.array_equal(out.cpu().numpy().view(np.uint32),
                           oracle.index_score(q, w, k, False).view(np.uint32))
     _status_clean(csa)
+
+
+def test_copy_batch_moves_every_byte(csa):
+    """csa_copy_batch: pinned host -> device, device -> pinned host and device -> device copies of
+    several sizes (one 16-byte chunk up to a few MB, an empty one), up to CSA_COPY_MAX in one
+    launch, each destination byte-equal to its source and the bytes around it untouched."""
+    import deepseek_v4_hybrid_c4_gb300 as m
+    g = torch.Generator().manual_seed(11)
+    sizes = [16, 4096, 137728, 131584, 0, (1 << 21) + 48, 1040, 16 * 1000]
+    pairs, checks = [], []
+    for i, n in enumerate(sizes):
+        src_host = (i % 2) == 0
+        words = max(n // 4, 1) + 8
+        data = torch.randint(-2**31, 2**31 - 1, (words,), generator=g, dtype=torch.int32)
+        src = data.pin_memory() if src_host else data.cuda()
+        dst_host = i % 3 == 1
+        fill = torch.full((words,), 0x5A5A5A5A, dtype=torch.int32)
+        dst = fill.pin_memory() if dst_host else fill.cuda()
+        pairs.append((src, dst, n))
+        checks.append((data, dst, n, words))
+    while len(pairs) < m.CSA_COPY_MAX:  # device -> device to fill the batch
+        n = 16 * (len(pairs) + 1)
+        data = torch.randint(-2**31, 2**31 - 1, (n // 4 + 8,), generator=g, dtype=torch.int32)
+        dst = torch.full((n // 4 + 8,), 0x5A5A5A5A, dtype=torch.int32).cuda()
+        pairs.append((data.cuda(), dst, n))
+        checks.append((data, dst, n, n // 4 + 8))
+    m.csa_copy_batch(m.copy_batch_args(pairs))
+    torch.cuda.synchronize()
+    assert m.csa_read_device_status() == 0
+    for data, dst, n, words in checks:
+        got = dst.cpu()
+        assert torch.equal(got[: n // 4], data[: n // 4]), n
+        assert (got[n // 4:] == 0x5A5A5A5A).all(), n
