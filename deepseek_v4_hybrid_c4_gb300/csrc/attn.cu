@@ -380,6 +380,49 @@ constexpr uint32_t A6_SMEM = A6_SM_KOK + 16 + 1024;         // + alignment slack
 static_assert(A6_SMEM <= 227 * 1024, "attn64 shared memory");
 static_assert(128 * R_PITCH <= A6_SM_P, "attn64 staging fits below P");
 
+// A key's row address in two halves.  key_issue starts the page-table (and working-set) loads
+// of a key whose selection entry is already in a register, without waiting for them;
+// key_resolve turns them into the row's address, with the bounds check of row_addr.  Issued a
+// tile ahead, the lookups of the tile after next run behind the current tile's products
+// instead of stalling its softmax threads (behind the SM's row gathers, a lookup takes 1-2 us).
+struct KeyRef {
+    int64_t slot;  // row within its page
+    int32_t pp;    // page id (the page table's entry; the logical page without a table)
+    int32_t sl;    // working-set slot, or -1
+    int32_t kind;  // 0: no key; 1: a compressed row (kc, kws); 2: a window row (kr)
+};
+
+__device__ __forceinline__ KeyRef key_issue(const AttnArgs& a, int b, int kind, int64_t r) {
+    KeyRef k;
+    k.kind = kind;
+    k.sl = -1;
+    k.pp = 0;
+    k.slot = 0;
+    if (kind == 0) return k;
+    const DPaged& p = kind == 1 ? a.kc : a.kr;
+    const int64_t lp = r / p.rpp;
+    k.slot = r - lp * p.rpp;
+    const int64_t e = (int64_t)(p.qpr > 1 ? b / p.qpr : b) * p.pt_stride + lp;
+    if (kind == 1 && a.kws.table) {
+        if (a.kws.touch) a.kws.touch[e] = a.kws.step;
+        k.sl = a.kws.table[e];
+    }
+    k.pp = p.pt ? __ldg(p.pt + e) : (int32_t)lp;
+    return k;
+}
+
+__device__ __forceinline__ const uint8_t* key_resolve(const AttnArgs& a, const KeyRef& k) {
+    if (k.kind == 0) return nullptr;
+    if (k.kind == 1 && a.kws.table && k.sl >= 0 && k.sl < a.kws.n_slots)
+        return a.kws.base + k.sl * a.kc.page_stride + k.slot * (int64_t)ROW_BYTES;
+    const DPaged& p = k.kind == 1 ? a.kc : a.kr;
+    if (k.pp < 0 || k.pp >= p.n_pages) {
+        raise_status(a.status, CSA_ERR_DEVICE_BOUNDS);
+        return nullptr;
+    }
+    return p.base + k.pp * p.page_stride + k.slot * (int64_t)ROW_BYTES;
+}
+
 __global__ void __launch_bounds__(A6_T, 1) attn64_kernel(AttnArgs a) {
     extern __shared__ uint8_t at_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(at_raw) + 1023) & ~uintptr_t(1023));
@@ -445,13 +488,13 @@ __global__ void __launch_bounds__(A6_T, 1) attn64_kernel(AttnArgs a) {
         st_shared_zero16(sbase + A6_SM_P + (uint32_t)(c < 512 ? c : c + 512) * 16u);
     cp_async_commit();
 
-    auto key_row = [&](int64_t j) -> const uint8_t* {
-        if (j < n_c) {
-            const int64_t g = a.sel ? (int64_t)__ldg(a.sel + (int64_t)b * a.sel_stride + j) : j;
-            return g >= 0 ? ws_row(a.kws, a.kc, b, g, true, a.status) : nullptr;
-        }
-        if (j < n_keys) return row_addr(a.kr, b, N - W + (j - n_c), ROW_BYTES, a.status);
-        return nullptr;
+    // key j: its selection entry (a load that nothing waits on until key_ref), then its lookups
+    auto key_entry = [&](int64_t j) -> int64_t {
+        return j < n_c && a.sel ? (int64_t)__ldg(a.sel + (int64_t)b * a.sel_stride + j) : j;
+    };
+    auto key_ref = [&](int64_t j, int64_t g) -> KeyRef {
+        if (j < n_c) return key_issue(a, b, g >= 0 ? 1 : 0, g);
+        return key_issue(a, b, j < n_keys ? 2 : 0, N - W + (j - n_c));
     };
     auto publish = [&](int st, const uint8_t* p) {  // warps 0, 1
         kptr[st * AT_KT + tid] = p;
@@ -490,13 +533,23 @@ __global__ void __launch_bounds__(A6_T, 1) attn64_kernel(AttnArgs a) {
     };
     if (t_fresh >= t1) pdl_launch_dependents();  // this split never waits (the merge waits for the grid)
     wait_for(t0);
-    if (soft) publish(0, key_row(t0 * AT_KT + tid));
+    if (soft) {
+        const int64_t j = t0 * AT_KT + tid;
+        publish(0, key_resolve(a, key_ref(j, key_entry(j))));
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     gather(0);
+    // the lookups of the next tile, and the selection entries of the one after (a selection
+    // is complete once the first wait returned; a dense split needs no entry loads)
     if (t0 + 1 < t1) wait_for(t0 + 1);
-    const uint8_t* p_next = soft && t0 + 1 < t1 ? key_row((t0 + 1) * AT_KT + tid) : nullptr;
+    KeyRef ref_next = {0, 0, -1, 0};
+    if (soft && t0 + 1 < t1) {
+        const int64_t j = (t0 + 1) * AT_KT + tid;
+        ref_next = key_ref(j, key_entry(j));
+    }
+    int64_t g_after = soft && t0 + 2 < t1 ? key_entry((t0 + 2) * AT_KT + tid) : 0;
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + A6_SM_TMEM);
     const uint32_t t_o = tmem, t_s = tmem + AT_DH;
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
@@ -508,10 +561,12 @@ __global__ void __launch_bounds__(A6_T, 1) attn64_kernel(AttnArgs a) {
         if (it > 0 && !mbar_wait(bar_o, (uint32_t)((it - 1) & 1))) ok = false;
         tc_fence_after();
         const bool more = tile + 1 < t1;
-        if (soft && more) publish(st ^ 1, p_next);
+        if (soft && more) publish(st ^ 1, key_resolve(a, ref_next));
         cp_async_wait_all();  // this tile's rows (and Q) landed
         fence_proxy_async_smem();
         __syncthreads();
+        // the lookups of the tile after next go out ahead of the next tile's rows
+        if (soft && tile + 2 < t1) ref_next = key_ref((tile + 2) * AT_KT + tid, g_after);
         if (more) gather(st ^ 1);  // the next tile's rows, behind this tile's products
         // ---- S = Q K^T  (M=128, N=64, K=512); rows 64..127 are not used
         if (tid == 0) {
@@ -528,8 +583,8 @@ __global__ void __launch_bounds__(A6_T, 1) attn64_kernel(AttnArgs a) {
                 }
             tc_commit(bar_s);
         }
-        if (tile + 2 < t1) wait_for(tile + 2);
-        if (soft && tile + 2 < t1) p_next = key_row((tile + 2) * AT_KT + tid);
+        if (tile + 2 < t1) wait_for(tile + 2);  // before the gather of tile + 2 (fresh rows of a dense step)
+        if (soft && tile + 3 < t1) g_after = key_entry((tile + 3) * AT_KT + tid);
         float alpha = 1.f;
         if (soft) {
             if (!mbar_wait(bar_s, (uint32_t)(it & 1))) ok = false;
