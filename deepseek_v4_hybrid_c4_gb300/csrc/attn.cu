@@ -364,7 +364,7 @@ __global__ void __launch_bounds__(A1_T, 1) attn_kernel(AttnArgs a) {
 // TMEM: O [0, 256) (lane h: head h, columns 0..255; lane 64 + h: head h, columns 256..511),
 // S [256, 320).
 constexpr int A6_H = 64;
-constexpr int A6_T = 384;  // warps 0-3 own the TMEM lane quarters; warps 4-11 only help gather and store
+constexpr int A6_T = 384;  // warps 0-3 own the TMEM lane quarters (0-1 the softmax); warps 2-11 issue the row gathers
 constexpr uint32_t A6_Q_SLAB = A6_H * 128;                  // 8 KiB
 constexpr uint32_t A6_SM_Q = 0;                             // 8 slabs x 64 rows x 128 B
 constexpr uint32_t A6_SM_K = 8 * A6_Q_SLAB;                 // 2 stages x 8 slabs x 64 rows x 128 B
@@ -501,9 +501,12 @@ __global__ void __launch_bounds__(A6_T, 1) attn64_kernel(AttnArgs a) {
         const unsigned m = __ballot_sync(0xffffffffu, p != nullptr);
         if (lane == 0) reinterpret_cast<uint32_t*>(kok + st)[warp] = m;
     };
-    auto gather = [&](int st) {  // every thread; kptr[st] published and visible
+    // Every thread but the softmax warps' (whose chain S -> softmax -> P V then runs while the
+    // others are still held issuing copies into a full request queue); kptr[st] published and
+    // visible.
+    auto gather = [&](int st) {
         const uint32_t kb = sbase + A6_SM_K + (uint32_t)st * A6_KST;
-        for (int c = tid; c < AT_KT * 64; c += A6_T) {
+        for (int c = tid - A6_H; c >= 0 && c < AT_KT * 64; c += A6_T - A6_H) {
             const uint32_t row = c >> 6, ch = c & 63;
             const uint32_t dst = kb + (ch >> 3) * K_SLAB + swz(row, ch & 7);
             const uint8_t* src = kptr[st * AT_KT + row];
