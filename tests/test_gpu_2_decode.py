@@ -251,6 +251,30 @@ def test_hisparse_mirror_and_working_set(entry):
     assert np.array_equal(batch.hs_touch.cpu().numpy(), want * 2)
 
 
+def test_hisparse_many_requests_pages_on_both_sides(entry):
+    """Twenty-four requests, so each attention split takes two key tiles (the lookups of a tile
+    are issued a tile ahead of its gather), with a working set that holds only part of the
+    selected pages: rows come from slots and from the mirror in the same tiles.  Both steps
+    match the oracle."""
+    import deepseek_v4_hybrid_c4_gb300 as m
+    lengths = [6000 + 100 * i for i in range(24)]
+    case = synth.make_decode_case("hs5", 64, lengths, H=16, Hi=4, n_pending=1)
+    batch, c_rpp = _hisparse_batch(entry, case, slots=700)
+    for step in (1, 2):
+        batch.out.zero_()
+        batch.hs_step = step
+        batch.run()
+        torch.cuda.synchronize()
+        assert m.csa_read_device_status() == 0
+        _check_against_oracle(case, batch)
+        n_in, _ = batch.hs_update()
+        if step == 1:
+            assert n_in == 700
+    table = batch.hs_table.cpu().numpy()
+    touch = batch.hs_touch.cpu().numpy()
+    assert (table >= 0).sum() == 700 and (touch == 2).sum() > 700  # some selected pages stayed in the mirror
+
+
 def test_hisparse_small_working_set_evicts(entry):
     """A working set smaller than one step's pages: the coordinator fills it, the rest stay in
     the mirror, and the step still matches the oracle with pages on both sides."""
