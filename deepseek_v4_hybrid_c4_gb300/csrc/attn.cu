@@ -734,8 +734,9 @@ __global__ void __launch_bounds__(A6_T, 1) attn64_kernel(AttnArgs a) {
 
 // Log-sum-exp merge of the splits: one CTA per (head, request); thread t owns columns
 // 4t .. 4t+3 (half t / 64).  Every split's (max, sum) and row piece are loaded at once.
-// Up to 16 splits every split's row piece is loaded at once; above, 8 at a time, so that four
-// CTAs fit on an SM (a batch of 8 requests x 64 heads is 512 CTAs: one wave).
+// Up to 16 splits every split's row piece is loaded at once (an instance for up to 8 splits
+// holds half the registers); above, 8 at a time, so that four CTAs fit on an SM (a batch of 8
+// requests x 64 heads is 512 CTAs: one wave).
 template <int MAXS>
 __global__ void __launch_bounds__(128, MAXS > 16 ? 4 : 0) attn_merge_kernel(AttnArgs a) {
     pdl_wait();
@@ -942,8 +943,11 @@ cudaError_t launch_attn(const AttnLaunch& h, cudaStream_t s, bool pdl) {
     cfg.gridDim = dim3((unsigned)h.H, (unsigned)h.B, 1);
     cfg.blockDim = dim3(128, 1, 1);
     cfg.dynamicSmemBytes = 0;
-    return a.S <= 16 ? cudaLaunchKernelEx(&cfg, attn_merge_kernel<16>, a)
-                     : cudaLaunchKernelEx(&cfg, attn_merge_kernel<AT_MAX_SPLITS>, a);
+    // up to 8 splits: 48 registers, so that eleven CTAs share an SM (the 32-request batch of 64
+    // heads, 2,048 CTAs of 5 splits, in little more than one wave instead of three)
+    return a.S <= 8    ? cudaLaunchKernelEx(&cfg, attn_merge_kernel<8>, a)
+           : a.S <= 16 ? cudaLaunchKernelEx(&cfg, attn_merge_kernel<16>, a)
+                       : cudaLaunchKernelEx(&cfg, attn_merge_kernel<AT_MAX_SPLITS>, a);
 }
 
 }  // namespace csa
