@@ -734,9 +734,10 @@ __global__ void __launch_bounds__(A6_T, 1) attn64_kernel(AttnArgs a) {
 
 // Log-sum-exp merge of the splits: one CTA per (head, request); thread t owns columns
 // 4t .. 4t+3 (half t / 64).  Every split's (max, sum) and row piece are loaded at once.
-// Up to 16 splits every split's row piece is loaded at once (an instance for up to 8 splits
-// holds half the registers); above, 8 at a time, so that four CTAs fit on an SM (a batch of 8
-// requests x 64 heads is 512 CTAs: one wave).
+// Up to 16 splits every split's row piece and (max, sum) pair is loaded at once into registers
+// (an instance for up to 8 splits holds half of them); above, the pairs go through shared
+// memory, so that every row piece is still in flight at once within the registers that let
+// four CTAs share an SM (a batch of 8 requests x 64 heads is 512 CTAs: one wave).
 template <int MAXS>
 __global__ void __launch_bounds__(128, MAXS > 16 ? 4 : 0) attn_merge_kernel(AttnArgs a) {
     pdl_wait();
@@ -772,31 +773,30 @@ __global__ void __launch_bounds__(128, MAXS > 16 ? 4 : 0) attn_merge_kernel(Attn
             }
         }
     } else {
+        // the splits' (max, sum) pairs through shared memory (each half's 64 threads share them),
+        // so that every split's row piece can be in flight at once in registers
+        __shared__ float2 mls[2][MAXS];
+        if ((t & 63) < S) mls[half][t & 63] = __ldcg(mlb + (int64_t)(t & 63) * H);
+        uint2 x[MAXS];
 #pragma unroll
         for (int s = 0; s < MAXS; ++s)
-            if (s < S) ml[s] = __ldcg(mlb + (int64_t)s * H);
+            if (s < S) x[s] = __ldcg(reinterpret_cast<const uint2*>(pb + (int64_t)s * H * D));
+        __syncthreads();
 #pragma unroll
         for (int s = 0; s < MAXS; ++s)
-            if (s < S && ml[s].y > 0.f) M = fmaxf(M, ml[s].x);
+            if (s < S && mls[half][s].y > 0.f) M = fmaxf(M, mls[half][s].x);
 #pragma unroll
-        for (int s0 = 0; s0 < MAXS; s0 += 8) {
-            uint2 x[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (s0 + j < S) x[j] = __ldcg(reinterpret_cast<const uint2*>(pb + (int64_t)(s0 + j) * H * D));
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int s = s0 + j;
-                if (s < S && ml[s].y > 0.f) {
-                    const float w = ml[s].y * ex2(ml[s].x - M);
-                    const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&x[j].x));
-                    const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&x[j].y));
-                    L += w;
-                    o0 = fmaf(w, f01.x, o0);
-                    o1 = fmaf(w, f01.y, o1);
-                    o2 = fmaf(w, f23.x, o2);
-                    o3 = fmaf(w, f23.y, o3);
-                }
+        for (int s = 0; s < MAXS; ++s) {
+            const float2 m2 = mls[half][s < S ? s : 0];
+            if (s < S && m2.y > 0.f) {
+                const float w = m2.y * ex2(m2.x - M);
+                const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&x[s].x));
+                const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&x[s].y));
+                L += w;
+                o0 = fmaf(w, f01.x, o0);
+                o1 = fmaf(w, f01.y, o1);
+                o2 = fmaf(w, f23.x, o2);
+                o3 = fmaf(w, f23.y, o3);
             }
         }
     }
