@@ -286,7 +286,9 @@ typedef struct {
     const void* q;               /* bf16 [B, H, 512] */
     const void* q_idx;           /* bf16 [B, Hi, 128] (ratio 4) */
     const float* w_h;            /* fp32 [B, Hi] (ratio 4) */
-    /* outputs (B * n_q entries with speculative verify) */
+    /* outputs (B * n_q entries with speculative verify); out and lse may also be page-locked
+       host memory that the device can address (the last kernel then writes them over the
+       host link, and the step's completion makes them visible to the host) */
     void* out;                   /* bf16 [B, H, 512] */
     float* lse;                  /* fp32 [B, H], nullable */
     int32_t* sel;                /* int32 [B, k], nullable (ratio 4): the selected candidates as a

@@ -380,6 +380,32 @@ def test_decode_graph_capture_replay(entry):
     assert_close(batch.out[0].float().cpu().numpy(), ref["out_f64"], "graph replay")
 
 
+@pytest.mark.parametrize("cfg,sd", [(0, 1), (3, 16), (4, 16)])
+def test_decode_outputs_into_pinned_host_memory(entry, cfg, sd):
+    """out and lse given as page-locked host memory: the merge kernel writes them over the host
+    link, and the host receives the same bits the device-side outputs hold (one request, 32
+    ragged requests, 8 dense C128 requests), from a captured graph."""
+    import deepseek_v4_hybrid_c4_gb300 as m
+    case = synth.config(cfg, scale_down=sd)
+    batch = entry.case_to_batch(case)
+    batch.run()
+    torch.cuda.synchronize()
+    out_d, lse_d = batch.out.cpu(), batch.lse.cpu()
+    h_out = torch.full(out_d.shape, -1, dtype=out_d.dtype).pin_memory()
+    h_lse = torch.full(lse_d.shape, float("nan"), dtype=lse_d.dtype).pin_memory()
+    p = type(batch.params).from_buffer_copy(batch.params)
+    p.out, p.lse = h_out.data_ptr(), h_lse.data_ptr()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        m.csa_decode(p, batch.ws, batch.ws_bytes, s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert m.csa_read_device_status() == 0
+    assert torch.equal(h_out.view(torch.int16), out_d.view(torch.int16))
+    assert torch.equal(h_lse.view(torch.int32), lse_d.view(torch.int32))
+
+
 def test_decode_is_deterministic(entry):
     """Two runs of the same step give the same selection order and the same output bits."""
     case = synth.config(3, scale_down=16)
