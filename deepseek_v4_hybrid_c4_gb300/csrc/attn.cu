@@ -944,8 +944,11 @@ cudaError_t launch_attn(const AttnLaunch& h, cudaStream_t s, bool pdl) {
     cfg.blockDim = dim3(128, 1, 1);
     cfg.dynamicSmemBytes = 0;
     // up to 8 splits: 48 registers, so that eleven CTAs share an SM (the 32-request batch of 64
-    // heads, 2,048 CTAs of 5 splits, in little more than one wave instead of three)
+    // heads, 2,048 CTAs of 5 splits, in little more than one wave instead of three); up to 10
+    // (a 1M request's 640 keys): 56 registers, eight CTAs per SM, so that the 384-512 merge CTAs
+    // of a speculative verify fit beside the attention's CTAs
     return a.S <= 8    ? cudaLaunchKernelEx(&cfg, attn_merge_kernel<8>, a)
+           : a.S <= 10 ? cudaLaunchKernelEx(&cfg, attn_merge_kernel<10>, a)
            : a.S <= 16 ? cudaLaunchKernelEx(&cfg, attn_merge_kernel<16>, a)
                        : cudaLaunchKernelEx(&cfg, attn_merge_kernel<AT_MAX_SPLITS>, a);
 }
