@@ -85,6 +85,14 @@ CSA_DEV void cp_async_wait_group() {
 }
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy (tensor cores, TMA).
 CSA_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// Bulk reduction by the copy engine: the u32 words of [src, src + bytes) in this CTA's shared memory
+// added into global memory at dst (16-byte aligned, bytes % 16 == 0), tracked by the bulk group.
+CSA_DEV void bulk_red_add_u32(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.u32 [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes) : "memory");
+}
+CSA_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Until every committed bulk operation of this thread has read its shared-memory source.
+CSA_DEV void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 CSA_DEV void st_shared_zero16(uint32_t addr) {
     asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");

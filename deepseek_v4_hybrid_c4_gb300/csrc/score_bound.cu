@@ -328,20 +328,19 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
                 pdl_wait();
                 waited = true;
             }
-            const int nb = 1 << a.hb;
-            for (int i = (int)threadIdx.x - 64; i < (a.nq << a.hb) / 4; i += SB_FLUSH_T) {
-                const uint32_t addr = smem_u32(hist) + 16u * (uint32_t)i;
-                const uint4 v = ld_shared_v4(addr);
-                if (v.x | v.y | v.z | v.w) {
-                    const int p = (4 * i) >> a.hb, bin = (4 * i) & (nb - 1);
-                    uint32_t* g = a.hist + ((int64_t)r * a.nq + p) * kHistBlock + bin;
-                    if (v.x) atomicAdd(g, v.x);
-                    if (v.y) atomicAdd(g + 1, v.y);
-                    if (v.z) atomicAdd(g + 2, v.z);
-                    if (v.w) atomicAdd(g + 3, v.w);
-                    st_shared_zero16(addr);
-                }
+            // one bulk reduction per position by the copy engine (the counts were made visible to
+            // it by every epilogue thread's proxy fence before the rendezvous)
+            if (threadIdx.x == 64) {
+                for (int p = 0; p < a.nq; ++p)
+                    bulk_red_add_u32(a.hist + ((int64_t)r * a.nq + p) * kHistBlock,
+                                     smem_u32(hist) + 4u * (uint32_t)(p << a.hb), 4u << a.hb);
+                bulk_commit();
+                bulk_wait_read_all();
             }
+        };
+        auto zero_hist = [&]() {  // after a rendezvous that follows the flush
+            for (int i = (int)threadIdx.x - 64; i < (a.nq << a.hb) / 4; i += SB_FLUSH_T)
+                st_shared_zero16(smem_u32(hist) + 16u * (uint32_t)i);
         };
         TileCursor c;
         int er = -1;
@@ -349,8 +348,11 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
             if (!c.seek(a, m0 + jl)) break;
             if (c.r != er) {
                 if (er >= 0 && a.hist) {
+                    fence_proxy_async_smem();
                     ok = rendezvous();
                     if (ok) flush(er);
+                    ok = ok && rendezvous();
+                    if (ok) zero_hist();
                     ok = ok && rendezvous();
                     if (!ok) break;
                 }
@@ -447,6 +449,7 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
         }
         if (!ok) raise_status(a.status, CSA_ERR_TIMEOUT);
         if (ok && er >= 0 && a.hist) {
+            fence_proxy_async_smem();
             if (rendezvous()) flush(er);
             else raise_status(a.status, CSA_ERR_TIMEOUT);
         }
